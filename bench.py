@@ -1,0 +1,452 @@
+"""Benchmark: buffered gated-delta decode, tokens/s per layer, and achieved HBM bandwidth.
+
+Workload: gated delta rule layer with 16 q/k heads shared by 32 value heads,
+d_k = d_v = 128, bf16 q/k/v and buffer, fp32 state, B = 256 requests, buffer
+size m = 8.  A step is one decode step of all B requests (one kvb_decode
+launch), with the fold of the requests whose buffer fills in that step.
+Request r starts at buffer occupancy r mod m, so every step holds B/m requests
+at each occupancy 0..m-1 and B/m folds: each step costs the cycle average.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line (rank 0).  Under torchrun (N > 1) every rank runs its
+own B requests on its own GPU (weak scaling, no data-path collective); the
+reported time is the maximum over ranks.
+"""
+from __future__ import annotations
+
+import os
+
+for _v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+    os.environ.setdefault(_v, "1")
+
+import argparse  # noqa: E402
+import hashlib  # noqa: E402
+import json  # noqa: E402
+import statistics  # noqa: E402
+import subprocess  # noqa: E402
+import sys  # noqa: E402
+import time  # noqa: E402
+
+import numpy as np  # noqa: E402
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from kv_buffered_decoding_gb300 import inputs as I  # noqa: E402
+
+WORKLOAD = I.WORKLOADS["gdn_B256_Hk16_Hv32_d128"]
+METRIC = "decode tok/s per layer (B=256, m=8) and achieved HBM GB/s vs peak"
+FALLBACK_HBM_GBS = 6800.0
+N_BANK = 8  # distinct input token sets cycled through the timed steps
+
+
+def workload_config(w=WORKLOAD):
+    L = w.layer
+    return {"workload": f"gated_delta_decode_B{w.batch}_Hk{L.n_qk_heads}_Hv{L.n_v_heads}"
+                        f"_d{L.d_k}_m{w.m}_bf16",
+            "batch": w.batch, "n_qk_heads": L.n_qk_heads, "n_v_heads": L.n_v_heads,
+            "d_k": L.d_k, "d_v": L.d_v, "m": w.m, "variant": "gated_delta",
+            "kv_dtype": "bf16", "state_dtype": "f32", "occupancy": "staggered (r mod m)",
+            "l2": "inputs larger than L2: 512 MiB of state read per step, no flush needed"}
+
+
+def step_bytes(w, lengths):
+    """Algorithmic HBM bytes of one decode step given each request's occupancy before it.
+
+    Per request: state read, q, the new token (k, v, log-gate, beta) read and
+    appended, the n buffered tokens (raw k, v, gate, beta) read, o written, and
+    the state written back when the step folds.
+    """
+    L = w.layer
+    S = L.n_v_heads * L.d_k * L.d_v * 4
+    entry = L.n_qk_heads * L.d_k * 2 + L.n_v_heads * L.d_v * 2 + 2 * L.n_v_heads * 4
+    q = L.n_qk_heads * L.d_k * 2
+    o = L.n_v_heads * L.d_v * 4
+    n = np.asarray(lengths, dtype=np.int64)
+    folds = int(np.count_nonzero(n + 1 >= w.m))
+    return int(len(n) * (S + q + 2 * entry + o) + int(n.sum()) * entry + folds * S)
+
+
+def hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        try:
+            with open(path) as f:
+                d = json.load(f)
+            for key in ("hbm_gbs", "hbm_GBps", "hbm"):
+                if key in d and isinstance(d[key], (int, float)):
+                    return float(d[key]), "of measured (MEASURED_PEAKS.json hbm_gbs)"
+        except (OSError, ValueError):
+            pass
+    return FALLBACK_HBM_GBS, "of fallback (6.8 TB/s, no MEASURED_PEAKS.json)"
+
+
+def kernel_hash():
+    h = hashlib.sha256()
+    for rel in ("kv_buffered_decoding_gb300/csrc/decode.cu",
+                "kv_buffered_decoding_gb300/csrc/kvb_device.cuh"):
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic():
+    """DRAM bytes per launch of the decode kernel from the committed ncu summary, if it
+    was taken on the current kernel source; else None."""
+    path = os.path.join(ROOT, "profiles", "decode_gdn_B256_traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+    except (OSError, ValueError):
+        return None
+    if d.get("kernel_hash") != kernel_hash():
+        return None
+    return d.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.out = None
+
+    def __enter__(self):
+        try:
+            self.out = open("/tmp/kvb_clocks_%d.csv" % os.getpid(), "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.out, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        if self.out:
+            self.out.close()
+
+    def summary(self):
+        if self.proc is None or self.out is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        sm, smax, reasons, power = [], [], set(), []
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.out.name) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax.append(float(parts[2]))
+                    power.append(float(parts[3]))
+                except ValueError:
+                    continue
+                for name, val in zip(names, parts[5:9]):
+                    if val.lower().startswith("active"):
+                        reasons.add(name)
+        os.unlink(self.out.name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "power_w_median": statistics.median(power), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+def max_over_ranks(ms, dist=None):
+    """The slowest rank's time: every rank ran its own requests, so the job ends with it."""
+    if dist is None or not dist.is_initialized() or dist.get_world_size() == 1:
+        return float(ms)
+    import torch
+    t = torch.tensor([float(ms)], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rate(world, batch, steps, elapsed_ms):
+    """Whole-job tokens/s: every rank decodes `batch` requests for `steps` steps."""
+    return world * batch * steps / (elapsed_ms / 1e3)
+
+
+# --------------------------------------------------------------------------- CPU arm
+def oracle_rate(w, budget_s, reqs_per_step=8, seed=11, max_steps=None):
+    """The fp64 oracle (as it stands) on a bounded sample of the workload: consecutive
+    decode steps of `reqs_per_step` requests (all 32 heads).  Returns (tok/s, steps, secs)."""
+    import oracle
+    rng = np.random.default_rng(seed)
+    L = w.layer
+    S = I.draw_state(rng, L, reqs_per_step).astype(np.float64)
+    steps, t0 = 0, time.perf_counter()
+    while True:
+        tok = I.draw_tokens(rng, L, (1, reqs_per_step))
+        _, S, _ = oracle.decode_sequence(S, tok, L.variant)
+        steps += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s or (max_steps and steps >= max_steps):
+            break
+    return reqs_per_step * steps / el, steps, el
+
+
+def run_reference(args, rank, world):
+    """The oracle as the reference arm, on the host cores, in this workload's unit."""
+    if rank != 0:
+        return
+    w = WORKLOAD
+    for _ in range(max(args.warmup, 0)):
+        oracle_rate(w, 0.0, reqs_per_step=1, max_steps=1)
+    # size each step so the K timed steps take about a minute
+    probe, _, _ = oracle_rate(w, 0.0, reqs_per_step=1, max_steps=1)
+    per_req = 1.0 / probe
+    reqs = int(max(1, min(8, round(60.0 / max(args.steps, 1) / per_req))))
+    t0 = time.perf_counter()
+    rate, steps, el = oracle_rate(w, 0.0, reqs_per_step=reqs, max_steps=args.steps)
+    el = time.perf_counter() - t0
+    value = reqs * steps / el
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tok/s",
+            "n_gpus": world, "steps": steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * el / steps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": workload_config(),
+            "cpu_baseline": {"value": value, "unit": "tok/s", "cores": 1, "kind": "oracle",
+                             "sample": f"{reqs} request(s) x 32 heads per step, {steps} steps, "
+                                       "fp64 per-token recurrence (numpy, one thread)"},
+            "e2e": {"value": value, "unit": "tok/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# --------------------------------------------------------------------------- GPU arm
+def run_ours(args, rank, world, local_rank):
+    import torch
+    from kv_buffered_decoding_gb300 import kvb
+
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    w = WORKLOAD
+    L = w.layer
+    B, m, bs = w.batch, w.m, w.block_size
+    cfg = kvb.make_config(kvb.KVB_GATED_DELTA, kvb.KVB_BF16, L.n_qk_heads, L.n_v_heads, L.d_k,
+                          L.d_v, m, bs, B, B, B, 1)
+    pool = kvb.Pool(cfg, device=dev)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(1000 + rank)
+    pool.state.normal_(0.0, 1.0 / np.sqrt(L.d_k), generator=gen)
+    perm = np.random.default_rng(7 + rank).permutation(B)
+    for r in range(B):
+        pool.set_request(r, r, [int(perm[r])])
+    rng = np.random.default_rng(w.seed + rank)
+    bank_np = [I.draw_tokens(rng, L, (B,)) for _ in range(N_BANK)]
+
+    def to_dev(tok):
+        return (torch.from_numpy(tok["q"]).to(torch.bfloat16).to(dev),
+                torch.from_numpy(tok["k"]).to(torch.bfloat16).to(dev),
+                torch.from_numpy(tok["v"]).to(torch.bfloat16).to(dev),
+                torch.from_numpy(tok["log_g"]).to(dev), torch.from_numpy(tok["beta"]).to(dev))
+
+    bank = [to_dev(t) for t in bank_np]
+    o = torch.empty(B, L.n_v_heads, L.d_v, dtype=torch.float32, device=dev)
+    req = np.arange(B, dtype=np.int32)
+    # staggered start: request r holds r mod m tokens
+    occ = req % m
+    for s in range(m - 1):
+        rows = np.nonzero(occ > s)[0].astype(np.int32)
+        sel = torch.from_numpy(rows).long().to(dev)
+        pool.decode(rows, *[x.index_select(0, sel) for x in bank[s % N_BANK]])
+    torch.cuda.synchronize()
+    assert np.array_equal(pool.get_lengths()[:B], occ)
+
+    for i in range(args.warmup):
+        pool.decode(req, *bank[i % N_BANK], o=o)
+    torch.cuda.synchronize()
+
+    # algorithmic bytes of each timed step, from the host's exact length model
+    lengths = pool.get_lengths()[:B].astype(np.int64)
+    total_bytes, lens = 0, lengths.copy()
+    for _ in range(args.steps):
+        total_bytes += step_bytes(w, lens)
+        lens = lens + 1
+        lens[lens >= m] = 0
+
+    stream = torch.cuda.current_stream(dev)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local_rank) as clocks:
+        start.record(stream)
+        for i in range(args.steps):
+            ev[i][0].record(stream)
+            pool.decode(req, *bank[i % N_BANK], o=o)
+            ev[i][1].record(stream)
+        stop.record(stream)
+        torch.cuda.synchronize()
+        # keep the GPU busy a moment longer for the clock sampler's last samples
+    elapsed_ms = start.elapsed_time(stop)
+    launch_ms = [a.elapsed_time(b) for a, b in ev]
+    clk = clocks.summary()
+    elapsed_ms = max_over_ranks(elapsed_ms, dist)
+    err = pool.get_error()
+    if err is not None:
+        raise RuntimeError(f"device error during bench: {err}")
+
+    value = job_rate(world, B, args.steps, elapsed_ms)
+    mean_launch_s = statistics.mean(launch_ms) / 1e3
+    bytes_per_launch = total_bytes / args.steps
+    achieved = bytes_per_launch / mean_launch_s / 1e9
+    peak, peak_src = hbm_peak()
+
+    # the same step end to end through the public API: pinned host inputs copied in,
+    # outputs copied back, inside the timed region
+    host_bank = []
+    for tok in bank_np:
+        hb = []
+        for key in ("q", "k", "v"):
+            hb.append(torch.from_numpy(tok[key]).to(torch.bfloat16).pin_memory())
+        for key in ("log_g", "beta"):
+            hb.append(torch.from_numpy(tok[key]).pin_memory())
+        host_bank.append(hb)
+    stage = [torch.empty_like(x, device=dev) for x in host_bank[0]]
+    o_host = torch.empty(B, L.n_v_heads, L.d_v, dtype=torch.float32).pin_memory()
+    h2d = sum(x.numel() * x.element_size() for x in host_bank[0])
+    d2h = o_host.numel() * o_host.element_size()
+    e2e_steps = args.steps
+    for i in range(min(args.warmup, 8)):
+        for s_, h_ in zip(stage, host_bank[i % N_BANK]):
+            s_.copy_(h_, non_blocking=True)
+        pool.decode(req, *stage, o=o)
+        o_host.copy_(o, non_blocking=True)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    s2, e2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s2.record(stream)
+    for i in range(e2e_steps):
+        for s_, h_ in zip(stage, host_bank[i % N_BANK]):
+            s_.copy_(h_, non_blocking=True)
+        pool.decode(req, *stage, o=o)
+        o_host.copy_(o, non_blocking=True)
+    e2.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = s2.elapsed_time(e2)
+    e2e_ms = max_over_ranks(e2e_ms, dist)
+    e2e_value = job_rate(world, B, e2e_steps, e2e_ms)
+
+    # in-run HBM copy probe (1 GiB each way), best of 10
+    src = torch.empty(1 << 28, dtype=torch.float32, device=dev).normal_(generator=gen)
+    dst = torch.empty_like(src)
+    probe = []
+    for _ in range(12):
+        a, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        kvb.copy_probe(src, dst)
+        b_.record(stream)
+        torch.cuda.synchronize()
+        probe.append(a.elapsed_time(b_))
+    copy_gbs = 2 * src.numel() * 4 / (min(probe[2:]) / 1e3) / 1e9
+    del src, dst
+
+    # recurrent decoding (m = 0) on the same workload, for the speed-up the method claims
+    cfg0 = kvb.make_config(kvb.KVB_GATED_DELTA, kvb.KVB_BF16, L.n_qk_heads, L.n_v_heads, L.d_k,
+                           L.d_v, 0, bs, 1, B, B, 1)
+    pool0 = kvb.Pool(cfg0, device=dev)
+    pool0.state.copy_(pool.state)
+    for r in range(B):
+        pool0.set_request(r, r, [])
+    n_rec = max(16, min(args.steps, 512))
+    for i in range(4):
+        pool0.decode(req, *bank[i % N_BANK], o=o)
+    torch.cuda.synchronize()
+    a, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for i in range(n_rec):
+        pool0.decode(req, *bank[i % N_BANK], o=o)
+    b_.record(stream)
+    torch.cuda.synchronize()
+    rec_ms = a.elapsed_time(b_) / n_rec
+
+    if rank != 0:
+        return
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        rate, steps, el = oracle_rate(w, args.cpu_seconds)
+        cpu = {"value": rate, "unit": "tok/s", "cores": 1, "kind": "oracle",
+               "sample": f"8 requests x 32 heads, {steps} consecutive decode steps "
+                         f"({el:.1f} s), fp64 per-token recurrence (numpy, one thread)"}
+    line = {
+        "metric": METRIC, "value": value, "unit": "tok/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": elapsed_ms / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic (seeded; state iid normal, q/k L2-normalised, beta = sigmoid(N), "
+                "log-decay = -0.1 softplus(N))",
+        "config": workload_config(),
+        "hbm_gbs": achieved,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": ncu_traffic(),
+                     "kernel": "decode_kernel<bf16, gated_delta, 128>",
+                     "algorithmic_bytes_per_launch": bytes_per_launch,
+                     "mean_launch_us": mean_launch_s * 1e6, "peak_source": peak_src},
+        "copy_probe_gbs": copy_gbs,
+        "frac_of_copy_probe": achieved / copy_gbs,
+        "recurrent_m0_ms_per_step": rec_ms,
+        "speedup_vs_recurrent": rec_ms / (elapsed_ms / args.steps),
+        "e2e": {"value": e2e_value, "unit": "tok/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": args.steps,
+        "clocks": clk,
+        "cpu_baseline": cpu,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=4096)
+    ap.add_argument("--warmup", type=int, default=32)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("gloo")
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+    else:
+        from kv_buffered_decoding_gb300 import build as _build
+        if rank == 0 or world == 1:
+            _build.build()
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+        run_ours(args, rank, world, local_rank)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

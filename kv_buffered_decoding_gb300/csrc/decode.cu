@@ -1,0 +1,304 @@
+// Buffered decode, recurrent decode (m = 0) and short-context decode kernels.
+//
+// KVBuffer ("KVBuffer: IO-aware Serving for Linear Attention", Figure 1):
+// each decode step loads a request's state S0 together with its buffered KVs
+// and computes the output; S0 is not written; when the buffer is full, all
+// buffered KVs are folded into S0 and the state is written back to its slot.
+// With S0 the state at the last fold, n tokens buffered since, and the current
+// token t = n+1 (A_i = cumulative log-gate since the fold):
+//   u_i = v_i                                                  plain / gated
+//   u_t = beta_t (v_t - e^{A_t} S0^T k_t - sum_{i<=n} e^{A_t-A_i} (k_t.k_i) u_i)
+//                                                              gated delta rule
+//   o_t = e^{A_t} S0^T q_t + sum_{i<=t} e^{A_t-A_i} (q_t.k_i) u_i
+//   fold:  S <- e^{A_t} S0 + sum_{i<=t} e^{A_t-A_i} k_i u_i^T
+// which equals the per-token recurrence exactly (up to rounding).  A gated
+// delta token's u is kept in the buffer (pseudo-value), so S0 is touched by two
+// mat-vecs per step (S0^T q_t, S0^T k_t) whatever the buffer occupancy.
+//
+// One CTA per (batch row, value head); 2*D threads.  Warp w owns state columns
+// [16w, 16w+16); lane = 4*rsub + c owns columns 16w+4c..+3 of rows rsub + 8j,
+// so every load of the state is a 64-byte segment of a row and the reduction
+// over rows is three xor-shuffles inside the warp.  The state tile stays in
+// registers from its load to the fold, so S crosses HBM once per step (twice
+// on a fold step, once in each direction).
+#include "kvb_device.cuh"
+
+namespace kvb {
+
+template <typename KT, int VARIANT, int D, bool RECURRENT>
+__global__ void __launch_bounds__(2 * D, 2)
+    decode_kernel(const PoolView P, const RowBatch rows, const TokenIO io) {
+  constexpr int DK = D, DV = D, NT = 2 * D, RPT = DK / 8, E = DK / 32;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int rsub = lane >> 2, col0 = warp * 16 + (lane & 3) * 4;
+  const int h = blockIdx.x;
+  const RowDesc d = rows.r[blockIdx.y];
+  const size_t b = (size_t)rows.row0 + blockIdx.y;
+  const int group = P.Hv / P.Hk;
+  const int hq = h / group;
+  const bool has_state = d.slot >= 0;
+  const int n = RECURRENT ? 0 : d.n;
+  const bool fold = RECURRENT || (d.flags & kFlagFlush);
+
+  extern __shared__ float4 dyn_smem[];
+  float *ks = reinterpret_cast<float *>(dyn_smem);  // [lmax][DK] keys of folded tokens
+  float *us = ks + (size_t)io.lmax * DK;            // [lmax][DV] their u
+  __shared__ __align__(16) float qs[DK];
+  __shared__ __align__(16) float kts[DK];
+  __shared__ float Acum[kMaxTok], wt[kMaxTok], sc[kMaxTok], cc[kMaxTok];
+  __shared__ int grow[kMaxTok];
+  __shared__ float e_t_s;
+  __shared__ int bad;
+
+  // 1. the state tile: the only large read, issued first so it overlaps the rest
+  float4 s[RPT];
+  float *Sp = P.state + (has_state ? ((size_t)d.slot * P.Hv + h) * DK * DV : 0);
+  if (has_state) {
+#pragma unroll
+    for (int j = 0; j < RPT; ++j) s[j] = ld_stream4(Sp + (rsub + 8 * j) * DV + col0);
+  } else {
+#pragma unroll
+    for (int j = 0; j < RPT; ++j) s[j] = f4(0.f);
+  }
+
+  // 2. buffer rows of tokens 0..n (n = the slot the current token goes to)
+  if (!RECURRENT && warp == 0) {
+    int anybad = 0;
+    for (int i = lane; i <= n; i += 32) {
+      const int g = buffer_row(P, d.req, i);
+      grow[i] = g;
+      anybad |= (g < 0);
+    }
+    anybad = __any_sync(kFull, anybad);
+    if (lane == 0) bad = anybad;
+  }
+  const KT *qg = static_cast<const KT *>(io.q) + (b * P.Hk + hq) * DK;
+  const KT *kg = static_cast<const KT *>(io.k) + (b * P.Hk + hq) * DK;
+  for (int i = tid; i < DK; i += NT) {
+    qs[i] = P.scale * to_float(qg[i]);
+    kts[i] = to_float(kg[i]);
+  }
+  float a_t = 0.f, beta_t = 0.f;
+  if (VARIANT != kPlain && io.log_g) a_t = io.log_g[b * P.Hv + h];
+  if (VARIANT == kGatedDelta) beta_t = io.beta[b * P.Hv + h];
+  __syncthreads();
+  if (!RECURRENT && bad) return;  // CTA-uniform
+
+  // 3. gate prefix sums and decay weights (warp 0); dot products (all warps)
+  if (VARIANT != kPlain) {
+    if (warp == 0) {
+      warp_prefix(
+          n + 1,
+          [&](int i) { return i < n ? P.gbuf[(size_t)grow[i] * P.Hv + h] : a_t; }, Acum, lane);
+      __syncwarp();
+      const float At = Acum[n];
+      for (int i = lane; i <= n; i += 32) wt[i] = expf(At - Acum[i]);
+      if (lane == 0) e_t_s = expf(At);
+    }
+  } else {
+    for (int i = tid; i <= n; i += NT) wt[i] = 1.f;
+    if (tid == 0) e_t_s = 1.f;
+  }
+  for (int i = warp; i <= n; i += NT / 32) {
+    const KT *kp = (i < n) ? static_cast<const KT *>(P.kbuf) + ((size_t)grow[i] * P.Hk + hq) * DK : kg;
+    float sq, sk = 0.f;
+    if constexpr (E == 4) {
+      const float4 kv = ld4(kp + lane * 4);
+      const float4 qv = *reinterpret_cast<const float4 *>(&qs[lane * 4]);
+      sq = qv.x * kv.x + qv.y * kv.y + qv.z * kv.z + qv.w * kv.w;
+      if (VARIANT == kGatedDelta) {
+        const float4 tv = *reinterpret_cast<const float4 *>(&kts[lane * 4]);
+        sk = tv.x * kv.x + tv.y * kv.y + tv.z * kv.z + tv.w * kv.w;
+      }
+      if (fold) *reinterpret_cast<float4 *>(&ks[i * DK + lane * 4]) = kv;
+    } else {
+      const float2 kv = ld2(kp + lane * 2);
+      const float2 qv = *reinterpret_cast<const float2 *>(&qs[lane * 2]);
+      sq = qv.x * kv.x + qv.y * kv.y;
+      if (VARIANT == kGatedDelta) {
+        const float2 tv = *reinterpret_cast<const float2 *>(&kts[lane * 2]);
+        sk = tv.x * kv.x + tv.y * kv.y;
+      }
+      if (fold) *reinterpret_cast<float2 *>(&ks[i * DK + lane * 2]) = kv;
+    }
+    sq = warp_sum(sq);
+    if (VARIANT == kGatedDelta) sk = warp_sum(sk);
+    if (lane == 0) {
+      sc[i] = sq;
+      cc[i] = sk;
+    }
+  }
+  __syncthreads();
+
+  // 4. S0^T q_t (and S0^T k_t) over this thread's rows, reduced over rows
+  float4 aq = f4(0.f), ak = f4(0.f);
+  if (has_state) {
+#pragma unroll
+    for (int j = 0; j < RPT; ++j) {
+      const int r = rsub + 8 * j;
+      fma4(aq, qs[r], s[j]);
+      if (VARIANT == kGatedDelta) fma4(ak, kts[r], s[j]);
+    }
+    aq = rows_sum4(aq);
+    if (VARIANT == kGatedDelta) ak = rows_sum4(ak);
+  }
+
+  // 5. buffered tokens' terms, tokens split over the 8 row lanes
+  float4 po = f4(0.f), pc = f4(0.f);
+  for (int i = rsub; i < n; i += 8) {
+    float4 ui;
+    if (VARIANT == kGatedDelta)
+      ui = ld4(P.ubuf + ((size_t)grow[i] * P.Hv + h) * DV + col0);
+    else
+      ui = ld4(static_cast<const KT *>(P.vbuf) + ((size_t)grow[i] * P.Hv + h) * DV + col0);
+    fma4(po, wt[i] * sc[i], ui);
+    if (VARIANT == kGatedDelta) fma4(pc, wt[i] * cc[i], ui);
+    if (fold) *reinterpret_cast<float4 *>(&us[i * DV + col0]) = ui;
+  }
+  po = rows_sum4(po);
+  if (VARIANT == kGatedDelta) pc = rows_sum4(pc);
+
+  const float e_t = e_t_s;
+  const float4 vt = ld4(static_cast<const KT *>(io.v) + (b * P.Hv + h) * DV + col0);
+  float4 ut = vt;
+  if (VARIANT == kGatedDelta) {
+    ut.x = beta_t * (vt.x - fmaf(e_t, ak.x, pc.x));
+    ut.y = beta_t * (vt.y - fmaf(e_t, ak.y, pc.y));
+    ut.z = beta_t * (vt.z - fmaf(e_t, ak.z, pc.z));
+    ut.w = beta_t * (vt.w - fmaf(e_t, ak.w, pc.w));
+  }
+  float4 o = add4(mul4(e_t, aq), po);
+  fma4(o, sc[n], ut);
+  if (rsub == 0) {
+    __stcs(reinterpret_cast<float4 *>(io.o + (b * P.Hv + h) * DV + col0), o);
+    if (!RECURRENT) {
+      const size_t g = grow[n];
+      st4(static_cast<KT *>(P.vbuf) + (g * P.Hv + h) * DV + col0, vt);
+      if (VARIANT == kGatedDelta) st4(P.ubuf + (g * P.Hv + h) * DV + col0, ut);
+    }
+    if (fold) *reinterpret_cast<float4 *>(&us[n * DV + col0]) = ut;
+  }
+  if (!RECURRENT) {
+    const size_t g = grow[n];
+    if (h % group == 0)
+      for (int i = tid; i < DK / 4; i += NT)
+        st4(static_cast<KT *>(P.kbuf) + (g * P.Hk + hq) * DK + 4 * i,
+            *reinterpret_cast<const float4 *>(&kts[4 * i]));
+    if (tid == 0) {
+      P.gbuf[g * P.Hv + h] = a_t;
+      P.bbuf[g * P.Hv + h] = beta_t;
+    }
+  }
+
+  // 6. fold: S <- e^{A_t} S0 + sum_i e^{A_t-A_i} k_i u_i^T, written back once
+  if (fold && has_state) {
+    __syncthreads();
+#pragma unroll
+    for (int j = 0; j < RPT; ++j) s[j] = mul4(e_t, s[j]);
+    for (int i = 0; i <= n; ++i) {
+      const float4 u = *reinterpret_cast<const float4 *>(&us[i * DV + col0]);
+      const float w = wt[i];
+#pragma unroll
+      for (int j = 0; j < RPT; ++j) fma4(s[j], w * ks[i * DK + rsub + 8 * j], u);
+    }
+#pragma unroll
+    for (int j = 0; j < RPT; ++j) st_stream4(Sp + (rsub + 8 * j) * DV + col0, s[j]);
+  }
+  if (!RECURRENT && h == 0 && tid == 0) P.dlen[d.req] = fold ? 0 : n + 1;
+}
+
+// Device-side lengths after an accept that folds nothing.
+__global__ void set_lengths_kernel(const PoolView P, const RowBatch rows) {
+  for (int i = threadIdx.x; i < rows.count; i += blockDim.x) P.dlen[rows.r[i].req] = rows.r[i].n;
+}
+
+// 128-bit grid-stride copy, four independent 16-byte transfers per thread per
+// iteration (the HBM bandwidth probe).
+__global__ void __launch_bounds__(256) copy_probe_kernel(const float4 *__restrict__ src,
+                                                         float4 *__restrict__ dst, size_t n16) {
+  const size_t stride = (size_t)gridDim.x * blockDim.x;
+  size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+  for (; i + 3 * stride < n16; i += 4 * stride) {
+    float4 a = __ldcs(src + i), b = __ldcs(src + i + stride);
+    float4 c = __ldcs(src + i + 2 * stride), e = __ldcs(src + i + 3 * stride);
+    __stcs(dst + i, a);
+    __stcs(dst + i + stride, b);
+    __stcs(dst + i + 2 * stride, c);
+    __stcs(dst + i + 3 * stride, e);
+  }
+  for (; i < n16; i += stride) __stcs(dst + i, __ldcs(src + i));
+}
+
+// ------------------------------------------------------------------ launchers
+template <typename KT, int VARIANT, int D, bool REC>
+static cudaError_t run_decode(const PoolView &P, const RowBatch &rows, const TokenIO &io,
+                              cudaStream_t stream) {
+  const size_t smem = (size_t)io.lmax * 2 * D * sizeof(float);
+  static bool configured = false;
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(decode_kernel<KT, VARIANT, D, REC>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         kMaxTok * 2 * D * (int)sizeof(float));
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  dim3 grid(P.Hv, rows.count);
+  decode_kernel<KT, VARIANT, D, REC><<<grid, 2 * D, smem, stream>>>(P, rows, io);
+  return cudaGetLastError();
+}
+
+template <typename KT, int VARIANT, int D>
+static cudaError_t pick_rec(const PoolView &P, const RowBatch &rows, const TokenIO &io, bool rec,
+                            cudaStream_t s) {
+  return rec ? run_decode<KT, VARIANT, D, true>(P, rows, io, s)
+             : run_decode<KT, VARIANT, D, false>(P, rows, io, s);
+}
+
+template <typename KT, int VARIANT>
+static cudaError_t pick_d(const PoolView &P, const RowBatch &rows, const TokenIO &io, int d,
+                          bool rec, cudaStream_t s) {
+  if (d == 128) return pick_rec<KT, VARIANT, 128>(P, rows, io, rec, s);
+  if (d == 64) return pick_rec<KT, VARIANT, 64>(P, rows, io, rec, s);
+  return kUnsupported;
+}
+
+template <typename KT>
+static cudaError_t pick_variant(const PoolView &P, const RowBatch &rows, const TokenIO &io,
+                                int variant, int d, bool rec, cudaStream_t s) {
+  switch (variant) {
+    case kPlain: return pick_d<KT, kPlain>(P, rows, io, d, rec, s);
+    case kGated: return pick_d<KT, kGated>(P, rows, io, d, rec, s);
+    case kGatedDelta: return pick_d<KT, kGatedDelta>(P, rows, io, d, rec, s);
+  }
+  return kUnsupported;
+}
+
+cudaError_t launch_decode(const PoolView &P, const RowBatch &rows, const TokenIO &io, int variant,
+                          int dtype, int d, bool recurrent, int flush_len, cudaStream_t stream) {
+  if (rows.count <= 0) return cudaSuccess;
+  TokenIO io2 = io;
+  io2.lmax = flush_len;
+  if (dtype == 0) return pick_variant<float>(P, rows, io2, variant, d, recurrent, stream);
+  if (dtype == 1) return pick_variant<__nv_bfloat16>(P, rows, io2, variant, d, recurrent, stream);
+  return kUnsupported;
+}
+
+cudaError_t launch_set_lengths(const PoolView &P, const RowBatch &rows, cudaStream_t stream) {
+  if (rows.count <= 0) return cudaSuccess;
+  set_lengths_kernel<<<1, 256, 0, stream>>>(P, rows);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_copy_probe(const void *src, void *dst, size_t bytes, cudaStream_t stream) {
+  int dev = 0, sms = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  const size_t n16 = bytes / 16;
+  copy_probe_kernel<<<sms * 8, 256, 0, stream>>>(static_cast<const float4 *>(src),
+                                                  static_cast<float4 *>(dst), n16);
+  return cudaGetLastError();
+}
+
+}  // namespace kvb

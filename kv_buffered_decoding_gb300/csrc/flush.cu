@@ -1,0 +1,144 @@
+// Deferred state update: fold every buffered token of a request into its state.
+//
+// KVBuffer ("KVBuffer: IO-aware Serving for Linear Attention", Figure 1
+// caption): when the buffer is full, the state is updated with all buffered
+// KVs on the GPU and written back to the state slot.  For L buffered tokens
+// with cumulative log-gates A_1..A_L and pseudo-values u_i (u_i = v_i except
+// for the gated delta rule, where u_i was computed when the token entered the
+// buffer):
+//     S <- e^{A_L} S0 + sum_{i<=L} e^{A_L-A_i} k_i u_i^T
+// a rank-L update, K^T diag(w) U, of the register-resident state tile.  At
+// L <= 64 this is 2 L flop per state element against 8 bytes of state traffic
+// per element (read + write), i.e. below the fp32 FMA ridge: the kernel is
+// bound by HBM, and the update runs on the FMA pipes.
+//
+// Used by kvb_flush and by kvb_accept when accepted drafts fill the buffer;
+// decode folds in-kernel (decode.cu).
+#include "kvb_device.cuh"
+
+namespace kvb {
+
+template <typename KT, int VARIANT, int D>
+__global__ void __launch_bounds__(2 * D, 2) flush_kernel(const PoolView P, const RowBatch rows) {
+  constexpr int DK = D, DV = D, NT = 2 * D, RPT = DK / 8;
+  constexpr bool DELTA = VARIANT == kGatedDelta;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int rsub = lane >> 2, col0 = warp * 16 + (lane & 3) * 4;
+  const int h = blockIdx.x;
+  const RowDesc d = rows.r[blockIdx.y];
+  const int hq = h / (P.Hv / P.Hk);
+  const int L = d.n;
+
+  extern __shared__ float4 dyn_smem[];
+  float *ks = reinterpret_cast<float *>(dyn_smem);  // [L][DK]
+  float *us = ks + (size_t)L * DK;                  // [L][DV]
+  __shared__ float Acum[kMaxTok], wt[kMaxTok];
+  __shared__ int grow[kMaxTok];
+  __shared__ float eL_s;
+  __shared__ int bad;
+
+  float *Sp = P.state + ((size_t)d.slot * P.Hv + h) * DK * DV;
+  float4 s[RPT];
+#pragma unroll
+  for (int j = 0; j < RPT; ++j) s[j] = ld_stream4(Sp + (rsub + 8 * j) * DV + col0);
+
+  if (warp == 0) {
+    int anybad = 0;
+    for (int i = lane; i < L; i += 32) {
+      const int g = buffer_row(P, d.req, i);
+      grow[i] = g;
+      anybad |= (g < 0);
+    }
+    anybad = __any_sync(kFull, anybad);
+    if (lane == 0) bad = anybad;
+  }
+  __syncthreads();
+  if (bad) return;
+
+  if (warp == 0) {
+    if (VARIANT != kPlain) {
+      warp_prefix(L, [&](int i) { return P.gbuf[(size_t)grow[i] * P.Hv + h]; }, Acum, lane);
+      __syncwarp();
+      const float AL = Acum[L - 1];
+      for (int i = lane; i < L; i += 32) wt[i] = expf(AL - Acum[i]);
+      if (lane == 0) eL_s = expf(AL);
+    } else {
+      for (int i = lane; i < L; i += 32) wt[i] = 1.f;
+      if (lane == 0) eL_s = 1.f;
+    }
+  }
+  for (int idx = tid; idx < L * (DK / 4); idx += NT) {
+    const int i = idx / (DK / 4), c = (idx % (DK / 4)) * 4;
+    *reinterpret_cast<float4 *>(&ks[(size_t)i * DK + c]) =
+        ld4(static_cast<const KT *>(P.kbuf) + ((size_t)grow[i] * P.Hk + hq) * DK + c);
+  }
+  for (int idx = tid; idx < L * (DV / 4); idx += NT) {
+    const int i = idx / (DV / 4), c = (idx % (DV / 4)) * 4;
+    float4 u;
+    if (DELTA)
+      u = ld4(P.ubuf + ((size_t)grow[i] * P.Hv + h) * DV + c);
+    else
+      u = ld4(static_cast<const KT *>(P.vbuf) + ((size_t)grow[i] * P.Hv + h) * DV + c);
+    *reinterpret_cast<float4 *>(&us[(size_t)i * DV + c]) = u;
+  }
+  __syncthreads();
+
+  const float eL = eL_s;
+#pragma unroll
+  for (int j = 0; j < RPT; ++j) s[j] = mul4(eL, s[j]);
+  for (int i = 0; i < L; ++i) {
+    const float4 u = *reinterpret_cast<const float4 *>(&us[(size_t)i * DV + col0]);
+    const float w = wt[i];
+#pragma unroll
+    for (int j = 0; j < RPT; ++j) fma4(s[j], w * ks[(size_t)i * DK + rsub + 8 * j], u);
+  }
+#pragma unroll
+  for (int j = 0; j < RPT; ++j) st_stream4(Sp + (rsub + 8 * j) * DV + col0, s[j]);
+  if (h == 0 && tid == 0) P.dlen[d.req] = 0;
+}
+
+template <typename KT, int VARIANT, int D>
+static cudaError_t run_flush(const PoolView &P, const RowBatch &rows, int max_len,
+                             cudaStream_t stream) {
+  static bool configured = false;
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(flush_kernel<KT, VARIANT, D>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (kMaxTok - 1) * 2 * D * (int)sizeof(float));
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  const size_t smem = (size_t)max_len * 2 * D * sizeof(float);
+  dim3 grid(P.Hv, rows.count);
+  flush_kernel<KT, VARIANT, D><<<grid, 2 * D, smem, stream>>>(P, rows);
+  return cudaGetLastError();
+}
+
+template <typename KT, int VARIANT>
+static cudaError_t flush_d(const PoolView &P, const RowBatch &rows, int d, int max_len,
+                           cudaStream_t s) {
+  if (d == 128) return run_flush<KT, VARIANT, 128>(P, rows, max_len, s);
+  if (d == 64) return run_flush<KT, VARIANT, 64>(P, rows, max_len, s);
+  return kUnsupported;
+}
+
+template <typename KT>
+static cudaError_t flush_variant(const PoolView &P, const RowBatch &rows, int variant, int d,
+                                 int max_len, cudaStream_t s) {
+  switch (variant) {
+    case kPlain: return flush_d<KT, kPlain>(P, rows, d, max_len, s);
+    case kGated: return flush_d<KT, kGated>(P, rows, d, max_len, s);
+    case kGatedDelta: return flush_d<KT, kGatedDelta>(P, rows, d, max_len, s);
+  }
+  return kUnsupported;
+}
+
+cudaError_t launch_flush(const PoolView &P, const RowBatch &rows, int variant, int dtype, int d,
+                         int max_len, cudaStream_t stream) {
+  if (rows.count <= 0) return cudaSuccess;
+  if (dtype == 0) return flush_variant<float>(P, rows, variant, d, max_len, stream);
+  if (dtype == 1) return flush_variant<__nv_bfloat16>(P, rows, variant, d, max_len, stream);
+  return kUnsupported;
+}
+
+}  // namespace kvb

@@ -1,0 +1,69 @@
+// Internal types shared by the host library (kvb_host.cpp) and the kernels.
+// Plain structs only: this header is included by both g++ and nvcc sources.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include <cuda_runtime_api.h>
+
+namespace kvb {
+
+// Most batch rows one launch carries in its parameter block; longer batches
+// are split into several launches by the host library.
+constexpr int kMaxRows = 512;
+
+// Device view of a pool: raw pointers into the caller's regions plus shapes.
+struct PoolView {
+  float *state;       // [slots][Hv][dk][dv]
+  void *kbuf;         // [rows][Hk][dk]  kv dtype
+  void *vbuf;         // [rows][Hv][dv]  kv dtype
+  float *ubuf;        // [rows][Hv][dv]  (gated delta) pseudo-values
+  float *gbuf;        // [rows][Hv]      log-gates
+  float *bbuf;        // [rows][Hv]      beta
+  const int32_t *table;  // [max_requests][max_blocks]
+  int32_t *dlen;      // [max_requests] device-side lengths
+  int32_t *err;       // [4] error word: kind, request, value, count
+  int Hk, Hv, bs, max_blocks, num_blocks;
+  float scale;
+};
+
+// One batch row: which request, its buffer length before this call, its
+// state slot (-1 = none) and flags.
+struct RowDesc {
+  int32_t req, n, slot, flags;
+};
+constexpr int32_t kFlagFlush = 1;  // decode: fold the buffer (incl. this token) into S
+
+// Rows of one launch, passed by value in the kernel parameter block.
+struct RowBatch {
+  int32_t count;  // rows in this launch (== gridDim.y)
+  int32_t row0;   // index of rows[0] in the caller's input arrays
+  RowDesc r[kMaxRows];
+};
+
+// Input / output pointers of a decode or verify launch (device).
+struct TokenIO {
+  const void *q, *k, *v;  // kv dtype
+  const float *log_g, *beta;
+  float *o;
+  int T;     // tokens per row (1 for decode)
+  int lmax;  // most tokens any row of the launch stages in shared memory
+};
+
+enum ErrKind : int32_t { kErrNone = 0, kErrBlockRange = 1 };
+
+// Launchers (kernels.cu).  `dtype` is KVB_F32 / KVB_BF16; `d` is d_k == d_v.
+// Return cudaSuccess or the launch error; kUnsupported for a missing instance.
+constexpr cudaError_t kUnsupported = cudaErrorNotSupported;
+
+cudaError_t launch_decode(const PoolView &P, const RowBatch &rows, const TokenIO &io, int variant,
+                          int dtype, int d, bool recurrent, int flush_len, cudaStream_t stream);
+cudaError_t launch_verify(const PoolView &P, const RowBatch &rows, const TokenIO &io, int variant,
+                          int dtype, int d, int max_len, cudaStream_t stream);
+cudaError_t launch_flush(const PoolView &P, const RowBatch &rows, int variant, int dtype, int d,
+                         int max_len, cudaStream_t stream);
+cudaError_t launch_set_lengths(const PoolView &P, const RowBatch &rows, cudaStream_t stream);
+cudaError_t launch_copy_probe(const void *src, void *dst, size_t bytes, cudaStream_t stream);
+
+}  // namespace kvb

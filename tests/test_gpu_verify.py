@@ -1,0 +1,118 @@
+"""GPU parity: speculative verify of T drafts and accept of a prefix (no temporary states).
+
+Workload: the scalar-gated layer (16 heads, d=128, bf16) with a 1024-token
+prefill state, B=64 requests, m=8, T in {4, 2, 6, 8} drafts per round and an
+accepted prefix length drawn uniformly from [0, T] per request and round.
+Every round compares the drafts' outputs with the oracle (recurrent output
+after the accepted history plus drafts 0..j), the buffer lengths bit for bit
+with an independent host model (n += j; fold all when n >= m), and the state
+of every request that folded with the recurrent replay of accepted tokens
+only.  Outputs and states are compared for a sample of requests (requests are
+independent); lengths for all.
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+
+import oracle
+from kv_buffered_decoding_gb300 import inputs as I
+from tests.gpu_harness import blocks_needed, dev, make_pool, rel_err, tol_for
+
+pytestmark = pytest.mark.gpu
+torch = pytest.importorskip("torch")
+if not torch.cuda.is_available():
+    pytest.skip("needs a CUDA GPU", allow_module_level=True)
+
+SAMPLE = np.array([0, 5, 31, 63])
+
+
+@pytest.fixture(scope="module")
+def prefill_state():
+    w = I.WORKLOADS["verify_B64_gated"]
+    rng = np.random.default_rng(w.seed)
+    pre = I.draw_tokens(rng, w.layer, (w.prefill, w.batch))
+    return oracle.gated_prefill_closed_form(pre, w.layer.variant).astype(np.float32)
+
+
+def _bt(x):
+    """[B, T, ...] -> [T, B, ...] for the oracle."""
+    return None if x is None else np.swapaxes(x, 0, 1)
+
+
+@pytest.mark.parametrize("T,rounds", [(4, 200), (2, 60), (6, 60), (8, 60)])
+def test_verify_accept_rounds(prefill_state, T, rounds):
+    w = I.WORKLOADS["verify_B64_gated"]
+    layer, B, m, bs = w.layer, w.batch, w.m, w.block_size
+    cap = m - 1 + T
+    nb = blocks_needed(cap, bs)
+    pool = make_pool(layer, m, B, nb, bs)
+    pool.state.copy_(torch.from_numpy(prefill_state))
+    perm = np.random.default_rng(w.seed + 100 + T).permutation(B * nb)
+    for r in range(B):
+        pool.set_request(r, r, perm[r * nb:(r + 1) * nb])
+    rng = np.random.default_rng(w.seed * 1000 + T)
+    req = np.arange(B)
+    S_hist = prefill_state[SAMPLE].astype(np.float64)
+    n_model = np.zeros(B, dtype=np.int64)
+    tol = tol_for(layer)
+    worst = 0.0
+    folds_checked = 0
+    for rnd in range(rounds):
+        tok = I.draw_tokens(rng, layer, (B, T))
+        o = pool.verify(req, dev(tok["q"], layer), dev(tok["k"], layer), dev(tok["v"], layer),
+                        dev(tok["log_g"], f32=True), None)
+        j = rng.integers(0, T + 1, size=B)
+        pool.accept(req, j)
+        drafts = {key: _bt(None if val is None else val[SAMPLE]) for key, val in tok.items()}
+        o_ref = oracle.verify(S_hist, drafts, layer.variant)          # [T, n_s, Hv, dv]
+        worst = max(worst, rel_err(np.swapaxes(o.cpu().numpy()[SAMPLE], 0, 1), o_ref))
+        S_hist = oracle.accept(S_hist, drafts, j[SAMPLE], layer.variant)
+        n_model = n_model + j
+        folded = n_model >= m
+        n_model[folded] = 0
+        assert np.array_equal(pool.get_lengths(), n_model.astype(np.int32)), rnd
+        for i, r in enumerate(SAMPLE):
+            if folded[r] and rnd % 10 == 0:
+                torch.cuda.synchronize()
+                assert rel_err(pool.state[r].cpu().numpy(), S_hist[i]) <= tol, (rnd, r)
+                folds_checked += 1
+    assert worst <= tol, worst
+    assert np.array_equal(pool.get_device_lengths(), pool.get_lengths())
+    # fold whatever is buffered: states equal the replay of accepted tokens only
+    pool.flush(req)
+    torch.cuda.synchronize()
+    assert rel_err(pool.state.cpu().numpy()[SAMPLE], S_hist) <= tol
+    assert pool.get_error() is None
+
+
+def test_accept_zero_and_full():
+    """j = 0 leaves length and state untouched; j = T equals T decode steps."""
+    w = I.WORKLOADS["verify_B64_gated"]
+    layer, m, bs, T = w.layer, 8, 8, 4
+    B = 3
+    rng = np.random.default_rng(7)
+    S0 = I.draw_state(rng, layer, B, scale=0.05)
+    pool = make_pool(layer, m, B, 2, bs)
+    pool.state.copy_(torch.from_numpy(S0))
+    for r in range(B):
+        pool.set_request(r, r, [2 * r + 1, 2 * r])
+    tok = I.draw_tokens(rng, layer, (B, T))
+    args = (dev(tok["q"], layer), dev(tok["k"], layer), dev(tok["v"], layer),
+            dev(tok["log_g"], f32=True), None)
+    pool.verify(np.arange(B), *args)
+    pool.accept(np.arange(B), [0, T, 2])
+    torch.cuda.synchronize()
+    assert list(pool.get_lengths()) == [0, T, 2]
+    assert torch.equal(pool.state[0].cpu(), torch.from_numpy(S0[0]))  # untouched, bit for bit
+    # request 1 then decodes: its history is exactly the 4 accepted drafts
+    nxt = I.draw_tokens(rng, layer, (1, B))
+    o = pool.decode([1], dev(nxt["q"][0, 1:2], layer), dev(nxt["k"][0, 1:2], layer),
+                    dev(nxt["v"][0, 1:2], layer), dev(nxt["log_g"][0, 1:2], f32=True), None)
+    hist = {key: (None if val is None else np.concatenate([np.swapaxes(tok[key], 0, 1)[:, 1],
+                                                          nxt[key][:, 1]]))
+            for key in ("q", "k", "v", "log_g")}
+    hist["beta"] = None
+    o_ref, _, _ = oracle.decode_sequence(S0[1], hist, layer.variant)
+    assert rel_err(o.cpu().numpy()[0], o_ref[-1]) <= tol_for(layer)
+    assert pool.get_error() is None
