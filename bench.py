@@ -360,6 +360,15 @@ def run_ours(args, rank, world, local_rank):
         torch.cuda.synchronize()
         probe.append(a.elapsed_time(b_))
     copy_gbs = 2 * src.numel() * 4 / (min(probe[2:]) / 1e3) / 1e9
+    tcopy = []
+    for _ in range(12):
+        a, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        dst.copy_(src)
+        b_.record(stream)
+        torch.cuda.synchronize()
+        tcopy.append(a.elapsed_time(b_))
+    torch_copy_gbs = 2 * src.numel() * 4 / (min(tcopy[2:]) / 1e3) / 1e9
     del src, dst
 
     # recurrent decoding (m = 0) on the same workload, for the speed-up the method claims
@@ -403,6 +412,7 @@ def run_ours(args, rank, world, local_rank):
                      "algorithmic_bytes_per_launch": bytes_per_launch,
                      "mean_launch_us": mean_launch_s * 1e6, "peak_source": peak_src},
         "copy_probe_gbs": copy_gbs,
+        "torch_copy_gbs": torch_copy_gbs,
         "frac_of_copy_probe": achieved / copy_gbs,
         "recurrent_m0_ms_per_step": rec_ms,
         "speedup_vs_recurrent": rec_ms / (elapsed_ms / args.steps),

@@ -60,14 +60,21 @@ def _run(cmd):
     return cmd, proc.returncode, proc.stdout
 
 
-def build(force: bool = False, verbose: bool = False, ptxas_verbose: bool = False) -> str:
-    """Compile every kernel for sm_103a and link libkvb.so; return its path."""
-    if not force and up_to_date():
+def build(force: bool = False, verbose: bool = False, ptxas_verbose: bool = False,
+          defines=(), out_dir: str | None = None) -> str:
+    """Compile every kernel for sm_103a and link libkvb.so; return its path.
+
+    ``defines`` (e.g. ``["KVB_DECODE_SPLIT=1"]``) and ``out_dir`` build a variant of
+    the library elsewhere without touching the in-tree one.
+    """
+    lib = LIB if out_dir is None else os.path.join(out_dir, "libkvb.so")
+    out_dir = OUT_DIR if out_dir is None else out_dir
+    if not force and not defines and lib == LIB and up_to_date():
         return LIB
-    os.makedirs(OUT_DIR, exist_ok=True)
-    obj_dir = os.path.join(OUT_DIR, "obj")
+    os.makedirs(out_dir, exist_ok=True)
+    obj_dir = os.path.join(out_dir, "obj")
     os.makedirs(obj_dir, exist_ok=True)
-    inc = ["-I", INCLUDE, "-I", CSRC]
+    inc = ["-I", INCLUDE, "-I", CSRC] + [f"-D{d}" for d in defines]
     jobs = []
     objs = []
     for src in CU_SOURCES:
@@ -95,13 +102,13 @@ def build(force: bool = False, verbose: bool = False, ptxas_verbose: bool = Fals
     if failed:
         msg = "\n".join(" ".join(c) + "\n" + out for c, out in failed)
         raise RuntimeError(f"libkvb build failed:\n{msg}")
-    tmp = LIB + ".tmp"
+    tmp = lib + ".tmp"
     link = [_nvcc(), *ARCH, "-shared", "-cudart", "static", "-o", tmp, *objs]
     cmd, rc, out = _run(link)
     if rc != 0:
         raise RuntimeError("libkvb link failed:\n" + " ".join(cmd) + "\n" + out)
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":

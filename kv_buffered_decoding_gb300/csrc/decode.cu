@@ -25,13 +25,14 @@
 
 namespace kvb {
 
-template <typename KT, int VARIANT, int D, bool RECURRENT>
-__global__ void __launch_bounds__(2 * D, 2)
+template <typename KT, int VARIANT, int D, bool RECURRENT, int NSPLIT>
+__global__ void __launch_bounds__(2 * D / NSPLIT, 4 / (2 * D / NSPLIT / 128))
     decode_kernel(const PoolView P, const RowBatch rows, const TokenIO io) {
-  constexpr int DK = D, DV = D, NT = 2 * D, RPT = DK / 8, E = DK / 32;
+  constexpr int DK = D, DV = D, NT = 2 * D / NSPLIT, RPT = DK / 8, E = DK / 32;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int rsub = lane >> 2, col0 = warp * 16 + (lane & 3) * 4;
-  const int h = blockIdx.x;
+  const int h = blockIdx.x / NSPLIT, part = blockIdx.x % NSPLIT;
+  const int rsub = lane >> 2, col0 = part * (DV / NSPLIT) + warp * 16 + (lane & 3) * 4;
+  const bool lead = part == 0;  // the column part that writes per-token scalars and keys
   const RowDesc d = rows.r[blockIdx.y];
   const size_t b = (size_t)rows.row0 + blockIdx.y;
   const int group = P.Hv / P.Hk;
@@ -61,6 +62,9 @@ __global__ void __launch_bounds__(2 * D, 2)
     for (int j = 0; j < RPT; ++j) s[j] = f4(0.f);
   }
 
+  // the current token's values for this thread's columns (needed after the mat-vec)
+  const float4 vt = ld4(static_cast<const KT *>(io.v) + (b * P.Hv + h) * DV + col0);
+
   // 2. buffer rows of tokens 0..n (n = the slot the current token goes to)
   if (!RECURRENT && warp == 0) {
     int anybad = 0;
@@ -83,6 +87,16 @@ __global__ void __launch_bounds__(2 * D, 2)
   if (VARIANT == kGatedDelta) beta_t = io.beta[b * P.Hv + h];
   __syncthreads();
   if (!RECURRENT && bad) return;  // CTA-uniform
+
+  // this lane's first buffered token's u (token rsub), fetched now so its latency
+  // overlaps the state loads instead of following the mat-vec
+  float4 u_first = f4(0.f);
+  if (!RECURRENT && rsub < n) {
+    if (VARIANT == kGatedDelta)
+      u_first = ld4(P.ubuf + ((size_t)grow[rsub] * P.Hv + h) * DV + col0);
+    else
+      u_first = ld4(static_cast<const KT *>(P.vbuf) + ((size_t)grow[rsub] * P.Hv + h) * DV + col0);
+  }
 
   // 3. gate prefix sums and decay weights (warp 0); dot products (all warps)
   if (VARIANT != kPlain) {
@@ -146,11 +160,13 @@ __global__ void __launch_bounds__(2 * D, 2)
   // 5. buffered tokens' terms, tokens split over the 8 row lanes
   float4 po = f4(0.f), pc = f4(0.f);
   for (int i = rsub; i < n; i += 8) {
-    float4 ui;
-    if (VARIANT == kGatedDelta)
-      ui = ld4(P.ubuf + ((size_t)grow[i] * P.Hv + h) * DV + col0);
-    else
-      ui = ld4(static_cast<const KT *>(P.vbuf) + ((size_t)grow[i] * P.Hv + h) * DV + col0);
+    float4 ui = u_first;
+    if (i != rsub) {
+      if (VARIANT == kGatedDelta)
+        ui = ld4(P.ubuf + ((size_t)grow[i] * P.Hv + h) * DV + col0);
+      else
+        ui = ld4(static_cast<const KT *>(P.vbuf) + ((size_t)grow[i] * P.Hv + h) * DV + col0);
+    }
     fma4(po, wt[i] * sc[i], ui);
     if (VARIANT == kGatedDelta) fma4(pc, wt[i] * cc[i], ui);
     if (fold) *reinterpret_cast<float4 *>(&us[i * DV + col0]) = ui;
@@ -159,7 +175,6 @@ __global__ void __launch_bounds__(2 * D, 2)
   if (VARIANT == kGatedDelta) pc = rows_sum4(pc);
 
   const float e_t = e_t_s;
-  const float4 vt = ld4(static_cast<const KT *>(io.v) + (b * P.Hv + h) * DV + col0);
   float4 ut = vt;
   if (VARIANT == kGatedDelta) {
     ut.x = beta_t * (vt.x - fmaf(e_t, ak.x, pc.x));
@@ -180,11 +195,11 @@ __global__ void __launch_bounds__(2 * D, 2)
   }
   if (!RECURRENT) {
     const size_t g = grow[n];
-    if (h % group == 0)
+    if (lead && h % group == 0)
       for (int i = tid; i < DK / 4; i += NT)
         st4(static_cast<KT *>(P.kbuf) + (g * P.Hk + hq) * DK + 4 * i,
             *reinterpret_cast<const float4 *>(&kts[4 * i]));
-    if (tid == 0) {
+    if (lead && tid == 0) {
       P.gbuf[g * P.Hv + h] = a_t;
       P.bbuf[g * P.Hv + h] = beta_t;
     }
@@ -204,7 +219,7 @@ __global__ void __launch_bounds__(2 * D, 2)
 #pragma unroll
     for (int j = 0; j < RPT; ++j) st_stream4(Sp + (rsub + 8 * j) * DV + col0, s[j]);
   }
-  if (!RECURRENT && h == 0 && tid == 0) P.dlen[d.req] = fold ? 0 : n + 1;
+  if (!RECURRENT && h == 0 && lead && tid == 0) P.dlen[d.req] = fold ? 0 : n + 1;
 }
 
 // Device-side lengths after an accept that folds nothing.
@@ -212,38 +227,46 @@ __global__ void set_lengths_kernel(const PoolView P, const RowBatch rows) {
   for (int i = threadIdx.x; i < rows.count; i += blockDim.x) P.dlen[rows.r[i].req] = rows.r[i].n;
 }
 
-// 128-bit grid-stride copy, four independent 16-byte transfers per thread per
-// iteration (the HBM bandwidth probe).
+// 128-bit grid-stride copy, eight independent 16-byte loads in flight per
+// thread before their stores (the HBM bandwidth probe).
 __global__ void __launch_bounds__(256) copy_probe_kernel(const float4 *__restrict__ src,
                                                          float4 *__restrict__ dst, size_t n16) {
+  constexpr int U = 8;
   const size_t stride = (size_t)gridDim.x * blockDim.x;
   size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
-  for (; i + 3 * stride < n16; i += 4 * stride) {
-    float4 a = __ldcs(src + i), b = __ldcs(src + i + stride);
-    float4 c = __ldcs(src + i + 2 * stride), e = __ldcs(src + i + 3 * stride);
-    __stcs(dst + i, a);
-    __stcs(dst + i + stride, b);
-    __stcs(dst + i + 2 * stride, c);
-    __stcs(dst + i + 3 * stride, e);
+  for (; i + (U - 1) * stride < n16; i += U * stride) {
+    float4 x[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) x[u] = __ldcs(src + i + u * stride);
+#pragma unroll
+    for (int u = 0; u < U; ++u) __stcs(dst + i + u * stride, x[u]);
   }
   for (; i < n16; i += stride) __stcs(dst + i, __ldcs(src + i));
 }
 
 // ------------------------------------------------------------------ launchers
+// Column parts per (row, head): two CTAs of 128 threads per 128-wide head keep
+// four CTAs resident per SM, so one CTA's latency-bound phases (buffer lookups,
+// reductions, stores) overlap other CTAs' state loads.
+#ifndef KVB_DECODE_SPLIT
+#define KVB_DECODE_SPLIT 2
+#endif
+
 template <typename KT, int VARIANT, int D, bool REC>
 static cudaError_t run_decode(const PoolView &P, const RowBatch &rows, const TokenIO &io,
                               cudaStream_t stream) {
+  constexpr int NS = (D == 128) ? KVB_DECODE_SPLIT : 1;
   const size_t smem = (size_t)io.lmax * 2 * D * sizeof(float);
   static bool configured = false;
   if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(decode_kernel<KT, VARIANT, D, REC>,
+    cudaError_t e = cudaFuncSetAttribute(decode_kernel<KT, VARIANT, D, REC, NS>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          kMaxTok * 2 * D * (int)sizeof(float));
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  dim3 grid(P.Hv, rows.count);
-  decode_kernel<KT, VARIANT, D, REC><<<grid, 2 * D, smem, stream>>>(P, rows, io);
+  dim3 grid(P.Hv * NS, rows.count);
+  decode_kernel<KT, VARIANT, D, REC, NS><<<grid, 2 * D / NS, smem, stream>>>(P, rows, io);
   return cudaGetLastError();
 }
 
@@ -296,7 +319,7 @@ cudaError_t launch_copy_probe(const void *src, void *dst, size_t bytes, cudaStre
   e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
   const size_t n16 = bytes / 16;
-  copy_probe_kernel<<<sms * 8, 256, 0, stream>>>(static_cast<const float4 *>(src),
+  copy_probe_kernel<<<sms * 4, 256, 0, stream>>>(static_cast<const float4 *>(src),
                                                   static_cast<float4 *>(dst), n16);
   return cudaGetLastError();
 }

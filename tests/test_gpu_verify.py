@@ -109,8 +109,7 @@ def test_accept_zero_and_full():
     nxt = I.draw_tokens(rng, layer, (1, B))
     o = pool.decode([1], dev(nxt["q"][0, 1:2], layer), dev(nxt["k"][0, 1:2], layer),
                     dev(nxt["v"][0, 1:2], layer), dev(nxt["log_g"][0, 1:2], f32=True), None)
-    hist = {key: (None if val is None else np.concatenate([np.swapaxes(tok[key], 0, 1)[:, 1],
-                                                          nxt[key][:, 1]]))
+    hist = {key: np.concatenate([np.swapaxes(tok[key], 0, 1)[:, 1], nxt[key][:, 1]])
             for key in ("q", "k", "v", "log_g")}
     hist["beta"] = None
     o_ref, _, _ = oracle.decode_sequence(S0[1], hist, layer.variant)
