@@ -95,15 +95,17 @@ typedef struct kvb_config {
  *         (e.g. to load a prefilled state); byte offset of (slot, head) is
  *         ((slot * n_v_heads + head) * d_k * d_v) * 4.
  *  kv:    the block-partitioned buffer; offsets of its parts in kvb_layout.
- *         Token slot p of a request lives in block table[p / block_size],
- *         row p % block_size.  For a global row g = block * block_size + row:
- *           K    [g][n_qk_heads][d_k]  kv dtype
- *           V    [g][n_v_heads][d_v]   kv dtype
- *           U    [g][n_v_heads][d_v]   fp32, gated delta only: the token's
- *                pseudo-value (the delta-rule value correction, computed once
- *                when the token enters the buffer)
- *           LOGG [g][n_v_heads]        fp32 log-gate (0 for plain)
- *           BETA [g][n_v_heads]        fp32 (gated delta only; 0 otherwise)
+ *         Token slot p of a request lives in block table[p / block_size] at
+ *         position p % block_size.  Within a block, each head's positions are
+ *         contiguous (so a request's buffered tokens for one head form one
+ *         contiguous run per block):
+ *           K    [block][n_qk_heads][block_size][d_k]  kv dtype
+ *           V    [block][n_v_heads][block_size][d_v]   kv dtype
+ *           U    [block][n_v_heads][block_size][d_v]   fp32, gated delta only:
+ *                the token's pseudo-value (the delta-rule value correction,
+ *                computed once when the token enters the buffer)
+ *           LOGG [block][n_v_heads][block_size]        fp32 log-gate (0 for plain)
+ *           BETA [block][n_v_heads][block_size]        fp32 (gated delta only)
  *  meta:  block tables, device lengths and the error word (layout private).
  */
 typedef struct kvb_layout {

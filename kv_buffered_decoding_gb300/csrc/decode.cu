@@ -47,7 +47,7 @@ __global__ void __launch_bounds__(2 * D / NSPLIT, 4 / (2 * D / NSPLIT / 128))
   __shared__ __align__(16) float qs[DK];
   __shared__ __align__(16) float kts[DK];
   __shared__ float Acum[kMaxTok], wt[kMaxTok], sc[kMaxTok], cc[kMaxTok];
-  __shared__ int grow[kMaxTok];
+  __shared__ size_t koff[kMaxTok], voff[kMaxTok];  // key element offset; V/U/gate row
   __shared__ float e_t_s;
   __shared__ int bad;
 
@@ -69,9 +69,12 @@ __global__ void __launch_bounds__(2 * D / NSPLIT, 4 / (2 * D / NSPLIT / 128))
   if (!RECURRENT && warp == 0) {
     int anybad = 0;
     for (int i = lane; i <= n; i += 32) {
-      const int g = buffer_row(P, d.req, i);
-      grow[i] = g;
+      const int g = buffer_row(P, d, i);
       anybad |= (g < 0);
+      if (g >= 0) {  // the only divisions by the block size
+        koff[i] = kv_row(P, g, hq, P.Hk) * DK;
+        voff[i] = kv_row(P, g, h, P.Hv);
+      }
     }
     anybad = __any_sync(kFull, anybad);
     if (lane == 0) bad = anybad;
@@ -93,9 +96,9 @@ __global__ void __launch_bounds__(2 * D / NSPLIT, 4 / (2 * D / NSPLIT / 128))
   float4 u_first = f4(0.f);
   if (!RECURRENT && rsub < n) {
     if (VARIANT == kGatedDelta)
-      u_first = ld4(P.ubuf + ((size_t)grow[rsub] * P.Hv + h) * DV + col0);
+      u_first = ld4(P.ubuf + voff[rsub] * DV + col0);
     else
-      u_first = ld4(static_cast<const KT *>(P.vbuf) + ((size_t)grow[rsub] * P.Hv + h) * DV + col0);
+      u_first = ld4(static_cast<const KT *>(P.vbuf) + voff[rsub] * DV + col0);
   }
 
   // 3. gate prefix sums and decay weights (warp 0); dot products (all warps)
@@ -103,7 +106,7 @@ __global__ void __launch_bounds__(2 * D / NSPLIT, 4 / (2 * D / NSPLIT / 128))
     if (warp == 0) {
       warp_prefix(
           n + 1,
-          [&](int i) { return i < n ? P.gbuf[(size_t)grow[i] * P.Hv + h] : a_t; }, Acum, lane);
+          [&](int i) { return i < n ? P.gbuf[voff[i]] : a_t; }, Acum, lane);
       __syncwarp();
       const float At = Acum[n];
       for (int i = lane; i <= n; i += 32) wt[i] = expf(At - Acum[i]);
@@ -114,7 +117,7 @@ __global__ void __launch_bounds__(2 * D / NSPLIT, 4 / (2 * D / NSPLIT / 128))
     if (tid == 0) e_t_s = 1.f;
   }
   for (int i = warp; i <= n; i += NT / 32) {
-    const KT *kp = (i < n) ? static_cast<const KT *>(P.kbuf) + ((size_t)grow[i] * P.Hk + hq) * DK : kg;
+    const KT *kp = (i < n) ? static_cast<const KT *>(P.kbuf) + koff[i] : kg;
     float sq, sk = 0.f;
     if constexpr (E == 4) {
       const float4 kv = ld4(kp + lane * 4);
@@ -163,9 +166,9 @@ __global__ void __launch_bounds__(2 * D / NSPLIT, 4 / (2 * D / NSPLIT / 128))
     float4 ui = u_first;
     if (i != rsub) {
       if (VARIANT == kGatedDelta)
-        ui = ld4(P.ubuf + ((size_t)grow[i] * P.Hv + h) * DV + col0);
+        ui = ld4(P.ubuf + voff[i] * DV + col0);
       else
-        ui = ld4(static_cast<const KT *>(P.vbuf) + ((size_t)grow[i] * P.Hv + h) * DV + col0);
+        ui = ld4(static_cast<const KT *>(P.vbuf) + voff[i] * DV + col0);
     }
     fma4(po, wt[i] * sc[i], ui);
     if (VARIANT == kGatedDelta) fma4(pc, wt[i] * cc[i], ui);
@@ -187,21 +190,21 @@ __global__ void __launch_bounds__(2 * D / NSPLIT, 4 / (2 * D / NSPLIT / 128))
   if (rsub == 0) {
     __stcs(reinterpret_cast<float4 *>(io.o + (b * P.Hv + h) * DV + col0), o);
     if (!RECURRENT) {
-      const size_t g = grow[n];
-      st4(static_cast<KT *>(P.vbuf) + (g * P.Hv + h) * DV + col0, vt);
-      if (VARIANT == kGatedDelta) st4(P.ubuf + (g * P.Hv + h) * DV + col0, ut);
+      const size_t g = n;
+      st4(static_cast<KT *>(P.vbuf) + voff[g] * DV + col0, vt);
+      if (VARIANT == kGatedDelta) st4(P.ubuf + voff[g] * DV + col0, ut);
     }
     if (fold) *reinterpret_cast<float4 *>(&us[n * DV + col0]) = ut;
   }
   if (!RECURRENT) {
-    const size_t g = grow[n];
+    const size_t g = n;
     if (lead && h % group == 0)
       for (int i = tid; i < DK / 4; i += NT)
-        st4(static_cast<KT *>(P.kbuf) + (g * P.Hk + hq) * DK + 4 * i,
+        st4(static_cast<KT *>(P.kbuf) + koff[g] + 4 * i,
             *reinterpret_cast<const float4 *>(&kts[4 * i]));
     if (lead && tid == 0) {
-      P.gbuf[g * P.Hv + h] = a_t;
-      P.bbuf[g * P.Hv + h] = beta_t;
+      P.gbuf[voff[g]] = a_t;
+      P.bbuf[voff[g]] = beta_t;
     }
   }
 
@@ -245,11 +248,18 @@ __global__ void __launch_bounds__(256) copy_probe_kernel(const float4 *__restric
 }
 
 // ------------------------------------------------------------------ launchers
-// Column parts per (row, head): two CTAs of 128 threads per 128-wide head keep
-// four CTAs resident per SM, so one CTA's latency-bound phases (buffer lookups,
-// reductions, stores) overlap other CTAs' state loads.
+// Column parts per (row, head) for d = 128: two 128-thread CTAs per head keep
+// four CTAs resident per SM, so one CTA's serial phases (buffer lookups, dot
+// products, barriers, stores) overlap the state loads of the others.
 #ifndef KVB_DECODE_SPLIT
 #define KVB_DECODE_SPLIT 2
+#endif
+
+// Decode implementation: 2 = persistent warp-specialized kernel with a TMA bulk
+// copy ring (decode_pipe.cu) where it applies, else decode_kernel; 0 = state
+// tile held in registers (decode_kernel).
+#ifndef KVB_DECODE_IMPL
+#define KVB_DECODE_IMPL 0
 #endif
 
 template <typename KT, int VARIANT, int D, bool REC>
@@ -297,8 +307,13 @@ static cudaError_t pick_variant(const PoolView &P, const RowBatch &rows, const T
 }
 
 cudaError_t launch_decode(const PoolView &P, const RowBatch &rows, const TokenIO &io, int variant,
-                          int dtype, int d, bool recurrent, int flush_len, cudaStream_t stream) {
+                          int dtype, int d, bool recurrent, int flush_len, int nmax,
+                          cudaStream_t stream) {
   if (rows.count <= 0) return cudaSuccess;
+  if (KVB_DECODE_IMPL == 2) {
+    const cudaError_t e = launch_decode_pipe(P, rows, io, variant, dtype, d, recurrent, nmax, stream);
+    if (e != kUnsupported) return e;
+  }
   TokenIO io2 = io;
   io2.lmax = flush_len;
   if (dtype == 0) return pick_variant<float>(P, rows, io2, variant, d, recurrent, stream);

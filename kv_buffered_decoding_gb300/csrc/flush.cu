@@ -45,7 +45,7 @@ __global__ void __launch_bounds__(2 * D, 2) flush_kernel(const PoolView P, const
   if (warp == 0) {
     int anybad = 0;
     for (int i = lane; i < L; i += 32) {
-      const int g = buffer_row(P, d.req, i);
+      const int g = buffer_row(P, d, i);
       grow[i] = g;
       anybad |= (g < 0);
     }
@@ -57,7 +57,7 @@ __global__ void __launch_bounds__(2 * D, 2) flush_kernel(const PoolView P, const
 
   if (warp == 0) {
     if (VARIANT != kPlain) {
-      warp_prefix(L, [&](int i) { return P.gbuf[(size_t)grow[i] * P.Hv + h]; }, Acum, lane);
+      warp_prefix(L, [&](int i) { return P.gbuf[kv_row(P, grow[i], h, P.Hv)]; }, Acum, lane);
       __syncwarp();
       const float AL = Acum[L - 1];
       for (int i = lane; i < L; i += 32) wt[i] = expf(AL - Acum[i]);
@@ -70,15 +70,15 @@ __global__ void __launch_bounds__(2 * D, 2) flush_kernel(const PoolView P, const
   for (int idx = tid; idx < L * (DK / 4); idx += NT) {
     const int i = idx / (DK / 4), c = (idx % (DK / 4)) * 4;
     *reinterpret_cast<float4 *>(&ks[(size_t)i * DK + c]) =
-        ld4(static_cast<const KT *>(P.kbuf) + ((size_t)grow[i] * P.Hk + hq) * DK + c);
+        ld4(static_cast<const KT *>(P.kbuf) + kv_row(P, grow[i], hq, P.Hk) * DK + c);
   }
   for (int idx = tid; idx < L * (DV / 4); idx += NT) {
     const int i = idx / (DV / 4), c = (idx % (DV / 4)) * 4;
     float4 u;
     if (DELTA)
-      u = ld4(P.ubuf + ((size_t)grow[i] * P.Hv + h) * DV + c);
+      u = ld4(P.ubuf + kv_row(P, grow[i], h, P.Hv) * DV + c);
     else
-      u = ld4(static_cast<const KT *>(P.vbuf) + ((size_t)grow[i] * P.Hv + h) * DV + c);
+      u = ld4(static_cast<const KT *>(P.vbuf) + kv_row(P, grow[i], h, P.Hv) * DV + c);
     *reinterpret_cast<float4 *>(&us[(size_t)i * DV + c]) = u;
   }
   __syncthreads();

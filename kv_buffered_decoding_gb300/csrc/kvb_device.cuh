@@ -13,6 +13,49 @@ constexpr int kMaxTok = 64 + 1;  // buffered tokens (capacity) + the current one
 
 enum Variant { kPlain = 0, kGated = 1, kGatedDelta = 2 };
 
+// Tries of mbarrier.try_wait before a wait is declared lost (each try may
+// suspend the thread for a while; data normally lands within microseconds).
+constexpr uint32_t kSpinLimit = 1u << 22;
+
+// ---------------------------------------------------------------- mbarrier + TMA bulk copy
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+// Bulk (non-tensor) asynchronous copy global -> shared, completing on `bar`.
+// Both addresses 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Wait for phase `parity` of `bar`, giving up after kSpinLimit tries.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity) {
+  for (uint32_t i = 0; i < kSpinLimit; ++i)
+    if (mbar_try_wait(bar, parity)) return true;
+  return false;
+}
+
 // ---------------------------------------------------------------- loads / stores
 // The state is streamed once per step: read and written with the evict-first
 // (".cs") policy so it does not push reusable data (buffer, q/k) out of L2.
@@ -108,15 +151,26 @@ __device__ __forceinline__ void record_error(int32_t *err, int32_t kind, int32_t
   atomicAdd(&err[3], 1);
 }
 
-// Global buffer row of token slot p of request `req`, or -1 if the block id is
-// out of range (the error is recorded).
-__device__ __forceinline__ int buffer_row(const PoolView &P, int req, int p) {
-  int blk = P.table[(size_t)req * P.max_blocks + p / P.bs];
+// Global buffer row of token slot p of the request in row descriptor d, or -1
+// if the block id is out of range (the error is recorded).  The first
+// kRowBlocks blocks come with the descriptor; later ones from the block table.
+__device__ __forceinline__ int buffer_row(const PoolView &P, const RowDesc &d, int p) {
+  const int bi = p / P.bs;
+  const int blk = bi < kRowBlocks ? d.blk[bi] : P.table[(size_t)d.req * P.max_blocks + bi];
   if (blk < 0 || blk >= P.num_blocks) {
-    record_error(P.err, kErrBlockRange, req, blk);
+    record_error(P.err, kErrBlockRange, d.req, blk);
     return -1;
   }
   return blk * P.bs + p % P.bs;
+}
+
+// Row index of buffer row g (= block * block_size + slot) for one head, in a
+// region laid out [block][heads][block_size][...]: within a block, each head's
+// slots are contiguous, so a request's buffered tokens for one head form one
+// contiguous run.
+__device__ __forceinline__ size_t kv_row(const PoolView &P, int g, int head, int nheads) {
+  const int blk = g / P.bs, pos = g - blk * P.bs;
+  return ((size_t)blk * nheads + head) * P.bs + pos;
 }
 
 // Inclusive prefix sums of the log-gates of `count` tokens, run by one warp.

@@ -139,6 +139,19 @@ int cuda_status(cudaError_t e) {
   return KVB_E_CUDA;
 }
 
+// A row descriptor from the host mirror: request, length, slot, flags and the
+// request's first block ids.
+kvb::RowDesc make_row(const kvb_pool *p, int32_t r, int32_t n, int32_t flags) {
+  kvb::RowDesc d;
+  d.req = r;
+  d.n = n;
+  d.slot = p->slot[r];
+  d.flags = flags;
+  const int32_t *row = p->table.data() + (size_t)r * p->cfg.max_blocks_per_req;
+  for (int i = 0; i < kvb::kRowBlocks; ++i) d.blk[i] = i < p->nblk[r] ? row[i] : -1;
+  return d;
+}
+
 enum Mode { kDecode, kShort };
 
 int decode_like(kvb_pool *p, int32_t B, const int32_t *req_ids, const void *q, const void *k,
@@ -162,21 +175,19 @@ int decode_like(kvb_pool *p, int32_t B, const int32_t *req_ids, const void *q, c
     const int32_t cnt = B - base < kvb::kMaxRows ? B - base : kvb::kMaxRows;
     p->rows.count = cnt;
     p->rows.row0 = base;
-    int lmax = recurrent ? 1 : 0;
+    int lmax = recurrent ? 1 : 0, nmax = 0;
     for (int32_t i = 0; i < cnt; ++i) {
       const int32_t r = req_ids[base + i];
       kvb::RowDesc &d = p->rows.r[i];
-      d.req = r;
-      d.n = recurrent ? 0 : p->len[r];
-      d.slot = p->slot[r];
-      d.flags = 0;
+      d = make_row(p, r, recurrent ? 0 : p->len[r], 0);
+      if (d.n > nmax) nmax = d.n;
       if (mode == kDecode && !recurrent && auto_flush && c.m > 0 && d.n + 1 >= c.m) {
         d.flags = kvb::kFlagFlush;
         if (d.n + 1 > lmax) lmax = d.n + 1;
       }
     }
     cudaError_t e = kvb::launch_decode(p->view, p->rows, io, c.variant, c.kv_dtype, c.d_k,
-                                       recurrent, lmax, stream);
+                                       recurrent, lmax, nmax, stream);
     if (e != cudaSuccess) return cuda_status(e);
     if (!recurrent) {
       for (int32_t i = 0; i < cnt; ++i) {
@@ -197,7 +208,7 @@ int launch_fold(kvb_pool *p, const std::vector<int32_t> &reqs, cudaStream_t stre
     int lmax = 0;
     for (size_t i = 0; i < cnt; ++i) {
       const int32_t r = reqs[base + i];
-      p->rows.r[i] = kvb::RowDesc{r, p->len[r], p->slot[r], 0};
+      p->rows.r[i] = make_row(p, r, p->len[r], 0);
       if (p->len[r] > lmax) lmax = p->len[r];
     }
     cudaError_t e = kvb::launch_flush(p->view, p->rows, c.variant, c.kv_dtype, c.d_k, lmax, stream);
@@ -384,7 +395,7 @@ int kvb_verify(kvb_pool *p, int32_t B, int32_t T, const int32_t *req_ids, const 
     int lmax = 0;
     for (int32_t i = 0; i < cnt; ++i) {
       const int32_t r = req_ids[base + i];
-      p->rows.r[i] = kvb::RowDesc{r, p->len[r], p->slot[r], 0};
+      p->rows.r[i] = make_row(p, r, p->len[r], 0);
       if (p->len[r] + T > lmax) lmax = p->len[r] + T;
     }
     cudaError_t e = kvb::launch_verify(p->view, p->rows, io, c.variant, c.kv_dtype, c.d_k, lmax,
@@ -423,7 +434,7 @@ int kvb_accept(kvb_pool *p, int32_t B, const int32_t *req_ids, const int32_t *n_
     p->rows.row0 = 0;
     for (size_t i = 0; i < cnt; ++i) {
       const int32_t r = keep[base + i];
-      p->rows.r[i] = kvb::RowDesc{r, p->len[r], p->slot[r], 0};
+      p->rows.r[i] = make_row(p, r, p->len[r], 0);
     }
     cudaError_t e = kvb::launch_set_lengths(p->view, p->rows, s);
     if (e != cudaSuccess) return cuda_status(e);

@@ -11,7 +11,11 @@ namespace kvb {
 
 // Most batch rows one launch carries in its parameter block; longer batches
 // are split into several launches by the host library.
-constexpr int kMaxRows = 512;
+constexpr int kMaxRows = 256;
+// Leading block ids of each request carried in its row descriptor, so the
+// kernels find the first kRowBlocks * block_size buffer slots without a
+// dependent load of the block table.
+constexpr int kRowBlocks = 4;
 
 // Device view of a pool: raw pointers into the caller's regions plus shapes.
 struct PoolView {
@@ -29,9 +33,10 @@ struct PoolView {
 };
 
 // One batch row: which request, its buffer length before this call, its
-// state slot (-1 = none) and flags.
+// state slot (-1 = none), flags, and its first block ids (-1 past its table).
 struct RowDesc {
   int32_t req, n, slot, flags;
+  int32_t blk[kRowBlocks];
 };
 constexpr int32_t kFlagFlush = 1;  // decode: fold the buffer (incl. this token) into S
 
@@ -51,14 +56,20 @@ struct TokenIO {
   int lmax;  // most tokens any row of the launch stages in shared memory
 };
 
-enum ErrKind : int32_t { kErrNone = 0, kErrBlockRange = 1 };
+enum ErrKind : int32_t { kErrNone = 0, kErrBlockRange = 1, kErrWaitTimeout = 2 };
 
 // Launchers (kernels.cu).  `dtype` is KVB_F32 / KVB_BF16; `d` is d_k == d_v.
 // Return cudaSuccess or the launch error; kUnsupported for a missing instance.
 constexpr cudaError_t kUnsupported = cudaErrorNotSupported;
 
+// nmax: the largest buffer length of any row; flush_len: the most tokens any
+// row folds (0 if none).
 cudaError_t launch_decode(const PoolView &P, const RowBatch &rows, const TokenIO &io, int variant,
-                          int dtype, int d, bool recurrent, int flush_len, cudaStream_t stream);
+                          int dtype, int d, bool recurrent, int flush_len, int nmax,
+                          cudaStream_t stream);
+cudaError_t launch_decode_pipe(const PoolView &P, const RowBatch &rows, const TokenIO &io,
+                               int variant, int dtype, int d, bool recurrent, int nmax,
+                               cudaStream_t stream);
 cudaError_t launch_verify(const PoolView &P, const RowBatch &rows, const TokenIO &io, int variant,
                           int dtype, int d, int max_len, cudaStream_t stream);
 cudaError_t launch_flush(const PoolView &P, const RowBatch &rows, int variant, int dtype, int d,

@@ -65,7 +65,7 @@ __global__ void __launch_bounds__(2 * D)
   if (warp == 0) {
     int anybad = 0;
     for (int i = lane; i < L; i += 32) {
-      const int g = buffer_row(P, d.req, i);
+      const int g = buffer_row(P, d, i);
       grow[i] = g;
       anybad |= (g < 0);
     }
@@ -91,7 +91,7 @@ __global__ void __launch_bounds__(2 * D)
       warp_prefix(
           L,
           [&](int i) {
-            return i < n ? P.gbuf[(size_t)grow[i] * P.Hv + h]
+            return i < n ? P.gbuf[kv_row(P, grow[i], h, P.Hv)]
                          : (lg ? lg[(b * T + (i - n)) * P.Hv + h] : 0.f);
           },
           Acum, lane);
@@ -104,15 +104,15 @@ __global__ void __launch_bounds__(2 * D)
     for (int idx = tid; idx < n * (DK / 4); idx += NT) {
       const int i = idx / (DK / 4), c = (idx % (DK / 4)) * 4;
       *reinterpret_cast<float4 *>(&ks[(size_t)i * DK + c]) =
-          ld4(static_cast<const KT *>(P.kbuf) + ((size_t)grow[i] * P.Hk + hq) * DK + c);
+          ld4(static_cast<const KT *>(P.kbuf) + kv_row(P, grow[i], hq, P.Hk) * DK + c);
     }
     for (int idx = tid; idx < n * (DV / 4); idx += NT) {
       const int i = idx / (DV / 4), c = (idx % (DV / 4)) * 4;
       float4 u;
       if (DELTA)
-        u = ld4(P.ubuf + ((size_t)grow[i] * P.Hv + h) * DV + c);
+        u = ld4(P.ubuf + kv_row(P, grow[i], h, P.Hv) * DV + c);
       else
-        u = ld4(static_cast<const KT *>(P.vbuf) + ((size_t)grow[i] * P.Hv + h) * DV + c);
+        u = ld4(static_cast<const KT *>(P.vbuf) + kv_row(P, grow[i], h, P.Hv) * DV + c);
       *reinterpret_cast<float4 *>(&us[(size_t)i * DV + c]) = u;
     }
   }
@@ -203,8 +203,8 @@ __global__ void __launch_bounds__(2 * D)
       __stcs(reinterpret_cast<float4 *>(io.o + ((b * T + j) * P.Hv + h) * DV + col0), o);
       *reinterpret_cast<float4 *>(&us[(size_t)t * DV + col0]) = ut;
       const size_t g = grow[t];
-      st4(static_cast<KT *>(P.vbuf) + (g * P.Hv + h) * DV + col0, vt);
-      if (DELTA) st4(P.ubuf + (g * P.Hv + h) * DV + col0, ut);
+      st4(static_cast<KT *>(P.vbuf) + kv_row(P, (int)g, h, P.Hv) * DV + col0, vt);
+      if (DELTA) st4(P.ubuf + kv_row(P, (int)g, h, P.Hv) * DV + col0, ut);
     }
     __syncwarp();  // u_t of this warp's columns visible to its other lanes
   }
@@ -213,13 +213,13 @@ __global__ void __launch_bounds__(2 * D)
   for (int idx = tid; idx < T * (DK / 4); idx += NT) {
     const int j = idx / (DK / 4), c = (idx % (DK / 4)) * 4;
     if (h % group == 0)
-      st4(static_cast<KT *>(P.kbuf) + ((size_t)grow[n + j] * P.Hk + hq) * DK + c,
+      st4(static_cast<KT *>(P.kbuf) + kv_row(P, grow[n + j], hq, P.Hk) * DK + c,
           *reinterpret_cast<const float4 *>(&ks[(size_t)(n + j) * DK + c]));
   }
   for (int j = tid; j < T; j += NT) {
     const size_t g = grow[n + j];
-    P.gbuf[g * P.Hv + h] = (VARIANT != kPlain && io.log_g) ? io.log_g[(b * T + j) * P.Hv + h] : 0.f;
-    P.bbuf[g * P.Hv + h] = DELTA ? io.beta[(b * T + j) * P.Hv + h] : 0.f;
+    P.gbuf[kv_row(P, (int)g, h, P.Hv)] = (VARIANT != kPlain && io.log_g) ? io.log_g[(b * T + j) * P.Hv + h] : 0.f;
+    P.bbuf[kv_row(P, (int)g, h, P.Hv)] = DELTA ? io.beta[(b * T + j) * P.Hv + h] : 0.f;
   }
 }
 

@@ -133,10 +133,10 @@ class Pool:
 
     Tensor views of the regions:
       state  [num_state_slots, Hv, d_k, d_v] fp32
-      kbuf   [num_blocks, block_size, Hk, d_k]  kv dtype
-      vbuf   [num_blocks, block_size, Hv, d_v]  kv dtype
-      ubuf   [num_blocks, block_size, Hv, d_v]  fp32 (gated delta only, else None)
-      gbuf, bbuf [num_blocks, block_size, Hv]   fp32
+      kbuf   [num_blocks, Hk, block_size, d_k]  kv dtype
+      vbuf   [num_blocks, Hv, block_size, d_v]  kv dtype
+      ubuf   [num_blocks, Hv, block_size, d_v]  fp32 (gated delta only, else None)
+      gbuf, bbuf [num_blocks, Hv, block_size]   fp32
     """
 
     def __init__(self, cfg: KvbConfig, device=None):
@@ -165,12 +165,12 @@ class Pool:
             return self._kv_mem[off: off + nbytes].view(dtype).view(*shape)
 
         rows = nb * bs
-        self.kbuf = sub(lay.k_off, rows * Hk * dk, self.kv_torch_dtype, (nb, bs, Hk, dk))
-        self.vbuf = sub(lay.v_off, rows * Hv * dv, self.kv_torch_dtype, (nb, bs, Hv, dv))
-        self.ubuf = (sub(lay.u_off, rows * Hv * dv, torch.float32, (nb, bs, Hv, dv))
+        self.kbuf = sub(lay.k_off, rows * Hk * dk, self.kv_torch_dtype, (nb, Hk, bs, dk))
+        self.vbuf = sub(lay.v_off, rows * Hv * dv, self.kv_torch_dtype, (nb, Hv, bs, dv))
+        self.ubuf = (sub(lay.u_off, rows * Hv * dv, torch.float32, (nb, Hv, bs, dv))
                      if cfg.variant == KVB_GATED_DELTA else None)
-        self.gbuf = sub(lay.logg_off, rows * Hv, torch.float32, (nb, bs, Hv))
-        self.bbuf = sub(lay.beta_off, rows * Hv, torch.float32, (nb, bs, Hv))
+        self.gbuf = sub(lay.logg_off, rows * Hv, torch.float32, (nb, Hv, bs))
+        self.bbuf = sub(lay.beta_off, rows * Hv, torch.float32, (nb, Hv, bs))
         h = _P()
         _check(self.lib.kvb_alloc_pool(ctypes.byref(cfg), self._state_mem.data_ptr(),
                                        self._kv_mem.data_ptr(), self._meta_mem.data_ptr(),

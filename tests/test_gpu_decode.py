@@ -28,7 +28,7 @@ if not torch.cuda.is_available():
 def _buffered_keys_at(pool, block_ids, n, bs):
     """Keys stored for token slots 0..n-1 of a request owning `block_ids`."""
     kb = pool.kbuf.float().cpu().numpy()
-    return np.stack([kb[block_ids[p // bs], p % bs] for p in range(n)]) if n else None
+    return np.stack([kb[block_ids[p // bs], :, p % bs] for p in range(n)]) if n else None
 
 
 def test_ungated_fp32_prefill_and_decode():

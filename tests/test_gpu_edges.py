@@ -144,28 +144,29 @@ def test_gdn_d64_grouped_heads_all_calls():
 
 
 def test_device_error_word_on_corrupt_table():
-    """A block id corrupted on the device is caught by the kernel's own check: the CTA
-    records (kind=1, request, value) and returns before using it; nothing faults."""
+    """A block id corrupted in the device block table is caught by the kernel's own check:
+    the CTA records (kind=1, request, value) and returns before using it; nothing faults.
+    The first blocks of a request travel in the launch's row descriptors, so the
+    corrupted entry is the fifth block (slots 16..19 at 4 slots per block)."""
     layer = I.GATED_LAYER
-    pool = make_pool(layer, 4, 2, 1, 4)
-    pool.state.zero_()
-    pool.set_request(0, 0, [0])
-    pool.set_request(1, 1, [1])
-    torch.cuda.synchronize()
-    # the block table is the first region of the metadata: request 0, block 0
-    bad = torch.tensor([12345], dtype=torch.int32).view(torch.uint8).cuda()
-    pool._meta_mem[0:4].copy_(bad)
+    pool = make_pool(layer, 4, 2, 8, 4, num_slots=1)
+    pool.set_request(0, -1, list(range(8)))
+    pool.set_request(1, -1, list(range(8, 16)))
     rng = np.random.default_rng(3)
-    tok = I.draw_tokens(rng, layer, (2,))
-    o = pool.decode([0, 1], *token_tensors(tok, layer, slice(None)))
+    tok = I.draw_tokens(rng, layer, (17, 2))
+    outs = [pool.short_ctx([0, 1], *token_tensors(tok, layer, t)).cpu().numpy() for t in range(16)]
+    torch.cuda.synchronize()
+    # the block table is the first region of the metadata: request 0, block 4
+    bad = torch.tensor([12345], dtype=torch.int32).view(torch.uint8).cuda()
+    pool._meta_mem[16:20].copy_(bad)
+    outs.append(pool.short_ctx([0, 1], *token_tensors(tok, layer, 16)).cpu().numpy())
     err = pool.get_error()
     assert err == (1, 0, 12345)
     assert pool.get_error() is None  # cleared
-    # request 1 was served normally
-    ref, _, _ = oracle.decode_sequence(np.zeros((16, 128, 128)),
-                                       {k_: (None if v_ is None else v_[None, 1])
-                                        for k_, v_ in tok.items()}, layer.variant)
-    assert rel_err(o.cpu().numpy()[1], ref[0]) <= tol_for(layer)
+    # request 1 was served normally throughout
+    ref = oracle.short_context({k_: (None if v_ is None else v_[:, 1]) for k_, v_ in tok.items()},
+                               layer.variant, layer.d_k, layer.d_v)
+    assert rel_err(np.stack(outs)[:, 1], ref) <= tol_for(layer)
 
 
 def test_copy_probe():
