@@ -205,13 +205,13 @@ def run_reference(args, rank, world):
         return
     w = WORKLOAD
     for _ in range(max(args.warmup, 0)):
-        oracle_rate(w, 0.0, reqs_per_step=1, max_steps=1)
+        oracle_rate(w, float("inf"), reqs_per_step=1, max_steps=1)
     # size each step so the K timed steps take about a minute
-    probe, _, _ = oracle_rate(w, 0.0, reqs_per_step=1, max_steps=1)
+    probe, _, _ = oracle_rate(w, float("inf"), reqs_per_step=1, max_steps=1)
     per_req = 1.0 / probe
     reqs = int(max(1, min(8, round(60.0 / max(args.steps, 1) / per_req))))
     t0 = time.perf_counter()
-    rate, steps, el = oracle_rate(w, 0.0, reqs_per_step=reqs, max_steps=args.steps)
+    rate, steps, el = oracle_rate(w, float("inf"), reqs_per_step=reqs, max_steps=args.steps)
     el = time.perf_counter() - t0
     value = reqs * steps / el
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tok/s",
