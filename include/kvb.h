@@ -104,7 +104,9 @@ typedef struct kvb_config {
  *           U    [block][n_v_heads][block_size][d_v]   fp32, gated delta only:
  *                the token's pseudo-value (the delta-rule value correction,
  *                computed once when the token enters the buffer)
- *           LOGG [block][n_v_heads][block_size]        fp32 log-gate (0 for plain)
+ *           LOGG [block][n_v_heads][block_size]        fp32 cumulative log-gate
+ *                A_i = a_1 + ... + a_i of the buffer's tokens since the last
+ *                fold (0 for plain)
  *           BETA [block][n_v_heads][block_size]        fp32 (gated delta only)
  *  meta:  block tables, device lengths and the error word (layout private).
  */

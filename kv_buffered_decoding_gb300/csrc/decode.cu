@@ -15,10 +15,12 @@
 // delta token's u is kept in the buffer (pseudo-value), so S0 is touched by two
 // mat-vecs per step (S0^T q_t, S0^T k_t) whatever the buffer occupancy.
 //
-// One CTA per (batch row, value head); 2*D threads.  Warp w owns state columns
-// [16w, 16w+16); lane = 4*rsub + c owns columns 16w+4c..+3 of rows rsub + 8j,
-// so every load of the state is a 64-byte segment of a row and the reduction
-// over rows is three xor-shuffles inside the warp.  The state tile stays in
+// Two CTAs of 128 threads per (batch row, value head) at d = 128, each owning 64
+// state columns.  Warp w owns 16 of them; lane = 4*rsub + c owns columns
+// 4c..4c+3 of rows 16*rsub .. 16*rsub+15, so every load of the state is a
+// 64-byte segment of a row, the q / k operands of four rows come in one
+// 128-bit shared load, and the reduction over rows is three xor-shuffles
+// inside the warp.  The state tile stays in
 // registers from its load to the fold, so S crosses HBM once per step (twice
 // on a fold step, once in each direction).
 #include "kvb_device.cuh"
@@ -26,13 +28,15 @@
 namespace kvb {
 
 template <typename KT, int VARIANT, int D, bool RECURRENT, int NSPLIT>
-__global__ void __launch_bounds__(2 * D / NSPLIT, 4 / (2 * D / NSPLIT / 128))
+__global__ void __launch_bounds__(2 * D / NSPLIT, 512 / (2 * D / NSPLIT))
     decode_kernel(const PoolView P, const RowBatch rows, const TokenIO io) {
-  constexpr int DK = D, DV = D, NT = 2 * D / NSPLIT, RPT = DK / 8, E = DK / 32;
+  constexpr int DK = D, DV = D, NT = 2 * D / NSPLIT, NW = NT / 32, RPT = DK / 8, E = DK / 32;
+  constexpr bool DELTA = VARIANT == kGatedDelta, GATED = VARIANT != kPlain;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int h = blockIdx.x / NSPLIT, part = blockIdx.x % NSPLIT;
-  const int rsub = lane >> 2, col0 = part * (DV / NSPLIT) + warp * 16 + (lane & 3) * 4;
-  const bool lead = part == 0;  // the column part that writes per-token scalars and keys
+  const int rsub = lane >> 2, row0 = rsub * RPT;  // this thread's rows: row0 .. row0 + RPT - 1
+  const int col0 = part * (DV / NSPLIT) + warp * 16 + (lane & 3) * 4;
+  const bool lead = part == 0;  // the column part that writes per-token keys and scalars
   const RowDesc d = rows.r[blockIdx.y];
   const size_t b = (size_t)rows.row0 + blockIdx.y;
   const int group = P.Hv / P.Hk;
@@ -46,32 +50,33 @@ __global__ void __launch_bounds__(2 * D / NSPLIT, 4 / (2 * D / NSPLIT / 128))
   float *us = ks + (size_t)io.lmax * DK;            // [lmax][DV] their u
   __shared__ __align__(16) float qs[DK];
   __shared__ __align__(16) float kts[DK];
-  __shared__ float Acum[kMaxTok], wt[kMaxTok], sc[kMaxTok], cc[kMaxTok];
+  __shared__ float wt[kMaxTok], sc[kMaxTok], cc[kMaxTok];
   __shared__ size_t koff[kMaxTok], voff[kMaxTok];  // key element offset; V/U/gate row
   __shared__ float e_t_s;
   __shared__ int bad;
 
-  // 1. the state tile: the only large read, issued first so it overlaps the rest
+  // 1. the state tile, into registers: the only large read, issued first
   float4 s[RPT];
   float *Sp = P.state + (has_state ? ((size_t)d.slot * P.Hv + h) * DK * DV : 0);
   if (has_state) {
 #pragma unroll
-    for (int j = 0; j < RPT; ++j) s[j] = ld_stream4(Sp + (rsub + 8 * j) * DV + col0);
+    for (int j = 0; j < RPT; ++j) s[j] = ld_stream4(Sp + (row0 + j) * DV + col0);
   } else {
 #pragma unroll
     for (int j = 0; j < RPT; ++j) s[j] = f4(0.f);
   }
-
-  // the current token's values for this thread's columns (needed after the mat-vec)
   const float4 vt = ld4(static_cast<const KT *>(io.v) + (b * P.Hv + h) * DV + col0);
+  float a_t = 0.f, beta_t = 0.f;
+  if (GATED && io.log_g) a_t = io.log_g[b * P.Hv + h];
+  if (DELTA) beta_t = io.beta[b * P.Hv + h];
 
-  // 2. buffer rows of tokens 0..n (n = the slot the current token goes to)
+  // 2. where tokens 0..n live (the only divisions by the block size); q, k to shared
   if (!RECURRENT && warp == 0) {
     int anybad = 0;
     for (int i = lane; i <= n; i += 32) {
       const int g = buffer_row(P, d, i);
       anybad |= (g < 0);
-      if (g >= 0) {  // the only divisions by the block size
+      if (g >= 0) {
         koff[i] = kv_row(P, g, hq, P.Hk) * DK;
         voff[i] = kv_row(P, g, h, P.Hv);
       }
@@ -85,142 +90,169 @@ __global__ void __launch_bounds__(2 * D / NSPLIT, 4 / (2 * D / NSPLIT / 128))
     qs[i] = P.scale * to_float(qg[i]);
     kts[i] = to_float(kg[i]);
   }
-  float a_t = 0.f, beta_t = 0.f;
-  if (VARIANT != kPlain && io.log_g) a_t = io.log_g[b * P.Hv + h];
-  if (VARIANT == kGatedDelta) beta_t = io.beta[b * P.Hv + h];
   __syncthreads();
   if (!RECURRENT && bad) return;  // CTA-uniform
 
-  // this lane's first buffered token's u (token rsub), fetched now so its latency
-  // overlaps the state loads instead of following the mat-vec
+  // this lane's first buffered token's u (token rsub), fetched before the mat-vec
   float4 u_first = f4(0.f);
   if (!RECURRENT && rsub < n) {
-    if (VARIANT == kGatedDelta)
+    if (DELTA)
       u_first = ld4(P.ubuf + voff[rsub] * DV + col0);
     else
       u_first = ld4(static_cast<const KT *>(P.vbuf) + voff[rsub] * DV + col0);
   }
 
-  // 3. gate prefix sums and decay weights (warp 0); dot products (all warps)
-  if (VARIANT != kPlain) {
+  // 3. decay weights (warp 0): the buffer stores each token's cumulative log-gate
+  //    since the last fold, so A_t = A_{n-1} + a_t and w_i = e^{A_t - A_i}
+  float At = 0.f;
+  if (GATED) {
     if (warp == 0) {
-      warp_prefix(
-          n + 1,
-          [&](int i) { return i < n ? P.gbuf[voff[i]] : a_t; }, Acum, lane);
-      __syncwarp();
-      const float At = Acum[n];
-      for (int i = lane; i <= n; i += 32) wt[i] = expf(At - Acum[i]);
+      const float A_prev = n > 0 ? P.gbuf[voff[n - 1]] : 0.f;
+      At = A_prev + a_t;
+      for (int i = lane; i <= n; i += 32) wt[i] = expf(At - (i < n ? P.gbuf[voff[i]] : At));
       if (lane == 0) e_t_s = expf(At);
     }
   } else {
     for (int i = tid; i <= n; i += NT) wt[i] = 1.f;
     if (tid == 0) e_t_s = 1.f;
   }
-  for (int i = warp; i <= n; i += NT / 32) {
-    const KT *kp = (i < n) ? static_cast<const KT *>(P.kbuf) + koff[i] : kg;
-    float sq, sk = 0.f;
-    if constexpr (E == 4) {
-      const float4 kv = ld4(kp + lane * 4);
-      const float4 qv = *reinterpret_cast<const float4 *>(&qs[lane * 4]);
-      sq = qv.x * kv.x + qv.y * kv.y + qv.z * kv.z + qv.w * kv.w;
-      if (VARIANT == kGatedDelta) {
-        const float4 tv = *reinterpret_cast<const float4 *>(&kts[lane * 4]);
-        sk = tv.x * kv.x + tv.y * kv.y + tv.z * kv.z + tv.w * kv.w;
-      }
-      if (fold) *reinterpret_cast<float4 *>(&ks[i * DK + lane * 4]) = kv;
+  //    dot products q.k_i (and k_t.k_i), two tokens per warp pass, one butterfly
+  //    reduction for all of a pass's sums
+  for (int i0 = 2 * warp; i0 <= n; i0 += 2 * NW) {
+    const int i1 = i0 + 1;
+    float ka[E], kb[E], qv[E], tv[E];
+    load_smem<E>(qs + lane * E, qv);
+    load_smem<E>(kts + lane * E, tv);
+    if (i0 < n) {
+      load_row<E>(static_cast<const KT *>(P.kbuf) + koff[i0] + lane * E, ka);
     } else {
-      const float2 kv = ld2(kp + lane * 2);
-      const float2 qv = *reinterpret_cast<const float2 *>(&qs[lane * 2]);
-      sq = qv.x * kv.x + qv.y * kv.y;
-      if (VARIANT == kGatedDelta) {
-        const float2 tv = *reinterpret_cast<const float2 *>(&kts[lane * 2]);
-        sk = tv.x * kv.x + tv.y * kv.y;
-      }
-      if (fold) *reinterpret_cast<float2 *>(&ks[i * DK + lane * 2]) = kv;
+#pragma unroll
+      for (int e = 0; e < E; ++e) ka[e] = tv[e];
     }
-    sq = warp_sum(sq);
-    if (VARIANT == kGatedDelta) sk = warp_sum(sk);
-    if (lane == 0) {
-      sc[i] = sq;
-      cc[i] = sk;
+    if (i1 < n) {
+      load_row<E>(static_cast<const KT *>(P.kbuf) + koff[i1] + lane * E, kb);
+    } else {
+#pragma unroll
+      for (int e = 0; e < E; ++e) kb[e] = (i1 == n) ? tv[e] : 0.f;
+    }
+    float qa = 0.f, qb = 0.f, ta = 0.f, tb = 0.f;
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+      qa = fmaf(qv[e], ka[e], qa);
+      qb = fmaf(qv[e], kb[e], qb);
+      if (DELTA) {
+        ta = fmaf(tv[e], ka[e], ta);
+        tb = fmaf(tv[e], kb[e], tb);
+      }
+    }
+    if (DELTA) {
+      const float r = butterfly4(qa, ta, qb, tb, lane);  // lanes 0, 8, 16, 24
+      const int which = lane >> 3;
+      if ((lane & 7) == 0) {
+        if (which == 0) sc[i0] = r;
+        else if (which == 1) cc[i0] = r;
+        else if (i1 <= n) (which == 2 ? sc : cc)[i1] = r;
+      }
+    } else {
+      const float r = butterfly2(qa, qb, lane);  // lanes 0, 16
+      if (lane == 0) sc[i0] = r;
+      else if (lane == 16 && i1 <= n) sc[i1] = r;
+    }
+    if (fold) {
+#pragma unroll
+      for (int e = 0; e < E; ++e) {
+        ks[i0 * DK + lane * E + e] = ka[e];
+        if (i1 <= n) ks[i1 * DK + lane * E + e] = kb[e];
+      }
     }
   }
   __syncthreads();
 
-  // 4. S0^T q_t (and S0^T k_t) over this thread's rows, reduced over rows
+  // 4. S0^T q_t (and S0^T k_t) over this thread's rows, operands four rows at a time
   float4 aq = f4(0.f), ak = f4(0.f);
   if (has_state) {
 #pragma unroll
-    for (int j = 0; j < RPT; ++j) {
-      const int r = rsub + 8 * j;
-      fma4(aq, qs[r], s[j]);
-      if (VARIANT == kGatedDelta) fma4(ak, kts[r], s[j]);
+    for (int j = 0; j < RPT; j += 4) {
+      const float4 q4 = *reinterpret_cast<const float4 *>(&qs[row0 + j]);
+      fma4(aq, q4.x, s[j]);
+      fma4(aq, q4.y, s[j + 1]);
+      fma4(aq, q4.z, s[j + 2]);
+      fma4(aq, q4.w, s[j + 3]);
+      if (DELTA) {
+        const float4 k4 = *reinterpret_cast<const float4 *>(&kts[row0 + j]);
+        fma4(ak, k4.x, s[j]);
+        fma4(ak, k4.y, s[j + 1]);
+        fma4(ak, k4.z, s[j + 2]);
+        fma4(ak, k4.w, s[j + 3]);
+      }
     }
-    aq = rows_sum4(aq);
-    if (VARIANT == kGatedDelta) ak = rows_sum4(ak);
   }
 
-  // 5. buffered tokens' terms, tokens split over the 8 row lanes
-  float4 po = f4(0.f), pc = f4(0.f);
+  // 5. add this lane's share of the buffered tokens' terms, then one reduction over
+  //    the 8 row lanes for both: o_part = e^{A_t} S0^T q + sum_i w_i (q.k_i) u_i
+  const float e_t = e_t_s;
+  float4 po = mul4(e_t, aq), pc = mul4(e_t, ak);
   for (int i = rsub; i < n; i += 8) {
     float4 ui = u_first;
     if (i != rsub) {
-      if (VARIANT == kGatedDelta)
+      if (DELTA)
         ui = ld4(P.ubuf + voff[i] * DV + col0);
       else
         ui = ld4(static_cast<const KT *>(P.vbuf) + voff[i] * DV + col0);
     }
-    fma4(po, wt[i] * sc[i], ui);
-    if (VARIANT == kGatedDelta) fma4(pc, wt[i] * cc[i], ui);
+    const float w = wt[i];
+    fma4(po, w * sc[i], ui);
+    if (DELTA) fma4(pc, w * cc[i], ui);
     if (fold) *reinterpret_cast<float4 *>(&us[i * DV + col0]) = ui;
   }
   po = rows_sum4(po);
-  if (VARIANT == kGatedDelta) pc = rows_sum4(pc);
+  if (DELTA) pc = rows_sum4(pc);
 
-  const float e_t = e_t_s;
   float4 ut = vt;
-  if (VARIANT == kGatedDelta) {
-    ut.x = beta_t * (vt.x - fmaf(e_t, ak.x, pc.x));
-    ut.y = beta_t * (vt.y - fmaf(e_t, ak.y, pc.y));
-    ut.z = beta_t * (vt.z - fmaf(e_t, ak.z, pc.z));
-    ut.w = beta_t * (vt.w - fmaf(e_t, ak.w, pc.w));
+  if (DELTA) {
+    ut.x = beta_t * (vt.x - pc.x);
+    ut.y = beta_t * (vt.y - pc.y);
+    ut.z = beta_t * (vt.z - pc.z);
+    ut.w = beta_t * (vt.w - pc.w);
   }
-  float4 o = add4(mul4(e_t, aq), po);
-  fma4(o, sc[n], ut);
+  fma4(po, sc[n], ut);
   if (rsub == 0) {
-    __stcs(reinterpret_cast<float4 *>(io.o + (b * P.Hv + h) * DV + col0), o);
+    __stcs(reinterpret_cast<float4 *>(io.o + (b * P.Hv + h) * DV + col0), po);
     if (!RECURRENT) {
-      const size_t g = n;
-      st4(static_cast<KT *>(P.vbuf) + voff[g] * DV + col0, vt);
-      if (VARIANT == kGatedDelta) st4(P.ubuf + voff[g] * DV + col0, ut);
+      st4(static_cast<KT *>(P.vbuf) + voff[n] * DV + col0, vt);
+      if (DELTA) st4(P.ubuf + voff[n] * DV + col0, ut);
     }
     if (fold) *reinterpret_cast<float4 *>(&us[n * DV + col0]) = ut;
   }
-  if (!RECURRENT) {
-    const size_t g = n;
-    if (lead && h % group == 0)
+  if (!RECURRENT && lead) {
+    if (h % group == 0)
       for (int i = tid; i < DK / 4; i += NT)
-        st4(static_cast<KT *>(P.kbuf) + koff[g] + 4 * i,
-            *reinterpret_cast<const float4 *>(&kts[4 * i]));
-    if (lead && tid == 0) {
-      P.gbuf[voff[g]] = a_t;
-      P.bbuf[voff[g]] = beta_t;
+        st4(static_cast<KT *>(P.kbuf) + koff[n] + 4 * i, *reinterpret_cast<const float4 *>(&kts[4 * i]));
+    if (tid == 0) {
+      P.gbuf[voff[n]] = At;  // cumulative since the last fold (0 for the plain variant)
+      P.bbuf[voff[n]] = beta_t;
     }
   }
 
-  // 6. fold: S <- e^{A_t} S0 + sum_i e^{A_t-A_i} k_i u_i^T, written back once
+  // 6. fold: S <- e^{A_t} S0 + sum_{i<=n} k_i (w_i u_i)^T, a rank-(n+1) update of the
+  //    register tile, written back once
   if (fold && has_state) {
     __syncthreads();
 #pragma unroll
     for (int j = 0; j < RPT; ++j) s[j] = mul4(e_t, s[j]);
     for (int i = 0; i <= n; ++i) {
-      const float4 u = *reinterpret_cast<const float4 *>(&us[i * DV + col0]);
-      const float w = wt[i];
+      const float4 u = mul4(wt[i], *reinterpret_cast<const float4 *>(&us[i * DV + col0]));
 #pragma unroll
-      for (int j = 0; j < RPT; ++j) fma4(s[j], w * ks[i * DK + rsub + 8 * j], u);
+      for (int j = 0; j < RPT; j += 4) {
+        const float4 k4 = *reinterpret_cast<const float4 *>(&ks[i * DK + row0 + j]);
+        fma4(s[j], k4.x, u);
+        fma4(s[j + 1], k4.y, u);
+        fma4(s[j + 2], k4.z, u);
+        fma4(s[j + 3], k4.w, u);
+      }
     }
 #pragma unroll
-    for (int j = 0; j < RPT; ++j) st_stream4(Sp + (rsub + 8 * j) * DV + col0, s[j]);
+    for (int j = 0; j < RPT; ++j) st_stream4(Sp + (row0 + j) * DV + col0, s[j]);
   }
   if (!RECURRENT && h == 0 && lead && tid == 0) P.dlen[d.req] = fold ? 0 : n + 1;
 }
@@ -253,13 +285,6 @@ __global__ void __launch_bounds__(256) copy_probe_kernel(const float4 *__restric
 // products, barriers, stores) overlap the state loads of the others.
 #ifndef KVB_DECODE_SPLIT
 #define KVB_DECODE_SPLIT 2
-#endif
-
-// Decode implementation: 2 = persistent warp-specialized kernel with a TMA bulk
-// copy ring (decode_pipe.cu) where it applies, else decode_kernel; 0 = state
-// tile held in registers (decode_kernel).
-#ifndef KVB_DECODE_IMPL
-#define KVB_DECODE_IMPL 0
 #endif
 
 template <typename KT, int VARIANT, int D, bool REC>
@@ -310,10 +335,6 @@ cudaError_t launch_decode(const PoolView &P, const RowBatch &rows, const TokenIO
                           int dtype, int d, bool recurrent, int flush_len, int nmax,
                           cudaStream_t stream) {
   if (rows.count <= 0) return cudaSuccess;
-  if (KVB_DECODE_IMPL == 2) {
-    const cudaError_t e = launch_decode_pipe(P, rows, io, variant, dtype, d, recurrent, nmax, stream);
-    if (e != kUnsupported) return e;
-  }
   TokenIO io2 = io;
   io2.lmax = flush_len;
   if (dtype == 0) return pick_variant<float>(P, rows, io2, variant, d, recurrent, stream);

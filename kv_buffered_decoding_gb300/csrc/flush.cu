@@ -3,7 +3,7 @@
 // KVBuffer ("KVBuffer: IO-aware Serving for Linear Attention", Figure 1
 // caption): when the buffer is full, the state is updated with all buffered
 // KVs on the GPU and written back to the state slot.  For L buffered tokens
-// with cumulative log-gates A_1..A_L and pseudo-values u_i (u_i = v_i except
+// with cumulative log-gates A_1..A_L (stored in the buffer) and pseudo-values u_i (u_i = v_i except
 // for the gated delta rule, where u_i was computed when the token entered the
 // buffer):
 //     S <- e^{A_L} S0 + sum_{i<=L} e^{A_L-A_i} k_i u_i^T
@@ -32,7 +32,7 @@ __global__ void __launch_bounds__(2 * D, 2) flush_kernel(const PoolView P, const
   extern __shared__ float4 dyn_smem[];
   float *ks = reinterpret_cast<float *>(dyn_smem);  // [L][DK]
   float *us = ks + (size_t)L * DK;                  // [L][DV]
-  __shared__ float Acum[kMaxTok], wt[kMaxTok];
+  __shared__ float wt[kMaxTok];
   __shared__ int grow[kMaxTok];
   __shared__ float eL_s;
   __shared__ int bad;
@@ -57,10 +57,9 @@ __global__ void __launch_bounds__(2 * D, 2) flush_kernel(const PoolView P, const
 
   if (warp == 0) {
     if (VARIANT != kPlain) {
-      warp_prefix(L, [&](int i) { return P.gbuf[kv_row(P, grow[i], h, P.Hv)]; }, Acum, lane);
-      __syncwarp();
-      const float AL = Acum[L - 1];
-      for (int i = lane; i < L; i += 32) wt[i] = expf(AL - Acum[i]);
+      // the buffer stores cumulative log-gates since the last fold
+      const float AL = P.gbuf[kv_row(P, grow[L - 1], h, P.Hv)];
+      for (int i = lane; i < L; i += 32) wt[i] = expf(AL - P.gbuf[kv_row(P, grow[i], h, P.Hv)]);
       if (lane == 0) eL_s = expf(AL);
     } else {
       for (int i = lane; i < L; i += 32) wt[i] = 1.f;

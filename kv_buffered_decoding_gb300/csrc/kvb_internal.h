@@ -56,7 +56,7 @@ struct TokenIO {
   int lmax;  // most tokens any row of the launch stages in shared memory
 };
 
-enum ErrKind : int32_t { kErrNone = 0, kErrBlockRange = 1, kErrWaitTimeout = 2 };
+enum ErrKind : int32_t { kErrNone = 0, kErrBlockRange = 1 };
 
 // Launchers (kernels.cu).  `dtype` is KVB_F32 / KVB_BF16; `d` is d_k == d_v.
 // Return cudaSuccess or the launch error; kUnsupported for a missing instance.
@@ -67,9 +67,6 @@ constexpr cudaError_t kUnsupported = cudaErrorNotSupported;
 cudaError_t launch_decode(const PoolView &P, const RowBatch &rows, const TokenIO &io, int variant,
                           int dtype, int d, bool recurrent, int flush_len, int nmax,
                           cudaStream_t stream);
-cudaError_t launch_decode_pipe(const PoolView &P, const RowBatch &rows, const TokenIO &io,
-                               int variant, int dtype, int d, bool recurrent, int nmax,
-                               cudaStream_t stream);
 cudaError_t launch_verify(const PoolView &P, const RowBatch &rows, const TokenIO &io, int variant,
                           int dtype, int d, int max_len, cudaStream_t stream);
 cudaError_t launch_flush(const PoolView &P, const RowBatch &rows, int variant, int dtype, int d,

@@ -84,17 +84,17 @@ __global__ void __launch_bounds__(2 * D)
   __syncthreads();
   if (bad) return;
 
-  // gate prefix over the chunk (warp 0); buffered keys and u to shared (others)
+  // cumulative log-gates over the chunk (warp 0): the buffer stores them for its
+  // tokens; the drafts continue the sum.  Buffered keys and u to shared (others).
   if (VARIANT != kPlain) {
     if (warp == 0) {
       const float *lg = io.log_g;
+      for (int i = lane; i < n; i += 32) Acum[i] = P.gbuf[kv_row(P, grow[i], h, P.Hv)];
+      const float A_prev = n > 0 ? P.gbuf[kv_row(P, grow[n - 1], h, P.Hv)] : 0.f;
       warp_prefix(
-          L,
-          [&](int i) {
-            return i < n ? P.gbuf[kv_row(P, grow[i], h, P.Hv)]
-                         : (lg ? lg[(b * T + (i - n)) * P.Hv + h] : 0.f);
-          },
-          Acum, lane);
+          T, [&](int j) { return lg ? lg[(b * T + j) * P.Hv + h] : 0.f; }, Acum + n, lane);
+      __syncwarp();
+      for (int j = lane; j < T; j += 32) Acum[n + j] += A_prev;
     }
   } else {
     for (int i = tid; i < L; i += NT) Acum[i] = 0.f;
@@ -218,7 +218,7 @@ __global__ void __launch_bounds__(2 * D)
   }
   for (int j = tid; j < T; j += NT) {
     const size_t g = grow[n + j];
-    P.gbuf[kv_row(P, (int)g, h, P.Hv)] = (VARIANT != kPlain && io.log_g) ? io.log_g[(b * T + j) * P.Hv + h] : 0.f;
+    P.gbuf[kv_row(P, (int)g, h, P.Hv)] = Acum[n + j];  // cumulative since the last fold
     P.bbuf[kv_row(P, (int)g, h, P.Hv)] = DELTA ? io.beta[(b * T + j) * P.Hv + h] : 0.f;
   }
 }
