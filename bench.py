@@ -227,6 +227,125 @@ def run_reference(args, rank, world):
     print(json.dumps(line), flush=True)
 
 
+# --------------------------------------------------------------------------- other rows
+def _entry_bytes(L, esz=2):
+    return L.n_qk_heads * L.d_k * esz + L.n_v_heads * L.d_v * esz + 2 * L.n_v_heads * 4
+
+
+def measure_paths(kvb, torch, dev, peak):
+    """Time the other calls of the path on this GPU against the same HBM roofline.
+
+    verify: T = 4 drafts per request against the stored state, accepted with j = 0 so
+    every round sees the same buffer; flush: fold 8 buffered tokens per request into the
+    state; short_ctx: buffer-only decode of requests holding 32..47 tokens.  Each entry
+    reports microseconds per call, algorithmic GB/s (raw q/k/v/gate/beta/state/output
+    bytes, as for decode) and the fraction of the peak.
+    """
+    out = {}
+    stream = torch.cuda.current_stream(dev)
+
+    def timed(fn, reps):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(reps):
+            fn()
+        b.record(stream)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / reps * 1e3
+
+    def tokens(L, lead, seed):
+        t = I.draw_tokens(np.random.default_rng(seed), L, lead)
+        res = [torch.from_numpy(t[k_]).to(torch.bfloat16).to(dev) for k_ in ("q", "k", "v")]
+        res.append(None if t["log_g"] is None else torch.from_numpy(t["log_g"]).to(dev))
+        res.append(None if t["beta"] is None else torch.from_numpy(t["beta"]).to(dev))
+        return res
+
+    def pool_for(L, B, m, nb, bs=8, slots=True):
+        v = kvb.KVB_GATED_DELTA if L.variant == I.GATED_DELTA else kvb.KVB_GATED
+        cfg = kvb.make_config(v, kvb.KVB_BF16, L.n_qk_heads, L.n_v_heads, L.d_k, L.d_v, m, bs,
+                              B * nb, B if slots else 0, B, nb)
+        pool = kvb.Pool(cfg, device=dev)
+        if slots:
+            pool.state.normal_(0.0, 1.0 / np.sqrt(L.d_k))
+        for r in range(B):
+            pool.set_request(r, r if slots else -1, list(range(r * nb, (r + 1) * nb)))
+        return pool
+
+    def rec(name, us, nbytes, note):
+        gbs = nbytes / us / 1e3
+        out[name] = {"us_per_call": us, "gbs": gbs, "frac": gbs / peak, "bytes": nbytes,
+                     "note": note}
+
+    # verify: gated delta bench layer at B=256 (HBM-bound) and the gated layer at B=64
+    for L, B, tag in ((I.GDN_LAYER, 256, "verify_gated_delta_B256_T4"),
+                      (I.GATED_LAYER, 64, "verify_gated_B64_T4")):
+        T, m, n0 = 4, 8, 3
+        pool = pool_for(L, B, m, 2)
+        req = np.arange(B, dtype=np.int32)
+        pre = tokens(L, (B,), 5)
+        for _ in range(n0):
+            pool.decode(req, *pre)
+        drafts = tokens(L, (B, T), 6)
+        zero = np.zeros(B, dtype=np.int32)
+
+        def one():
+            pool.verify(req, *drafts)
+            pool.accept(req, zero)
+        us = timed(one, 50)
+        S = L.n_v_heads * L.d_k * L.d_v * 4
+        q = L.n_qk_heads * L.d_k * 2
+        o = L.n_v_heads * L.d_v * 4
+        e = _entry_bytes(L)
+        nbytes = B * (S + T * (q + 2 * e + o) + n0 * e)
+        rec(tag, us, nbytes, "verify + accept(0) per round; state %d MiB%s" % (
+            B * S >> 20, " (L2-resident)" if B * S < 100 * 2 ** 20 else ""))
+        pool.close()
+
+    # flush: 8 buffered tokens per request folded into the state (gated delta, B=256)
+    L, B = I.GDN_LAYER, 256
+    pool = pool_for(L, B, 8, 1)
+    req = np.arange(B, dtype=np.int32)
+    toks = tokens(L, (B,), 7)
+    S = L.n_v_heads * L.d_k * L.d_v * 4
+    e = _entry_bytes(L)
+    times = []
+    for rep in range(8):
+        for _ in range(8):
+            pool.decode(req, *toks, auto_flush=False)
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        pool.flush(req)
+        b.record(stream)
+        torch.cuda.synchronize()
+        times.append(a.elapsed_time(b) * 1e3)
+    us = statistics.median(times[2:])
+    rec("flush_gated_delta_B256_L8", us, B * (2 * S + 8 * e), "one kvb_flush of 8 tokens per request")
+    pool.close()
+
+    # short context: buffer-only decode, gated layer, B=256 requests holding 32..47 tokens
+    L, B = I.GATED_LAYER, 256
+    pool = pool_for(L, B, 8, 8, slots=False)
+    req = np.arange(B, dtype=np.int32)
+    toks = tokens(L, (B,), 8)
+    for _ in range(32):
+        pool.short_ctx(req, *toks)
+    base = pool.get_lengths()[:B].astype(np.int64)
+    reps = 13  # after 3 untimed calls: lengths go from base + 3 to base + 15
+    us = timed(lambda: pool.short_ctx(req, *toks), reps)
+    mean_n = float(base.mean()) + 3 + (reps - 1) / 2.0
+    q = L.n_qk_heads * L.d_k * 2
+    o = L.n_v_heads * L.d_v * 4
+    e = _entry_bytes(L)
+    rec("short_ctx_gated_B256_n32to47", us, int(B * (q + 2 * e + o + mean_n * e)),
+        "buffer-only decode, no state; buffer reads dominate")
+    pool.close()
+    return out
+
+
 # --------------------------------------------------------------------------- GPU arm
 def run_ours(args, rank, world, local_rank):
     import torch
@@ -406,6 +525,11 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.synchronize()
     rec_ms = a.elapsed_time(b_) / n_rec
 
+    paths = None
+    if world == 1 and not args.no_paths:
+        del pool0
+        paths = measure_paths(kvb, torch, dev, peak)
+
     if rank != 0:
         return
     cpu = None
@@ -437,6 +561,7 @@ def run_ours(args, rank, world, local_rank):
         "gpu_launches": args.steps,
         "clocks": clk,
         "cpu_baseline": cpu,
+        "paths": paths,
     }
     print(json.dumps(line), flush=True)
 
@@ -449,6 +574,7 @@ def main():
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-paths", action="store_true", help="skip the verify/flush/short timings")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

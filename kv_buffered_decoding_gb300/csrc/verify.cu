@@ -14,21 +14,58 @@
 // The drafts' K, V, u, gates go to buffer slots n..n+T-1; kvb_accept later
 // keeps a prefix of them by length alone.
 //
-// One CTA per (batch row, value head), the same thread layout as decode: warp
-// w owns 16 state columns, lanes split rows by 8; the state tile stays in
-// registers while the drafts are processed four at a time.
+// Two CTAs of 128 threads per (batch row, value head) at d = 128, with the
+// decode kernel's layout: warp w owns 16 state columns, each lane 16
+// consecutive rows of four of them, and the tile stays in registers.  The 2T
+// mat-vecs run eight vectors at a time (four drafts' S0^T q and S0^T k) and
+// are reduced over the row lanes by one three-level transpose-reduction; the
+// score dot products use butterfly reductions; the forward substitution is
+// done per lane for its four columns without any cross-lane reduction.
 #include "kvb_device.cuh"
 
 namespace kvb {
 
-template <typename KT, int VARIANT, int D>
-__global__ void __launch_bounds__(2 * D)
+// Sum eight per-lane float4 vectors over the three row-lane bits (lane bits 4,
+// 3, 2): on return, the lane whose row-lane index is r (lane >> 2) holds the
+// total of vector r.  28 shuffles instead of 96 for eight separate reductions.
+__device__ __forceinline__ float4 shfl_xor4(float4 v, int off) {
+  return make_float4(__shfl_xor_sync(kFull, v.x, off), __shfl_xor_sync(kFull, v.y, off),
+                     __shfl_xor_sync(kFull, v.z, off), __shfl_xor_sync(kFull, v.w, off));
+}
+__device__ __forceinline__ float4 reduce8_rows(const float4 (&acc)[8], int lane) {
+  const bool b4 = lane & 16, b3 = lane & 8, b2 = lane & 4;
+  float4 k1[4], k2[2];
+#pragma unroll
+  for (int x = 0; x < 4; ++x)
+    k1[x] = add4(b4 ? acc[4 + x] : acc[x], shfl_xor4(b4 ? acc[x] : acc[4 + x], 16));
+#pragma unroll
+  for (int x = 0; x < 2; ++x)
+    k2[x] = add4(b3 ? k1[2 + x] : k1[x], shfl_xor4(b3 ? k1[x] : k1[2 + x], 8));
+  return add4(b2 ? k2[1] : k2[0], shfl_xor4(b2 ? k2[0] : k2[1], 4));
+}
+
+// Pair p of the chunk's score table, in order of draft j then token l <= n + j.
+__device__ __forceinline__ void pair_jl(int p, int n, int &j, int &l) {
+  j = 0;
+  while (p > n + j) {
+    p -= n + j + 1;
+    ++j;
+  }
+  l = p;
+}
+
+template <typename KT, int VARIANT, int D, int NSPLIT>
+__global__ void __launch_bounds__(2 * D / NSPLIT, 512 / (2 * D / NSPLIT))
     verify_kernel(const PoolView P, const RowBatch rows, const TokenIO io) {
-  constexpr int DK = D, DV = D, NT = 2 * D, RPT = DK / 8, E = DK / 32;
-  constexpr bool DELTA = VARIANT == kGatedDelta;
+  constexpr int DK = D, DV = D, NT = 2 * D / NSPLIT, NW = NT / 32, RPT = DK / 8, E = DK / 32;
+  constexpr int CW = DV / NSPLIT;  // columns of this CTA
+  constexpr bool DELTA = VARIANT == kGatedDelta, GATED = VARIANT != kPlain;
+  constexpr int DG = DELTA ? 4 : 8;  // drafts per group of eight mat-vec vectors
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int rsub = lane >> 2, col0 = warp * 16 + (lane & 3) * 4;
-  const int h = blockIdx.x;
+  const int h = blockIdx.x / NSPLIT, part = blockIdx.x % NSPLIT;
+  const int rsub = lane >> 2, row0 = rsub * RPT;
+  const int colL = warp * 16 + (lane & 3) * 4, col0 = part * CW + colL;
+  const bool lead = part == 0;
   const RowDesc d = rows.r[blockIdx.y];
   const size_t b = (size_t)rows.row0 + blockIdx.y;
   const int group = P.Hv / P.Hk;
@@ -37,60 +74,76 @@ __global__ void __launch_bounds__(2 * D)
   const int n = d.n, T = io.T, L = n + T;
   const int LM = io.lmax;  // >= L for every row of the launch
 
-  // shared layout (dynamic): ks[LM][DK] keys of the chunk, us[LM][DV] u of the
-  // chunk, qs[T][DK] scaled draft queries, yq[T][DV], yk[T][DV] mat-vecs,
-  // sw[T][LM], cw[T][LM] decay-weighted scores, Acum[LM], grow[LM]
+  // shared: ks[LM][DK] keys of the chunk; qs[T][DK] scaled draft queries; and for
+  // this CTA's columns: us[LM][CW] u's of the chunk, yq/yk[T][CW] mat-vecs,
+  // vs[T][CW] draft values; sw/cw[T][LM] decay-weighted scores; Acum[LM]; bt[T];
+  // koff/voff[LM]
   extern __shared__ float4 dyn_smem[];
   float *ks = reinterpret_cast<float *>(dyn_smem);
-  float *us = ks + (size_t)LM * DK;
-  float *qs = us + (size_t)LM * DV;
-  float *yq = qs + (size_t)T * DK;
-  float *yk = yq + (size_t)T * DV;
-  float *sw = yk + (size_t)T * DV;
+  float *qs = ks + (size_t)LM * DK;
+  float *us = qs + (size_t)T * DK;
+  float *yq = us + (size_t)LM * CW;
+  float *yk = yq + (size_t)T * CW;
+  float *vs = yk + (size_t)T * CW;
+  float *sw = vs + (size_t)T * CW;
   float *cw = sw + (size_t)T * LM;
   float *Acum = cw + (size_t)T * LM;
-  int *grow = reinterpret_cast<int *>(Acum + LM);
+  float *bt = Acum + ((LM + 1) & ~1);                                // even counts keep
+  size_t *koff = reinterpret_cast<size_t *>(bt + ((T + 1) & ~1));  // koff 8-byte aligned
+  size_t *voff = koff + LM;
   __shared__ int bad;
 
+  // 1. the state tile, into registers
   float4 s[RPT];
   const float *Sp = P.state + (has_state ? ((size_t)d.slot * P.Hv + h) * DK * DV : 0);
   if (has_state) {
 #pragma unroll
-    for (int j = 0; j < RPT; ++j) s[j] = ld_stream4(Sp + (rsub + 8 * j) * DV + col0);
+    for (int j = 0; j < RPT; ++j) s[j] = ld_stream4(Sp + (row0 + j) * DV + col0);
   } else {
 #pragma unroll
     for (int j = 0; j < RPT; ++j) s[j] = f4(0.f);
   }
 
+  // 2. where the chunk's tokens live; draft queries, keys, values, betas to shared
   if (warp == 0) {
     int anybad = 0;
     for (int i = lane; i < L; i += 32) {
       const int g = buffer_row(P, d, i);
-      grow[i] = g;
       anybad |= (g < 0);
+      if (g >= 0) {
+        koff[i] = kv_row(P, g, hq, P.Hk) * DK;
+        voff[i] = kv_row(P, g, h, P.Hv);
+      }
     }
     anybad = __any_sync(kFull, anybad);
     if (lane == 0) bad = anybad;
   }
-  // draft queries and keys (fp32, queries scaled)
   const KT *qg = static_cast<const KT *>(io.q) + b * T * P.Hk * DK;
   const KT *kg = static_cast<const KT *>(io.k) + b * T * P.Hk * DK;
-  for (int idx = tid; idx < T * DK; idx += NT) {
-    const int j = idx / DK, c = idx % DK;
+  for (int idx = tid; idx < T * (DK / 4); idx += NT) {
+    const int j = idx / (DK / 4), c = (idx % (DK / 4)) * 4;
     const size_t src = ((size_t)j * P.Hk + hq) * DK + c;
-    qs[idx] = P.scale * to_float(qg[src]);
-    ks[(size_t)(n + j) * DK + c] = to_float(kg[src]);
+    *reinterpret_cast<float4 *>(&qs[j * DK + c]) = mul4(P.scale, ld4(qg + src));
+    *reinterpret_cast<float4 *>(&ks[(n + j) * DK + c]) = ld4(kg + src);
   }
+  const KT *vg = static_cast<const KT *>(io.v) + b * T * P.Hv * DV;
+  for (int idx = tid; idx < T * (CW / 4); idx += NT) {
+    const int j = idx / (CW / 4), c = (idx % (CW / 4)) * 4;
+    *reinterpret_cast<float4 *>(&vs[j * CW + c]) =
+        ld4(vg + ((size_t)j * P.Hv + h) * DV + part * CW + c);
+  }
+  if (DELTA)
+    for (int j = tid; j < T; j += NT) bt[j] = io.beta[(b * T + j) * P.Hv + h];
   __syncthreads();
-  if (bad) return;
+  if (bad) return;  // CTA-uniform
 
-  // cumulative log-gates over the chunk (warp 0): the buffer stores them for its
-  // tokens; the drafts continue the sum.  Buffered keys and u to shared (others).
-  if (VARIANT != kPlain) {
+  // 3. cumulative log-gates of the chunk (warp 0): stored for the buffered tokens,
+  //    continued over the drafts.  Buffered keys and u's to shared (all threads).
+  if (GATED) {
     if (warp == 0) {
       const float *lg = io.log_g;
-      for (int i = lane; i < n; i += 32) Acum[i] = P.gbuf[kv_row(P, grow[i], h, P.Hv)];
-      const float A_prev = n > 0 ? P.gbuf[kv_row(P, grow[n - 1], h, P.Hv)] : 0.f;
+      for (int i = lane; i < n; i += 32) Acum[i] = P.gbuf[voff[i]];
+      const float A_prev = n > 0 ? P.gbuf[voff[n - 1]] : 0.f;
       warp_prefix(
           T, [&](int j) { return lg ? lg[(b * T + j) * P.Hv + h] : 0.f; }, Acum + n, lane);
       __syncwarp();
@@ -99,150 +152,174 @@ __global__ void __launch_bounds__(2 * D)
   } else {
     for (int i = tid; i < L; i += NT) Acum[i] = 0.f;
   }
-  {
-    // every thread helps stage the n buffered tokens; warp 0 joins after its scan
-    for (int idx = tid; idx < n * (DK / 4); idx += NT) {
-      const int i = idx / (DK / 4), c = (idx % (DK / 4)) * 4;
-      *reinterpret_cast<float4 *>(&ks[(size_t)i * DK + c]) =
-          ld4(static_cast<const KT *>(P.kbuf) + kv_row(P, grow[i], hq, P.Hk) * DK + c);
-    }
-    for (int idx = tid; idx < n * (DV / 4); idx += NT) {
-      const int i = idx / (DV / 4), c = (idx % (DV / 4)) * 4;
-      float4 u;
-      if (DELTA)
-        u = ld4(P.ubuf + kv_row(P, grow[i], h, P.Hv) * DV + c);
-      else
-        u = ld4(static_cast<const KT *>(P.vbuf) + kv_row(P, grow[i], h, P.Hv) * DV + c);
-      *reinterpret_cast<float4 *>(&us[(size_t)i * DV + c]) = u;
-    }
+  for (int idx = tid; idx < n * (DK / 4); idx += NT) {
+    const int i = idx / (DK / 4), c = (idx % (DK / 4)) * 4;
+    *reinterpret_cast<float4 *>(&ks[i * DK + c]) =
+        ld4(static_cast<const KT *>(P.kbuf) + koff[i] + c);
+  }
+  for (int idx = tid; idx < n * (CW / 4); idx += NT) {
+    const int i = idx / (CW / 4), c = (idx % (CW / 4)) * 4;
+    float4 u;
+    if (DELTA)
+      u = ld4(P.ubuf + voff[i] * DV + part * CW + c);
+    else
+      u = ld4(static_cast<const KT *>(P.vbuf) + voff[i] * DV + part * CW + c);
+    *reinterpret_cast<float4 *>(&us[i * CW + c]) = u;
   }
   __syncthreads();
 
-  // decay-weighted scores: sw[j][l] = e^{A_{n+j}-A_l} q_j.k_l (l <= n+j),
-  // cw[j][l] = e^{A_{n+j}-A_l} k_{n+j}.k_l (l < n+j); one warp per pair
-  const int npairs = T * L;
-  for (int p = warp; p < npairs; p += NT / 32) {
-    const int j = p / L, l = p % L;
-    if (l > n + j) continue;  // warp-uniform
-    const float *kl = &ks[(size_t)l * DK];
-    const float *qj = &qs[(size_t)j * DK];
-    const float *kj = &ks[(size_t)(n + j) * DK];
-    float sq = dot_smem<E>(qj + lane * E, kl + lane * E);
-    float sk = DELTA ? dot_smem<E>(kj + lane * E, kl + lane * E) : 0.f;
-    sq = warp_sum(sq);
-    if (DELTA) sk = warp_sum(sk);
-    if (lane == 0) {
-      const float w = (VARIANT != kPlain) ? expf(Acum[n + j] - Acum[l]) : 1.f;
-      sw[j * LM + l] = w * sq;
-      cw[j * LM + l] = (l < n + j) ? w * sk : 0.f;
+  // 4. decay-weighted scores, two (draft, token) pairs per warp pass:
+  //    sw[j][l] = e^{A_{n+j}-A_l} q_j.k_l (l <= n+j); cw[j][l] = e^{A_{n+j}-A_l} k_{n+j}.k_l (l < n+j)
+  const int npairs = T * (n + 1) + T * (T - 1) / 2;
+  for (int p0 = 2 * warp; p0 < npairs; p0 += 2 * NW) {
+    int ja, la, jb = 0, lb = 0;
+    pair_jl(p0, n, ja, la);
+    const bool has_b = p0 + 1 < npairs;
+    if (has_b) pair_jl(p0 + 1, n, jb, lb);
+    float q0[E], k0[E], x0[E], q1[E], k1[E], x1[E];
+    load_smem<E>(qs + ja * DK + lane * E, q0);
+    load_smem<E>(ks + (n + ja) * DK + lane * E, k0);
+    load_smem<E>(ks + la * DK + lane * E, x0);
+    load_smem<E>(qs + jb * DK + lane * E, q1);
+    load_smem<E>(ks + (n + jb) * DK + lane * E, k1);
+    load_smem<E>(ks + lb * DK + lane * E, x1);
+    float qa = 0.f, ka = 0.f, qb = 0.f, kb = 0.f;
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+      qa = fmaf(q0[e], x0[e], qa);
+      qb = fmaf(q1[e], x1[e], qb);
+      if (DELTA) {
+        ka = fmaf(k0[e], x0[e], ka);
+        kb = fmaf(k1[e], x1[e], kb);
+      }
+    }
+    float r;
+    int which;
+    if (DELTA) {
+      r = butterfly4(qa, ka, qb, kb, lane);
+      which = lane >> 3;  // 0: q a, 1: k a, 2: q b, 3: k b
+    } else {
+      r = butterfly2(qa, qb, lane);
+      which = (lane >> 4) * 2;  // 0: q a, 2: q b
+    }
+    if ((lane & 7) == 0 && (DELTA || (lane & 15) == 0)) {
+      const bool second = which >= 2;
+      if (!second || has_b) {
+        const int j = second ? jb : ja, l = second ? lb : la;
+        const float w = GATED ? expf(Acum[n + j] - Acum[l]) : 1.f;
+        if ((which & 1) == 0)
+          sw[j * LM + l] = w * r;
+        else
+          cw[j * LM + l] = (l < n + j) ? w * r : 0.f;
+      }
     }
   }
 
-  // mat-vecs, drafts four at a time, straight from the register-resident tile
-  for (int j0 = 0; j0 < T; j0 += 4) {
-    float4 aq[4], ak[4];
+  // 5. mat-vecs from the register tile, eight vectors at a time
+  for (int g0 = 0; g0 < T; g0 += DG) {
+    float4 acc[8];
 #pragma unroll
-    for (int x = 0; x < 4; ++x) aq[x] = ak[x] = f4(0.f);
+    for (int x = 0; x < 8; ++x) acc[x] = f4(0.f);
     if (has_state) {
 #pragma unroll
-      for (int jr = 0; jr < RPT; ++jr) {
-        const int r = rsub + 8 * jr;
+      for (int jj = 0; jj < RPT; jj += 4) {
 #pragma unroll
-        for (int x = 0; x < 4; ++x) {
-          if (j0 + x < T) {
-            fma4(aq[x], qs[(size_t)(j0 + x) * DK + r], s[jr]);
-            if (DELTA) fma4(ak[x], ks[(size_t)(n + j0 + x) * DK + r], s[jr]);
+        for (int x = 0; x < DG; ++x) {
+          const int j = g0 + x < T ? g0 + x : T - 1;  // duplicates past T are not stored
+          const float4 q4 = *reinterpret_cast<const float4 *>(&qs[j * DK + row0 + jj]);
+          fma4(acc[x], q4.x, s[jj]);
+          fma4(acc[x], q4.y, s[jj + 1]);
+          fma4(acc[x], q4.z, s[jj + 2]);
+          fma4(acc[x], q4.w, s[jj + 3]);
+          if (DELTA) {
+            const float4 k4 = *reinterpret_cast<const float4 *>(&ks[(n + j) * DK + row0 + jj]);
+            fma4(acc[4 + x], k4.x, s[jj]);
+            fma4(acc[4 + x], k4.y, s[jj + 1]);
+            fma4(acc[4 + x], k4.z, s[jj + 2]);
+            fma4(acc[4 + x], k4.w, s[jj + 3]);
           }
         }
       }
-#pragma unroll
-      for (int x = 0; x < 4; ++x) {
-        aq[x] = rows_sum4(aq[x]);
-        if (DELTA) ak[x] = rows_sum4(ak[x]);
-      }
     }
-    if (rsub == 0) {
-#pragma unroll
-      for (int x = 0; x < 4; ++x) {
-        if (j0 + x < T) {
-          *reinterpret_cast<float4 *>(&yq[(size_t)(j0 + x) * DV + col0]) = aq[x];
-          if (DELTA) *reinterpret_cast<float4 *>(&yk[(size_t)(j0 + x) * DV + col0]) = ak[x];
-        }
-      }
+    const float4 tot = reduce8_rows(acc, lane);  // vector rsub of this group
+    const int x = DELTA ? (rsub & 3) : rsub;
+    if (g0 + x < T) {
+      float *dst = (DELTA && rsub >= 4) ? yk : yq;
+      *reinterpret_cast<float4 *>(&dst[(g0 + x) * CW + colL]) = tot;
     }
   }
   __syncthreads();
 
-  // per draft, in order: u_j (forward substitution for the delta rule), o_j
-  const KT *vg = static_cast<const KT *>(io.v) + b * T * P.Hv * DV;
+  // 6. per draft, in order: u (forward substitution for the delta rule) and o,
+  //    for this lane's four columns; every row lane computes the same values
   for (int j = 0; j < T; ++j) {
     const int t = n + j;  // chunk position of this draft
-    float4 po = f4(0.f), pc = f4(0.f);
-    for (int l = rsub; l < t; l += 8) {
-      const float4 u = *reinterpret_cast<const float4 *>(&us[(size_t)l * DV + col0]);
+    const float e_j = GATED ? expf(Acum[t]) : 1.f;
+    float4 po = mul4(e_j, *reinterpret_cast<const float4 *>(&yq[j * CW + colL]));
+    float4 pc = f4(0.f);
+    if (DELTA) pc = mul4(e_j, *reinterpret_cast<const float4 *>(&yk[j * CW + colL]));
+    for (int l = 0; l < t; ++l) {
+      const float4 u = *reinterpret_cast<const float4 *>(&us[l * CW + colL]);
       fma4(po, sw[j * LM + l], u);
       if (DELTA) fma4(pc, cw[j * LM + l], u);
     }
-    po = rows_sum4(po);
-    if (DELTA) pc = rows_sum4(pc);
-    const float e_j = (VARIANT != kPlain) ? expf(Acum[t]) : 1.f;
-    const float4 vt = ld4(vg + ((size_t)j * P.Hv + h) * DV + col0);
+    const float4 vt = *reinterpret_cast<const float4 *>(&vs[j * CW + colL]);
     float4 ut = vt;
     if (DELTA) {
-      const float bj = io.beta[(b * T + j) * P.Hv + h];
-      const float4 z = *reinterpret_cast<const float4 *>(&yk[(size_t)j * DV + col0]);
-      ut.x = bj * (vt.x - fmaf(e_j, z.x, pc.x));
-      ut.y = bj * (vt.y - fmaf(e_j, z.y, pc.y));
-      ut.z = bj * (vt.z - fmaf(e_j, z.z, pc.z));
-      ut.w = bj * (vt.w - fmaf(e_j, z.w, pc.w));
+      const float bj = bt[j];
+      ut.x = bj * (vt.x - pc.x);
+      ut.y = bj * (vt.y - pc.y);
+      ut.z = bj * (vt.z - pc.z);
+      ut.w = bj * (vt.w - pc.w);
     }
-    const float4 y = *reinterpret_cast<const float4 *>(&yq[(size_t)j * DV + col0]);
-    float4 o = add4(mul4(e_j, y), po);
-    fma4(o, sw[j * LM + t], ut);
+    fma4(po, sw[j * LM + t], ut);
     if (rsub == 0) {
-      __stcs(reinterpret_cast<float4 *>(io.o + ((b * T + j) * P.Hv + h) * DV + col0), o);
-      *reinterpret_cast<float4 *>(&us[(size_t)t * DV + col0]) = ut;
-      const size_t g = grow[t];
-      st4(static_cast<KT *>(P.vbuf) + kv_row(P, (int)g, h, P.Hv) * DV + col0, vt);
-      if (DELTA) st4(P.ubuf + kv_row(P, (int)g, h, P.Hv) * DV + col0, ut);
+      __stcs(reinterpret_cast<float4 *>(io.o + ((b * T + j) * P.Hv + h) * DV + col0), po);
+      *reinterpret_cast<float4 *>(&us[t * CW + colL]) = ut;
+      st4(static_cast<KT *>(P.vbuf) + voff[t] * DV + col0, vt);
+      if (DELTA) st4(P.ubuf + voff[t] * DV + col0, ut);
     }
-    __syncwarp();  // u_t of this warp's columns visible to its other lanes
+    __syncwarp();  // u of this draft visible to the warp's other lanes
   }
 
-  // drafts' keys and gates into the buffer
-  for (int idx = tid; idx < T * (DK / 4); idx += NT) {
-    const int j = idx / (DK / 4), c = (idx % (DK / 4)) * 4;
+  // 7. drafts' keys, cumulative gates and betas into the buffer
+  if (lead) {
     if (h % group == 0)
-      st4(static_cast<KT *>(P.kbuf) + kv_row(P, grow[n + j], hq, P.Hk) * DK + c,
-          *reinterpret_cast<const float4 *>(&ks[(size_t)(n + j) * DK + c]));
-  }
-  for (int j = tid; j < T; j += NT) {
-    const size_t g = grow[n + j];
-    P.gbuf[kv_row(P, (int)g, h, P.Hv)] = Acum[n + j];  // cumulative since the last fold
-    P.bbuf[kv_row(P, (int)g, h, P.Hv)] = DELTA ? io.beta[(b * T + j) * P.Hv + h] : 0.f;
+      for (int idx = tid; idx < T * (DK / 4); idx += NT) {
+        const int j = idx / (DK / 4), c = (idx % (DK / 4)) * 4;
+        st4(static_cast<KT *>(P.kbuf) + koff[n + j] + c,
+            *reinterpret_cast<const float4 *>(&ks[(n + j) * DK + c]));
+      }
+    for (int j = tid; j < T; j += NT) {
+      P.gbuf[voff[n + j]] = Acum[n + j];  // cumulative since the last fold
+      P.bbuf[voff[n + j]] = DELTA ? bt[j] : 0.f;
+    }
   }
 }
 
 // ------------------------------------------------------------------ launcher
-static size_t verify_smem(int d, int T, int LM) {
-  return sizeof(float) * ((size_t)LM * d * 2 + (size_t)T * d * 3 + (size_t)T * LM * 2 + LM) +
-         sizeof(int) * (size_t)LM;
+static size_t verify_smem(int d, int split, int T, int LM) {
+  const size_t cw = d / split;
+  const size_t floats = (size_t)LM * d + (size_t)T * d + (size_t)LM * cw + 3 * (size_t)T * cw +
+                        2 * (size_t)T * LM + ((LM + 1) & ~1) + ((T + 1) & ~1);
+  return floats * sizeof(float) + 2 * (size_t)LM * sizeof(size_t);
 }
 
 template <typename KT, int VARIANT, int D>
 static cudaError_t run_verify(const PoolView &P, const RowBatch &rows, const TokenIO &io,
                               cudaStream_t stream) {
+  constexpr int NS = D == 128 ? 2 : 1;
   static bool configured = false;
   if (!configured) {
-    const size_t most = verify_smem(D, kMaxTok - 1, kMaxTok - 1);
-    cudaError_t e = cudaFuncSetAttribute(verify_kernel<KT, VARIANT, D>,
+    const size_t most = verify_smem(D, NS, kMaxTok - 1, kMaxTok - 1);
+    cudaError_t e = cudaFuncSetAttribute(verify_kernel<KT, VARIANT, D, NS>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)most);
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  const size_t smem = verify_smem(D, io.T, io.lmax);
-  dim3 grid(P.Hv, rows.count);
-  verify_kernel<KT, VARIANT, D><<<grid, 2 * D, smem, stream>>>(P, rows, io);
+  const size_t smem = verify_smem(D, NS, io.T, io.lmax);
+  dim3 grid(P.Hv * NS, rows.count);
+  verify_kernel<KT, VARIANT, D, NS><<<grid, 2 * D / NS, smem, stream>>>(P, rows, io);
   return cudaGetLastError();
 }
 
