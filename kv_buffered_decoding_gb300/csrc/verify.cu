@@ -297,6 +297,293 @@ __global__ void __launch_bounds__(2 * D / NSPLIT, 512 / (2 * D / NSPLIT))
   }
 }
 
+// ------------------------------------------------------------------ tensor-core verify
+// The 2T mat-vecs as one small matrix product per head on the tensor cores:
+// Y^T = X^T S0 with X = [q_0..q_{T-1}, k_0..k_{T-1}] (d_k x V, V = 2T for the
+// delta rule, T otherwise, padded to 16) and S0 the d_k x d_v state.  Each warp
+// owns 32 state columns and walks the 128 rows in k-steps of 8 with
+// mma.sync.m16n8k8 (tf32 in, fp32 accumulate).  A lane (g = lane/4, t = lane%4)
+// loads rows 8ks+t and 8ks+t+4 of its columns 32w+4g..32w+4g+3 as two
+// coalesced 128-bit loads; element i of each becomes the B fragment of n-tile
+// i (n-tile i covers columns 32w+4p+i, p = 0..7), so no data moves between
+// lanes and the sum over rows happens inside the MMA.  The state is rounded to
+// tf32 (cvt.rna, relative error <= 2^-11 per element, about 2^-12 in the
+// outputs); q and k come from bf16 and are exact in tf32.  Used for bf16
+// pools at d = 128; the fp32 path keeps verify_kernel.
+__device__ __forceinline__ uint32_t to_tf32(float x) {
+  uint32_t r;
+  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+  return r;
+}
+__device__ __forceinline__ void mma_tf32(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                         uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+template <int VARIANT>
+__global__ void __launch_bounds__(128, 4)
+    verify_mma_kernel(const PoolView P, const RowBatch rows, const TokenIO io) {
+  using KT = __nv_bfloat16;
+  constexpr int D = 128, DK = D, DV = D, NT = 128, NW = 4, E = 4;
+  constexpr bool DELTA = VARIANT == kGatedDelta, GATED = VARIANT != kPlain;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int g = lane >> 2, t = lane & 3;
+  const int h = blockIdx.x;
+  const RowDesc d = rows.r[blockIdx.y];
+  const size_t b = (size_t)rows.row0 + blockIdx.y;
+  const int group = P.Hv / P.Hk;
+  const int hq = h / group;
+  const bool has_state = d.slot >= 0;
+  const int n = d.n, T = io.T, L = n + T;
+  const int LM = io.lmax;
+  const int V = DELTA ? 2 * T : T;     // mat-vec vectors
+  const int MT = (V + 15) / 16;        // 16-vector m-tiles
+  const int VP = MT * 16;
+
+  // shared: Xs[VP][DK] vectors (q scaled, then k; zero padding); ks[LM][DK] chunk
+  // keys; us[LM][DV] chunk u's; Y[V][DV] mat-vec results; vs[T][DV] draft values;
+  // sw/cw[T][LM]; Acum[LM]; bt[T]; koff/voff[LM]
+  extern __shared__ float4 dyn_smem[];
+  float *Xs = reinterpret_cast<float *>(dyn_smem);
+  float *ks = Xs + (size_t)VP * DK;
+  float *us = ks + (size_t)LM * DK;
+  float *Y = us + (size_t)LM * DV;
+  float *vs = Y + (size_t)V * DV;
+  float *sw = vs + (size_t)T * DV;
+  float *cw = sw + (size_t)T * LM;
+  float *Acum = cw + (size_t)T * LM;
+  float *bt = Acum + ((LM + 1) & ~1);
+  size_t *koff = reinterpret_cast<size_t *>(bt + ((T + 1) & ~1));
+  size_t *voff = koff + LM;
+  __shared__ int bad;
+
+  const float *Sp = P.state + (has_state ? ((size_t)d.slot * P.Hv + h) * DK * DV : 0);
+  const int cbase = warp * 32 + 4 * g;  // this lane's four columns
+
+  // 1. where the chunk's tokens live; vectors, draft keys, values, betas to shared
+  if (warp == 0) {
+    int anybad = 0;
+    for (int i = lane; i < L; i += 32) {
+      const int gr = buffer_row(P, d, i);
+      anybad |= (gr < 0);
+      if (gr >= 0) {
+        koff[i] = kv_row(P, gr, hq, P.Hk) * DK;
+        voff[i] = kv_row(P, gr, h, P.Hv);
+      }
+    }
+    anybad = __any_sync(kFull, anybad);
+    if (lane == 0) bad = anybad;
+  }
+  const KT *qg = static_cast<const KT *>(io.q) + b * T * P.Hk * DK;
+  const KT *kg = static_cast<const KT *>(io.k) + b * T * P.Hk * DK;
+  for (int idx = tid; idx < VP * (DK / 4); idx += NT) {
+    const int m = idx / (DK / 4), c = (idx % (DK / 4)) * 4;
+    float4 x = f4(0.f);
+    if (m < T) {
+      x = mul4(P.scale, ld4(qg + ((size_t)m * P.Hk + hq) * DK + c));
+    } else if (DELTA && m < 2 * T) {
+      x = ld4(kg + ((size_t)(m - T) * P.Hk + hq) * DK + c);
+    }
+    *reinterpret_cast<float4 *>(&Xs[m * DK + c]) = x;
+  }
+  for (int idx = tid; idx < T * (DK / 4); idx += NT) {
+    const int j = idx / (DK / 4), c = (idx % (DK / 4)) * 4;
+    *reinterpret_cast<float4 *>(&ks[(n + j) * DK + c]) = ld4(kg + ((size_t)j * P.Hk + hq) * DK + c);
+  }
+  const KT *vg = static_cast<const KT *>(io.v) + b * T * P.Hv * DV;
+  for (int idx = tid; idx < T * (DV / 4); idx += NT) {
+    const int j = idx / (DV / 4), c = (idx % (DV / 4)) * 4;
+    *reinterpret_cast<float4 *>(&vs[j * DV + c]) = ld4(vg + ((size_t)j * P.Hv + h) * DV + c);
+  }
+  if (DELTA)
+    for (int j = tid; j < T; j += NT) bt[j] = io.beta[(b * T + j) * P.Hv + h];
+  __syncthreads();
+  if (bad) return;  // CTA-uniform
+
+  // 2. cumulative gates; buffered keys and u's to shared
+  if (GATED) {
+    if (warp == 0) {
+      const float *lg = io.log_g;
+      for (int i = lane; i < n; i += 32) Acum[i] = P.gbuf[voff[i]];
+      const float A_prev = n > 0 ? P.gbuf[voff[n - 1]] : 0.f;
+      warp_prefix(
+          T, [&](int j) { return lg ? lg[(b * T + j) * P.Hv + h] : 0.f; }, Acum + n, lane);
+      __syncwarp();
+      for (int j = lane; j < T; j += 32) Acum[n + j] += A_prev;
+    }
+  } else {
+    for (int i = tid; i < L; i += NT) Acum[i] = 0.f;
+  }
+  for (int idx = tid; idx < n * (DK / 4); idx += NT) {
+    const int i = idx / (DK / 4), c = (idx % (DK / 4)) * 4;
+    *reinterpret_cast<float4 *>(&ks[i * DK + c]) = ld4(static_cast<const KT *>(P.kbuf) + koff[i] + c);
+  }
+  for (int idx = tid; idx < n * (DV / 4); idx += NT) {
+    const int i = idx / (DV / 4), c = (idx % (DV / 4)) * 4;
+    float4 u;
+    if (DELTA)
+      u = ld4(P.ubuf + voff[i] * DV + c);
+    else
+      u = ld4(static_cast<const KT *>(P.vbuf) + voff[i] * DV + c);
+    *reinterpret_cast<float4 *>(&us[i * DV + c]) = u;
+  }
+  __syncthreads();
+
+  // 3. the mat-vecs on the tensor cores (each m-tile: 16 vectors x 32 columns per warp)
+  for (int mt = 0; mt < MT; ++mt) {
+    float acc[4][4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
+    if (has_state) {
+      const float *xa = Xs + (size_t)(mt * 16 + g) * DK;
+      const float *xb = xa + 8 * DK;
+#pragma unroll 4
+      for (int kstep = 0; kstep < DK / 8; ++kstep) {
+        const int r0 = kstep * 8 + t;
+        const float4 s0 = ld_stream4(Sp + (size_t)r0 * DV + cbase);
+        const float4 s1 = ld_stream4(Sp + (size_t)(r0 + 4) * DV + cbase);
+        const uint32_t a[4] = {__float_as_uint(xa[r0]), __float_as_uint(xb[r0]),
+                               __float_as_uint(xa[r0 + 4]), __float_as_uint(xb[r0 + 4])};
+        mma_tf32(acc[0], a, to_tf32(s0.x), to_tf32(s1.x));
+        mma_tf32(acc[1], a, to_tf32(s0.y), to_tf32(s1.y));
+        mma_tf32(acc[2], a, to_tf32(s0.z), to_tf32(s1.z));
+        mma_tf32(acc[3], a, to_tf32(s0.w), to_tf32(s1.w));
+      }
+    }
+    // D[m][p] of n-tile i is vector m at column warp*32 + 4p + i
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int m0 = mt * 16 + g, m1 = m0 + 8;
+      const int c0 = warp * 32 + 8 * t + i, c1 = c0 + 4;
+      if (m0 < V) {
+        Y[m0 * DV + c0] = acc[i][0];
+        Y[m0 * DV + c1] = acc[i][1];
+      }
+      if (m1 < V) {
+        Y[m1 * DV + c0] = acc[i][2];
+        Y[m1 * DV + c1] = acc[i][3];
+      }
+    }
+  }
+
+  // 4. decay-weighted scores, two pairs per warp pass (as in verify_kernel)
+  const int npairs = T * (n + 1) + T * (T - 1) / 2;
+  const float *qsv = Xs;  // scaled draft queries are vectors 0..T-1
+  for (int p0 = 2 * warp; p0 < npairs; p0 += 2 * NW) {
+    int ja, la, jb = 0, lb = 0;
+    pair_jl(p0, n, ja, la);
+    const bool has_b = p0 + 1 < npairs;
+    if (has_b) pair_jl(p0 + 1, n, jb, lb);
+    float q0[E], k0[E], x0[E], q1[E], k1[E], x1[E];
+    load_smem<E>(qsv + ja * DK + lane * E, q0);
+    load_smem<E>(ks + (n + ja) * DK + lane * E, k0);
+    load_smem<E>(ks + la * DK + lane * E, x0);
+    load_smem<E>(qsv + jb * DK + lane * E, q1);
+    load_smem<E>(ks + (n + jb) * DK + lane * E, k1);
+    load_smem<E>(ks + lb * DK + lane * E, x1);
+    float qa = 0.f, ka = 0.f, qb = 0.f, kb = 0.f;
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+      qa = fmaf(q0[e], x0[e], qa);
+      qb = fmaf(q1[e], x1[e], qb);
+      if (DELTA) {
+        ka = fmaf(k0[e], x0[e], ka);
+        kb = fmaf(k1[e], x1[e], kb);
+      }
+    }
+    float r;
+    int which;
+    if (DELTA) {
+      r = butterfly4(qa, ka, qb, kb, lane);
+      which = lane >> 3;
+    } else {
+      r = butterfly2(qa, qb, lane);
+      which = (lane >> 4) * 2;
+    }
+    if ((lane & 7) == 0 && (DELTA || (lane & 15) == 0)) {
+      const bool second = which >= 2;
+      if (!second || has_b) {
+        const int j = second ? jb : ja, l = second ? lb : la;
+        const float w = GATED ? expf(Acum[n + j] - Acum[l]) : 1.f;
+        if ((which & 1) == 0)
+          sw[j * LM + l] = w * r;
+        else
+          cw[j * LM + l] = (l < n + j) ? w * r : 0.f;
+      }
+    }
+  }
+  __syncthreads();
+
+  // 5. per draft, in order, one column per thread: u (forward substitution for the
+  //    delta rule) and o
+  const int c = tid;
+  for (int j = 0; j < T; ++j) {
+    const int tpos = n + j;
+    const float e_j = GATED ? expf(Acum[tpos]) : 1.f;
+    float po = e_j * Y[j * DV + c];
+    float pc = DELTA ? e_j * Y[(T + j) * DV + c] : 0.f;
+    for (int l = 0; l < tpos; ++l) {
+      const float u = us[l * DV + c];
+      po = fmaf(sw[j * LM + l], u, po);
+      if (DELTA) pc = fmaf(cw[j * LM + l], u, pc);
+    }
+    const float vt = vs[j * DV + c];
+    const float ut = DELTA ? bt[j] * (vt - pc) : vt;
+    po = fmaf(sw[j * LM + tpos], ut, po);
+    __stcs(io.o + ((b * T + j) * P.Hv + h) * DV + c, po);
+    us[tpos * DV + c] = ut;  // read later only by this thread
+  }
+  __syncthreads();
+
+  // 6. drafts into the buffer: values and u's, keys (one value head per q/k head),
+  //    cumulative gates, betas
+  for (int idx = tid; idx < T * (DV / 4); idx += NT) {
+    const int j = idx / (DV / 4), cc4 = (idx % (DV / 4)) * 4;
+    const size_t dst = voff[n + j] * DV + cc4;
+    st4(static_cast<KT *>(P.vbuf) + dst, *reinterpret_cast<const float4 *>(&vs[j * DV + cc4]));
+    if (DELTA) st4(P.ubuf + dst, *reinterpret_cast<const float4 *>(&us[(n + j) * DV + cc4]));
+  }
+  if (h % group == 0)
+    for (int idx = tid; idx < T * (DK / 4); idx += NT) {
+      const int j = idx / (DK / 4), cc4 = (idx % (DK / 4)) * 4;
+      st4(static_cast<KT *>(P.kbuf) + koff[n + j] + cc4,
+          *reinterpret_cast<const float4 *>(&ks[(n + j) * DK + cc4]));
+    }
+  for (int j = tid; j < T; j += NT) {
+    P.gbuf[voff[n + j]] = Acum[n + j];
+    P.bbuf[voff[n + j]] = DELTA ? bt[j] : 0.f;
+  }
+}
+
+static size_t verify_mma_smem(int variant, int T, int LM) {
+  const int D = 128;
+  const size_t V = variant == kGatedDelta ? 2 * T : T;
+  const size_t VP = (V + 15) / 16 * 16;
+  const size_t floats = VP * D + (size_t)LM * D + (size_t)LM * D + V * D + (size_t)T * D +
+                        2 * (size_t)T * LM + ((LM + 1) & ~1) + ((T + 1) & ~1);
+  return floats * sizeof(float) + 2 * (size_t)LM * sizeof(size_t);
+}
+
+template <int VARIANT>
+static cudaError_t run_verify_mma(const PoolView &P, const RowBatch &rows, const TokenIO &io,
+                                  cudaStream_t stream) {
+  const size_t smem = verify_mma_smem(VARIANT, io.T, io.lmax);
+  static size_t configured = 0;
+  if (smem > configured) {
+    cudaError_t e = cudaFuncSetAttribute(verify_mma_kernel<VARIANT>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    configured = smem;
+  }
+  dim3 grid(P.Hv, rows.count);
+  verify_mma_kernel<VARIANT><<<grid, 128, smem, stream>>>(P, rows, io);
+  return cudaGetLastError();
+}
+
 // ------------------------------------------------------------------ launcher
 static size_t verify_smem(int d, int split, int T, int LM) {
   const size_t cw = d / split;
@@ -348,7 +635,17 @@ cudaError_t launch_verify(const PoolView &P, const RowBatch &rows, const TokenIO
   TokenIO io2 = io;
   io2.lmax = max_len;
   if (dtype == 0) return verify_variant<float>(P, rows, io2, variant, d, stream);
-  if (dtype == 1) return verify_variant<__nv_bfloat16>(P, rows, io2, variant, d, stream);
+  if (dtype == 1) {
+    // tensor-core path for bf16 pools at d = 128 when its shared memory fits
+    if (d == 128 && verify_mma_smem(variant, io2.T, io2.lmax) <= 227 * 1024 - 1024) {
+      switch (variant) {
+        case kPlain: return run_verify_mma<kPlain>(P, rows, io2, stream);
+        case kGated: return run_verify_mma<kGated>(P, rows, io2, stream);
+        case kGatedDelta: return run_verify_mma<kGatedDelta>(P, rows, io2, stream);
+      }
+    }
+    return verify_variant<__nv_bfloat16>(P, rows, io2, variant, d, stream);
+  }
   return kUnsupported;
 }
 

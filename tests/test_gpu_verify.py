@@ -115,3 +115,46 @@ def test_accept_zero_and_full():
     o_ref, _, _ = oracle.decode_sequence(S0[1], hist, layer.variant)
     assert rel_err(o.cpu().numpy()[0], o_ref[-1]) <= tol_for(layer)
     assert pool.get_error() is None
+
+
+@pytest.mark.parametrize("T", [4, 6])
+def test_verify_gated_delta_d128(T):
+    """Gated delta rule at d=128 with grouped heads (the tensor-core verify path for
+    bf16): 30 rounds of verify + random prefix accept; outputs every round, state at
+    every fold and after a final flush."""
+    layer = I.Layer(I.GATED_DELTA, 2, 4, 128, 128, "bf16", qk_dist="l2norm")
+    B, m, bs = 8, 8, 8
+    nb = blocks_needed(m - 1 + T, bs)
+    rng = np.random.default_rng(40 + T)
+    S0 = I.draw_state(rng, layer, B)
+    pool = make_pool(layer, m, B, nb, bs)
+    pool.state.copy_(torch.from_numpy(S0))
+    perm = rng.permutation(B * nb)
+    for r in range(B):
+        pool.set_request(r, r, perm[r * nb:(r + 1) * nb])
+    req = np.arange(B)
+    S_hist = S0.astype(np.float64)
+    n_model = np.zeros(B, dtype=np.int64)
+    tol = tol_for(layer)
+    for rnd in range(30):
+        tok = I.draw_tokens(rng, layer, (B, T))
+        o = pool.verify(req, dev(tok["q"], layer), dev(tok["k"], layer), dev(tok["v"], layer),
+                        dev(tok["log_g"], f32=True), dev(tok["beta"], f32=True))
+        j = rng.integers(0, T + 1, size=B)
+        pool.accept(req, j)
+        drafts = {key: _bt(val) for key, val in tok.items()}
+        o_ref = oracle.verify(S_hist, drafts, layer.variant)
+        assert rel_err(np.swapaxes(o.cpu().numpy(), 0, 1), o_ref) <= tol, rnd
+        S_hist = oracle.accept(S_hist, drafts, j, layer.variant)
+        n_model = n_model + j
+        folded = n_model >= m
+        n_model[folded] = 0
+        assert np.array_equal(pool.get_lengths(), n_model.astype(np.int32)), rnd
+        if folded.any():
+            torch.cuda.synchronize()
+            st = pool.state.cpu().numpy()
+            assert rel_err(st[folded], S_hist[folded]) <= tol, rnd
+    pool.flush(req)
+    torch.cuda.synchronize()
+    assert rel_err(pool.state.cpu().numpy(), S_hist) <= tol
+    assert pool.get_error() is None
