@@ -7,7 +7,8 @@
 // for the gated delta rule, where u_i was computed when the token entered the
 // buffer):
 //     S <- e^{A_L} S0 + sum_{i<=L} e^{A_L-A_i} k_i u_i^T
-// a rank-L update, K^T diag(w) U, of the register-resident state tile.  At
+// a rank-L update, K^T diag(w) U, of the register-resident state tile (two
+// CTAs per head at d = 128, 16 consecutive rows per lane as in decode).  At
 // L <= 64 this is 2 L flop per state element against 8 bytes of state traffic
 // per element (read + write), i.e. below the fp32 FMA ridge: the kernel is
 // bound by HBM, and the update runs on the FMA pipes.
@@ -18,36 +19,42 @@
 
 namespace kvb {
 
-template <typename KT, int VARIANT, int D>
-__global__ void __launch_bounds__(2 * D, 2) flush_kernel(const PoolView P, const RowBatch rows) {
-  constexpr int DK = D, DV = D, NT = 2 * D, RPT = DK / 8;
+template <typename KT, int VARIANT, int D, int NSPLIT>
+__global__ void __launch_bounds__(2 * D / NSPLIT, 512 / (2 * D / NSPLIT))
+    flush_kernel(const PoolView P, const RowBatch rows) {
+  constexpr int DK = D, DV = D, NT = 2 * D / NSPLIT, RPT = DK / 8;
+  constexpr int CW = DV / NSPLIT;
   constexpr bool DELTA = VARIANT == kGatedDelta;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int rsub = lane >> 2, col0 = warp * 16 + (lane & 3) * 4;
-  const int h = blockIdx.x;
+  const int h = blockIdx.x / NSPLIT, part = blockIdx.x % NSPLIT;
+  const int rsub = lane >> 2, row0 = rsub * RPT;
+  const int colL = warp * 16 + (lane & 3) * 4, col0 = part * CW + colL;
   const RowDesc d = rows.r[blockIdx.y];
   const int hq = h / (P.Hv / P.Hk);
   const int L = d.n;
 
   extern __shared__ float4 dyn_smem[];
-  float *ks = reinterpret_cast<float *>(dyn_smem);  // [L][DK]
-  float *us = ks + (size_t)L * DK;                  // [L][DV]
+  float *ks = reinterpret_cast<float *>(dyn_smem);  // [L][DK] keys
+  float *us = ks + (size_t)L * DK;                  // [L][CW] w_i u_i for this CTA's columns
   __shared__ float wt[kMaxTok];
-  __shared__ int grow[kMaxTok];
+  __shared__ size_t koff[kMaxTok], voff[kMaxTok];
   __shared__ float eL_s;
   __shared__ int bad;
 
   float *Sp = P.state + ((size_t)d.slot * P.Hv + h) * DK * DV;
   float4 s[RPT];
 #pragma unroll
-  for (int j = 0; j < RPT; ++j) s[j] = ld_stream4(Sp + (rsub + 8 * j) * DV + col0);
+  for (int j = 0; j < RPT; ++j) s[j] = ld_stream4(Sp + (row0 + j) * DV + col0);
 
   if (warp == 0) {
     int anybad = 0;
     for (int i = lane; i < L; i += 32) {
       const int g = buffer_row(P, d, i);
-      grow[i] = g;
       anybad |= (g < 0);
+      if (g >= 0) {
+        koff[i] = kv_row(P, g, hq, P.Hk) * DK;
+        voff[i] = kv_row(P, g, h, P.Hv);
+      }
     }
     anybad = __any_sync(kFull, anybad);
     if (lane == 0) bad = anybad;
@@ -55,11 +62,11 @@ __global__ void __launch_bounds__(2 * D, 2) flush_kernel(const PoolView P, const
   __syncthreads();
   if (bad) return;
 
+  // weights from the stored cumulative log-gates (warp 0); keys to shared (all)
   if (warp == 0) {
     if (VARIANT != kPlain) {
-      // the buffer stores cumulative log-gates since the last fold
-      const float AL = P.gbuf[kv_row(P, grow[L - 1], h, P.Hv)];
-      for (int i = lane; i < L; i += 32) wt[i] = expf(AL - P.gbuf[kv_row(P, grow[i], h, P.Hv)]);
+      const float AL = P.gbuf[voff[L - 1]];
+      for (int i = lane; i < L; i += 32) wt[i] = expf(AL - P.gbuf[voff[i]]);
       if (lane == 0) eL_s = expf(AL);
     } else {
       for (int i = lane; i < L; i += 32) wt[i] = 1.f;
@@ -69,47 +76,55 @@ __global__ void __launch_bounds__(2 * D, 2) flush_kernel(const PoolView P, const
   for (int idx = tid; idx < L * (DK / 4); idx += NT) {
     const int i = idx / (DK / 4), c = (idx % (DK / 4)) * 4;
     *reinterpret_cast<float4 *>(&ks[(size_t)i * DK + c]) =
-        ld4(static_cast<const KT *>(P.kbuf) + kv_row(P, grow[i], hq, P.Hk) * DK + c);
+        ld4(static_cast<const KT *>(P.kbuf) + koff[i] + c);
   }
-  for (int idx = tid; idx < L * (DV / 4); idx += NT) {
-    const int i = idx / (DV / 4), c = (idx % (DV / 4)) * 4;
+  __syncthreads();
+  for (int idx = tid; idx < L * (CW / 4); idx += NT) {
+    const int i = idx / (CW / 4), c = (idx % (CW / 4)) * 4;
     float4 u;
     if (DELTA)
-      u = ld4(P.ubuf + kv_row(P, grow[i], h, P.Hv) * DV + c);
+      u = ld4(P.ubuf + voff[i] * DV + part * CW + c);
     else
-      u = ld4(static_cast<const KT *>(P.vbuf) + kv_row(P, grow[i], h, P.Hv) * DV + c);
-    *reinterpret_cast<float4 *>(&us[(size_t)i * DV + c]) = u;
+      u = ld4(static_cast<const KT *>(P.vbuf) + voff[i] * DV + part * CW + c);
+    *reinterpret_cast<float4 *>(&us[(size_t)i * CW + c]) = mul4(wt[i], u);
   }
   __syncthreads();
 
+  // S <- e^{A_L} S0 + sum_i k_i (w_i u_i)^T, keys four rows per 128-bit load
   const float eL = eL_s;
 #pragma unroll
   for (int j = 0; j < RPT; ++j) s[j] = mul4(eL, s[j]);
   for (int i = 0; i < L; ++i) {
-    const float4 u = *reinterpret_cast<const float4 *>(&us[(size_t)i * DV + col0]);
-    const float w = wt[i];
+    const float4 u = *reinterpret_cast<const float4 *>(&us[(size_t)i * CW + colL]);
 #pragma unroll
-    for (int j = 0; j < RPT; ++j) fma4(s[j], w * ks[(size_t)i * DK + rsub + 8 * j], u);
+    for (int j = 0; j < RPT; j += 4) {
+      const float4 k4 = *reinterpret_cast<const float4 *>(&ks[(size_t)i * DK + row0 + j]);
+      fma4(s[j], k4.x, u);
+      fma4(s[j + 1], k4.y, u);
+      fma4(s[j + 2], k4.z, u);
+      fma4(s[j + 3], k4.w, u);
+    }
   }
 #pragma unroll
-  for (int j = 0; j < RPT; ++j) st_stream4(Sp + (rsub + 8 * j) * DV + col0, s[j]);
-  if (h == 0 && tid == 0) P.dlen[d.req] = 0;
+  for (int j = 0; j < RPT; ++j) st_stream4(Sp + (row0 + j) * DV + col0, s[j]);
+  if (h == 0 && part == 0 && tid == 0) P.dlen[d.req] = 0;
 }
 
 template <typename KT, int VARIANT, int D>
 static cudaError_t run_flush(const PoolView &P, const RowBatch &rows, int max_len,
                              cudaStream_t stream) {
+  constexpr int NS = D == 128 ? 2 : 1;
   static bool configured = false;
   if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(flush_kernel<KT, VARIANT, D>,
+    cudaError_t e = cudaFuncSetAttribute(flush_kernel<KT, VARIANT, D, NS>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (kMaxTok - 1) * 2 * D * (int)sizeof(float));
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  const size_t smem = (size_t)max_len * 2 * D * sizeof(float);
-  dim3 grid(P.Hv, rows.count);
-  flush_kernel<KT, VARIANT, D><<<grid, 2 * D, smem, stream>>>(P, rows);
+  const size_t smem = (size_t)max_len * (D + D / NS) * sizeof(float);
+  dim3 grid(P.Hv * NS, rows.count);
+  flush_kernel<KT, VARIANT, D, NS><<<grid, 2 * D / NS, smem, stream>>>(P, rows);
   return cudaGetLastError();
 }
 

@@ -67,6 +67,8 @@ constexpr cudaError_t kUnsupported = cudaErrorNotSupported;
 cudaError_t launch_decode(const PoolView &P, const RowBatch &rows, const TokenIO &io, int variant,
                           int dtype, int d, bool recurrent, int flush_len, int nmax,
                           cudaStream_t stream);
+cudaError_t launch_short(const PoolView &P, const RowBatch &rows, const TokenIO &io, int variant,
+                         int dtype, int d, cudaStream_t stream);
 cudaError_t launch_verify(const PoolView &P, const RowBatch &rows, const TokenIO &io, int variant,
                           int dtype, int d, int max_len, cudaStream_t stream);
 cudaError_t launch_flush(const PoolView &P, const RowBatch &rows, int variant, int dtype, int d,
