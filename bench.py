@@ -271,7 +271,8 @@ def measure_paths(kvb, torch, dev, peak):
         if slots:
             pool.state.normal_(0.0, 1.0 / np.sqrt(L.d_k))
         for r in range(B):
-            pool.set_request(r, r if slots else -1, list(range(r * nb, (r + 1) * nb)))
+            blocks = list(range(r * nb, (r + 1) * nb)) if m > 0 or not slots else []
+            pool.set_request(r, r if slots else -1, blocks)
         return pool
 
     def rec(name, us, nbytes, note):
@@ -303,6 +304,40 @@ def measure_paths(kvb, torch, dev, peak):
         rec(tag, us, nbytes, "verify + accept(0) per round; state %d MiB%s" % (
             B * S >> 20, " (L2-resident)" if B * S < 100 * 2 ** 20 else ""))
         pool.close()
+
+    # verify latency against the number of drafts: buffered verify vs the recurrent
+    # temporary-state baseline (Figure 2), gated delta layer at B=256, plus the memory
+    # each needs per request (state + buffer slots vs state + T temporary states)
+    L, B = I.GDN_LAYER, 256
+    S = L.n_v_heads * L.d_k * L.d_v * 4
+    slot_bytes = _entry_bytes(L) + L.n_v_heads * L.d_v * 4  # raw k/v/gate/beta + pseudo-value
+    cmp = {}
+    for T in (2, 4, 6, 8):
+        pool = pool_for(L, B, 8, 2)
+        base = pool_for(L, B, 0, 1)
+        base.state.copy_(pool.state)
+        req = np.arange(B, dtype=np.int32)
+        pre = tokens(L, (B,), 9)
+        for _ in range(3):
+            pool.decode(req, *pre)
+        drafts = tokens(L, (B, T), 10 + T)
+        zero = np.zeros(B, dtype=np.int32)
+        temp = torch.empty(B, T, L.n_v_heads, L.d_k, L.d_v, dtype=torch.float32, device=dev)
+        o = torch.empty(B, T, L.n_v_heads, L.d_v, dtype=torch.float32, device=dev)
+
+        def kvb_round():
+            pool.verify(req, *drafts, o=o)
+            pool.accept(req, zero)
+
+        us_kvb = timed(kvb_round, 30)
+        us_base = timed(lambda: base.verify_tempstate(req, *drafts, temp=temp, o=o), 30)
+        cmp[str(T)] = {"buffered_us": us_kvb, "tempstate_us": us_base,
+                       "buffered_bytes_per_request": S + (8 - 1 + T) * slot_bytes,
+                       "tempstate_bytes_per_request": (1 + T) * S}
+        del temp
+        pool.close()
+        base.close()
+    out["verify_vs_tempstate_gated_delta_B256"] = cmp
 
     # flush: 8 buffered tokens per request folded into the state (gated delta, B=256)
     L, B = I.GDN_LAYER, 256

@@ -202,6 +202,25 @@ int kvb_verify(kvb_pool *pool, int32_t B, int32_t T, const int32_t *req_ids, con
 int kvb_accept(kvb_pool *pool, int32_t B, const int32_t *req_ids, const int32_t *n_accepted,
                kvb_stream_t stream);
 
+/* The comparison baseline of Figure 2: a serving system with only a state pool
+   verifies T drafts with the recurrent form and stores a temporary state after
+   every draft.  For pools with m == 0 (KVB_E_STATE otherwise); every request
+   must own a state slot.  Inputs and o as in kvb_verify.  temp_states: device
+   fp32 [B][T][n_v_heads][d_k][d_v], caller-allocated, 16-byte aligned; row b
+   belongs to req_ids[b] and entry j receives the state after drafts 0..j.  The
+   requests' own states are only read. */
+int kvb_verify_tempstate(kvb_pool *pool, int32_t B, int32_t T, const int32_t *req_ids,
+                         const void *q, const void *k, const void *v, const float *log_g,
+                         const float *beta, float *o, float *temp_states, kvb_stream_t stream);
+
+/* Accept for the baseline: request req_ids[b] takes temporary state
+   n_accepted[b] - 1 from the same temp_states layout as its state (Figure 2:
+   the state is replaced by the temporary state of the last accepted draft);
+   n_accepted[b] = 0 keeps the state.  0 <= n_accepted[b] <= T (KVB_E_ARG). */
+int kvb_accept_tempstate(kvb_pool *pool, int32_t B, int32_t T, const int32_t *req_ids,
+                         const int32_t *n_accepted, const float *temp_states,
+                         kvb_stream_t stream);
+
 /* Host copy of every request's buffer length (max_requests int32). Host only,
    no synchronization: the host keeps an exact mirror of the device lengths. */
 int kvb_get_lengths(const kvb_pool *pool, int32_t *host_out);

@@ -444,6 +444,67 @@ int kvb_accept(kvb_pool *p, int32_t B, const int32_t *req_ids, const int32_t *n_
   return launch_fold(p, fold, s);
 }
 
+int kvb_verify_tempstate(kvb_pool *p, int32_t B, int32_t T, const int32_t *req_ids,
+                         const void *q, const void *k, const void *v, const float *log_g,
+                         const float *beta, float *o, float *temp_states, kvb_stream_t stream) {
+  if (!p) return KVB_E_ARG;
+  if (p->cfg.m != 0) return KVB_E_STATE;
+  if (T < 1 || T > KVB_MAX_DRAFTS) return KVB_E_ARG;
+  int st = check_reqs(p, B, req_ids);
+  if (st || B == 0) return st;
+  if ((st = check_io(p, q, k, v, log_g, beta, o))) return st;
+  if (!temp_states || !aligned(temp_states, 16)) return KVB_E_ARG;
+  for (int32_t b = 0; b < B; ++b)
+    if (p->slot[req_ids[b]] < 0) return KVB_E_STATE;
+  const kvb_config &c = p->cfg;
+  const kvb::TokenIO io{q, k, v, log_g, beta, o, T, 0};
+  for (int32_t base = 0; base < B; base += kvb::kMaxRows) {
+    const int32_t cnt = B - base < kvb::kMaxRows ? B - base : kvb::kMaxRows;
+    p->rows.count = cnt;
+    p->rows.row0 = base;
+    for (int32_t i = 0; i < cnt; ++i) p->rows.r[i] = make_row(p, req_ids[base + i], 0, 0);
+    cudaError_t e = kvb::launch_verify_tempstate(p->view, p->rows, io, c.variant, c.kv_dtype, c.d_k,
+                                                 temp_states, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_status(e);
+  }
+  return KVB_OK;
+}
+
+int kvb_accept_tempstate(kvb_pool *p, int32_t B, int32_t T, const int32_t *req_ids,
+                         const int32_t *n_accepted, const float *temp_states,
+                         kvb_stream_t stream) {
+  if (!p) return KVB_E_ARG;
+  if (p->cfg.m != 0) return KVB_E_STATE;
+  if (T < 1 || T > KVB_MAX_DRAFTS) return KVB_E_ARG;
+  int st = check_reqs(p, B, req_ids);
+  if (st || B == 0) return st;
+  if (!n_accepted || !temp_states || !aligned(temp_states, 16)) return KVB_E_ARG;
+  for (int32_t b = 0; b < B; ++b) {
+    if (n_accepted[b] < 0 || n_accepted[b] > T) return KVB_E_ARG;
+    if (p->slot[req_ids[b]] < 0) return KVB_E_STATE;
+  }
+  // only rows that accepted something copy a state; row0 keeps the temp_states row
+  int32_t i = 0;
+  for (int32_t b = 0; b < B; ++b) {
+    if (n_accepted[b] == 0) continue;
+    if (i == kvb::kMaxRows || (i > 0 && b != p->rows.row0 + i)) {
+      cudaError_t e = kvb::launch_accept_tempstate(p->view, p->rows, temp_states, T, p->cfg.d_k,
+                                                   reinterpret_cast<cudaStream_t>(stream));
+      if (e != cudaSuccess) return cuda_status(e);
+      i = 0;
+    }
+    if (i == 0) p->rows.row0 = b;
+    p->rows.r[i++] = make_row(p, req_ids[b], n_accepted[b], 0);
+    p->rows.count = i;
+  }
+  if (i > 0) {
+    cudaError_t e = kvb::launch_accept_tempstate(p->view, p->rows, temp_states, T, p->cfg.d_k,
+                                                 reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_status(e);
+  }
+  return KVB_OK;
+}
+
 int kvb_get_lengths(const kvb_pool *p, int32_t *host_out) {
   if (!p || !host_out) return KVB_E_ARG;
   std::memcpy(host_out, p->len.data(), p->len.size() * sizeof(int32_t));

@@ -73,6 +73,11 @@ cudaError_t launch_verify(const PoolView &P, const RowBatch &rows, const TokenIO
                           int dtype, int d, int max_len, cudaStream_t stream);
 cudaError_t launch_flush(const PoolView &P, const RowBatch &rows, int variant, int dtype, int d,
                          int max_len, cudaStream_t stream);
+cudaError_t launch_verify_tempstate(const PoolView &P, const RowBatch &rows, const TokenIO &io,
+                                    int variant, int dtype, int d, float *temp,
+                                    cudaStream_t stream);
+cudaError_t launch_accept_tempstate(const PoolView &P, const RowBatch &rows, const float *temp,
+                                    int T, int d, cudaStream_t stream);
 cudaError_t launch_set_lengths(const PoolView &P, const RowBatch &rows, cudaStream_t stream);
 cudaError_t launch_copy_probe(const void *src, void *dst, size_t bytes, cudaStream_t stream);
 

@@ -30,7 +30,7 @@ KVB_MAX_DRAFTS = 64
 # every symbol include/kvb.h declares
 EXPORTS = ("kvb_pool_layout", "kvb_alloc_pool", "kvb_free_pool", "kvb_set_request",
            "kvb_release_request", "kvb_decode", "kvb_short_ctx", "kvb_flush", "kvb_verify",
-           "kvb_accept", "kvb_get_lengths", "kvb_get_device_lengths", "kvb_get_error",
+           "kvb_accept", "kvb_verify_tempstate", "kvb_accept_tempstate", "kvb_get_lengths", "kvb_get_device_lengths", "kvb_get_error",
            "kvb_strerror", "kvb_copy_probe", "kvb_version")
 
 
@@ -82,6 +82,9 @@ def load_library(path: str = LIB_PATH):
         "kvb_flush": (ctypes.c_int, [_P, _I32, _I32P, _P]),
         "kvb_verify": (ctypes.c_int, [_P, _I32, _I32, _I32P, _P, _P, _P, _P, _P, _P, _P]),
         "kvb_accept": (ctypes.c_int, [_P, _I32, _I32P, _I32P, _P]),
+        "kvb_verify_tempstate": (ctypes.c_int, [_P, _I32, _I32, _I32P, _P, _P, _P, _P, _P, _P, _P,
+                                                _P]),
+        "kvb_accept_tempstate": (ctypes.c_int, [_P, _I32, _I32, _I32P, _I32P, _P, _P]),
         "kvb_get_lengths": (ctypes.c_int, [_P, _I32P]),
         "kvb_get_device_lengths": (ctypes.c_int, [_P, _I32P, _P]),
         "kvb_get_error": (ctypes.c_int, [_P, _P, _I32P]),
@@ -269,6 +272,33 @@ class Pool:
         if len(acc) != len(ids):
             raise ValueError("n_accepted must have one entry per request")
         _check(self.lib.kvb_accept(self.handle, len(ids), p, pa, self._stream()), "kvb_accept")
+
+    def verify_tempstate(self, req_ids, q, k, v, log_g=None, beta=None, temp=None, o=None):
+        """The recurrent verify of the comparison baseline: returns (o, temp) where temp
+        [B, T, Hv, d_k, d_v] holds the state after each draft."""
+        ids, p = _i32(req_ids)
+        B, T = len(ids), q.shape[1]
+        c = self.cfg
+        if o is None:
+            o = self.torch.empty(B, T, c.n_v_heads, c.d_v, dtype=self.torch.float32,
+                                 device=self.device)
+        if temp is None:
+            temp = self.torch.empty(B, T, c.n_v_heads, c.d_k, c.d_v, dtype=self.torch.float32,
+                                    device=self.device)
+        ptrs = self._token_ptrs((B, T), q, k, v, log_g, beta, o)
+        tp = self._ptr(temp, self.torch.float32, (B, T, c.n_v_heads, c.d_k, c.d_v), "temp")
+        _check(self.lib.kvb_verify_tempstate(self.handle, B, T, p, *ptrs, tp, self._stream()),
+               "kvb_verify_tempstate")
+        return o, temp
+
+    def accept_tempstate(self, req_ids, n_accepted, temp):
+        ids, p = _i32(req_ids)
+        acc, pa = _i32(n_accepted)
+        B, T = len(ids), temp.shape[1]
+        c = self.cfg
+        tp = self._ptr(temp, self.torch.float32, (B, T, c.n_v_heads, c.d_k, c.d_v), "temp")
+        _check(self.lib.kvb_accept_tempstate(self.handle, B, T, p, pa, tp, self._stream()),
+               "kvb_accept_tempstate")
 
     def get_lengths(self) -> np.ndarray:
         out = np.zeros(self.cfg.max_requests, dtype=np.int32)
