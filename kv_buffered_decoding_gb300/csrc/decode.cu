@@ -93,7 +93,15 @@ __global__ void __launch_bounds__(2 * D / NSPLIT, 512 / (2 * D / NSPLIT))
   __syncthreads();
   if (!RECURRENT && bad) return;  // CTA-uniform
 
-  // this lane's first buffered token's u (token rsub), fetched before the mat-vec
+  // 3. issue every small load this thread needs after the mat-vec: the keys of its
+  //    warp's first dot-product pass, its first buffered u, and (warp 0) the
+  //    cumulative gates; their latency then overlaps the state tile's arrival
+  const int p0 = 2 * warp, p1 = p0 + 1;
+  float ka[E], kb[E];
+#pragma unroll
+  for (int e = 0; e < E; ++e) ka[e] = kb[e] = 0.f;
+  if (p0 < n) load_row<E>(static_cast<const KT *>(P.kbuf) + koff[p0] + lane * E, ka);
+  if (p1 < n) load_row<E>(static_cast<const KT *>(P.kbuf) + koff[p1] + lane * E, kb);
   float4 u_first = f4(0.f);
   if (!RECURRENT && rsub < n) {
     if (DELTA)
@@ -101,15 +109,40 @@ __global__ void __launch_bounds__(2 * D / NSPLIT, 512 / (2 * D / NSPLIT))
     else
       u_first = ld4(static_cast<const KT *>(P.vbuf) + voff[rsub] * DV + col0);
   }
+  float Ai0 = 0.f, Ai1 = 0.f;  // warp 0: cumulative gates of tokens lane, lane + 32
+  if (GATED && warp == 0) {
+    if (lane < n) Ai0 = P.gbuf[voff[lane]];
+    if (lane + 32 < n) Ai1 = P.gbuf[voff[lane + 32]];
+  }
 
-  // 3. decay weights (warp 0): the buffer stores each token's cumulative log-gate
+  // 4. S0^T q_t (and S0^T k_t) over this thread's rows, operands four rows at a time
+  float4 aq = f4(0.f), ak = f4(0.f);
+  if (has_state) {
+#pragma unroll
+    for (int j = 0; j < RPT; j += 4) {
+      const float4 q4 = *reinterpret_cast<const float4 *>(&qs[row0 + j]);
+      fma4(aq, q4.x, s[j]);
+      fma4(aq, q4.y, s[j + 1]);
+      fma4(aq, q4.z, s[j + 2]);
+      fma4(aq, q4.w, s[j + 3]);
+      if (DELTA) {
+        const float4 k4 = *reinterpret_cast<const float4 *>(&kts[row0 + j]);
+        fma4(ak, k4.x, s[j]);
+        fma4(ak, k4.y, s[j + 1]);
+        fma4(ak, k4.z, s[j + 2]);
+        fma4(ak, k4.w, s[j + 3]);
+      }
+    }
+  }
+
+  // 5. decay weights (warp 0): the buffer stores each token's cumulative log-gate
   //    since the last fold, so A_t = A_{n-1} + a_t and w_i = e^{A_t - A_i}
   float At = 0.f;
   if (GATED) {
     if (warp == 0) {
-      const float A_prev = n > 0 ? P.gbuf[voff[n - 1]] : 0.f;
+      const float A_prev = n > 0 ? __shfl_sync(kFull, n - 1 < 32 ? Ai0 : Ai1, (n - 1) & 31) : 0.f;
       At = A_prev + a_t;
-      for (int i = lane; i <= n; i += 32) wt[i] = expf(At - (i < n ? P.gbuf[voff[i]] : At));
+      for (int i = lane; i <= n; i += 32) wt[i] = expf(At - (i < n ? (i < 32 ? Ai0 : Ai1) : At));
       if (lane == 0) e_t_s = expf(At);
     }
   } else {
@@ -117,21 +150,21 @@ __global__ void __launch_bounds__(2 * D / NSPLIT, 512 / (2 * D / NSPLIT))
     if (tid == 0) e_t_s = 1.f;
   }
   //    dot products q.k_i (and k_t.k_i), two tokens per warp pass, one butterfly
-  //    reduction for all of a pass's sums
-  for (int i0 = 2 * warp; i0 <= n; i0 += 2 * NW) {
+  //    reduction for all of a pass's sums; the first pass's keys are already loaded
+  for (int i0 = p0; i0 <= n; i0 += 2 * NW) {
     const int i1 = i0 + 1;
-    float ka[E], kb[E], qv[E], tv[E];
+    float qv[E], tv[E];
     load_smem<E>(qs + lane * E, qv);
     load_smem<E>(kts + lane * E, tv);
-    if (i0 < n) {
-      load_row<E>(static_cast<const KT *>(P.kbuf) + koff[i0] + lane * E, ka);
-    } else {
+    if (i0 != p0) {
+      if (i0 < n) load_row<E>(static_cast<const KT *>(P.kbuf) + koff[i0] + lane * E, ka);
+      if (i1 < n) load_row<E>(static_cast<const KT *>(P.kbuf) + koff[i1] + lane * E, kb);
+    }
+    if (i0 == n) {
 #pragma unroll
       for (int e = 0; e < E; ++e) ka[e] = tv[e];
     }
-    if (i1 < n) {
-      load_row<E>(static_cast<const KT *>(P.kbuf) + koff[i1] + lane * E, kb);
-    } else {
+    if (i1 >= n) {
 #pragma unroll
       for (int e = 0; e < E; ++e) kb[e] = (i1 == n) ? tv[e] : 0.f;
     }
@@ -168,27 +201,7 @@ __global__ void __launch_bounds__(2 * D / NSPLIT, 512 / (2 * D / NSPLIT))
   }
   __syncthreads();
 
-  // 4. S0^T q_t (and S0^T k_t) over this thread's rows, operands four rows at a time
-  float4 aq = f4(0.f), ak = f4(0.f);
-  if (has_state) {
-#pragma unroll
-    for (int j = 0; j < RPT; j += 4) {
-      const float4 q4 = *reinterpret_cast<const float4 *>(&qs[row0 + j]);
-      fma4(aq, q4.x, s[j]);
-      fma4(aq, q4.y, s[j + 1]);
-      fma4(aq, q4.z, s[j + 2]);
-      fma4(aq, q4.w, s[j + 3]);
-      if (DELTA) {
-        const float4 k4 = *reinterpret_cast<const float4 *>(&kts[row0 + j]);
-        fma4(ak, k4.x, s[j]);
-        fma4(ak, k4.y, s[j + 1]);
-        fma4(ak, k4.z, s[j + 2]);
-        fma4(ak, k4.w, s[j + 3]);
-      }
-    }
-  }
-
-  // 5. add this lane's share of the buffered tokens' terms, then one reduction over
+  // 6. add this lane's share of the buffered tokens' terms, then one reduction over
   //    the 8 row lanes for both: o_part = e^{A_t} S0^T q + sum_i w_i (q.k_i) u_i
   const float e_t = e_t_s;
   float4 po = mul4(e_t, aq), pc = mul4(e_t, ak);
@@ -234,7 +247,7 @@ __global__ void __launch_bounds__(2 * D / NSPLIT, 512 / (2 * D / NSPLIT))
     }
   }
 
-  // 6. fold: S <- e^{A_t} S0 + sum_{i<=n} k_i (w_i u_i)^T, a rank-(n+1) update of the
+  // 7. fold: S <- e^{A_t} S0 + sum_{i<=n} k_i (w_i u_i)^T, a rank-(n+1) update of the
   //    register tile, written back once
   if (fold && has_state) {
     __syncthreads();
