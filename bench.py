@@ -339,6 +339,28 @@ def measure_paths(kvb, torch, dev, peak):
         base.close()
     out["verify_vs_tempstate_gated_delta_B256"] = cmp
 
+    # Figure 3 of the page: decode latency averaged over a full buffer cycle
+    # (occupancies 0..m-1 and the fold) for each buffer size m, normalised to m = 0
+    # (recurrent decoding); scalar-gated layer, 16 heads, d = 128, B = 256 and the
+    # 32-request batch of the sweep workload (whose 32 MiB of state stays in L2)
+    for B in (256, 32):
+        L = I.GATED_LAYER
+        sweep = {}
+        for m in (0, 2, 4, 8, 16):
+            nbpr = max(1, -(-m // 8))
+            pool = pool_for(L, B, m, nbpr)
+            req = np.arange(B, dtype=np.int32)
+            toks = tokens(L, (B,), 20 + m)
+            cycle = max(m, 1)
+            us = timed(lambda: pool.decode(req, *toks), 8 * cycle)
+            sweep[str(m)] = us
+            pool.close()
+        out["fig3_gated_B%d" % B] = {
+            "us_per_step": sweep,
+            "normalised_to_m0": {m_: v / sweep["0"] for m_, v in sweep.items()},
+            "note": "timed over whole cycles from a cycle-aligned start (every request folds "
+                    "on the same step); state %d MiB" % (B * L.n_v_heads * L.d_k * L.d_v * 4 >> 20)}
+
     # flush: 8 buffered tokens per request folded into the state (gated delta, B=256)
     L, B = I.GDN_LAYER, 256
     pool = pool_for(L, B, 8, 1)
