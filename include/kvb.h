@@ -221,6 +221,28 @@ int kvb_accept_tempstate(kvb_pool *pool, int32_t B, int32_t T, const int32_t *re
                          const int32_t *n_accepted, const float *temp_states,
                          kvb_stream_t stream);
 
+/* Allocation-free kvb_verify_tempstate, for callers that cannot allocate device
+   memory: an engine whose memory planner has already handed all device memory
+   out, or code that must not call cudaMalloc because it synchronizes the device
+   inside a latency-critical loop.  The paper has no counterpart; this is a
+   library convenience.  The temporary states live in a fixed array inside the
+   library (KVB_STATIC_TEMP_BYTES of device memory, held by every GPU that loads
+   the library until the process exits), so B * T * n_v_heads * d_k * d_v * 4
+   bytes must fit in it (KVB_E_CAPACITY otherwise, before anything runs).
+   Inputs, o and the rules are those of kvb_verify_tempstate.  n_accepted (host,
+   may be NULL) applies kvb_accept_tempstate in the same call: request
+   req_ids[b] takes the state after its first n_accepted[b] drafts.
+   The first call on a device looks up the array's device address; make it
+   before any stream capture.  All calls share the array and it keeps the last
+   call's contents (every temporary state is written before it is read, so
+   nothing needs clearing); calls whose GPU work overlaps, from other streams or
+   threads, race on it.  Calls no allocator. */
+#define KVB_STATIC_TEMP_BYTES ((size_t)64 << 20)
+int kvb_verify_tempstate_static(kvb_pool *pool, int32_t B, int32_t T, const int32_t *req_ids,
+                                const void *q, const void *k, const void *v, const float *log_g,
+                                const float *beta, float *o, const int32_t *n_accepted,
+                                kvb_stream_t stream);
+
 /* Host copy of every request's buffer length (max_requests int32). Host only,
    no synchronization: the host keeps an exact mirror of the device lengths. */
 int kvb_get_lengths(const kvb_pool *pool, int32_t *host_out);

@@ -14,6 +14,8 @@
 // and every S_j is written to its temporary slot: T state writes per round,
 // the traffic (and memory) the buffered verify avoids.
 // tempstate_accept_kernel copies temporary state j-1 into the request's slot.
+#include <mutex>
+
 #include "kvb_device.cuh"
 
 namespace kvb {
@@ -168,6 +170,52 @@ cudaError_t launch_accept_tempstate(const PoolView &P, const RowBatch &rows, con
   dim3 grid(P.Hv, rows.count);
   tempstate_accept_kernel<<<grid, 256, 0, stream>>>(P, rows, temp, T, d, d);
   return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------ no allocation
+// Temporary states for kvb_verify_tempstate_static: a fixed array inside the
+// library, for callers that cannot allocate device memory.  Every GPU that
+// loads the library holds it until the process exits.
+constexpr size_t kStaticTempFloats = (size_t)KVB_STATIC_TEMP_BYTES / sizeof(float);
+static __device__ __align__(256) float g_static_temp[kStaticTempFloats];
+
+// Device address of g_static_temp on the current device.  Host code cannot use
+// the array's name as a device address, so it is looked up once per device
+// (with that device current) and cached.
+static cudaError_t static_temp_address(float **out) {
+  constexpr int kMaxDevices = 64;
+  static std::mutex mu;
+  static float *addr[kMaxDevices] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!addr[dev]) {
+    void *p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_static_temp);
+    if (e != cudaSuccess) return e;
+    addr[dev] = static_cast<float *>(p);
+  }
+  *out = addr[dev];
+  return cudaSuccess;
+}
+
+cudaError_t launch_verify_tempstate_static(const PoolView &P, const RowBatch &rows,
+                                           const TokenIO &io, int variant, int dtype, int d,
+                                           cudaStream_t stream) {
+  float *temp = nullptr;
+  cudaError_t e = static_temp_address(&temp);
+  if (e != cudaSuccess) return e;
+  return launch_verify_tempstate(P, rows, io, variant, dtype, d, temp, stream);
+}
+
+cudaError_t launch_accept_tempstate_static(const PoolView &P, const RowBatch &rows, int T, int d,
+                                           cudaStream_t stream) {
+  float *temp = nullptr;
+  cudaError_t e = static_temp_address(&temp);
+  if (e != cudaSuccess) return e;
+  return launch_accept_tempstate(P, rows, temp, T, d, stream);
 }
 
 }  // namespace kvb

@@ -505,6 +505,55 @@ int kvb_accept_tempstate(kvb_pool *p, int32_t B, int32_t T, const int32_t *req_i
   return KVB_OK;
 }
 
+int kvb_verify_tempstate_static(kvb_pool *p, int32_t B, int32_t T, const int32_t *req_ids,
+                                const void *q, const void *k, const void *v, const float *log_g,
+                                const float *beta, float *o, const int32_t *n_accepted,
+                                kvb_stream_t stream) {
+  if (!p) return KVB_E_ARG;
+  if (p->cfg.m != 0) return KVB_E_STATE;
+  if (T < 1 || T > KVB_MAX_DRAFTS) return KVB_E_ARG;
+  int st = check_reqs(p, B, req_ids);
+  if (st || B == 0) return st;
+  if ((st = check_io(p, q, k, v, log_g, beta, o))) return st;
+  const kvb_config &c = p->cfg;
+  const size_t need = (size_t)B * T * c.n_v_heads * c.d_k * c.d_v * sizeof(float);
+  if (need > KVB_STATIC_TEMP_BYTES) return KVB_E_CAPACITY;
+  for (int32_t b = 0; b < B; ++b) {
+    if (p->slot[req_ids[b]] < 0) return KVB_E_STATE;
+    if (n_accepted && (n_accepted[b] < 0 || n_accepted[b] > T)) return KVB_E_ARG;
+  }
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const kvb::TokenIO io{q, k, v, log_g, beta, o, T, 0};
+  for (int32_t base = 0; base < B; base += kvb::kMaxRows) {
+    const int32_t cnt = B - base < kvb::kMaxRows ? B - base : kvb::kMaxRows;
+    p->rows.count = cnt;
+    p->rows.row0 = base;
+    for (int32_t i = 0; i < cnt; ++i) p->rows.r[i] = make_row(p, req_ids[base + i], 0, 0);
+    cudaError_t e = kvb::launch_verify_tempstate_static(p->view, p->rows, io, c.variant,
+                                                        c.kv_dtype, c.d_k, s);
+    if (e != cudaSuccess) return cuda_status(e);
+  }
+  if (!n_accepted) return KVB_OK;
+  // rows that accepted something take their temporary state; consecutive rows per launch
+  int32_t i = 0;
+  for (int32_t b = 0; b < B; ++b) {
+    if (n_accepted[b] == 0) continue;
+    if (i == kvb::kMaxRows || (i > 0 && b != p->rows.row0 + i)) {
+      cudaError_t e = kvb::launch_accept_tempstate_static(p->view, p->rows, T, c.d_k, s);
+      if (e != cudaSuccess) return cuda_status(e);
+      i = 0;
+    }
+    if (i == 0) p->rows.row0 = b;
+    p->rows.r[i++] = make_row(p, req_ids[b], n_accepted[b], 0);
+    p->rows.count = i;
+  }
+  if (i > 0) {
+    cudaError_t e = kvb::launch_accept_tempstate_static(p->view, p->rows, T, c.d_k, s);
+    if (e != cudaSuccess) return cuda_status(e);
+  }
+  return KVB_OK;
+}
+
 int kvb_get_lengths(const kvb_pool *p, int32_t *host_out) {
   if (!p || !host_out) return KVB_E_ARG;
   std::memcpy(host_out, p->len.data(), p->len.size() * sizeof(int32_t));

@@ -7,6 +7,8 @@
 
 #include <cuda_runtime_api.h>
 
+#include "kvb.h"
+
 namespace kvb {
 
 // Most batch rows one launch carries in its parameter block; longer batches
@@ -78,6 +80,13 @@ cudaError_t launch_verify_tempstate(const PoolView &P, const RowBatch &rows, con
                                     cudaStream_t stream);
 cudaError_t launch_accept_tempstate(const PoolView &P, const RowBatch &rows, const float *temp,
                                     int T, int d, cudaStream_t stream);
+// The same two launches with the temporary states in the library's fixed
+// device array (kvb_verify_tempstate_static).
+cudaError_t launch_verify_tempstate_static(const PoolView &P, const RowBatch &rows,
+                                           const TokenIO &io, int variant, int dtype, int d,
+                                           cudaStream_t stream);
+cudaError_t launch_accept_tempstate_static(const PoolView &P, const RowBatch &rows, int T, int d,
+                                           cudaStream_t stream);
 cudaError_t launch_set_lengths(const PoolView &P, const RowBatch &rows, cudaStream_t stream);
 cudaError_t launch_copy_probe(const void *src, void *dst, size_t bytes, cudaStream_t stream);
 

@@ -26,11 +26,13 @@ KVB_PLAIN, KVB_GATED, KVB_GATED_DELTA = 0, 1, 2
 KVB_F32, KVB_BF16 = 0, 1
 KVB_MAX_CAPACITY = 64
 KVB_MAX_DRAFTS = 64
+KVB_STATIC_TEMP_BYTES = 64 << 20
 
 # every symbol include/kvb.h declares
 EXPORTS = ("kvb_pool_layout", "kvb_alloc_pool", "kvb_free_pool", "kvb_set_request",
            "kvb_release_request", "kvb_decode", "kvb_short_ctx", "kvb_flush", "kvb_verify",
-           "kvb_accept", "kvb_verify_tempstate", "kvb_accept_tempstate", "kvb_get_lengths", "kvb_get_device_lengths", "kvb_get_error",
+           "kvb_accept", "kvb_verify_tempstate", "kvb_accept_tempstate",
+           "kvb_verify_tempstate_static", "kvb_get_lengths", "kvb_get_device_lengths", "kvb_get_error",
            "kvb_strerror", "kvb_copy_probe", "kvb_version")
 
 
@@ -85,6 +87,8 @@ def load_library(path: str = LIB_PATH):
         "kvb_verify_tempstate": (ctypes.c_int, [_P, _I32, _I32, _I32P, _P, _P, _P, _P, _P, _P, _P,
                                                 _P]),
         "kvb_accept_tempstate": (ctypes.c_int, [_P, _I32, _I32, _I32P, _I32P, _P, _P]),
+        "kvb_verify_tempstate_static": (ctypes.c_int, [_P, _I32, _I32, _I32P, _P, _P, _P, _P, _P,
+                                                       _P, _I32P, _P]),
         "kvb_get_lengths": (ctypes.c_int, [_P, _I32P]),
         "kvb_get_device_lengths": (ctypes.c_int, [_P, _I32P, _P]),
         "kvb_get_error": (ctypes.c_int, [_P, _P, _I32P]),
@@ -299,6 +303,25 @@ class Pool:
         tp = self._ptr(temp, self.torch.float32, (B, T, c.n_v_heads, c.d_k, c.d_v), "temp")
         _check(self.lib.kvb_accept_tempstate(self.handle, B, T, p, pa, tp, self._stream()),
                "kvb_accept_tempstate")
+
+    def verify_tempstate_static(self, req_ids, q, k, v, log_g=None, beta=None, o=None,
+                                n_accepted=None):
+        """kvb_verify_tempstate_static: the baseline verify with the temporary states in
+        the library's fixed device array (no allocation); optional accept in the same call."""
+        ids, p = _i32(req_ids)
+        B, T = len(ids), q.shape[1]
+        c = self.cfg
+        if o is None:
+            o = self.torch.empty(B, T, c.n_v_heads, c.d_v, dtype=self.torch.float32,
+                                 device=self.device)
+        ptrs = self._token_ptrs((B, T), q, k, v, log_g, beta, o)
+        acc_p = None
+        if n_accepted is not None:
+            acc, acc_p = _i32(n_accepted)
+        _check(self.lib.kvb_verify_tempstate_static(self.handle, B, T, p, *ptrs, acc_p,
+                                                    self._stream()),
+               "kvb_verify_tempstate_static")
+        return o
 
     def get_lengths(self) -> np.ndarray:
         out = np.zeros(self.cfg.max_requests, dtype=np.int32)
