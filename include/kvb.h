@@ -180,6 +180,21 @@ int kvb_short_ctx(kvb_pool *pool, int32_t B, const int32_t *req_ids, const void 
    KVB_E_STATE. */
 int kvb_flush(kvb_pool *pool, int32_t n_req, const int32_t *req_ids, kvb_stream_t stream);
 
+/* Short-to-long promotion: a short-context request (no state slot) that is
+   to continue past what its buffer holds is given its own state.  Short
+   requests are served from buffered keys and values alone, with no state
+   (abstract); this call creates the state at the point where that stops:
+   request req_ids[b] takes the free state slot state_slots[b] (host array),
+   its buffered tokens are folded into that slot starting from S = 0 (the
+   Figure 1 state update with an all-zero state), and its buffer is emptied.
+   A request with an empty buffer gets an all-zero state.  Afterwards the
+   request is a state-backed request like any other (kvb_decode, kvb_verify,
+   kvb_flush) and keeps its blocks as its buffer.
+   Errors: KVB_E_STATE if a request already has a state or has a pending
+   verify; KVB_E_RANGE if a slot is out of range, owned, or listed twice. */
+int kvb_promote(kvb_pool *pool, int32_t B, const int32_t *req_ids, const int32_t *state_slots,
+                kvb_stream_t stream);
+
 /* Verify T draft tokens per request in parallel (Figure 2: the drafts' KVs go
    into the buffer and no temporary state is stored).  Inputs are laid out
    [B][T][heads][dim] (log_g, beta: [B][T][n_v_heads]); o: [B][T][n_v_heads][d_v].

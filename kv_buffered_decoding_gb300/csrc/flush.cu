@@ -13,8 +13,9 @@
 // per element (read + write), i.e. below the fp32 FMA ridge: the kernel is
 // bound by HBM, and the update runs on the FMA pipes.
 //
-// Used by kvb_flush and by kvb_accept when accepted drafts fill the buffer;
-// decode folds in-kernel (decode.cu).
+// Used by kvb_flush, by kvb_accept when accepted drafts fill the buffer and by
+// kvb_promote (rows flagged kFlagFromZero start from S = 0); decode folds
+// in-kernel (decode.cu).
 #include "kvb_device.cuh"
 
 namespace kvb {
@@ -43,8 +44,13 @@ __global__ void __launch_bounds__(2 * D / NSPLIT, 512 / (2 * D / NSPLIT))
 
   float *Sp = P.state + ((size_t)d.slot * P.Hv + h) * DK * DV;
   float4 s[RPT];
+  if (d.flags & kFlagFromZero) {  // promotion: the slot's contents are not a state yet
 #pragma unroll
-  for (int j = 0; j < RPT; ++j) s[j] = ld_stream4(Sp + (row0 + j) * DV + col0);
+    for (int j = 0; j < RPT; ++j) s[j] = f4(0.f);
+  } else {
+#pragma unroll
+    for (int j = 0; j < RPT; ++j) s[j] = ld_stream4(Sp + (row0 + j) * DV + col0);
+  }
 
   if (warp == 0) {
     int anybad = 0;

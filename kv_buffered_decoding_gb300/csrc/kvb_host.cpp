@@ -201,7 +201,8 @@ int decode_like(kvb_pool *p, int32_t B, const int32_t *req_ids, const void *q, c
   return KVB_OK;
 }
 
-int launch_fold(kvb_pool *p, const std::vector<int32_t> &reqs, cudaStream_t stream) {
+int launch_fold(kvb_pool *p, const std::vector<int32_t> &reqs, cudaStream_t stream,
+                int32_t flags = 0) {
   const kvb_config &c = p->cfg;
   for (size_t base = 0; base < reqs.size(); base += kvb::kMaxRows) {
     const size_t cnt = reqs.size() - base < (size_t)kvb::kMaxRows ? reqs.size() - base : kvb::kMaxRows;
@@ -210,7 +211,7 @@ int launch_fold(kvb_pool *p, const std::vector<int32_t> &reqs, cudaStream_t stre
     int lmax = 0;
     for (size_t i = 0; i < cnt; ++i) {
       const int32_t r = reqs[base + i];
-      p->rows.r[i] = make_row(p, r, p->len[r], 0);
+      p->rows.r[i] = make_row(p, r, p->len[r], flags);
       if (p->len[r] > lmax) lmax = p->len[r];
     }
     cudaError_t e = kvb::launch_flush(p->view, p->rows, c.variant, c.kv_dtype, c.d_k, lmax, stream);
@@ -372,6 +373,37 @@ int kvb_flush(kvb_pool *p, int32_t n_req, const int32_t *req_ids, kvb_stream_t s
     if (p->len[r] > 0) todo.push_back(r);
   }
   return launch_fold(p, todo, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int kvb_promote(kvb_pool *p, int32_t B, const int32_t *req_ids, const int32_t *state_slots,
+                kvb_stream_t stream) {
+  if (!p) return KVB_E_ARG;
+  int st = check_reqs(p, B, req_ids);
+  if (st || B == 0) return st;
+  if (!state_slots) return KVB_E_ARG;
+  const kvb_config &c = p->cfg;
+  for (int32_t b = 0; b < B; ++b) {
+    const int32_t r = req_ids[b], sl = state_slots[b];
+    if (p->slot[r] >= 0 || p->pending_T[r]) return KVB_E_STATE;
+    if (sl < 0 || sl >= c.num_state_slots || p->slot_owner[sl] >= 0) return KVB_E_RANGE;
+    for (int32_t j = 0; j < b; ++j)
+      if (state_slots[j] == sl) return KVB_E_RANGE;
+  }
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const size_t state_bytes = (size_t)c.n_v_heads * c.d_k * c.d_v * sizeof(float);
+  std::vector<int32_t> fold;
+  for (int32_t b = 0; b < B; ++b) {
+    const int32_t r = req_ids[b], sl = state_slots[b];
+    p->slot[r] = sl;
+    p->slot_owner[sl] = r;
+    if (p->len[r] > 0) {
+      fold.push_back(r);
+    } else if (cudaMemsetAsync(p->view.state + (size_t)sl * state_bytes / sizeof(float), 0,
+                               state_bytes, s) != cudaSuccess) {
+      return KVB_E_CUDA;
+    }
+  }
+  return launch_fold(p, fold, s, kvb::kFlagFromZero);
 }
 
 int kvb_verify(kvb_pool *p, int32_t B, int32_t T, const int32_t *req_ids, const void *q,

@@ -41,6 +41,7 @@ struct RowDesc {
   int32_t blk[kRowBlocks];
 };
 constexpr int32_t kFlagFlush = 1;  // decode: fold the buffer (incl. this token) into S
+constexpr int32_t kFlagFromZero = 2;  // flush: start from S = 0 instead of the slot's state
 
 // Rows of one launch, passed by value in the kernel parameter block.
 struct RowBatch {

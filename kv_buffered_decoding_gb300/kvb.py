@@ -30,7 +30,8 @@ KVB_STATIC_TEMP_BYTES = 64 << 20
 
 # every symbol include/kvb.h declares
 EXPORTS = ("kvb_pool_layout", "kvb_alloc_pool", "kvb_free_pool", "kvb_set_request",
-           "kvb_release_request", "kvb_decode", "kvb_short_ctx", "kvb_flush", "kvb_verify",
+           "kvb_release_request", "kvb_decode", "kvb_short_ctx", "kvb_flush", "kvb_promote",
+           "kvb_verify",
            "kvb_accept", "kvb_verify_tempstate", "kvb_accept_tempstate",
            "kvb_verify_tempstate_static", "kvb_get_lengths", "kvb_get_device_lengths", "kvb_get_error",
            "kvb_strerror", "kvb_copy_probe", "kvb_version")
@@ -87,6 +88,7 @@ def load_library(path: str = LIB_PATH):
         "kvb_verify_tempstate": (ctypes.c_int, [_P, _I32, _I32, _I32P, _P, _P, _P, _P, _P, _P, _P,
                                                 _P]),
         "kvb_accept_tempstate": (ctypes.c_int, [_P, _I32, _I32, _I32P, _I32P, _P, _P]),
+        "kvb_promote": (ctypes.c_int, [_P, _I32, _I32P, _I32P, _P]),
         "kvb_verify_tempstate_static": (ctypes.c_int, [_P, _I32, _I32, _I32P, _P, _P, _P, _P, _P,
                                                        _P, _I32P, _P]),
         "kvb_get_lengths": (ctypes.c_int, [_P, _I32P]),
@@ -276,6 +278,15 @@ class Pool:
         if len(acc) != len(ids):
             raise ValueError("n_accepted must have one entry per request")
         _check(self.lib.kvb_accept(self.handle, len(ids), p, pa, self._stream()), "kvb_accept")
+
+    def promote(self, req_ids, state_slots):
+        """kvb_promote: give short-context requests a state slot, folding their buffered
+        tokens into it from S = 0."""
+        ids, p = _i32(req_ids)
+        sl, ps = _i32(state_slots)
+        if len(sl) != len(ids):
+            raise ValueError("promote: one state slot per request")
+        _check(self.lib.kvb_promote(self.handle, len(ids), p, ps, self._stream()), "kvb_promote")
 
     def verify_tempstate(self, req_ids, q, k, v, log_g=None, beta=None, temp=None, o=None):
         """The recurrent verify of the comparison baseline: returns (o, temp) where temp
