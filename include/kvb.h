@@ -180,6 +180,24 @@ int kvb_short_ctx(kvb_pool *pool, int32_t B, const int32_t *req_ids, const void 
    KVB_E_STATE. */
 int kvb_flush(kvb_pool *pool, int32_t n_req, const int32_t *req_ids, kvb_stream_t stream);
 
+/* Chunked prefill: run each listed request's prompt through its state, 64
+   tokens per chunk, on the tensor cores (the chunkwise form of linear
+   attention that KVBuffer's buffer also uses; abstract).  Request req_ids[b]
+   processes lengths[b] tokens (host array; NULL means L each, 0 <= lengths[b]
+   <= L) taken from inputs laid out [B][L][heads][dim] (log_g, beta:
+   [B][L][n_v_heads]); o: [B][L][n_v_heads][d_v] fp32 receives every prompt
+   token's output (rows past lengths[b] are not written).  The state starts
+   from the request's slot, or from S = 0 when from_zero is nonzero (a new
+   request; then the slot's contents are never read), and holds the state
+   after the prompt when the call completes.  Requires a state slot, an empty
+   buffer and no pending verify (KVB_E_STATE otherwise: flush first), and
+   d_k = d_v in {64, 128} (KVB_E_UNSUPPORTED otherwise).  The buffer is not
+   touched. */
+int kvb_prefill(kvb_pool *pool, int32_t B, int32_t L, const int32_t *req_ids,
+                const int32_t *lengths, const void *q, const void *k, const void *v,
+                const float *log_g, const float *beta, float *o, int32_t from_zero,
+                kvb_stream_t stream);
+
 /* Short-to-long promotion: a short-context request (no state slot) that is
    to continue past what its buffer holds is given its own state.  Short
    requests are served from buffered keys and values alone, with no state

@@ -201,4 +201,28 @@ __device__ __forceinline__ void warp_prefix(int count, GateFn gate, float *A, in
   }
 }
 
+// ------------------------------------------------------------------ tensor cores
+// tf32 value of x, rounded to nearest (ties away): the operand form of
+// mma.sync kind tf32, which reads the top 19 bits of a 32-bit register.
+__device__ __forceinline__ uint32_t to_tf32(float x) {
+  uint32_t r;
+  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+  return r;
+}
+// x = hi + lo with hi, lo tf32: a product of two such pairs, summed as
+// hi*hi + hi*lo + lo*hi, keeps about 21 significant bits (fp32-like).
+__device__ __forceinline__ void split_tf32(float x, uint32_t &hi, uint32_t &lo) {
+  hi = to_tf32(x);
+  lo = to_tf32(x - __uint_as_float(hi));
+}
+// d += a b for a 16x8 tile, k = 8, tf32 operands, fp32 accumulation.
+__device__ __forceinline__ void mma_tf32(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                         uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
 }  // namespace kvb

@@ -375,6 +375,37 @@ int kvb_flush(kvb_pool *p, int32_t n_req, const int32_t *req_ids, kvb_stream_t s
   return launch_fold(p, todo, reinterpret_cast<cudaStream_t>(stream));
 }
 
+int kvb_prefill(kvb_pool *p, int32_t B, int32_t L, const int32_t *req_ids,
+                const int32_t *lengths, const void *q, const void *k, const void *v,
+                const float *log_g, const float *beta, float *o, int32_t from_zero,
+                kvb_stream_t stream) {
+  if (!p) return KVB_E_ARG;
+  if (L < 0) return KVB_E_ARG;
+  int st = check_reqs(p, B, req_ids);
+  if (st || B == 0) return st;
+  if ((st = check_io(p, q, k, v, log_g, beta, o))) return st;
+  const kvb_config &c = p->cfg;
+  if (c.d_k != c.d_v || (c.d_k != 64 && c.d_k != 128)) return KVB_E_UNSUPPORTED;
+  for (int32_t b = 0; b < B; ++b) {
+    const int32_t r = req_ids[b];
+    if (p->slot[r] < 0 || p->len[r] != 0 || p->pending_T[r]) return KVB_E_STATE;
+    if (lengths && (lengths[b] < 0 || lengths[b] > L)) return KVB_E_ARG;
+  }
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const kvb::TokenIO io{q, k, v, log_g, beta, o, L, 0};
+  const int32_t flags = from_zero ? kvb::kFlagFromZero : 0;
+  for (int32_t base = 0; base < B; base += kvb::kMaxRows) {
+    const int32_t cnt = B - base < kvb::kMaxRows ? B - base : kvb::kMaxRows;
+    p->rows.count = cnt;
+    p->rows.row0 = base;
+    for (int32_t i = 0; i < cnt; ++i)
+      p->rows.r[i] = make_row(p, req_ids[base + i], lengths ? lengths[base + i] : L, flags);
+    cudaError_t e = kvb::launch_prefill(p->view, p->rows, io, c.variant, c.kv_dtype, c.d_k, s);
+    if (e != cudaSuccess) return cuda_status(e);
+  }
+  return KVB_OK;
+}
+
 int kvb_promote(kvb_pool *p, int32_t B, const int32_t *req_ids, const int32_t *state_slots,
                 kvb_stream_t stream) {
   if (!p) return KVB_E_ARG;

@@ -88,6 +88,9 @@ cudaError_t launch_verify_tempstate_static(const PoolView &P, const RowBatch &ro
                                            cudaStream_t stream);
 cudaError_t launch_accept_tempstate_static(const PoolView &P, const RowBatch &rows, int T, int d,
                                            cudaStream_t stream);
+// Chunked prefill of rows.r[i].n prompt tokens per row (io.T = padded length).
+cudaError_t launch_prefill(const PoolView &P, const RowBatch &rows, const TokenIO &io,
+                           int variant, int dtype, int d, cudaStream_t stream);
 cudaError_t launch_set_lengths(const PoolView &P, const RowBatch &rows, cudaStream_t stream);
 cudaError_t launch_copy_probe(const void *src, void *dst, size_t bytes, cudaStream_t stream);
 

@@ -310,19 +310,6 @@ __global__ void __launch_bounds__(2 * D / NSPLIT, 512 / (2 * D / NSPLIT))
 // tf32 (cvt.rna, relative error <= 2^-11 per element, about 2^-12 in the
 // outputs); q and k come from bf16 and are exact in tf32.  Used for bf16
 // pools at d = 128; the fp32 path keeps verify_kernel.
-__device__ __forceinline__ uint32_t to_tf32(float x) {
-  uint32_t r;
-  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
-  return r;
-}
-__device__ __forceinline__ void mma_tf32(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
-                                         uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
-      "{%8,%9}, {%0,%1,%2,%3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
 
 template <int VARIANT>
 __global__ void __launch_bounds__(128, 4)

@@ -30,7 +30,8 @@ KVB_STATIC_TEMP_BYTES = 64 << 20
 
 # every symbol include/kvb.h declares
 EXPORTS = ("kvb_pool_layout", "kvb_alloc_pool", "kvb_free_pool", "kvb_set_request",
-           "kvb_release_request", "kvb_decode", "kvb_short_ctx", "kvb_flush", "kvb_promote",
+           "kvb_release_request", "kvb_decode", "kvb_short_ctx", "kvb_flush", "kvb_prefill",
+           "kvb_promote",
            "kvb_verify",
            "kvb_accept", "kvb_verify_tempstate", "kvb_accept_tempstate",
            "kvb_verify_tempstate_static", "kvb_get_lengths", "kvb_get_device_lengths", "kvb_get_error",
@@ -89,6 +90,8 @@ def load_library(path: str = LIB_PATH):
                                                 _P]),
         "kvb_accept_tempstate": (ctypes.c_int, [_P, _I32, _I32, _I32P, _I32P, _P, _P]),
         "kvb_promote": (ctypes.c_int, [_P, _I32, _I32P, _I32P, _P]),
+        "kvb_prefill": (ctypes.c_int, [_P, _I32, _I32, _I32P, _I32P, _P, _P, _P, _P, _P, _P,
+                                       _I32, _P]),
         "kvb_verify_tempstate_static": (ctypes.c_int, [_P, _I32, _I32, _I32P, _P, _P, _P, _P, _P,
                                                        _P, _I32P, _P]),
         "kvb_get_lengths": (ctypes.c_int, [_P, _I32P]),
@@ -278,6 +281,26 @@ class Pool:
         if len(acc) != len(ids):
             raise ValueError("n_accepted must have one entry per request")
         _check(self.lib.kvb_accept(self.handle, len(ids), p, pa, self._stream()), "kvb_accept")
+
+    def prefill(self, req_ids, q, k, v, log_g=None, beta=None, o=None, lengths=None,
+                from_zero=True):
+        """kvb_prefill: run prompts [B, L, heads, dim] through the requests' states in
+        64-token chunks; returns o [B, L, Hv, d_v] (rows past lengths[b] untouched)."""
+        ids, p = _i32(req_ids)
+        B, L = len(ids), q.shape[1]
+        c = self.cfg
+        if o is None:
+            o = self.torch.empty(B, L, c.n_v_heads, c.d_v, dtype=self.torch.float32,
+                                 device=self.device)
+        ptrs = self._token_ptrs((B, L), q, k, v, log_g, beta, o)
+        lp = None
+        if lengths is not None:
+            lens, lp = _i32(lengths)
+            if len(lens) != B:
+                raise ValueError("prefill: one length per request")
+        _check(self.lib.kvb_prefill(self.handle, B, L, p, lp, *ptrs, int(bool(from_zero)),
+                                    self._stream()), "kvb_prefill")
+        return o
 
     def promote(self, req_ids, state_slots):
         """kvb_promote: give short-context requests a state slot, folding their buffered
