@@ -38,6 +38,8 @@ from kv_buffered_decoding_gb300 import inputs as I  # noqa: E402
 WORKLOAD = I.WORKLOADS["gdn_B256_Hk16_Hv32_d128"]
 METRIC = "decode tok/s per layer (B=256, m=8) and achieved HBM GB/s vs peak"
 FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+TF32_PER_BF16 = 1.1 / 2.25  # nominal dense tf32 / bf16 tensor rates of the part
 N_BANK = 8  # distinct input token sets cycled through the timed steps
 
 
@@ -80,6 +82,41 @@ def hbm_peak():
         except (OSError, ValueError):
             pass
     return FALLBACK_HBM_GBS, "of fallback (6.8 TB/s, no MEASURED_PEAKS.json)"
+
+
+def tensor_peak_tf32():
+    """Dense tf32 tensor peak (TFLOP/s): the measured bf16 GEMM burst rate times the
+    nominal tf32/bf16 ratio, or the fallback bf16 figure times the same ratio."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        try:
+            with open(path) as f:
+                d = json.load(f)
+            for key in ("bf16_tflops", "bf16_TFLOPs", "bf16"):
+                if key in d and isinstance(d[key], (int, float)):
+                    return float(d[key]) * TF32_PER_BF16, \
+                        "of measured bf16 burst x nominal tf32/bf16 ratio"
+        except (OSError, ValueError):
+            pass
+    return FALLBACK_BF16_TFLOPS * TF32_PER_BF16, \
+        "of fallback (1.9 PFLOP/s bf16 x nominal tf32/bf16 ratio)"
+
+
+def prefill_flops(L, n_tokens, chunk=64):
+    """Arithmetic of the chunked form per call: per chunk and value head, Y = [Q; K] S
+    (K rows for the delta rule only), the masked Gram triangles, the forward
+    substitution (delta rule), the intra-chunk output and the state update; two flops
+    per multiply-add.  n_tokens counts the prompt tokens of all requests."""
+    C, dk, dv = chunk, L.d_k, L.d_v
+    delta = L.variant == I.GATED_DELTA
+    tri_incl, tri_strict = C * (C + 1) // 2, C * (C - 1) // 2
+    per_chunk = (2 * (2 if delta else 1) * C * dk * dv      # Y
+                 + 2 * tri_incl * dk                         # Mq
+                 + (2 * tri_strict * dk if delta else 0)     # Mk
+                 + (2 * tri_strict * dv if delta else 0)     # substitution
+                 + 2 * tri_incl * dv                         # O intra-chunk
+                 + 2 * C * dk * dv)                          # state update
+    return per_chunk * (n_tokens / C) * L.n_v_heads
 
 
 def kernel_hash():
@@ -400,6 +437,31 @@ def measure_paths(kvb, torch, dev, peak):
     rec("short_ctx_gated_B256_n32to47", us, int(B * (q + 2 * e + o + mean_n * e)),
         "buffer-only decode, no state; buffer reads dominate")
     pool.close()
+
+    # chunked prefill: 1024-token prompts from S = 0, 32 requests, both layers; bound by
+    # the tensor cores (tf32 mma.sync), reported against the tf32 peak and HBM
+    tf_peak, tf_src = tensor_peak_tf32()
+    for L, tag in ((I.GATED_LAYER, "prefill_gated_B32_L1024"),
+                   (I.GDN_LAYER, "prefill_gated_delta_B32_L1024")):
+        B, Lp = 32, 1024
+        pool = pool_for(L, B, 8, 1)
+        req = np.arange(B, dtype=np.int32)
+        prompt = tokens(L, (B, Lp), 30)
+        o_buf = torch.empty(B, Lp, L.n_v_heads, L.d_v, dtype=torch.float32, device=dev)
+        us = timed(lambda: pool.prefill(req, *prompt, o=o_buf), 5)
+        e = _entry_bytes(L)
+        nbytes = B * Lp * (e + L.n_qk_heads * L.d_k * 2 + L.n_v_heads * L.d_v * 4) \
+            + 2 * B * L.n_v_heads * L.d_k * L.d_v * 4
+        flops = prefill_flops(L, B * Lp)
+        tflops = flops / us / 1e6
+        out[tag] = {"us_per_call": us, "mtok_per_s": B * Lp / us, "tflops": tflops,
+                    "tensor_frac": tflops / tf_peak, "tensor_peak_tflops": tf_peak,
+                    "tensor_peak_source": tf_src, "gbs": nbytes / us / 1e3,
+                    "frac": nbytes / us / 1e3 / peak, "bytes": nbytes, "flops": flops,
+                    "note": "chunk 64, tf32 mma.sync with hi/lo splits (fp32-accurate); "
+                            "algorithmic flops of the chunked form"}
+        del o_buf, prompt
+        pool.close()
     return out
 
 

@@ -215,10 +215,12 @@ __device__ __forceinline__ void split_tf32(float x, uint32_t &hi, uint32_t &lo) 
   hi = to_tf32(x);
   lo = to_tf32(x - __uint_as_float(hi));
 }
-// d += a b for a 16x8 tile, k = 8, tf32 operands, fp32 accumulation.
+// d += a b for a 16x8 tile, k = 8, tf32 operands, fp32 accumulation.  Not
+// volatile: the product has no side effects, so the compiler may interleave
+// independent tiles.
 __device__ __forceinline__ void mma_tf32(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
                                          uint32_t b1) {
-  asm volatile(
+  asm(
       "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
       "{%8,%9}, {%0,%1,%2,%3};"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])

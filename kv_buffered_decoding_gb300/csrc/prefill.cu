@@ -40,8 +40,10 @@ struct PrefillShape {
   static constexpr bool BF16 = sizeof(KT) == 2;
   static constexpr int STAGES = BF16 ? 2 : 1;
   static constexpr int LDI = BF16 ? D + 8 : D + 4;  // input rows, elements (16-byte multiple)
-  static constexpr int LDS = D + 4;                 // fp32 rows of S and U
-  static constexpr int LDX = C + 4;                 // fp32 rows of the packed Gram buffer
+  // fp32 rows of S, U and the Gram buffer: a stride of 8 banks (mod 32) makes
+  // the fragment loads (lane g -> column, lane t -> row) conflict-free
+  static constexpr int LDS = D + 8;
+  static constexpr int LDX = C + 8;
   static constexpr size_t S_OFF = 0;
   static constexpr size_t U_OFF = S_OFF + (size_t)D * LDS * 4;
   static constexpr size_t X_OFF = U_OFF + (size_t)C * LDS * 4;
@@ -83,14 +85,20 @@ __device__ __forceinline__ void operand(float x, uint32_t &hi, uint32_t &lo) {
   }
 }
 
-// d += a b with a, b in (hi, lo) form; small terms first.
+// The two halves of d += a b with a, b in (hi, lo) form: the small cross
+// terms first, then hi * hi.  Callers issue the first half for every tile of
+// a step before the second, so consecutive products use different
+// accumulators.
 template <bool AX, bool BX>
-__device__ __forceinline__ void mma_pair(float (&d)[4], const uint32_t (&ah)[4],
-                                         const uint32_t (&al)[4], uint32_t bh0, uint32_t bh1,
-                                         uint32_t bl0, uint32_t bl1) {
-  if (!BX) mma_tf32(d, ah, bl0, bl1);
-  if (!AX) mma_tf32(d, al, bh0, bh1);
-  mma_tf32(d, ah, bh0, bh1);
+__device__ __forceinline__ void mma_small(float (&d)[4], const uint32_t (&ah)[4],
+                                          const uint32_t (&al)[4], const uint32_t (&bh)[2],
+                                          const uint32_t (&bl)[2]) {
+  if (!BX) mma_tf32(d, ah, bl[0], bl[1]);
+  if (!AX) mma_tf32(d, al, bh[0], bh[1]);
+}
+__device__ __forceinline__ void mma_big(float (&d)[4], const uint32_t (&ah)[4],
+                                        const uint32_t (&bh)[2]) {
+  mma_tf32(d, ah, bh[0], bh[1]);
 }
 
 // A fragment (16 x 8, row-major source): rows r0+g, r0+g+8; columns c0+t, c0+t+4.
@@ -113,6 +121,50 @@ __device__ __forceinline__ void load_at(const T *src, int ld, int m0, int k0, in
   operand<EXACT>(to_float(src[(k0 + t + 4) * ld + m0 + g + 8]), hi[3], lo[3]);
 }
 
+// Masked Gram rows 16 mt .. 16 mt + 15 against the chunk's keys, n-tiles nst ..
+// nst + GNT - 1 (tiles wholly above the diagonal are skipped).  KK: Mk[i][j] =
+// beta_i e^{A_i-A_j} k_i.k_j for j < i, stored at X[i][j]; otherwise Mq[i][j] =
+// scale e^{A_i-A_j} q_i.k_j for j <= i, stored transposed at X[j][i+1].
+template <bool XIN, bool KK, int GNT, int D, int LDI, int LDX, typename KT>
+__device__ __forceinline__ void gram_rows(const KT *asrc, const KT *ks, int mt, int nst,
+                                          const float *Acum, const float *bs, float scale,
+                                          float *Xs, int g, int t) {
+  float acc[GNT][4];
+#pragma unroll
+  for (int n = 0; n < GNT; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
+#pragma unroll 2
+  for (int k0 = 0; k0 < D; k0 += 8) {
+    uint32_t ah[4], al[4], bh[GNT][2], bl[GNT][2];
+    load_a<XIN>(asrc, LDI, 16 * mt, k0, g, t, ah, al);
+#pragma unroll
+    for (int n = 0; n < GNT; ++n) {
+      const int row = 8 * (nst + n) + g;
+      operand<XIN>(to_float(ks[row * LDI + k0 + t]), bh[n][0], bl[n][0]);
+      operand<XIN>(to_float(ks[row * LDI + k0 + t + 4]), bh[n][1], bl[n][1]);
+    }
+#pragma unroll
+    for (int n = 0; n < GNT; ++n)
+      if (nst + n <= 2 * mt + 1) mma_small<XIN, XIN>(acc[n], ah, al, bh[n], bl[n]);
+#pragma unroll
+    for (int n = 0; n < GNT; ++n)
+      if (nst + n <= 2 * mt + 1) mma_big(acc[n], ah, bh[n]);
+  }
+#pragma unroll
+  for (int n = 0; n < GNT; ++n) {
+    const int nt = nst + n;
+    if (nt > 2 * mt + 1) continue;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int i = 16 * mt + g + (e >> 1) * 8, j = 8 * nt + 2 * t + (e & 1);
+      if (KK) {
+        if (j < i) Xs[i * LDX + j] = bs[i] * expf(Acum[i] - Acum[j]) * acc[n][e];
+      } else {
+        if (j <= i) Xs[j * LDX + i + 1] = scale * expf(Acum[i] - Acum[j]) * acc[n][e];
+      }
+    }
+  }
+}
+
 template <typename KT, int VARIANT, int D>
 __global__ void __launch_bounds__(kPrefillThreads, 1)
     prefill_kernel(const PoolView P, const RowBatch rows, const TokenIO io) {
@@ -122,8 +174,8 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
   constexpr bool XIN = Sh::BF16;  // q, k, v exact in tf32
   constexpr int NW3 = D / 32;     // n-tiles per warp in Y and O
   constexpr int MT = DELTA ? 4 : 2;  // m-tiles per warp in Y and O
-  constexpr int WPM = 128 / D;       // warps per m-tile in the state update
-  constexpr int NPW = (D / 8) / WPM;  // n-tiles per warp in the state update
+  constexpr int MT6 = D / 16;  // m-tiles (state rows) per warp in the state update
+  constexpr int NPW = D / 64;  // n-tiles (state columns) per warp in the state update
 
   extern __shared__ float4 dyn_smem[];
   char *sm = reinterpret_cast<char *>(dyn_smem);
@@ -227,47 +279,10 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
     }
     __syncthreads();
 
-    // Gram matrices: Mk[i][j] = beta_i e^{A_i-A_j} k_i.k_j (j < i) at X[i][j];
-    // Mq[i][j] = scale e^{A_i-A_j} q_i.k_j (j <= i) at X[j][i+1]
-    {
-      constexpr int GNT = DELTA ? 8 : 4;  // n-tiles per warp
-      const bool kk = DELTA && warp < 4;
-      const int mt = DELTA ? (warp & 3) : (warp >> 1);
-      const int nst = DELTA ? 0 : (warp & 1) * 4;
-      const KT *asrc = kk ? ks : qs;
-      float acc[GNT][4];
-#pragma unroll
-      for (int n = 0; n < GNT; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
-#pragma unroll 2
-      for (int k0 = 0; k0 < D; k0 += 8) {
-        uint32_t ah[4], al[4];
-        load_a<XIN>(asrc, LDI, 16 * mt, k0, g, t, ah, al);
-#pragma unroll
-        for (int n = 0; n < GNT; ++n) {
-          const int nt = nst + n;
-          if (nt > 2 * mt + 1) continue;  // above the diagonal
-          uint32_t bh0, bl0, bh1, bl1;
-          operand<XIN>(to_float(ks[(8 * nt + g) * LDI + k0 + t]), bh0, bl0);
-          operand<XIN>(to_float(ks[(8 * nt + g) * LDI + k0 + t + 4]), bh1, bl1);
-          mma_pair<XIN, XIN>(acc[n], ah, al, bh0, bh1, bl0, bl1);
-        }
-      }
-#pragma unroll
-      for (int n = 0; n < GNT; ++n) {
-        const int nt = nst + n;
-        if (nt > 2 * mt + 1) continue;
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int i = 16 * mt + g + (e >> 1) * 8, j = 8 * nt + 2 * t + (e & 1);
-          if (kk) {
-            if (j < i) Xs[i * LDX + j] = bs[i] * expf(Acum[i] - Acum[j]) * acc[n][e];
-          } else {
-            if (j <= i) Xs[j * LDX + i + 1] = P.scale * expf(Acum[i] - Acum[j]) * acc[n][e];
-          }
-        }
-      }
-    }
-    __syncthreads();
+    // Gram matrix needed first: Mk for the delta rule, else Mq (all warps).  No
+    // barrier after it: Y below neither reads nor writes X.
+    gram_rows<XIN, DELTA, 4, D, LDI, LDX>(DELTA ? ks : qs, ks, warp >> 1, (warp & 1) * 4, Acum, bs,
+                                          P.scale, Xs, g, t);
 
     // Y = [Q; K] S.  Q rows stay in registers as the output accumulator
     // (e^{A_i} scale q_i^T S); K rows become R_i = beta_i (v_i - e^{A_i} S^T k_i).
@@ -295,8 +310,9 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
           uint32_t ah[4], al[4];
           load_a<XIN>(asrc, LDI, 16 * (mb + m), k0, g, t, ah, al);
 #pragma unroll
-          for (int n = 0; n < NW3; ++n)
-            mma_pair<XIN, false>(y[m][n], ah, al, bh[n][0], bh[n][1], bl[n][0], bl[n][1]);
+          for (int n = 0; n < NW3; ++n) mma_small<XIN, false>(y[m][n], ah, al, bh[n], bl[n]);
+#pragma unroll
+          for (int n = 0; n < NW3; ++n) mma_big(y[m][n], ah, bh[n]);
         }
       }
 #pragma unroll
@@ -315,7 +331,11 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
     }
     __syncthreads();
 
-    // (I + Mk) U = R by forward substitution, one column per thread (delta rule)
+    // Delta rule: (I + Mk) U = R by forward substitution, one column per thread
+    // of warps 4..7, while warps 0..3 build Mq (above the diagonal of X, apart
+    // from the Mk entries the substitution reads).
+    if (DELTA && warp < 4)
+      gram_rows<XIN, false, 8, D, LDI, LDX>(qs, ks, warp, 0, Acum, bs, P.scale, Xs, g, t);
     if (DELTA && tid >= 128 && tid - 128 < D) {
       const int col = tid - 128;
       float u[C];
@@ -369,8 +389,9 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
           split_tf32(kb <= ra ? Xs[kb * LDX + ra + 1] : 0.f, ah[2], al[2]);
           split_tf32(kb <= rb ? Xs[kb * LDX + rb + 1] : 0.f, ah[3], al[3]);
 #pragma unroll
-          for (int n = 0; n < NW3; ++n)
-            mma_pair<false, BX>(y[m][n], ah, al, bh[n][0], bh[n][1], bl[n][0], bl[n][1]);
+          for (int n = 0; n < NW3; ++n) mma_small<false, BX>(y[m][n], ah, al, bh[n], bl[n]);
+#pragma unroll
+          for (int n = 0; n < NW3; ++n) mma_big(y[m][n], ah, bh[n]);
         }
       }
 #pragma unroll
@@ -387,26 +408,29 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
         }
     }
 
-    // S <- e^{A_{C-1}} S + K^T diag(w) U (no barrier: O and this step only read U)
+    // S <- e^{A_{C-1}} S + K^T diag(w) U (no barrier: O and this step only read
+    // U).  Warp w owns state columns 8 (NPW w) .. 8 (NPW w + NPW) - 1 over all
+    // rows, so each w_i u_i is split into tf32 parts once.
     {
-      const int mt = warp / WPM, nst = (warp % WPM) * NPW;
+      const int nst = warp * NPW;
       const float eL = eA[C - 1];
-      float acc[NPW][4];
+      float acc[MT6][NPW][4];
 #pragma unroll
-      for (int n = 0; n < NPW; ++n) {
-        const int col = 8 * (nst + n) + 2 * t;
-        const float2 lo = *reinterpret_cast<const float2 *>(&Ss[(16 * mt + g) * LDS + col]);
-        const float2 hi = *reinterpret_cast<const float2 *>(&Ss[(16 * mt + g + 8) * LDS + col]);
-        acc[n][0] = eL * lo.x;
-        acc[n][1] = eL * lo.y;
-        acc[n][2] = eL * hi.x;
-        acc[n][3] = eL * hi.y;
-      }
+      for (int m = 0; m < MT6; ++m)
+#pragma unroll
+        for (int n = 0; n < NPW; ++n) {
+          const int col = 8 * (nst + n) + 2 * t;
+          const float2 lo = *reinterpret_cast<const float2 *>(&Ss[(16 * m + g) * LDS + col]);
+          const float2 hi = *reinterpret_cast<const float2 *>(&Ss[(16 * m + g + 8) * LDS + col]);
+          acc[m][n][0] = eL * lo.x;
+          acc[m][n][1] = eL * lo.y;
+          acc[m][n][2] = eL * hi.x;
+          acc[m][n][3] = eL * hi.y;
+        }
 #pragma unroll 1
       for (int k0 = 0; k0 < C; k0 += 8) {
-        uint32_t ah[4], al[4];
-        load_at<XIN>(ks, LDI, 16 * mt, k0, g, t, ah, al);
         const float w0 = wL[k0 + t], w1 = wL[k0 + t + 4];
+        uint32_t bh[NPW][2], bl[NPW][2];
 #pragma unroll
         for (int n = 0; n < NPW; ++n) {
           const int col = 8 * (nst + n) + g;
@@ -418,20 +442,30 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
             u0 = to_float(vs[(k0 + t) * LDI + col]);
             u1 = to_float(vs[(k0 + t + 4) * LDI + col]);
           }
-          uint32_t bh0, bl0, bh1, bl1;
-          split_tf32(w0 * u0, bh0, bl0);
-          split_tf32(w1 * u1, bh1, bl1);
-          mma_pair<XIN, false>(acc[n], ah, al, bh0, bh1, bl0, bl1);
+          split_tf32(w0 * u0, bh[n][0], bl[n][0]);
+          split_tf32(w1 * u1, bh[n][1], bl[n][1]);
+        }
+#pragma unroll
+        for (int m = 0; m < MT6; ++m) {
+          uint32_t ah[4], al[4];
+          load_at<XIN>(ks, LDI, 16 * m, k0, g, t, ah, al);
+#pragma unroll
+          for (int n = 0; n < NPW; ++n) mma_small<XIN, false>(acc[m][n], ah, al, bh[n], bl[n]);
+#pragma unroll
+          for (int n = 0; n < NPW; ++n) mma_big(acc[m][n], ah, bh[n]);
         }
       }
-      // each warp rewrites only the tile it read; Y read S before the last barrier
+      // each warp rewrites only the columns it read; Y read S before the last barrier
 #pragma unroll
-      for (int n = 0; n < NPW; ++n) {
-        const int col = 8 * (nst + n) + 2 * t;
-        *reinterpret_cast<float2 *>(&Ss[(16 * mt + g) * LDS + col]) = make_float2(acc[n][0], acc[n][1]);
-        *reinterpret_cast<float2 *>(&Ss[(16 * mt + g + 8) * LDS + col]) =
-            make_float2(acc[n][2], acc[n][3]);
-      }
+      for (int m = 0; m < MT6; ++m)
+#pragma unroll
+        for (int n = 0; n < NPW; ++n) {
+          const int col = 8 * (nst + n) + 2 * t;
+          *reinterpret_cast<float2 *>(&Ss[(16 * m + g) * LDS + col]) =
+              make_float2(acc[m][n][0], acc[m][n][1]);
+          *reinterpret_cast<float2 *>(&Ss[(16 * m + g + 8) * LDS + col]) =
+              make_float2(acc[m][n][2], acc[m][n][3]);
+        }
     }
   }
   __syncthreads();
