@@ -38,7 +38,8 @@ output is the recurrent output with the earlier drafts in the history, and the
 state after accepting a prefix of j drafts is the recurrent state after those j
 tokens.  Short-context decoding (abstract: outputs computed directly from
 buffered keys and values, without creating the state) is the recurrence from
-S = 0.
+S = 0.  A tree of drafts is verified node by node along each node's path from
+the root, and accepting a node keeps exactly that path.
 
 Parity status: every function here is pinned by tests that do not reuse this
 code (closed forms, exact rational arithmetic, reductions between variants, the
@@ -162,6 +163,48 @@ def accept(S_pre, drafts: dict, n_accepted, variant: int, scale: float = 1.0):
         _, S_r, _ = decode_sequence(S_pre[r], sub, variant, scale)
         S_out[r] = S_r
     return S_out
+
+
+def tree_path(parents, j: int):
+    """Draft indices on the path from the root to draft j, root first.
+
+    parents[i] is the draft that draft i continues (-1: it continues the last
+    accepted token), always an earlier index.
+    """
+    path = []
+    while j >= 0:
+        path.append(int(j))
+        j = int(parents[j])
+    return path[::-1]
+
+
+def verify_tree(S_pre, drafts: dict, parents, variant: int, scale: float = 1.0):
+    """Outputs of a tree of T drafts verified against the pre-round state.
+
+    Tree-shaped speculation (the draft trees the page cites for speculative
+    decoding): draft j's output is the recurrent output after the history plus
+    the drafts on the path from the root to j, in path order.  drafts laid out
+    [T, ...] as in decode_sequence; returns o: [T, ..., Hv, d_v].  A chain
+    (parents[j] = j - 1) is ordinary verification.
+    """
+    T = drafts["v"].shape[0]
+    o = np.empty(drafts["v"].shape, dtype=np.float64)
+    for j in range(T):
+        path = tree_path(parents, j)
+        sub = {key: (None if val is None else val[path]) for key, val in drafts.items()}
+        o_path, _, _ = decode_sequence(S_pre, sub, variant, scale)
+        o[j] = o_path[-1]
+    return o
+
+
+def accept_tree(S_pre, drafts: dict, parents, node: int, variant: int, scale: float = 1.0):
+    """State after accepting the path from the root to draft ``node`` (-1: none)."""
+    if node < 0:
+        return _f64(S_pre).copy()
+    path = tree_path(parents, node)
+    sub = {key: (None if val is None else val[path]) for key, val in drafts.items()}
+    _, S, _ = decode_sequence(S_pre, sub, variant, scale)
+    return S
 
 
 def short_context(tokens: dict, variant: int, d_k: int, d_v: int, scale: float = 1.0):

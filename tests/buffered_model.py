@@ -18,6 +18,8 @@ exactness claim of "KVBuffer: IO-aware Serving for Linear Attention",
 * verify T drafts: the decode formula applied to each draft in turn, each
   draft appended to the buffer, the state untouched (Figure 2);
   accept(j): keep the first j drafts; flush all if the buffer holds >= m.
+* a draft tree: each draft sees the committed buffer plus its ancestors only;
+  accepting a node keeps its path from the root.
 
 It shares no code with the oracle or the library.
 """
@@ -94,6 +96,36 @@ class BufferedHead:
         T = self._pending
         n = len(self.buf) - T
         self.buf = self.buf[: n + j]
+        if len(self.buf) >= self.m:
+            self.flush()
+
+    def verify_tree(self, drafts, parents):
+        """Draft tree: draft j sees the committed buffer plus its ancestors' entries
+        in path order (parents[j] < j, -1 for a child of the last accepted token).
+        The committed buffer is unchanged; returns the drafts' outputs."""
+        base = list(self.buf)
+        entries, outs = [], []
+        for j, (q, k, v, a, b) in enumerate(drafts):
+            anc, p = [], parents[j]
+            while p >= 0:
+                anc.append(p)
+                p = parents[p]
+            self.buf = base + [entries[i] for i in reversed(anc)]
+            o, entry = self._token_out(q, k, v, a, b)
+            entries.append(entry)
+            outs.append(o)
+        self.buf = base
+        self._tree = (entries, list(parents))
+        return np.array(outs)
+
+    def accept_path(self, node):
+        """Keep the path from the root to draft ``node`` (-1: none); flush at >= m."""
+        entries, parents = self._tree
+        path, p = [], node
+        while p >= 0:
+            path.append(p)
+            p = parents[p]
+        self.buf = self.buf + [entries[i] for i in reversed(path)]
         if len(self.buf) >= self.m:
             self.flush()
 

@@ -16,6 +16,9 @@ What pins what:
 * buffered form          the KVBuffer algorithm (brute-force model) equals the oracle
                          for every flush threshold m <= 6, every variant
 * verify / accept        accept(j) equals the replay of j tokens; j = 0 keeps the state
+* draft trees            exact rationals along each root path (plain), constant-gate path
+                         weights (order), chain = verify, star = single decodes, and the
+                         buffered algorithm with an ancestor mask
 * short context          equals the closed form from S = 0
 * GQA mapping            value head h reads q/k head h // (Hv/Hk)
 """
@@ -328,11 +331,119 @@ def pin_hand_worked(orc):
         assert np.abs(S_T[0, 0] - np.array(c["S_final"])).max() <= 1e-12, c["name"]
 
 
+TREE = [-1, 0, 0, 1, -1, 3, 2]  # two roots; draft 0 branches into 1 and 2; depth 4
+
+
+def _walk(parents, j):
+    nodes = []
+    while j != -1:
+        nodes.append(j)
+        j = parents[j]
+    return nodes[::-1]
+
+
+def pin_tree_exact_rational(orc):
+    """Draft trees, plain form on integers: draft j's output is q_j^T (S_pre + sum over
+    its root path of k v^T), in exact rational arithmetic; constant gate g: the path
+    weights g^(depth - position) fix the path order."""
+    rng = np.random.default_rng(70)
+    T, dk, dv = len(TREE), 3, 2
+    S_pre = rng.integers(-3, 4, size=(dk, dv))
+    q, k, v = (rng.integers(-3, 4, size=(T, d)) for d in (dk, dk, dv))
+    drafts = {"q": q[:, None, :].astype(float), "k": k[:, None, :].astype(float),
+              "v": v[:, None, :].astype(float), "log_g": None, "beta": None}
+    o = orc.verify_tree(S_pre[None].astype(float), drafts, TREE, PLAIN)
+    for j in range(T):
+        S = [[Fraction(int(S_pre[a][c])) for c in range(dv)] for a in range(dk)]
+        for i in _walk(TREE, j):
+            for a in range(dk):
+                for c in range(dv):
+                    S[a][c] += int(k[i][a]) * int(v[i][c])
+        exp = [sum(int(q[j][a]) * S[a][c] for a in range(dk)) for c in range(dv)]
+        assert np.array_equal(o[j, 0], np.array([float(x) for x in exp])), j
+    S_acc = orc.accept_tree(S_pre[None].astype(float), drafts, TREE, 5, PLAIN)
+    exp = S_pre + sum(np.outer(k[i], v[i]) for i in (0, 1, 3, 5))
+    assert np.array_equal(S_acc[0], exp.astype(float))
+    assert np.array_equal(orc.accept_tree(S_pre[None].astype(float), drafts, TREE, -1, PLAIN)[0],
+                          S_pre.astype(float))
+    # constant gate: o_j = q_j^T (g^D S_pre + sum_p g^(D-p) k_(path p) v_(path p)^T)
+    g = 0.7
+    drafts_g = dict(drafts, log_g=np.full((T, 1), np.log(g)))
+    og = orc.verify_tree(S_pre[None].astype(float), drafts_g, TREE, GATED)
+    for j in range(T):
+        path = _walk(TREE, j)
+        D = len(path)
+        S = g ** D * S_pre.astype(float)
+        for pos, i in enumerate(path, start=1):
+            S = S + g ** (D - pos) * np.outer(k[i], v[i])
+        assert np.abs(og[j, 0] - S.T @ q[j]).max() <= 1e-12, j
+
+
+def pin_tree_reductions(orc):
+    """A chain tree is ordinary verification and accept; a star tree is T independent
+    single-token decodes from the same state."""
+    rng = np.random.default_rng(71)
+    T = 5
+    for variant in (PLAIN, GATED, GATED_DELTA):
+        tok = _tokens(rng, T, 1, 1, 2, 4, 3, variant, unit_k=True)
+        drafts = {key: (None if val is None else val[:, 0]) for key, val in tok.items()}
+        S_pre = _rand(rng, 2, 4, 3)
+        chain = list(range(-1, T - 1))
+        assert np.abs(orc.verify_tree(S_pre, drafts, chain, variant)
+                      - orc.verify(S_pre, drafts, variant)).max() <= 1e-12
+        for j in range(T + 1):
+            acc = orc.accept(S_pre[None], tok, np.array([j]), variant)[0]
+            assert np.abs(orc.accept_tree(S_pre, drafts, chain, j - 1, variant) - acc).max() <= 1e-12
+        star = [-1] * T
+        o_star = orc.verify_tree(S_pre, drafts, star, variant)
+        for j in range(T):
+            one = {key: (None if val is None else val[j:j + 1]) for key, val in drafts.items()}
+            o1, _, _ = orc.decode_sequence(S_pre, one, variant)
+            assert np.abs(o_star[j] - o1[0]).max() <= 1e-12
+
+
+def pin_buffered_tree_equals_recurrent(orc):
+    """The buffered algorithm with an ancestor mask (committed buffer + the draft's path)
+    equals the oracle's tree verification, and accepting a path equals its replay."""
+    rng = np.random.default_rng(72)
+    dk, dv = 4, 3
+    for variant in (PLAIN, GATED, GATED_DELTA):
+        for trial in range(4):
+            m = 6
+            S0 = _rand(rng, dk, dv)
+            head = BufferedHead(S0, variant, m)
+            S_hist = S0[None].copy()
+            n0 = int(rng.integers(0, 3))
+            pre = _tokens(rng, n0, 1, 1, 1, dk, dv, variant, unit_k=True)
+            for t in range(n0):
+                head.decode(pre["q"][t, 0, 0], pre["k"][t, 0, 0], pre["v"][t, 0, 0],
+                            None if pre["log_g"] is None else pre["log_g"][t, 0, 0],
+                            None if pre["beta"] is None else pre["beta"][t, 0, 0])
+            if n0:
+                _, S_hist, _ = orc.decode_sequence(
+                    S_hist, {key: (None if val is None else val[:, 0]) for key, val in pre.items()},
+                    variant)
+            T = 6
+            parents = [-1] + [int(rng.integers(-1, j)) for j in range(1, T)]
+            tok = _tokens(rng, T, 1, 1, 1, dk, dv, variant, unit_k=True)
+            drafts = {key: (None if val is None else val[:, 0]) for key, val in tok.items()}
+            dl = [(tok["q"][t, 0, 0], tok["k"][t, 0, 0], tok["v"][t, 0, 0],
+                   None if tok["log_g"] is None else tok["log_g"][t, 0, 0],
+                   None if tok["beta"] is None else tok["beta"][t, 0, 0]) for t in range(T)]
+            o = head.verify_tree(dl, parents)
+            assert np.abs(o - orc.verify_tree(S_hist, drafts, parents, variant)[:, 0]).max() <= 1e-10
+            node = int(rng.integers(-1, T))
+            head.accept_path(node)
+            S_acc = orc.accept_tree(S_hist, drafts, parents, node, variant)
+            assert np.abs(head.current_state() - S_acc[0]).max() <= 1e-10
+
+
 PINS = [pin_plain_closed_form, pin_plain_exact_rational, pin_gated_constant_gate,
         pin_gated_product_of_gates, pin_gated_unit_gate_is_plain, pin_delta_beta_zero_decay,
         pin_delta_overwrite, pin_delta_gradient_step, pin_delta_ut_chunk_form,
         pin_buffered_equals_recurrent, pin_verify_accept, pin_short_context, pin_gqa_mapping,
-        pin_gated_prefill_closed_form, pin_hand_worked]
+        pin_gated_prefill_closed_form, pin_hand_worked, pin_tree_exact_rational,
+        pin_tree_reductions, pin_buffered_tree_equals_recurrent]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
@@ -399,7 +510,16 @@ def _mut_gqa_modulo(x, n_v_heads):
     return np.concatenate([x] * (n_v_heads // hk), axis=-2)
 
 
+def _mut_tree_path_without_node(parents, j):
+    return _ORIG_TREE_PATH(parents, j)[:-1]
+
+
+def _mut_tree_path_leaf_first(parents, j):
+    return _ORIG_TREE_PATH(parents, j)[::-1]
+
+
 _ORIG_STEP = kvb_oracle.recurrent_step
+_ORIG_TREE_PATH = kvb_oracle.tree_path
 
 MUTANTS = {
     "gate_dropped": ("recurrent_step", _mut_gate_dropped),
@@ -409,6 +529,8 @@ MUTANTS = {
     "gate_after_write": ("recurrent_step", _mut_gate_after_write),
     "output_not_transposed": ("recurrent_step", _mut_output_not_transposed),
     "gqa_modulo": ("expand_qk", _mut_gqa_modulo),
+    "tree_path_without_node": ("tree_path", _mut_tree_path_without_node),
+    "tree_path_leaf_first": ("tree_path", _mut_tree_path_leaf_first),
 }
 
 
