@@ -235,6 +235,33 @@ int kvb_verify(kvb_pool *pool, int32_t B, int32_t T, const int32_t *req_ids, con
 int kvb_accept(kvb_pool *pool, int32_t B, const int32_t *req_ids, const int32_t *n_accepted,
                kvb_stream_t stream);
 
+/* Verify a tree of T draft tokens per request (tree-shaped speculation, as
+   in the draft trees the page cites for speculative decoding; Figure 2's
+   buffered verification with each draft seeing only its own path).
+   parents (host, [B][T]): parents[b*T + j] is the draft that draft j
+   continues, -1 for a child of the last accepted token; it must be < j
+   (KVB_E_ARG otherwise), so drafts come in topological order.  Draft j's
+   output is the recurrent output after the request's history and the drafts
+   on the path from the root to j.  As in kvb_verify, the drafts occupy buffer
+   slots n .. n+T-1 and the state is only read; inputs and o are laid out as
+   there.  A verify_tree must be followed by kvb_accept_tree (kvb_accept gives
+   KVB_E_STATE).  Launches carry at most 128 rows each. */
+int kvb_verify_tree(kvb_pool *pool, int32_t B, int32_t T, const int32_t *req_ids,
+                    const int32_t *parents, const void *q, const void *k, const void *v,
+                    const float *log_g, const float *beta, float *o, kvb_stream_t stream);
+
+/* Accept one path of a verified draft tree: request req_ids[b] keeps the
+   drafts on the path from the root to draft accepted[b] (host array; -1
+   keeps none), in path order, and drops the rest; its length grows by the
+   path length.  Entries of the kept drafts are moved to the front of the
+   draft slots on `stream` when the path is not already the leading drafts;
+   a buffer that then holds >= m tokens is folded into the state as in
+   kvb_accept.  Also accepts after a chain kvb_verify (the path to draft j is
+   drafts 0..j).  Every listed request must have a pending verify
+   (KVB_E_STATE otherwise). */
+int kvb_accept_tree(kvb_pool *pool, int32_t B, const int32_t *req_ids, const int32_t *accepted,
+                    kvb_stream_t stream);
+
 /* The comparison baseline of Figure 2: a serving system with only a state pool
    verifies T drafts with the recurrent form and stores a temporary state after
    every draft.  For pools with m == 0 (KVB_E_STATE otherwise); every request

@@ -201,6 +201,19 @@ __device__ __forceinline__ void warp_prefix(int count, GateFn gate, float *A, in
   }
 }
 
+// One thread: ancestor sets of a draft tree (bit i = draft i; a draft counts as
+// its own ancestor) and, when A is given, the drafts' log-gates (A[j] on entry)
+// turned into cumulative values along each draft's path from A_root.
+__device__ __forceinline__ void tree_walk(const int8_t *parent, int T, float A_root, float *A,
+                                          unsigned long long *anc) {
+  for (int j = 0; j < T; ++j) {
+    int p = parent[j];
+    if (p >= j || p < -1) p = -1;  // validated by the host; keeps every index in range
+    anc[j] = (p < 0 ? 0ull : anc[p]) | (1ull << j);
+    if (A) A[j] += p < 0 ? A_root : A[p];
+  }
+}
+
 // ------------------------------------------------------------------ tensor cores
 // tf32 value of x, rounded to nearest (ties away): the operand form of
 // mma.sync kind tf32, which reads the top 19 bits of a 32-bit register.

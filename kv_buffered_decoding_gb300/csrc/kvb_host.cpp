@@ -98,6 +98,11 @@ struct kvb_pool {
   std::vector<uint32_t> stamp;
   uint32_t stamp_gen = 0;
   kvb::RowBatch rows;  // parameter block under construction (8 KB, kept off the stack)
+  // draft trees: parents of each request's pending tree verify, and the tree
+  // parameter block under construction (8 KB)
+  std::vector<int8_t> tree_host;
+  std::vector<uint8_t> pending_tree;
+  kvb::TreeArg<true> tree_arg;
 
   int capacity(int r) const { return nblk[r] * cfg.block_size; }
 };
@@ -277,6 +282,8 @@ int kvb_alloc_pool(const kvb_config *cfg, void *state_mem, void *kv_mem, void *m
   p->slot.assign(R, -1);
   p->nblk.assign(R, 0);
   p->pending_T.assign(R, 0);
+  p->pending_tree.assign(R, 0);
+  p->tree_host.assign(R * (size_t)KVB_MAX_DRAFTS, -1);
   p->active.assign(R, 0);
   p->stamp.assign(R, 0u);
   p->table.assign(R * (size_t)cfg->max_blocks_per_req, -1);
@@ -330,6 +337,7 @@ int kvb_set_request(kvb_pool *p, int32_t req, int32_t state_slot, int32_t n_bloc
   p->nblk[req] = n_blocks;
   p->len[req] = 0;
   p->pending_T[req] = 0;
+  p->pending_tree[req] = 0;
   return KVB_OK;
 }
 
@@ -345,6 +353,7 @@ int kvb_release_request(kvb_pool *p, int32_t req) {
   p->nblk[req] = 0;
   p->len[req] = 0;
   p->pending_T[req] = 0;
+  p->pending_tree[req] = 0;
   return KVB_OK;
 }
 
@@ -437,9 +446,14 @@ int kvb_promote(kvb_pool *p, int32_t B, const int32_t *req_ids, const int32_t *s
   return launch_fold(p, fold, s, kvb::kFlagFromZero);
 }
 
-int kvb_verify(kvb_pool *p, int32_t B, int32_t T, const int32_t *req_ids, const void *q,
-               const void *k, const void *v, const float *log_g, const float *beta, float *o,
-               kvb_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// Verify of a chain (parents == nullptr) or of a draft tree (host parents [B][T]).
+int verify_impl(kvb_pool *p, int32_t B, int32_t T, const int32_t *req_ids,
+                const int32_t *parents, const void *q, const void *k, const void *v,
+                const float *log_g, const float *beta, float *o, cudaStream_t stream) {
   if (!p) return KVB_E_ARG;
   if (p->cfg.m == 0) return KVB_E_STATE;
   if (T < 1 || T > KVB_MAX_DRAFTS) return KVB_E_ARG;
@@ -450,11 +464,17 @@ int kvb_verify(kvb_pool *p, int32_t B, int32_t T, const int32_t *req_ids, const 
     const int32_t r = req_ids[b];
     if (p->pending_T[r]) return KVB_E_STATE;
     if (p->len[r] + T > p->capacity(r)) return KVB_E_CAPACITY;
+    if (parents)
+      for (int32_t j = 0; j < T; ++j) {
+        const int32_t par = parents[(size_t)b * T + j];
+        if (par < -1 || par >= j) return KVB_E_ARG;
+      }
   }
   const kvb_config &c = p->cfg;
   const kvb::TokenIO io{q, k, v, log_g, beta, o, T, 0};
-  for (int32_t base = 0; base < B; base += kvb::kMaxRows) {
-    const int32_t cnt = B - base < kvb::kMaxRows ? B - base : kvb::kMaxRows;
+  const int32_t per_launch = parents ? kvb::kTreeRows : kvb::kMaxRows;
+  for (int32_t base = 0; base < B; base += per_launch) {
+    const int32_t cnt = B - base < per_launch ? B - base : per_launch;
     p->rows.count = cnt;
     p->rows.row0 = base;
     int lmax = 0;
@@ -462,37 +482,35 @@ int kvb_verify(kvb_pool *p, int32_t B, int32_t T, const int32_t *req_ids, const 
       const int32_t r = req_ids[base + i];
       p->rows.r[i] = make_row(p, r, p->len[r], 0);
       if (p->len[r] + T > lmax) lmax = p->len[r] + T;
+      if (parents)
+        for (int32_t j = 0; j < T; ++j)
+          p->tree_arg.p[i][j] = static_cast<int8_t>(parents[(size_t)(base + i) * T + j]);
     }
     cudaError_t e = kvb::launch_verify(p->view, p->rows, io, c.variant, c.kv_dtype, c.d_k, lmax,
-                                       reinterpret_cast<cudaStream_t>(stream));
+                                       stream, parents ? &p->tree_arg : nullptr);
     if (e != cudaSuccess) return cuda_status(e);
-    for (int32_t i = 0; i < cnt; ++i) p->pending_T[req_ids[base + i]] = T;
+    for (int32_t i = 0; i < cnt; ++i) {
+      const int32_t r = req_ids[base + i];
+      p->pending_T[r] = T;
+      p->pending_tree[r] = parents != nullptr;
+      if (parents)
+        for (int32_t j = 0; j < T; ++j)
+          p->tree_host[(size_t)r * KVB_MAX_DRAFTS + j] = p->tree_arg.p[i][j];
+    }
   }
   return KVB_OK;
 }
 
-int kvb_accept(kvb_pool *p, int32_t B, const int32_t *req_ids, const int32_t *n_accepted,
-               kvb_stream_t stream) {
-  if (!p) return KVB_E_ARG;
-  int st = check_reqs(p, B, req_ids);
-  if (st || B == 0) return st;
-  if (!n_accepted) return KVB_E_ARG;
-  for (int32_t b = 0; b < B; ++b) {
-    const int32_t r = req_ids[b];
-    if (!p->pending_T[r]) return KVB_E_STATE;
-    if (n_accepted[b] < 0 || n_accepted[b] > p->pending_T[r]) return KVB_E_ARG;
-  }
+// Lengths after an accept: fold the rows whose buffer reached m, set the
+// device length of the others.
+int finish_accept(kvb_pool *p, const std::vector<int32_t> &reqs, cudaStream_t s) {
   std::vector<int32_t> fold, keep;
-  for (int32_t b = 0; b < B; ++b) {
-    const int32_t r = req_ids[b];
-    p->len[r] += n_accepted[b];
-    p->pending_T[r] = 0;
+  for (int32_t r : reqs) {
     if (p->slot[r] >= 0 && p->cfg.m > 0 && p->len[r] >= p->cfg.m)
       fold.push_back(r);
     else
       keep.push_back(r);
   }
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   for (size_t base = 0; base < keep.size(); base += kvb::kMaxRows) {
     const size_t cnt = keep.size() - base < (size_t)kvb::kMaxRows ? keep.size() - base : kvb::kMaxRows;
     p->rows.count = (int32_t)cnt;
@@ -505,6 +523,101 @@ int kvb_accept(kvb_pool *p, int32_t B, const int32_t *req_ids, const int32_t *n_
     if (e != cudaSuccess) return cuda_status(e);
   }
   return launch_fold(p, fold, s);
+}
+
+}  // namespace
+
+extern "C" {
+
+int kvb_verify(kvb_pool *p, int32_t B, int32_t T, const int32_t *req_ids, const void *q,
+               const void *k, const void *v, const float *log_g, const float *beta, float *o,
+               kvb_stream_t stream) {
+  return verify_impl(p, B, T, req_ids, nullptr, q, k, v, log_g, beta, o,
+                     reinterpret_cast<cudaStream_t>(stream));
+}
+
+int kvb_verify_tree(kvb_pool *p, int32_t B, int32_t T, const int32_t *req_ids,
+                    const int32_t *parents, const void *q, const void *k, const void *v,
+                    const float *log_g, const float *beta, float *o, kvb_stream_t stream) {
+  if (!parents) return KVB_E_ARG;
+  return verify_impl(p, B, T, req_ids, parents, q, k, v, log_g, beta, o,
+                     reinterpret_cast<cudaStream_t>(stream));
+}
+
+int kvb_accept_tree(kvb_pool *p, int32_t B, const int32_t *req_ids, const int32_t *accepted,
+                    kvb_stream_t stream) {
+  if (!p) return KVB_E_ARG;
+  int st = check_reqs(p, B, req_ids);
+  if (st || B == 0) return st;
+  if (!accepted) return KVB_E_ARG;
+  for (int32_t b = 0; b < B; ++b) {
+    const int32_t r = req_ids[b];
+    if (!p->pending_T[r]) return KVB_E_STATE;
+    if (accepted[b] < -1 || accepted[b] >= p->pending_T[r]) return KVB_E_ARG;
+  }
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const kvb_config &c = p->cfg;
+  // accepted paths, root first; rows whose path is not already the leading drafts
+  // are compacted on the device before the lengths change
+  std::vector<int32_t> reqs(B);
+  int32_t cnt = 0;
+  auto flush_compact = [&]() -> int {
+    if (cnt == 0) return KVB_OK;
+    p->rows.count = cnt;
+    p->rows.row0 = 0;
+    cudaError_t e = kvb::launch_tree_compact(p->view, p->rows, p->tree_arg, c.variant,
+                                             c.kv_dtype, c.d_k, s);
+    cnt = 0;
+    return e == cudaSuccess ? KVB_OK : cuda_status(e);
+  };
+  for (int32_t b = 0; b < B; ++b) {
+    const int32_t r = req_ids[b];
+    reqs[b] = r;
+    int8_t path[KVB_MAX_DRAFTS];
+    int32_t len = 0;
+    if (p->pending_tree[r]) {
+      int8_t rev[KVB_MAX_DRAFTS];
+      for (int32_t j = accepted[b]; j >= 0; j = p->tree_host[(size_t)r * KVB_MAX_DRAFTS + j])
+        rev[len++] = static_cast<int8_t>(j);
+      for (int32_t l = 0; l < len; ++l) path[l] = rev[len - 1 - l];
+    } else {
+      for (int32_t l = 0; l <= accepted[b]; ++l) path[len++] = static_cast<int8_t>(l);
+    }
+    bool moved = false;
+    for (int32_t l = 0; l < len; ++l) moved |= path[l] != l;
+    if (moved) {
+      p->rows.r[cnt] = make_row(p, r, p->len[r], len);
+      for (int32_t l = 0; l < len; ++l) p->tree_arg.p[cnt][l] = path[l];
+      if (++cnt == kvb::kTreeRows && (st = flush_compact())) return st;
+    }
+    p->len[r] += len;
+    p->pending_T[r] = 0;
+    p->pending_tree[r] = 0;
+  }
+  if ((st = flush_compact())) return st;
+  return finish_accept(p, reqs, s);
+}
+
+
+int kvb_accept(kvb_pool *p, int32_t B, const int32_t *req_ids, const int32_t *n_accepted,
+               kvb_stream_t stream) {
+  if (!p) return KVB_E_ARG;
+  int st = check_reqs(p, B, req_ids);
+  if (st || B == 0) return st;
+  if (!n_accepted) return KVB_E_ARG;
+  for (int32_t b = 0; b < B; ++b) {
+    const int32_t r = req_ids[b];
+    if (!p->pending_T[r] || p->pending_tree[r]) return KVB_E_STATE;
+    if (n_accepted[b] < 0 || n_accepted[b] > p->pending_T[r]) return KVB_E_ARG;
+  }
+  std::vector<int32_t> reqs(B);
+  for (int32_t b = 0; b < B; ++b) {
+    const int32_t r = req_ids[b];
+    reqs[b] = r;
+    p->len[r] += n_accepted[b];
+    p->pending_T[r] = 0;
+  }
+  return finish_accept(p, reqs, reinterpret_cast<cudaStream_t>(stream));
 }
 
 int kvb_verify_tempstate(kvb_pool *p, int32_t B, int32_t T, const int32_t *req_ids,

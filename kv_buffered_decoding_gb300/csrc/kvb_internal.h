@@ -50,6 +50,18 @@ struct RowBatch {
   RowDesc r[kMaxRows];
 };
 
+// Draft trees of one launch, carried in the kernel parameter block: for row i
+// of the launch and draft j, p[i][j] is the parent draft (-1: the last
+// accepted token), always < j.  Accept reuses it for the accepted path (the
+// draft index at each path position).  Chain launches pass the empty form.
+constexpr int kTreeRows = 128;  // rows per tree launch
+template <bool TREE>
+struct TreeArg {};
+template <>
+struct TreeArg<true> {
+  int8_t p[kTreeRows][KVB_MAX_DRAFTS];
+};
+
 // Input / output pointers of a decode or verify launch (device).
 struct TokenIO {
   const void *q, *k, *v;  // kv dtype
@@ -73,7 +85,14 @@ cudaError_t launch_decode(const PoolView &P, const RowBatch &rows, const TokenIO
 cudaError_t launch_short(const PoolView &P, const RowBatch &rows, const TokenIO &io, int variant,
                          int dtype, int d, cudaStream_t stream);
 cudaError_t launch_verify(const PoolView &P, const RowBatch &rows, const TokenIO &io, int variant,
-                          int dtype, int d, int max_len, cudaStream_t stream);
+                          int dtype, int d, int max_len, cudaStream_t stream,
+                          const TreeArg<true> *tree = nullptr);
+// Move each row's accepted draft path to the front of its draft slots: row i
+// (RowDesc.n = length before the drafts, RowDesc.flags = path length) copies
+// the entry of draft path.p[i][l] into slot n + l, l in path order.
+cudaError_t launch_tree_compact(const PoolView &P, const RowBatch &rows,
+                                const TreeArg<true> &path, int variant, int dtype, int d,
+                                cudaStream_t stream);
 cudaError_t launch_flush(const PoolView &P, const RowBatch &rows, int variant, int dtype, int d,
                          int max_len, cudaStream_t stream);
 cudaError_t launch_verify_tempstate(const PoolView &P, const RowBatch &rows, const TokenIO &io,

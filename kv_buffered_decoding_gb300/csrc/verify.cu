@@ -54,9 +54,10 @@ __device__ __forceinline__ void pair_jl(int p, int n, int &j, int &l) {
   l = p;
 }
 
-template <typename KT, int VARIANT, int D, int NSPLIT>
+template <typename KT, int VARIANT, int D, int NSPLIT, bool TREE>
 __global__ void __launch_bounds__(2 * D / NSPLIT, 512 / (2 * D / NSPLIT))
-    verify_kernel(const PoolView P, const RowBatch rows, const TokenIO io) {
+    verify_kernel(const PoolView P, const RowBatch rows, const TokenIO io,
+                  const __grid_constant__ TreeArg<TREE> tree) {
   constexpr int DK = D, DV = D, NT = 2 * D / NSPLIT, NW = NT / 32, RPT = DK / 8, E = DK / 32;
   constexpr int CW = DV / NSPLIT;  // columns of this CTA
   constexpr bool DELTA = VARIANT == kGatedDelta, GATED = VARIANT != kPlain;
@@ -92,6 +93,7 @@ __global__ void __launch_bounds__(2 * D / NSPLIT, 512 / (2 * D / NSPLIT))
   size_t *koff = reinterpret_cast<size_t *>(bt + ((T + 1) & ~1));  // koff 8-byte aligned
   size_t *voff = koff + LM;
   __shared__ int bad;
+  __shared__ unsigned long long anc[KVB_MAX_DRAFTS];  // draft trees: ancestor sets
 
   // 1. the state tile, into registers
   float4 s[RPT];
@@ -144,13 +146,22 @@ __global__ void __launch_bounds__(2 * D / NSPLIT, 512 / (2 * D / NSPLIT))
       const float *lg = io.log_g;
       for (int i = lane; i < n; i += 32) Acum[i] = P.gbuf[voff[i]];
       const float A_prev = n > 0 ? P.gbuf[voff[n - 1]] : 0.f;
-      warp_prefix(
-          T, [&](int j) { return lg ? lg[(b * T + j) * P.Hv + h] : 0.f; }, Acum + n, lane);
-      __syncwarp();
-      for (int j = lane; j < T; j += 32) Acum[n + j] += A_prev;
+      if constexpr (TREE) {  // cumulative along each draft's path
+        for (int j = lane; j < T; j += 32) Acum[n + j] = lg ? lg[(b * T + j) * P.Hv + h] : 0.f;
+        __syncwarp();
+        if (lane == 0) tree_walk(tree.p[blockIdx.y], T, A_prev, Acum + n, anc);
+      } else {
+        warp_prefix(
+            T, [&](int j) { return lg ? lg[(b * T + j) * P.Hv + h] : 0.f; }, Acum + n, lane);
+        __syncwarp();
+        for (int j = lane; j < T; j += 32) Acum[n + j] += A_prev;
+      }
     }
   } else {
     for (int i = tid; i < L; i += NT) Acum[i] = 0.f;
+    if constexpr (TREE) {
+      if (tid == 0) tree_walk(tree.p[blockIdx.y], T, 0.f, nullptr, anc);
+    }
   }
   for (int idx = tid; idx < n * (DK / 4); idx += NT) {
     const int i = idx / (DK / 4), c = (idx % (DK / 4)) * 4;
@@ -206,11 +217,13 @@ __global__ void __launch_bounds__(2 * D / NSPLIT, 512 / (2 * D / NSPLIT))
       const bool second = which >= 2;
       if (!second || has_b) {
         const int j = second ? jb : ja, l = second ? lb : la;
-        const float w = GATED ? expf(Acum[n + j] - Acum[l]) : 1.f;
+        // draft trees: a draft sees the buffer and its own path only
+        const bool on_path = !TREE || l < n || ((anc[j] >> (l - n)) & 1ull);
+        const float w = GATED && on_path ? expf(Acum[n + j] - Acum[l]) : 1.f;
         if ((which & 1) == 0)
-          sw[j * LM + l] = w * r;
+          sw[j * LM + l] = on_path ? w * r : 0.f;
         else
-          cw[j * LM + l] = (l < n + j) ? w * r : 0.f;
+          cw[j * LM + l] = (on_path && l < n + j) ? w * r : 0.f;
       }
     }
   }
@@ -311,9 +324,10 @@ __global__ void __launch_bounds__(2 * D / NSPLIT, 512 / (2 * D / NSPLIT))
 // outputs); q and k come from bf16 and are exact in tf32.  Used for bf16
 // pools at d = 128; the fp32 path keeps verify_kernel.
 
-template <int VARIANT>
+template <int VARIANT, bool TREE>
 __global__ void __launch_bounds__(128, 4)
-    verify_mma_kernel(const PoolView P, const RowBatch rows, const TokenIO io) {
+    verify_mma_kernel(const PoolView P, const RowBatch rows, const TokenIO io,
+                      const __grid_constant__ TreeArg<TREE> tree) {
   using KT = __nv_bfloat16;
   constexpr int D = 128, DK = D, DV = D, NT = 128, NW = 4, E = 4;
   constexpr bool DELTA = VARIANT == kGatedDelta, GATED = VARIANT != kPlain;
@@ -347,6 +361,7 @@ __global__ void __launch_bounds__(128, 4)
   size_t *koff = reinterpret_cast<size_t *>(bt + ((T + 1) & ~1));
   size_t *voff = koff + LM;
   __shared__ int bad;
+  __shared__ unsigned long long anc[KVB_MAX_DRAFTS];  // draft trees: ancestor sets
 
   const float *Sp = P.state + (has_state ? ((size_t)d.slot * P.Hv + h) * DK * DV : 0);
   const int cbase = warp * 32 + 4 * g;  // this lane's four columns
@@ -397,13 +412,22 @@ __global__ void __launch_bounds__(128, 4)
       const float *lg = io.log_g;
       for (int i = lane; i < n; i += 32) Acum[i] = P.gbuf[voff[i]];
       const float A_prev = n > 0 ? P.gbuf[voff[n - 1]] : 0.f;
-      warp_prefix(
-          T, [&](int j) { return lg ? lg[(b * T + j) * P.Hv + h] : 0.f; }, Acum + n, lane);
-      __syncwarp();
-      for (int j = lane; j < T; j += 32) Acum[n + j] += A_prev;
+      if constexpr (TREE) {  // cumulative along each draft's path
+        for (int j = lane; j < T; j += 32) Acum[n + j] = lg ? lg[(b * T + j) * P.Hv + h] : 0.f;
+        __syncwarp();
+        if (lane == 0) tree_walk(tree.p[blockIdx.y], T, A_prev, Acum + n, anc);
+      } else {
+        warp_prefix(
+            T, [&](int j) { return lg ? lg[(b * T + j) * P.Hv + h] : 0.f; }, Acum + n, lane);
+        __syncwarp();
+        for (int j = lane; j < T; j += 32) Acum[n + j] += A_prev;
+      }
     }
   } else {
     for (int i = tid; i < L; i += NT) Acum[i] = 0.f;
+    if constexpr (TREE) {
+      if (tid == 0) tree_walk(tree.p[blockIdx.y], T, 0.f, nullptr, anc);
+    }
   }
   for (int idx = tid; idx < n * (DK / 4); idx += NT) {
     const int i = idx / (DK / 4), c = (idx % (DK / 4)) * 4;
@@ -495,11 +519,13 @@ __global__ void __launch_bounds__(128, 4)
       const bool second = which >= 2;
       if (!second || has_b) {
         const int j = second ? jb : ja, l = second ? lb : la;
-        const float w = GATED ? expf(Acum[n + j] - Acum[l]) : 1.f;
+        // draft trees: a draft sees the buffer and its own path only
+        const bool on_path = !TREE || l < n || ((anc[j] >> (l - n)) & 1ull);
+        const float w = GATED && on_path ? expf(Acum[n + j] - Acum[l]) : 1.f;
         if ((which & 1) == 0)
-          sw[j * LM + l] = w * r;
+          sw[j * LM + l] = on_path ? w * r : 0.f;
         else
-          cw[j * LM + l] = (l < n + j) ? w * r : 0.f;
+          cw[j * LM + l] = (on_path && l < n + j) ? w * r : 0.f;
       }
     }
   }
@@ -555,19 +581,19 @@ static size_t verify_mma_smem(int variant, int T, int LM) {
   return floats * sizeof(float) + 2 * (size_t)LM * sizeof(size_t);
 }
 
-template <int VARIANT>
+template <int VARIANT, bool TREE>
 static cudaError_t run_verify_mma(const PoolView &P, const RowBatch &rows, const TokenIO &io,
-                                  cudaStream_t stream) {
+                                  const TreeArg<TREE> &tree, cudaStream_t stream) {
   const size_t smem = verify_mma_smem(VARIANT, io.T, io.lmax);
   static size_t configured = 0;
   if (smem > configured) {
-    cudaError_t e = cudaFuncSetAttribute(verify_mma_kernel<VARIANT>,
+    cudaError_t e = cudaFuncSetAttribute(verify_mma_kernel<VARIANT, TREE>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     configured = smem;
   }
   dim3 grid(P.Hv, rows.count);
-  verify_mma_kernel<VARIANT><<<grid, 128, smem, stream>>>(P, rows, io);
+  verify_mma_kernel<VARIANT, TREE><<<grid, 128, smem, stream>>>(P, rows, io, tree);
   return cudaGetLastError();
 }
 
@@ -579,61 +605,127 @@ static size_t verify_smem(int d, int split, int T, int LM) {
   return floats * sizeof(float) + 2 * (size_t)LM * sizeof(size_t);
 }
 
-template <typename KT, int VARIANT, int D>
+template <typename KT, int VARIANT, int D, bool TREE>
 static cudaError_t run_verify(const PoolView &P, const RowBatch &rows, const TokenIO &io,
-                              cudaStream_t stream) {
+                              const TreeArg<TREE> &tree, cudaStream_t stream) {
   constexpr int NS = D == 128 ? 2 : 1;
   static bool configured = false;
   if (!configured) {
     const size_t most = verify_smem(D, NS, kMaxTok - 1, kMaxTok - 1);
-    cudaError_t e = cudaFuncSetAttribute(verify_kernel<KT, VARIANT, D, NS>,
+    cudaError_t e = cudaFuncSetAttribute(verify_kernel<KT, VARIANT, D, NS, TREE>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)most);
     if (e != cudaSuccess) return e;
     configured = true;
   }
   const size_t smem = verify_smem(D, NS, io.T, io.lmax);
   dim3 grid(P.Hv * NS, rows.count);
-  verify_kernel<KT, VARIANT, D, NS><<<grid, 2 * D / NS, smem, stream>>>(P, rows, io);
+  verify_kernel<KT, VARIANT, D, NS, TREE><<<grid, 2 * D / NS, smem, stream>>>(P, rows, io, tree);
   return cudaGetLastError();
 }
 
-template <typename KT, int VARIANT>
+template <typename KT, int VARIANT, bool TREE>
 static cudaError_t verify_d(const PoolView &P, const RowBatch &rows, const TokenIO &io, int d,
-                            cudaStream_t s) {
-  if (d == 128) return run_verify<KT, VARIANT, 128>(P, rows, io, s);
-  if (d == 64) return run_verify<KT, VARIANT, 64>(P, rows, io, s);
+                            const TreeArg<TREE> &tree, cudaStream_t s) {
+  if (d == 128) return run_verify<KT, VARIANT, 128, TREE>(P, rows, io, tree, s);
+  if (d == 64) return run_verify<KT, VARIANT, 64, TREE>(P, rows, io, tree, s);
   return kUnsupported;
 }
 
-template <typename KT>
+template <typename KT, bool TREE>
 static cudaError_t verify_variant(const PoolView &P, const RowBatch &rows, const TokenIO &io,
-                                  int variant, int d, cudaStream_t s) {
+                                  int variant, int d, const TreeArg<TREE> &tree, cudaStream_t s) {
   switch (variant) {
-    case kPlain: return verify_d<KT, kPlain>(P, rows, io, d, s);
-    case kGated: return verify_d<KT, kGated>(P, rows, io, d, s);
-    case kGatedDelta: return verify_d<KT, kGatedDelta>(P, rows, io, d, s);
+    case kPlain: return verify_d<KT, kPlain, TREE>(P, rows, io, d, tree, s);
+    case kGated: return verify_d<KT, kGated, TREE>(P, rows, io, d, tree, s);
+    case kGatedDelta: return verify_d<KT, kGatedDelta, TREE>(P, rows, io, d, tree, s);
+  }
+  return kUnsupported;
+}
+
+template <bool TREE>
+static cudaError_t verify_dispatch(const PoolView &P, const RowBatch &rows, const TokenIO &io,
+                                   int variant, int dtype, int d, const TreeArg<TREE> &tree,
+                                   cudaStream_t stream) {
+  if (dtype == 0) return verify_variant<float, TREE>(P, rows, io, variant, d, tree, stream);
+  if (dtype == 1) {
+    // tensor-core path for bf16 pools at d = 128 when its shared memory fits
+    if (d == 128 && verify_mma_smem(variant, io.T, io.lmax) <= 227 * 1024 - 1024) {
+      switch (variant) {
+        case kPlain: return run_verify_mma<kPlain, TREE>(P, rows, io, tree, stream);
+        case kGated: return run_verify_mma<kGated, TREE>(P, rows, io, tree, stream);
+        case kGatedDelta: return run_verify_mma<kGatedDelta, TREE>(P, rows, io, tree, stream);
+      }
+    }
+    return verify_variant<__nv_bfloat16, TREE>(P, rows, io, variant, d, tree, stream);
   }
   return kUnsupported;
 }
 
 cudaError_t launch_verify(const PoolView &P, const RowBatch &rows, const TokenIO &io, int variant,
-                          int dtype, int d, int max_len, cudaStream_t stream) {
+                          int dtype, int d, int max_len, cudaStream_t stream,
+                          const TreeArg<true> *tree) {
   if (rows.count <= 0) return cudaSuccess;
   TokenIO io2 = io;
   io2.lmax = max_len;
-  if (dtype == 0) return verify_variant<float>(P, rows, io2, variant, d, stream);
-  if (dtype == 1) {
-    // tensor-core path for bf16 pools at d = 128 when its shared memory fits
-    if (d == 128 && verify_mma_smem(variant, io2.T, io2.lmax) <= 227 * 1024 - 1024) {
-      switch (variant) {
-        case kPlain: return run_verify_mma<kPlain>(P, rows, io2, stream);
-        case kGated: return run_verify_mma<kGated>(P, rows, io2, stream);
-        case kGatedDelta: return run_verify_mma<kGatedDelta>(P, rows, io2, stream);
-      }
-    }
-    return verify_variant<__nv_bfloat16>(P, rows, io2, variant, d, stream);
+  if (tree) {
+    if (rows.count > kTreeRows) return kUnsupported;
+    return verify_dispatch<true>(P, rows, io2, variant, dtype, d, *tree, stream);
   }
-  return kUnsupported;
+  return verify_dispatch<false>(P, rows, io2, variant, dtype, d, TreeArg<false>{}, stream);
+}
+
+// ------------------------------------------------------------------ tree accept
+// Compaction after a draft tree is accepted: the accepted path's entries (key,
+// value, pseudo-value, cumulative gate, beta) move to the front of the draft
+// slots in path order.  Path positions are visited in order with a barrier in
+// between: the entry read at position l (slot n + path[l], path[l] >= l) is
+// never one written before it, and a slot written at l is read only at an
+// earlier position.  One CTA per (row, value head); the key rows of a q/k head
+// are moved by its first value head.
+template <typename KT>
+__global__ void __launch_bounds__(128)
+    tree_compact_kernel(const PoolView P, const RowBatch rows,
+                        const __grid_constant__ TreeArg<true> path, int D, int delta) {
+  const RowDesc d = rows.r[blockIdx.y];
+  const int h = blockIdx.x, group = P.Hv / P.Hk, hq = h / group;
+  const int n = d.n, len = d.flags;
+  KT *kb = static_cast<KT *>(P.kbuf);
+  KT *vb = static_cast<KT *>(P.vbuf);
+  for (int l = 0; l < len; ++l) {
+    const int src = path.p[blockIdx.y][l];
+    if (src == l) continue;  // uniform over the CTA
+    const int gs = buffer_row(P, d, n + src), gd = buffer_row(P, d, n + l);
+    if (gs < 0 || gd < 0) return;  // uniform; recorded in the error word
+    const size_t vs = kv_row(P, gs, h, P.Hv), vd = kv_row(P, gd, h, P.Hv);
+    for (int c = threadIdx.x; c < D; c += blockDim.x) vb[vd * D + c] = vb[vs * D + c];
+    if (delta)
+      for (int c = threadIdx.x; c < D; c += blockDim.x) P.ubuf[vd * D + c] = P.ubuf[vs * D + c];
+    if (threadIdx.x == 0) {
+      P.gbuf[vd] = P.gbuf[vs];
+      P.bbuf[vd] = P.bbuf[vs];
+    }
+    if (h % group == 0) {
+      const size_t ks = kv_row(P, gs, hq, P.Hk) * D, kd = kv_row(P, gd, hq, P.Hk) * D;
+      for (int c = threadIdx.x; c < D; c += blockDim.x) kb[kd + c] = kb[ks + c];
+    }
+    __syncthreads();
+  }
+}
+
+cudaError_t launch_tree_compact(const PoolView &P, const RowBatch &rows,
+                                const TreeArg<true> &path, int variant, int dtype, int d,
+                                cudaStream_t stream) {
+  if (rows.count <= 0) return cudaSuccess;
+  if (rows.count > kTreeRows) return kUnsupported;
+  dim3 grid(P.Hv, rows.count);
+  const int delta = variant == kGatedDelta;
+  if (dtype == 0)
+    tree_compact_kernel<float><<<grid, 128, 0, stream>>>(P, rows, path, d, delta);
+  else if (dtype == 1)
+    tree_compact_kernel<__nv_bfloat16><<<grid, 128, 0, stream>>>(P, rows, path, d, delta);
+  else
+    return kUnsupported;
+  return cudaGetLastError();
 }
 
 }  // namespace kvb

@@ -33,7 +33,8 @@ EXPORTS = ("kvb_pool_layout", "kvb_alloc_pool", "kvb_free_pool", "kvb_set_reques
            "kvb_release_request", "kvb_decode", "kvb_short_ctx", "kvb_flush", "kvb_prefill",
            "kvb_promote",
            "kvb_verify",
-           "kvb_accept", "kvb_verify_tempstate", "kvb_accept_tempstate",
+           "kvb_accept", "kvb_verify_tree", "kvb_accept_tree", "kvb_verify_tempstate",
+           "kvb_accept_tempstate",
            "kvb_verify_tempstate_static", "kvb_get_lengths", "kvb_get_device_lengths", "kvb_get_error",
            "kvb_strerror", "kvb_copy_probe", "kvb_version")
 
@@ -90,6 +91,9 @@ def load_library(path: str = LIB_PATH):
                                                 _P]),
         "kvb_accept_tempstate": (ctypes.c_int, [_P, _I32, _I32, _I32P, _I32P, _P, _P]),
         "kvb_promote": (ctypes.c_int, [_P, _I32, _I32P, _I32P, _P]),
+        "kvb_verify_tree": (ctypes.c_int, [_P, _I32, _I32, _I32P, _I32P, _P, _P, _P, _P, _P, _P,
+                                           _P]),
+        "kvb_accept_tree": (ctypes.c_int, [_P, _I32, _I32P, _I32P, _P]),
         "kvb_prefill": (ctypes.c_int, [_P, _I32, _I32, _I32P, _I32P, _P, _P, _P, _P, _P, _P,
                                        _I32, _P]),
         "kvb_verify_tempstate_static": (ctypes.c_int, [_P, _I32, _I32, _I32P, _P, _P, _P, _P, _P,
@@ -310,6 +314,27 @@ class Pool:
         if len(sl) != len(ids):
             raise ValueError("promote: one state slot per request")
         _check(self.lib.kvb_promote(self.handle, len(ids), p, ps, self._stream()), "kvb_promote")
+
+    def verify_tree(self, req_ids, parents, q, k, v, log_g=None, beta=None, o=None):
+        """kvb_verify_tree: drafts [B, T, ...] with parents [B, T] (host ints, -1 = root)."""
+        ids, p = _i32(req_ids)
+        B, T = len(ids), q.shape[1]
+        par, pp = _i32(np.asarray(parents).reshape(B, T))
+        c = self.cfg
+        if o is None:
+            o = self.torch.empty(B, T, c.n_v_heads, c.d_v, dtype=self.torch.float32,
+                                 device=self.device)
+        ptrs = self._token_ptrs((B, T), q, k, v, log_g, beta, o)
+        _check(self.lib.kvb_verify_tree(self.handle, B, T, p, pp, *ptrs, self._stream()),
+               "kvb_verify_tree")
+        return o
+
+    def accept_tree(self, req_ids, accepted):
+        """kvb_accept_tree: keep the root path of draft accepted[b] (-1: none)."""
+        ids, p = _i32(req_ids)
+        acc, pa = _i32(accepted)
+        _check(self.lib.kvb_accept_tree(self.handle, len(ids), p, pa, self._stream()),
+               "kvb_accept_tree")
 
     def verify_tempstate(self, req_ids, q, k, v, log_g=None, beta=None, temp=None, o=None):
         """The recurrent verify of the comparison baseline: returns (o, temp) where temp
