@@ -342,6 +342,41 @@ def measure_paths(kvb, torch, dev, peak):
             B * S >> 20, " (L2-resident)" if B * S < 100 * 2 ** 20 else ""))
         pool.close()
 
+    # draft tree: 8 drafts as a binary tree of depth 4 (every request the same shape)
+    # against a chain of 8, gated delta layer at B=256; accept(-1 / 0) keeps the buffer
+    L, B, T, n0 = I.GDN_LAYER, 256, 8, 3
+    pool = pool_for(L, B, 8, 2)
+    req = np.arange(B, dtype=np.int32)
+    pre = tokens(L, (B,), 5)
+    for _ in range(n0):
+        pool.decode(req, *pre)
+    drafts = tokens(L, (B, T), 7)
+    parents = np.tile(np.array([-1, 0, 0, 1, 1, 2, 2, 3], dtype=np.int32), (B, 1))
+    none = np.full(B, -1, dtype=np.int32)
+    zero = np.zeros(B, dtype=np.int32)
+    o_t = torch.empty(B, T, L.n_v_heads, L.d_v, dtype=torch.float32, device=dev)
+
+    def tree_round():
+        pool.verify_tree(req, parents, *drafts, o=o_t)
+        pool.accept_tree(req, none)
+
+    def chain_round():
+        pool.verify(req, *drafts, o=o_t)
+        pool.accept(req, zero)
+    us_tree = timed(tree_round, 30)
+    us_chain = timed(chain_round, 30)
+    S = L.n_v_heads * L.d_k * L.d_v * 4
+    q = L.n_qk_heads * L.d_k * 2
+    o = L.n_v_heads * L.d_v * 4
+    e = _entry_bytes(L)
+    nbytes = B * (S + T * (q + 2 * e + o) + n0 * e)
+    rec("verify_tree_gated_delta_B256_T8", us_tree, nbytes,
+        "binary draft tree of depth 4 (8 drafts) + accept_tree(-1) per round; two launches "
+        "of 128 rows")
+    out["verify_tree_gated_delta_B256_T8"]["chain_T8_us"] = us_chain
+    del o_t
+    pool.close()
+
     # verify latency against the number of drafts: buffered verify vs the recurrent
     # temporary-state baseline (Figure 2), gated delta layer at B=256, plus the memory
     # each needs per request (state + buffer slots vs state + T temporary states)
