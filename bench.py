@@ -121,7 +121,7 @@ def prefill_flops(L, n_tokens, chunk=64):
 
 def kernel_hash():
     h = hashlib.sha256()
-    for rel in ("kv_buffered_decoding_gb300/csrc/decode.cu",
+    for rel in ("kv_buffered_decoding_gb300/csrc/decode_stream.cu",
                 "kv_buffered_decoding_gb300/csrc/kvb_device.cuh"):
         with open(os.path.join(ROOT, rel), "rb") as f:
             h.update(f.read())
@@ -702,7 +702,7 @@ def run_ours(args, rank, world, local_rank):
         "hbm_gbs": achieved,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": ncu_traffic(),
-                     "kernel": "decode_kernel<bf16, gated_delta, 128>",
+                     "kernel": "decode_stream_kernel<bf16, gated_delta> (persistent, d=128)",
                      "algorithmic_bytes_per_launch": bytes_per_launch,
                      "mean_launch_us": mean_launch_s * 1e6, "peak_source": peak_src},
         "copy_probe_gbs": copy_gbs,

@@ -1,0 +1,356 @@
+// Buffered decode as a persistent, software-pipelined kernel (d = 128).
+//
+// The arithmetic is the one of decode_kernel (decode.cu; "KVBuffer: IO-aware
+// Serving for Linear Attention", Figure 1): o_t = e^{A_t} S0^T q_t +
+// sum_{i<=t} e^{A_t-A_i} (q_t.k_i) u_i with the gated-delta pseudo-value u_t,
+// and a fold S <- e^{A_t} S0 + sum_i e^{A_t-A_i} k_i u_i^T when the buffer fills.
+// What changes is how the bytes move.  A work item is one (row, value head,
+// half of the state columns): a 32 KB tile of S0 plus the token's q/k/v and up
+// to kStageTok buffered tokens.  Each CTA walks items c, c + G, c + 2G, ...
+// (G = resident CTAs): once item i's tile has moved from shared memory into
+// registers, cp.async brings item i + G's tile into the same buffer and every
+// small operand (q, k_t, v_t, buffered keys, pseudo-values, cumulative gates)
+// into the other of two small stages, while item i computes.  HBM then streams without gaps, instead of idling
+// while every resident CTA of an SM computes.  The tile is stored with its
+// 16-byte chunks XOR-swizzled on row bit 4, so the per-thread reads (16 rows x
+// 4 columns) are free of bank conflicts.
+#include "kvb_device.cuh"
+
+namespace kvb {
+namespace {
+
+constexpr int kD = 128, kCW = 64;       // head dim; state columns per item
+constexpr int kTileF4 = kD * kCW / 4;   // float4 chunks of a tile (2048)
+constexpr int kStreamThreads = 128;
+
+// The small operands of one item (double-buffered); the state tile has a
+// single buffer, refilled as soon as the tile has moved into registers.
+template <typename KT>
+struct alignas(16) Stage {
+  KT q[kD], k[kD];                      // current token's q and k (raw)
+  KT v[kCW];                            // current token's v, this item's columns
+  KT keys[kStageTok][kD];               // buffered keys (raw)
+  float uv[kStageTok][kCW];             // buffered u (gated delta) / v, this item's columns
+  float A[kStageTok];                   // buffered cumulative log-gates
+  float a_t, beta_t;
+  size_t koff[kStageTok + 1], voff[kStageTok + 1];  // tokens 0..n (n: this token's slot)
+  int bad;
+};
+
+__device__ __forceinline__ int tile_slot(int r, int ch) { return r * 16 + (ch ^ (((r >> 4) & 1) << 2)); }
+
+__device__ __forceinline__ void cp16(void *smem, const void *gmem) {
+  const unsigned s = static_cast<unsigned>(__cvta_generic_to_shared(smem));
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(s), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void cp4(void *smem, const void *gmem) {
+  const unsigned s = static_cast<unsigned>(__cvta_generic_to_shared(smem));
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;\n" ::"r"(s), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+__device__ __forceinline__ void cp_wait_all() { asm volatile("cp.async.wait_group 0;\n" ::: "memory"); }
+
+// Four consecutive raw values as floats (fp32: one 16-byte load; bf16: 8 bytes).
+__device__ __forceinline__ float4 raw4(const float *p) { return *reinterpret_cast<const float4 *>(p); }
+__device__ __forceinline__ float4 raw4(const __nv_bfloat16 *p) {
+  const uint2 w = *reinterpret_cast<const uint2 *>(p);
+  return make_float4(__uint_as_float(w.x << 16), __uint_as_float(w.x & 0xffff0000u),
+                     __uint_as_float(w.y << 16), __uint_as_float(w.y & 0xffff0000u));
+}
+
+template <typename KT, int VARIANT>
+__global__ void __launch_bounds__(kStreamThreads, 4)
+    decode_stream_kernel(const PoolView P, const RowBatch rows, const TokenIO io, int items) {
+  constexpr bool DELTA = VARIANT == kGatedDelta, GATED = VARIANT != kPlain;
+  constexpr int RPT = 16, E = kD / 32;
+  constexpr int VEC = 16 / (int)sizeof(KT);  // elements per 16-byte copy
+  constexpr int NQ = kD / VEC;               // 16-byte chunks of q (or k, or a key)
+  constexpr int NV = kCW / VEC;              // 16-byte chunks of v_t's columns
+  constexpr int NU = DELTA ? kCW / 4 : kCW / VEC;  // chunks of a buffered u / v row part
+  using St = Stage<KT>;
+  extern __shared__ float4 dyn_smem[];
+  float4 *tile = dyn_smem;                                // [kTileF4] swizzled
+  St *stages = reinterpret_cast<St *>(dyn_smem + kTileF4);  // [2]
+  __shared__ __align__(16) float qs[kD], kts[kD];
+  __shared__ float wt[kStageTok + 1], sc[kStageTok + 1], cc[kStageTok + 1];
+  __shared__ float e_t_s, At_s;
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int rsub = lane >> 2, row0 = rsub * RPT;
+  const int chunk = warp * 4 + (lane & 3);  // this thread's float4 column chunk in the item
+  const int colL = chunk * 4;               // ... as a column within the item's 64
+  const int group = P.Hv / P.Hk;
+  const int per_row = P.Hv * 2;
+
+  // stage item `it`: its tile into the tile buffer, the rest into stages[st];
+  // every thread commits one cp.async group
+  auto issue = [&](int it, int st) {
+    St &S = stages[st];
+    const int y = it / per_row, x = it - y * per_row, h = x >> 1, part = x & 1;
+    const RowDesc d = rows.r[y];
+    const size_t b = (size_t)rows.row0 + y;
+    const int hq = h / group, n = d.n;
+    const float *Sp = P.state + ((size_t)d.slot * P.Hv + h) * kD * kD + part * kCW;
+    for (int i = tid; i < kTileF4; i += kStreamThreads) {
+      const int r = i >> 4, ch = i & 15;
+      cp16(&tile[tile_slot(r, ch)], Sp + (size_t)r * kD + ch * 4);
+    }
+    const KT *qg = static_cast<const KT *>(io.q) + (b * P.Hk + hq) * kD;
+    const KT *kg = static_cast<const KT *>(io.k) + (b * P.Hk + hq) * kD;
+    const KT *vg = static_cast<const KT *>(io.v) + (b * P.Hv + h) * kD + part * kCW;
+    if (tid < NQ) {
+      cp16(&S.q[tid * VEC], qg + tid * VEC);
+    } else if (tid < 2 * NQ) {
+      cp16(&S.k[(tid - NQ) * VEC], kg + (tid - NQ) * VEC);
+    } else if (tid < 2 * NQ + NV) {
+      cp16(&S.v[(tid - 2 * NQ) * VEC], vg + (tid - 2 * NQ) * VEC);
+    } else if (tid == kStreamThreads - 1) {
+      if (GATED && io.log_g) cp4(&S.a_t, io.log_g + b * P.Hv + h);
+      else S.a_t = 0.f;
+    } else if (tid == kStreamThreads - 2) {
+      if (DELTA) cp4(&S.beta_t, io.beta + b * P.Hv + h);
+      else S.beta_t = 0.f;
+    }
+    if (warp == 0) {  // where tokens 0..n live, then their keys, u / v and gates
+      int anybad = 0;
+      for (int i = lane; i <= n; i += 32) {
+        const int g = buffer_row(P, d, i);
+        anybad |= (g < 0);
+        if (g >= 0) {
+          S.koff[i] = kv_row(P, g, hq, P.Hk) * kD;
+          S.voff[i] = kv_row(P, g, h, P.Hv);
+        }
+      }
+      anybad = __any_sync(kFull, anybad);
+      if (lane == 0) S.bad = anybad;
+      __syncwarp();
+      if (!anybad) {
+        const KT *kb = static_cast<const KT *>(P.kbuf);
+        for (int c = lane; c < n * NQ; c += 32) {
+          const int i = c / NQ, p = c - i * NQ;
+          cp16(&S.keys[i][p * VEC], kb + S.koff[i] + p * VEC);
+        }
+        for (int c = lane; c < n * NU; c += 32) {
+          const int i = c / NU, p = c - i * NU;
+          if (DELTA)
+            cp16(&S.uv[i][p * 4], P.ubuf + S.voff[i] * kD + part * kCW + p * 4);
+          else  // raw values land in the first half of the row; widened when read
+            cp16(reinterpret_cast<KT *>(S.uv[i]) + p * VEC,
+                 static_cast<const KT *>(P.vbuf) + S.voff[i] * kD + part * kCW + p * VEC);
+        }
+        if (GATED)
+          for (int i = lane; i < n; i += 32) cp4(&S.A[i], P.gbuf + S.voff[i]);
+      }
+    }
+    cp_commit();
+  };
+
+  int it = blockIdx.x, st = 0;
+  if (it < items) issue(it, 0);
+  for (; it < items; it += gridDim.x, st ^= 1) {
+    cp_wait_all();
+    __syncthreads();  // item `it` staged; every thread is done with the other stage
+    const St &S = stages[st];
+    const bool bad = S.bad != 0;  // CTA-uniform; the error is recorded
+
+    const int y = it / per_row, x = it - y * per_row, h = x >> 1, part = x & 1;
+    const bool lead = part == 0;
+    const RowDesc d = rows.r[y];
+    const size_t b = (size_t)rows.row0 + y;
+    const int n = d.n;
+    const bool fold = (d.flags & kFlagFlush) != 0;
+    const int col0 = part * kCW + colL;  // this thread's global column
+
+    // 1. tile into registers; q, k_t as floats; then the next item streams in
+    float4 s[RPT];
+#pragma unroll
+    for (int j = 0; j < RPT; ++j) s[j] = tile[tile_slot(row0 + j, chunk)];
+    qs[tid] = P.scale * to_float(S.q[tid]);
+    kts[tid] = to_float(S.k[tid]);
+    if (GATED && warp == 0 && lane == 0) {
+      const float A_prev = n > 0 && !bad ? S.A[n - 1] : 0.f;
+      At_s = A_prev + S.a_t;
+    }
+    __syncthreads();  // the tile buffer is free
+    if (it + (int)gridDim.x < items) issue(it + gridDim.x, st ^ 1);
+    if (bad) continue;
+
+    // 2. S0^T q_t and S0^T k_t over this thread's rows
+    float4 aq = f4(0.f), ak = f4(0.f);
+#pragma unroll
+    for (int j = 0; j < RPT; j += 4) {
+      const float4 q4 = *reinterpret_cast<const float4 *>(&qs[row0 + j]);
+      fma4(aq, q4.x, s[j]);
+      fma4(aq, q4.y, s[j + 1]);
+      fma4(aq, q4.z, s[j + 2]);
+      fma4(aq, q4.w, s[j + 3]);
+      if (DELTA) {
+        const float4 k4 = *reinterpret_cast<const float4 *>(&kts[row0 + j]);
+        fma4(ak, k4.x, s[j]);
+        fma4(ak, k4.y, s[j + 1]);
+        fma4(ak, k4.z, s[j + 2]);
+        fma4(ak, k4.w, s[j + 3]);
+      }
+    }
+
+    // 3. decay weights w_i = e^{A_t - A_i} (warp 0) and the dot products q.k_i,
+    //    k_t.k_i, two tokens per warp pass with one butterfly reduction
+    const float At = GATED ? At_s : 0.f;
+    if (warp == 0) {
+      for (int i = lane; i <= n; i += 32) wt[i] = GATED ? expf(At - (i < n ? S.A[i] : At)) : 1.f;
+      if (lane == 0) e_t_s = GATED ? expf(At) : 1.f;
+    }
+    for (int i0 = 2 * warp; i0 <= n; i0 += 8) {
+      const int i1 = i0 + 1;
+      float qv[E], tv[E], ka[E], kb[E];
+      load_smem<E>(qs + lane * E, qv);
+      load_smem<E>(kts + lane * E, tv);
+      if (i0 < n) {
+        const float4 r4 = raw4(&S.keys[i0][lane * E]);
+        ka[0] = r4.x; ka[1] = r4.y; ka[2] = r4.z; ka[3] = r4.w;
+      } else {
+#pragma unroll
+        for (int e = 0; e < E; ++e) ka[e] = tv[e];
+      }
+      if (i1 < n) {
+        const float4 r4 = raw4(&S.keys[i1][lane * E]);
+        kb[0] = r4.x; kb[1] = r4.y; kb[2] = r4.z; kb[3] = r4.w;
+      } else {
+#pragma unroll
+        for (int e = 0; e < E; ++e) kb[e] = (i1 == n) ? tv[e] : 0.f;
+      }
+      float qa = 0.f, qb = 0.f, ta = 0.f, tb = 0.f;
+#pragma unroll
+      for (int e = 0; e < E; ++e) {
+        qa = fmaf(qv[e], ka[e], qa);
+        qb = fmaf(qv[e], kb[e], qb);
+        if (DELTA) {
+          ta = fmaf(tv[e], ka[e], ta);
+          tb = fmaf(tv[e], kb[e], tb);
+        }
+      }
+      if (DELTA) {
+        const float r = butterfly4(qa, ta, qb, tb, lane);  // lanes 0, 8, 16, 24
+        const int which = lane >> 3;
+        if ((lane & 7) == 0) {
+          if (which == 0) sc[i0] = r;
+          else if (which == 1) cc[i0] = r;
+          else if (i1 <= n) (which == 2 ? sc : cc)[i1] = r;
+        }
+      } else {
+        const float r = butterfly2(qa, qb, lane);  // lanes 0, 16
+        if (lane == 0) sc[i0] = r;
+        else if (lane == 16 && i1 <= n) sc[i1] = r;
+      }
+    }
+    __syncthreads();
+
+    // 4. this lane's share of the buffered terms, one reduction over the row lanes
+    const float e_t = e_t_s;
+    float4 po = mul4(e_t, aq), pc = mul4(e_t, ak);
+    for (int i = rsub; i < n; i += 8) {
+      const float4 ui = DELTA ? *reinterpret_cast<const float4 *>(&S.uv[i][colL])
+                              : raw4(reinterpret_cast<const KT *>(S.uv[i]) + colL);
+      const float w = wt[i];
+      fma4(po, w * sc[i], ui);
+      if (DELTA) fma4(pc, w * cc[i], ui);
+    }
+    po = rows_sum4(po);
+    if (DELTA) pc = rows_sum4(pc);
+    const float4 vt = raw4(&S.v[colL]);
+    float4 ut = vt;
+    if (DELTA) {
+      const float bt = S.beta_t;
+      ut.x = bt * (vt.x - pc.x);
+      ut.y = bt * (vt.y - pc.y);
+      ut.z = bt * (vt.z - pc.z);
+      ut.w = bt * (vt.w - pc.w);
+    }
+    fma4(po, sc[n], ut);
+    if (rsub == 0) {
+      __stcs(reinterpret_cast<float4 *>(io.o + (b * P.Hv + h) * kD + col0), po);
+      st4(static_cast<KT *>(P.vbuf) + S.voff[n] * kD + col0, vt);
+      if (DELTA) st4(P.ubuf + S.voff[n] * kD + col0, ut);
+    }
+    if (lead) {
+      if (h % group == 0 && tid < kD / 4)
+        st4(static_cast<KT *>(P.kbuf) + S.koff[n] + 4 * tid,
+            *reinterpret_cast<const float4 *>(&kts[4 * tid]));
+      if (tid == 0) {
+        P.gbuf[S.voff[n]] = At;  // cumulative since the last fold (0 for the plain variant)
+        P.bbuf[S.voff[n]] = S.beta_t;
+      }
+    }
+
+    // 5. fold: S <- e^{A_t} S0 + sum_{i<=n} k_i (w_i u_i)^T, written back once
+    if (fold) {
+#pragma unroll
+      for (int j = 0; j < RPT; ++j) s[j] = mul4(e_t, s[j]);
+      for (int i = 0; i <= n; ++i) {
+        const float4 u = i < n ? mul4(wt[i], DELTA ? *reinterpret_cast<const float4 *>(&S.uv[i][colL])
+                                                   : raw4(reinterpret_cast<const KT *>(S.uv[i]) + colL))
+                               : ut;
+#pragma unroll
+        for (int j = 0; j < RPT; j += 4) {
+          const float4 k4 = i < n ? raw4(&S.keys[i][row0 + j])
+                                  : *reinterpret_cast<const float4 *>(&kts[row0 + j]);
+          fma4(s[j], k4.x, u);
+          fma4(s[j + 1], k4.y, u);
+          fma4(s[j + 2], k4.z, u);
+          fma4(s[j + 3], k4.w, u);
+        }
+      }
+      float *Sp = P.state + ((size_t)d.slot * P.Hv + h) * kD * kD;
+#pragma unroll
+      for (int j = 0; j < RPT; ++j) st_stream4(Sp + (size_t)(row0 + j) * kD + col0, s[j]);
+    }
+    if (h == 0 && lead && tid == 0) P.dlen[d.req] = fold ? 0 : n + 1;
+  }
+}
+
+template <typename KT, int VARIANT>
+cudaError_t run_stream(const PoolView &P, const RowBatch &rows, const TokenIO &io,
+                       cudaStream_t stream) {
+  constexpr size_t smem = kTileF4 * sizeof(float4) + 2 * sizeof(Stage<KT>);
+  static int grid_cap = 0;
+  if (grid_cap == 0) {
+    cudaError_t e = cudaFuncSetAttribute(decode_stream_kernel<KT, VARIANT>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    int dev = 0, sms = 0, per_sm = 0;
+    if (e == cudaSuccess) e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e == cudaSuccess)
+      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_stream_kernel<KT, VARIANT>,
+                                                        kStreamThreads, smem);
+    if (e != cudaSuccess) return e;
+    if (per_sm < 1) return kUnsupported;
+    grid_cap = sms * per_sm;
+  }
+  const int items = rows.count * P.Hv * 2;
+  const int grid = items < grid_cap ? items : grid_cap;
+  decode_stream_kernel<KT, VARIANT><<<grid, kStreamThreads, smem, stream>>>(P, rows, io, items);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_decode_stream(const PoolView &P, const RowBatch &rows, const TokenIO &io,
+                                 int variant, int dtype, cudaStream_t stream) {
+  if (rows.count <= 0) return cudaSuccess;
+  if (dtype == 1) {
+    switch (variant) {
+      case kPlain: return run_stream<__nv_bfloat16, kPlain>(P, rows, io, stream);
+      case kGated: return run_stream<__nv_bfloat16, kGated>(P, rows, io, stream);
+      case kGatedDelta: return run_stream<__nv_bfloat16, kGatedDelta>(P, rows, io, stream);
+    }
+  } else if (dtype == 0) {
+    switch (variant) {
+      case kPlain: return run_stream<float, kPlain>(P, rows, io, stream);
+      case kGated: return run_stream<float, kGated>(P, rows, io, stream);
+      case kGatedDelta: return run_stream<float, kGatedDelta>(P, rows, io, stream);
+    }
+  }
+  return kUnsupported;
+}
+
+}  // namespace kvb

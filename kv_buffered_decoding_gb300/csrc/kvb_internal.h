@@ -50,6 +50,10 @@ struct RowBatch {
   RowDesc r[kMaxRows];
 };
 
+// Buffered tokens the persistent decode (decode_stream.cu) stages per item;
+// launches whose rows hold more take decode_kernel.
+constexpr int kStageTok = 8;
+
 // Draft trees of one launch, carried in the kernel parameter block: for row i
 // of the launch and draft j, p[i][j] is the parent draft (-1: the last
 // accepted token), always < j.  Accept reuses it for the accepted path (the
@@ -107,6 +111,10 @@ cudaError_t launch_verify_tempstate_static(const PoolView &P, const RowBatch &ro
                                            cudaStream_t stream);
 cudaError_t launch_accept_tempstate_static(const PoolView &P, const RowBatch &rows, int T, int d,
                                            cudaStream_t stream);
+// Buffered decode (d = 128, at most kStageTok buffered tokens per row) as a
+// persistent pipelined kernel.
+cudaError_t launch_decode_stream(const PoolView &P, const RowBatch &rows, const TokenIO &io,
+                                 int variant, int dtype, cudaStream_t stream);
 // Chunked prefill of rows.r[i].n prompt tokens per row (io.T = padded length).
 cudaError_t launch_prefill(const PoolView &P, const RowBatch &rows, const TokenIO &io,
                            int variant, int dtype, int d, cudaStream_t stream);
