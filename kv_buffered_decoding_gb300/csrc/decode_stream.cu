@@ -95,51 +95,73 @@ __global__ void __launch_bounds__(kStreamThreads, 4)
       const int r = i >> 4, ch = i & 15;
       cp16(&tile[tile_slot(r, ch)], Sp + (size_t)r * kD + ch * 4);
     }
+    // small copies, dealt round-robin over the warps (each warp index runs on its
+    // own scheduler in every CTA, so per-warp work is kept even)
     const KT *qg = static_cast<const KT *>(io.q) + (b * P.Hk + hq) * kD;
     const KT *kg = static_cast<const KT *>(io.k) + (b * P.Hk + hq) * kD;
     const KT *vg = static_cast<const KT *>(io.v) + (b * P.Hv + h) * kD + part * kCW;
-    if (tid < NQ) {
-      cp16(&S.q[tid * VEC], qg + tid * VEC);
-    } else if (tid < 2 * NQ) {
-      cp16(&S.k[(tid - NQ) * VEC], kg + (tid - NQ) * VEC);
-    } else if (tid < 2 * NQ + NV) {
-      cp16(&S.v[(tid - 2 * NQ) * VEC], vg + (tid - 2 * NQ) * VEC);
-    } else if (tid == kStreamThreads - 1) {
-      if (GATED && io.log_g) cp4(&S.a_t, io.log_g + b * P.Hv + h);
-      else S.a_t = 0.f;
-    } else if (tid == kStreamThreads - 2) {
-      if (DELTA) cp4(&S.beta_t, io.beta + b * P.Hv + h);
-      else S.beta_t = 0.f;
-    }
-    if (warp == 0) {  // where tokens 0..n live, then their keys, u / v and gates
-      int anybad = 0;
-      for (int i = lane; i <= n; i += 32) {
-        const int g = buffer_row(P, d, i);
-        anybad |= (g < 0);
-        if (g >= 0) {
-          S.koff[i] = kv_row(P, g, hq, P.Hk) * kD;
-          S.voff[i] = kv_row(P, g, h, P.Hv);
-        }
+    constexpr int NSMALL = 2 * NQ + NV + 2;
+    for (int t = (tid & 31) * 4 + warp; t < NSMALL; t += kStreamThreads) {
+      if (t < NQ) {
+        cp16(&S.q[t * VEC], qg + t * VEC);
+      } else if (t < 2 * NQ) {
+        cp16(&S.k[(t - NQ) * VEC], kg + (t - NQ) * VEC);
+      } else if (t < 2 * NQ + NV) {
+        cp16(&S.v[(t - 2 * NQ) * VEC], vg + (t - 2 * NQ) * VEC);
+      } else if (t == 2 * NQ + NV) {
+        if (GATED && io.log_g) cp4(&S.a_t, io.log_g + b * P.Hv + h);
+        else S.a_t = 0.f;
+      } else {
+        if (DELTA) cp4(&S.beta_t, io.beta + b * P.Hv + h);
+        else S.beta_t = 0.f;
       }
-      anybad = __any_sync(kFull, anybad);
+    }
+    // buffered tokens: every warp finds where tokens 0..n live (lane i: token i);
+    // keys are copied by warps 0-1, u / v rows by warps 2-3, gates by warp 3
+    size_t ko = 0, vo = 0;
+    int anybad = 0;
+    if (lane <= n) {
+      const int g = buffer_row(P, d, lane);
+      anybad = g < 0;
+      if (g >= 0) {
+        ko = kv_row(P, g, hq, P.Hk) * kD;
+        vo = kv_row(P, g, h, P.Hv);
+      }
+    }
+    anybad = __any_sync(kFull, anybad);
+    if (warp == 3) {
+      if (lane <= n) {
+        S.koff[lane] = ko;
+        S.voff[lane] = vo;
+      }
       if (lane == 0) S.bad = anybad;
-      __syncwarp();
-      if (!anybad) {
+    }
+    if (!anybad) {
+      const int l2 = (warp & 1) * 32 + lane;  // lane among the two warps of a task
+      // (uniform trip counts: every lane of the warp takes part in each shuffle)
+      if (warp < 2) {
         const KT *kb = static_cast<const KT *>(P.kbuf);
-        for (int c = lane; c < n * NQ; c += 32) {
-          const int i = c / NQ, p = c - i * NQ;
-          cp16(&S.keys[i][p * VEC], kb + S.koff[i] + p * VEC);
+        for (int c0 = 0; c0 < n * NQ; c0 += 64) {
+          const int c = c0 + l2;
+          const bool ok = c < n * NQ;
+          const int i = ok ? c / NQ : 0, p = c - i * NQ;
+          const size_t off = __shfl_sync(kFull, ko, i);
+          if (ok) cp16(&S.keys[i][p * VEC], kb + off + p * VEC);
         }
-        for (int c = lane; c < n * NU; c += 32) {
-          const int i = c / NU, p = c - i * NU;
+      } else {
+        for (int c0 = 0; c0 < n * NU; c0 += 64) {
+          const int c = c0 + l2;
+          const bool ok = c < n * NU;
+          const int i = ok ? c / NU : 0, p = c - i * NU;
+          const size_t row = __shfl_sync(kFull, vo, i) * kD + part * kCW;
+          if (!ok) continue;
           if (DELTA)
-            cp16(&S.uv[i][p * 4], P.ubuf + S.voff[i] * kD + part * kCW + p * 4);
+            cp16(&S.uv[i][p * 4], P.ubuf + row + p * 4);
           else  // raw values land in the first half of the row; widened when read
             cp16(reinterpret_cast<KT *>(S.uv[i]) + p * VEC,
-                 static_cast<const KT *>(P.vbuf) + S.voff[i] * kD + part * kCW + p * VEC);
+                 static_cast<const KT *>(P.vbuf) + row + p * VEC);
         }
-        if (GATED)
-          for (int i = lane; i < n; i += 32) cp4(&S.A[i], P.gbuf + S.voff[i]);
+        if (GATED && warp == 3 && lane < n) cp4(&S.A[lane], P.gbuf + vo);
       }
     }
     cp_commit();
@@ -196,7 +218,7 @@ __global__ void __launch_bounds__(kStreamThreads, 4)
     // 3. decay weights w_i = e^{A_t - A_i} (warp 0) and the dot products q.k_i,
     //    k_t.k_i, two tokens per warp pass with one butterfly reduction
     const float At = GATED ? At_s : 0.f;
-    if (warp == 0) {
+    if (warp == 1) {
       for (int i = lane; i <= n; i += 32) wt[i] = GATED ? expf(At - (i < n ? S.A[i] : At)) : 1.f;
       if (lane == 0) e_t_s = GATED ? expf(At) : 1.f;
     }
@@ -273,9 +295,9 @@ __global__ void __launch_bounds__(kStreamThreads, 4)
       if (DELTA) st4(P.ubuf + S.voff[n] * kD + col0, ut);
     }
     if (lead) {
-      if (h % group == 0 && tid < kD / 4)
-        st4(static_cast<KT *>(P.kbuf) + S.koff[n] + 4 * tid,
-            *reinterpret_cast<const float4 *>(&kts[4 * tid]));
+      if (h % group == 0 && warp == 2)  // 32 lanes x 4 elements of k_t
+        st4(static_cast<KT *>(P.kbuf) + S.koff[n] + 4 * lane,
+            *reinterpret_cast<const float4 *>(&kts[4 * lane]));
       if (tid == 0) {
         P.gbuf[S.voff[n]] = At;  // cumulative since the last fold (0 for the plain variant)
         P.bbuf[S.voff[n]] = S.beta_t;
