@@ -60,7 +60,8 @@ __device__ __forceinline__ float4 raw4(const __nv_bfloat16 *p) {
 
 template <typename KT, int VARIANT>
 __global__ void __launch_bounds__(kStreamThreads, 4)
-    decode_stream_kernel(const PoolView P, const RowBatch rows, const TokenIO io, int items) {
+    decode_stream_kernel(const PoolView P, const __grid_constant__ RowBatch rows, const TokenIO io,
+                         int items, FastDiv per_row_div) {
   constexpr bool DELTA = VARIANT == kGatedDelta, GATED = VARIANT != kPlain;
   constexpr int RPT = 16, E = kD / 32;
   constexpr int VEC = 16 / (int)sizeof(KT);  // elements per 16-byte copy
@@ -86,8 +87,8 @@ __global__ void __launch_bounds__(kStreamThreads, 4)
   // every thread commits one cp.async group
   auto issue = [&](int it, int st) {
     St &S = stages[st];
-    const int y = it / per_row, x = it - y * per_row, h = x >> 1, part = x & 1;
-    const RowDesc d = rows.r[y];
+    const int y = fast_div(it, per_row_div), x = it - y * per_row, h = x >> 1, part = x & 1;
+    const RowDesc &d = rows.r[y];
     const size_t b = (size_t)rows.row0 + y;
     const int hq = h / group, n = d.n;
     const float *Sp = P.state + ((size_t)d.slot * P.Hv + h) * kD * kD + part * kCW;
@@ -175,9 +176,9 @@ __global__ void __launch_bounds__(kStreamThreads, 4)
     const St &S = stages[st];
     const bool bad = S.bad != 0;  // CTA-uniform; the error is recorded
 
-    const int y = it / per_row, x = it - y * per_row, h = x >> 1, part = x & 1;
+    const int y = fast_div(it, per_row_div), x = it - y * per_row, h = x >> 1, part = x & 1;
     const bool lead = part == 0;
-    const RowDesc d = rows.r[y];
+    const RowDesc &d = rows.r[y];
     const size_t b = (size_t)rows.row0 + y;
     const int n = d.n;
     const bool fold = (d.flags & kFlagFlush) != 0;
@@ -350,7 +351,8 @@ cudaError_t run_stream(const PoolView &P, const RowBatch &rows, const TokenIO &i
   }
   const int items = rows.count * P.Hv * 2;
   const int grid = items < grid_cap ? items : grid_cap;
-  decode_stream_kernel<KT, VARIANT><<<grid, kStreamThreads, smem, stream>>>(P, rows, io, items);
+  decode_stream_kernel<KT, VARIANT><<<grid, kStreamThreads, smem, stream>>>(
+      P, rows, io, items, make_fastdiv((uint32_t)P.Hv * 2));
   return cudaGetLastError();
 }
 

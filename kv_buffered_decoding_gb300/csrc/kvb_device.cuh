@@ -164,13 +164,13 @@ __device__ __forceinline__ void record_error(int32_t *err, int32_t kind, int32_t
 // if the block id is out of range (the error is recorded).  The first
 // kRowBlocks blocks come with the descriptor; later ones from the block table.
 __device__ __forceinline__ int buffer_row(const PoolView &P, const RowDesc &d, int p) {
-  const int bi = p / P.bs;
+  const int bi = P.bs_shift >= 0 ? p >> P.bs_shift : p / P.bs;
   const int blk = bi < kRowBlocks ? d.blk[bi] : P.table[(size_t)d.req * P.max_blocks + bi];
   if (blk < 0 || blk >= P.num_blocks) {
     record_error(P.err, kErrBlockRange, d.req, blk);
     return -1;
   }
-  return blk * P.bs + p % P.bs;
+  return blk * P.bs + (p - bi * P.bs);
 }
 
 // Row index of buffer row g (= block * block_size + slot) for one head, in a
@@ -178,7 +178,7 @@ __device__ __forceinline__ int buffer_row(const PoolView &P, const RowDesc &d, i
 // slots are contiguous, so a request's buffered tokens for one head form one
 // contiguous run.
 __device__ __forceinline__ size_t kv_row(const PoolView &P, int g, int head, int nheads) {
-  const int blk = g / P.bs, pos = g - blk * P.bs;
+  const int blk = P.bs_shift >= 0 ? g >> P.bs_shift : g / P.bs, pos = g - blk * P.bs;
   return ((size_t)blk * nheads + head) * P.bs + pos;
 }
 
@@ -212,6 +212,11 @@ __device__ __forceinline__ void tree_walk(const int8_t *parent, int T, float A_r
     anc[j] = (p < 0 ? 0ull : anc[p]) | (1ull << j);
     if (A) A[j] += p < 0 ? A_root : A[p];
   }
+}
+
+// n / d for a divisor prepared by make_fastdiv (0 <= n < 2^31).
+__device__ __forceinline__ int fast_div(int n, FastDiv f) {
+  return (int)((__umulhi((uint32_t)n, f.m) + (uint32_t)n) >> f.s);
 }
 
 // ------------------------------------------------------------------ tensor cores

@@ -274,6 +274,9 @@ int kvb_alloc_pool(const kvb_config *cfg, void *state_mem, void *kv_mem, void *m
   v.Hk = cfg->n_qk_heads;
   v.Hv = cfg->n_v_heads;
   v.bs = cfg->block_size;
+  v.bs_shift = -1;
+  for (int sh = 0; sh < 31; ++sh)
+    if (cfg->block_size == (1 << sh)) v.bs_shift = sh;
   v.max_blocks = cfg->max_blocks_per_req;
   v.num_blocks = cfg->num_blocks;
   v.scale = cfg->scale;

@@ -32,7 +32,23 @@ struct PoolView {
   int32_t *err;       // [4] error word: kind, request, value, count
   int Hk, Hv, bs, max_blocks, num_blocks;
   float scale;
+  int bs_shift;  // log2(bs) when bs is a power of two, else -1
 };
+
+// Division by a fixed divisor d >= 1 for 0 <= n < 2^31 as a multiply and a
+// shift: n / d = (umulhi(n, m) + n) >> s with s = ceil(log2 d) and
+// m = floor(2^32 (2^s - d) / d) + 1 (the round-up method of Granlund and
+// Montgomery, "Division by invariant integers using multiplication").
+struct FastDiv {
+  uint32_t m;
+  int s;
+};
+inline FastDiv make_fastdiv(uint32_t d) {
+  int s = 0;
+  while ((1ull << s) < d) ++s;
+  const uint64_t m = ((((uint64_t)1 << s) - d) << 32) / d + 1;
+  return FastDiv{(uint32_t)m, s};
+}
 
 // One batch row: which request, its buffer length before this call, its
 // state slot (-1 = none), flags, and its first block ids (-1 past its table).
