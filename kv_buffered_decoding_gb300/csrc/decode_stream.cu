@@ -4,13 +4,14 @@
 // Serving for Linear Attention", Figure 1): o_t = e^{A_t} S0^T q_t +
 // sum_{i<=t} e^{A_t-A_i} (q_t.k_i) u_i with the gated-delta pseudo-value u_t,
 // and a fold S <- e^{A_t} S0 + sum_i e^{A_t-A_i} k_i u_i^T when the buffer fills.
-// What changes is how the bytes move.  A work item is one (row, value head,
-// half of the state columns): a 32 KB tile of S0 plus the token's q/k/v and up
-// to kStageTok buffered tokens.  Each CTA walks items c, c + G, c + 2G, ...
-// (G = resident CTAs): once item i's tile has moved from shared memory into
-// registers, cp.async brings item i + G's tile into the same buffer and every
-// small operand (q, k_t, v_t, buffered keys, pseudo-values, cumulative gates)
-// into the other of two small stages, while item i computes.  HBM then streams without gaps, instead of idling
+// What changes is how the bytes move.  A work unit is one (row, value head):
+// two 32 KB column halves of S0 plus the token's q/k/v and up to kStageTok
+// buffered tokens.  Each CTA walks units c, c + G, c + 2G, ... (G = resident
+// CTAs).  Once a half's tile has moved from shared memory into registers,
+// cp.async brings the next tile (the unit's second half, or the next unit's
+// first half with all its small operands: q, k_t, v_t, buffered keys,
+// pseudo-values, cumulative gates) into the freed buffer while the half
+// computes.  HBM then streams without gaps, instead of idling
 // while every resident CTA of an SM computes.  The tile is stored with its
 // 16-byte chunks XOR-swizzled on row bit 4, so the per-thread reads (16 rows x
 // 4 columns) are free of bank conflicts.
@@ -23,14 +24,13 @@ constexpr int kD = 128, kCW = 64;       // head dim; state columns per item
 constexpr int kTileF4 = kD * kCW / 4;   // float4 chunks of a tile (2048)
 constexpr int kStreamThreads = 128;
 
-// The small operands of one item (double-buffered); the state tile has a
-// single buffer, refilled as soon as the tile has moved into registers.
+// The small operands of one head (double-buffered); the state tile has a
+// single buffer, refilled as soon as a tile has moved into registers.
 template <typename KT>
 struct alignas(16) Stage {
-  KT q[kD], k[kD];                      // current token's q and k (raw)
-  KT v[kCW];                            // current token's v, this item's columns
+  KT q[kD], k[kD], v[kD];               // current token's q, k, v (raw)
   KT keys[kStageTok][kD];               // buffered keys (raw)
-  float uv[kStageTok][kCW];             // buffered u (gated delta) / v, this item's columns
+  float uv[kStageTok][kD];              // buffered u (gated delta) / v rows
   float A[kStageTok];                   // buffered cumulative log-gates
   float a_t, beta_t;
   size_t koff[kStageTok + 1], voff[kStageTok + 1];  // tokens 0..n (n: this token's slot)
@@ -58,16 +58,19 @@ __device__ __forceinline__ float4 raw4(const __nv_bfloat16 *p) {
                      __uint_as_float(w.y << 16), __uint_as_float(w.y & 0xffff0000u));
 }
 
+// A work unit is one (row, value head); its two 64-column halves of the state
+// pass through the tile buffer one after the other, and everything that does
+// not depend on the columns (staging of q, k, v and the buffered tokens, the
+// score dot products, the decay weights) is done once per unit.
 template <typename KT, int VARIANT>
 __global__ void __launch_bounds__(kStreamThreads, 4)
     decode_stream_kernel(const PoolView P, const __grid_constant__ RowBatch rows, const TokenIO io,
-                         int items, FastDiv per_row_div) {
+                         int units, FastDiv hv_div) {
   constexpr bool DELTA = VARIANT == kGatedDelta, GATED = VARIANT != kPlain;
   constexpr int RPT = 16, E = kD / 32;
   constexpr int VEC = 16 / (int)sizeof(KT);  // elements per 16-byte copy
-  constexpr int NQ = kD / VEC;               // 16-byte chunks of q (or k, or a key)
-  constexpr int NV = kCW / VEC;              // 16-byte chunks of v_t's columns
-  constexpr int NU = DELTA ? kCW / 4 : kCW / VEC;  // chunks of a buffered u / v row part
+  constexpr int NQ = kD / VEC;               // 16-byte chunks of q, k, v or a key
+  constexpr int NU = DELTA ? kD / 4 : kD / VEC;  // chunks of a buffered u / v row
   using St = Stage<KT>;
   extern __shared__ float4 dyn_smem[];
   float4 *tile = dyn_smem;                                // [kTileF4] swizzled
@@ -78,38 +81,39 @@ __global__ void __launch_bounds__(kStreamThreads, 4)
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int rsub = lane >> 2, row0 = rsub * RPT;
-  const int chunk = warp * 4 + (lane & 3);  // this thread's float4 column chunk in the item
-  const int colL = chunk * 4;               // ... as a column within the item's 64
+  const int chunk = warp * 4 + (lane & 3);  // this thread's float4 column chunk in a half
+  const int colL = chunk * 4;               // ... as a column within the half
   const int group = P.Hv / P.Hk;
-  const int per_row = P.Hv * 2;
 
-  // stage item `it`: its tile into the tile buffer, the rest into stages[st];
-  // every thread commits one cp.async group
-  auto issue = [&](int it, int st) {
-    St &S = stages[st];
-    const int y = fast_div(it, per_row_div), x = it - y * per_row, h = x >> 1, part = x & 1;
-    const RowDesc &d = rows.r[y];
-    const size_t b = (size_t)rows.row0 + y;
-    const int hq = h / group, n = d.n;
-    const float *Sp = P.state + ((size_t)d.slot * P.Hv + h) * kD * kD + part * kCW;
+  // one half of unit u's state tile into the tile buffer (no commit)
+  auto issue_tile = [&](int u, int part) {
+    const int y = fast_div(u, hv_div), h = u - y * P.Hv;
+    const float *Sp = P.state + ((size_t)rows.r[y].slot * P.Hv + h) * kD * kD + part * kCW;
     for (int i = tid; i < kTileF4; i += kStreamThreads) {
       const int r = i >> 4, ch = i & 15;
       cp16(&tile[tile_slot(r, ch)], Sp + (size_t)r * kD + ch * 4);
     }
-    // small copies, dealt round-robin over the warps (each warp index runs on its
-    // own scheduler in every CTA, so per-warp work is kept even)
+  };
+  // unit u's small operands into stages[st] (no commit)
+  auto issue_small = [&](int u, int st) {
+    St &S = stages[st];
+    const int y = fast_div(u, hv_div), h = u - y * P.Hv;
+    const RowDesc &d = rows.r[y];
+    const size_t b = (size_t)rows.row0 + y;
+    const int hq = h / group, n = d.n;
+    // dealt round-robin over the warps (warp i of every CTA runs on scheduler i)
     const KT *qg = static_cast<const KT *>(io.q) + (b * P.Hk + hq) * kD;
     const KT *kg = static_cast<const KT *>(io.k) + (b * P.Hk + hq) * kD;
-    const KT *vg = static_cast<const KT *>(io.v) + (b * P.Hv + h) * kD + part * kCW;
-    constexpr int NSMALL = 2 * NQ + NV + 2;
+    const KT *vg = static_cast<const KT *>(io.v) + (b * P.Hv + h) * kD;
+    constexpr int NSMALL = 3 * NQ + 2;
     for (int t = (tid & 31) * 4 + warp; t < NSMALL; t += kStreamThreads) {
       if (t < NQ) {
         cp16(&S.q[t * VEC], qg + t * VEC);
       } else if (t < 2 * NQ) {
         cp16(&S.k[(t - NQ) * VEC], kg + (t - NQ) * VEC);
-      } else if (t < 2 * NQ + NV) {
+      } else if (t < 3 * NQ) {
         cp16(&S.v[(t - 2 * NQ) * VEC], vg + (t - 2 * NQ) * VEC);
-      } else if (t == 2 * NQ + NV) {
+      } else if (t == 3 * NQ) {
         if (GATED && io.log_g) cp4(&S.a_t, io.log_g + b * P.Hv + h);
         else S.a_t = 0.f;
       } else {
@@ -154,51 +158,33 @@ __global__ void __launch_bounds__(kStreamThreads, 4)
           const int c = c0 + l2;
           const bool ok = c < n * NU;
           const int i = ok ? c / NU : 0, p = c - i * NU;
-          const size_t row = __shfl_sync(kFull, vo, i) * kD + part * kCW;
+          const size_t row = __shfl_sync(kFull, vo, i) * kD;
           if (!ok) continue;
           if (DELTA)
             cp16(&S.uv[i][p * 4], P.ubuf + row + p * 4);
-          else  // raw values land in the first half of the row; widened when read
+          else  // raw values fill the first half of the row; widened when read
             cp16(reinterpret_cast<KT *>(S.uv[i]) + p * VEC,
                  static_cast<const KT *>(P.vbuf) + row + p * VEC);
         }
         if (GATED && warp == 3 && lane < n) cp4(&S.A[lane], P.gbuf + vo);
       }
     }
-    cp_commit();
+  };
+  auto tile_to_regs = [&](float4 (&s)[RPT]) {
+#pragma unroll
+    for (int j = 0; j < RPT; ++j) s[j] = tile[tile_slot(row0 + j, chunk)];
   };
 
-  int it = blockIdx.x, st = 0;
-  if (it < items) issue(it, 0);
-  for (; it < items; it += gridDim.x, st ^= 1) {
-    cp_wait_all();
-    __syncthreads();  // item `it` staged; every thread is done with the other stage
-    const St &S = stages[st];
-    const bool bad = S.bad != 0;  // CTA-uniform; the error is recorded
-
-    const int y = fast_div(it, per_row_div), x = it - y * per_row, h = x >> 1, part = x & 1;
+  // one half of the unit's columns: outputs, appends and (on a fold) the state
+  auto half = [&](float4 (&s)[RPT], const St &S, int part, int y, int h) {
     const bool lead = part == 0;
     const RowDesc &d = rows.r[y];
     const size_t b = (size_t)rows.row0 + y;
     const int n = d.n;
     const bool fold = (d.flags & kFlagFlush) != 0;
-    const int col0 = part * kCW + colL;  // this thread's global column
+    const int col0 = part * kCW + colL;  // this thread's column within the head
 
-    // 1. tile into registers; q, k_t as floats; then the next item streams in
-    float4 s[RPT];
-#pragma unroll
-    for (int j = 0; j < RPT; ++j) s[j] = tile[tile_slot(row0 + j, chunk)];
-    qs[tid] = P.scale * to_float(S.q[tid]);
-    kts[tid] = to_float(S.k[tid]);
-    if (GATED && warp == 0 && lane == 0) {
-      const float A_prev = n > 0 && !bad ? S.A[n - 1] : 0.f;
-      At_s = A_prev + S.a_t;
-    }
-    __syncthreads();  // the tile buffer is free
-    if (it + (int)gridDim.x < items) issue(it + gridDim.x, st ^ 1);
-    if (bad) continue;
-
-    // 2. S0^T q_t and S0^T k_t over this thread's rows
+    // S0^T q_t and S0^T k_t over this thread's rows
     float4 aq = f4(0.f), ak = f4(0.f);
 #pragma unroll
     for (int j = 0; j < RPT; j += 4) {
@@ -216,71 +202,73 @@ __global__ void __launch_bounds__(kStreamThreads, 4)
       }
     }
 
-    // 3. decay weights w_i = e^{A_t - A_i} (warp 0) and the dot products q.k_i,
-    //    k_t.k_i, two tokens per warp pass with one butterfly reduction
-    const float At = GATED ? At_s : 0.f;
-    if (warp == 1) {
-      for (int i = lane; i <= n; i += 32) wt[i] = GATED ? expf(At - (i < n ? S.A[i] : At)) : 1.f;
-      if (lane == 0) e_t_s = GATED ? expf(At) : 1.f;
-    }
-    for (int i0 = 2 * warp; i0 <= n; i0 += 8) {
-      const int i1 = i0 + 1;
-      float qv[E], tv[E], ka[E], kb[E];
-      load_smem<E>(qs + lane * E, qv);
-      load_smem<E>(kts + lane * E, tv);
-      if (i0 < n) {
-        const float4 r4 = raw4(&S.keys[i0][lane * E]);
-        ka[0] = r4.x; ka[1] = r4.y; ka[2] = r4.z; ka[3] = r4.w;
-      } else {
-#pragma unroll
-        for (int e = 0; e < E; ++e) ka[e] = tv[e];
+    // first half only: decay weights w_i = e^{A_t - A_i} (warp 1) and the dot
+    // products q.k_i, k_t.k_i, two tokens per warp pass, one butterfly each
+    if (lead) {
+      const float At = GATED ? At_s : 0.f;
+      if (warp == 1) {
+        for (int i = lane; i <= n; i += 32) wt[i] = GATED ? expf(At - (i < n ? S.A[i] : At)) : 1.f;
+        if (lane == 0) e_t_s = GATED ? expf(At) : 1.f;
       }
-      if (i1 < n) {
-        const float4 r4 = raw4(&S.keys[i1][lane * E]);
-        kb[0] = r4.x; kb[1] = r4.y; kb[2] = r4.z; kb[3] = r4.w;
-      } else {
+      for (int i0 = 2 * warp; i0 <= n; i0 += 8) {
+        const int i1 = i0 + 1;
+        float qv[E], tv[E], ka[E], kb[E];
+        load_smem<E>(qs + lane * E, qv);
+        load_smem<E>(kts + lane * E, tv);
+        if (i0 < n) {
+          const float4 r4 = raw4(&S.keys[i0][lane * E]);
+          ka[0] = r4.x; ka[1] = r4.y; ka[2] = r4.z; ka[3] = r4.w;
+        } else {
 #pragma unroll
-        for (int e = 0; e < E; ++e) kb[e] = (i1 == n) ? tv[e] : 0.f;
-      }
-      float qa = 0.f, qb = 0.f, ta = 0.f, tb = 0.f;
+          for (int e = 0; e < E; ++e) ka[e] = tv[e];
+        }
+        if (i1 < n) {
+          const float4 r4 = raw4(&S.keys[i1][lane * E]);
+          kb[0] = r4.x; kb[1] = r4.y; kb[2] = r4.z; kb[3] = r4.w;
+        } else {
 #pragma unroll
-      for (int e = 0; e < E; ++e) {
-        qa = fmaf(qv[e], ka[e], qa);
-        qb = fmaf(qv[e], kb[e], qb);
+          for (int e = 0; e < E; ++e) kb[e] = (i1 == n) ? tv[e] : 0.f;
+        }
+        float qa = 0.f, qb = 0.f, ta = 0.f, tb = 0.f;
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+          qa = fmaf(qv[e], ka[e], qa);
+          qb = fmaf(qv[e], kb[e], qb);
+          if (DELTA) {
+            ta = fmaf(tv[e], ka[e], ta);
+            tb = fmaf(tv[e], kb[e], tb);
+          }
+        }
         if (DELTA) {
-          ta = fmaf(tv[e], ka[e], ta);
-          tb = fmaf(tv[e], kb[e], tb);
+          const float r = butterfly4(qa, ta, qb, tb, lane);  // lanes 0, 8, 16, 24
+          const int which = lane >> 3;
+          if ((lane & 7) == 0) {
+            if (which == 0) sc[i0] = r;
+            else if (which == 1) cc[i0] = r;
+            else if (i1 <= n) (which == 2 ? sc : cc)[i1] = r;
+          }
+        } else {
+          const float r = butterfly2(qa, qb, lane);  // lanes 0, 16
+          if (lane == 0) sc[i0] = r;
+          else if (lane == 16 && i1 <= n) sc[i1] = r;
         }
       }
-      if (DELTA) {
-        const float r = butterfly4(qa, ta, qb, tb, lane);  // lanes 0, 8, 16, 24
-        const int which = lane >> 3;
-        if ((lane & 7) == 0) {
-          if (which == 0) sc[i0] = r;
-          else if (which == 1) cc[i0] = r;
-          else if (i1 <= n) (which == 2 ? sc : cc)[i1] = r;
-        }
-      } else {
-        const float r = butterfly2(qa, qb, lane);  // lanes 0, 16
-        if (lane == 0) sc[i0] = r;
-        else if (lane == 16 && i1 <= n) sc[i1] = r;
-      }
+      __syncthreads();
     }
-    __syncthreads();
 
-    // 4. this lane's share of the buffered terms, one reduction over the row lanes
+    // this lane's share of the buffered terms, one reduction over the row lanes
     const float e_t = e_t_s;
     float4 po = mul4(e_t, aq), pc = mul4(e_t, ak);
     for (int i = rsub; i < n; i += 8) {
-      const float4 ui = DELTA ? *reinterpret_cast<const float4 *>(&S.uv[i][colL])
-                              : raw4(reinterpret_cast<const KT *>(S.uv[i]) + colL);
+      const float4 ui = DELTA ? *reinterpret_cast<const float4 *>(&S.uv[i][col0])
+                              : raw4(reinterpret_cast<const KT *>(S.uv[i]) + col0);
       const float w = wt[i];
       fma4(po, w * sc[i], ui);
       if (DELTA) fma4(pc, w * cc[i], ui);
     }
     po = rows_sum4(po);
     if (DELTA) pc = rows_sum4(pc);
-    const float4 vt = raw4(&S.v[colL]);
+    const float4 vt = raw4(&S.v[col0]);
     float4 ut = vt;
     if (DELTA) {
       const float bt = S.beta_t;
@@ -300,18 +288,18 @@ __global__ void __launch_bounds__(kStreamThreads, 4)
         st4(static_cast<KT *>(P.kbuf) + S.koff[n] + 4 * lane,
             *reinterpret_cast<const float4 *>(&kts[4 * lane]));
       if (tid == 0) {
-        P.gbuf[S.voff[n]] = At;  // cumulative since the last fold (0 for the plain variant)
+        P.gbuf[S.voff[n]] = GATED ? At_s : 0.f;  // cumulative since the last fold
         P.bbuf[S.voff[n]] = S.beta_t;
       }
     }
 
-    // 5. fold: S <- e^{A_t} S0 + sum_{i<=n} k_i (w_i u_i)^T, written back once
+    // fold: S <- e^{A_t} S0 + sum_{i<=n} k_i (w_i u_i)^T, written back once
     if (fold) {
 #pragma unroll
       for (int j = 0; j < RPT; ++j) s[j] = mul4(e_t, s[j]);
       for (int i = 0; i <= n; ++i) {
-        const float4 u = i < n ? mul4(wt[i], DELTA ? *reinterpret_cast<const float4 *>(&S.uv[i][colL])
-                                                   : raw4(reinterpret_cast<const KT *>(S.uv[i]) + colL))
+        const float4 u = i < n ? mul4(wt[i], DELTA ? *reinterpret_cast<const float4 *>(&S.uv[i][col0])
+                                                   : raw4(reinterpret_cast<const KT *>(S.uv[i]) + col0))
                                : ut;
 #pragma unroll
         for (int j = 0; j < RPT; j += 4) {
@@ -327,7 +315,45 @@ __global__ void __launch_bounds__(kStreamThreads, 4)
 #pragma unroll
       for (int j = 0; j < RPT; ++j) st_stream4(Sp + (size_t)(row0 + j) * kD + col0, s[j]);
     }
-    if (h == 0 && lead && tid == 0) P.dlen[d.req] = fold ? 0 : n + 1;
+    if (h == 0 && !lead && tid == 0) P.dlen[d.req] = fold ? 0 : n + 1;
+  };
+
+  int u = blockIdx.x, st = 0;
+  if (u < units) {
+    issue_tile(u, 0);
+    issue_small(u, 0);
+    cp_commit();
+  }
+  for (; u < units; u += gridDim.x, st ^= 1) {
+    const int y = fast_div(u, hv_div), h = u - y * P.Hv;
+    const St &S = stages[st];
+    float4 s[RPT];
+    // first half: its tile and the unit's small operands are staged
+    cp_wait_all();
+    __syncthreads();  // also: every thread is done with the previous unit
+    const bool bad = S.bad != 0;  // CTA-uniform; the error is recorded
+    tile_to_regs(s);
+    qs[tid] = P.scale * to_float(S.q[tid]);
+    kts[tid] = to_float(S.k[tid]);
+    if (GATED && tid == 0) {
+      const int n = rows.r[y].n;
+      At_s = (n > 0 && !bad ? S.A[n - 1] : 0.f) + S.a_t;
+    }
+    __syncthreads();  // the tile buffer is free
+    issue_tile(u, 1);
+    cp_commit();
+    if (!bad) half(s, S, 0, y, h);
+    // second half
+    cp_wait_all();
+    __syncthreads();
+    tile_to_regs(s);
+    __syncthreads();  // the tile buffer is free; the other small stage is unused
+    if (u + (int)gridDim.x < units) {
+      issue_tile(u + gridDim.x, 0);
+      issue_small(u + gridDim.x, st ^ 1);
+      cp_commit();
+    }
+    if (!bad) half(s, S, 1, y, h);
   }
 }
 
@@ -349,10 +375,10 @@ cudaError_t run_stream(const PoolView &P, const RowBatch &rows, const TokenIO &i
     if (per_sm < 1) return kUnsupported;
     grid_cap = sms * per_sm;
   }
-  const int items = rows.count * P.Hv * 2;
-  const int grid = items < grid_cap ? items : grid_cap;
+  const int units = rows.count * P.Hv;
+  const int grid = units < grid_cap ? units : grid_cap;
   decode_stream_kernel<KT, VARIANT><<<grid, kStreamThreads, smem, stream>>>(
-      P, rows, io, items, make_fastdiv((uint32_t)P.Hv * 2));
+      P, rows, io, units, make_fastdiv((uint32_t)P.Hv));
   return cudaGetLastError();
 }
 
