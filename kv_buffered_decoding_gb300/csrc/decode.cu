@@ -348,7 +348,8 @@ cudaError_t launch_decode(const PoolView &P, const RowBatch &rows, const TokenIO
                           int dtype, int d, bool recurrent, int flush_len, int nmax,
                           cudaStream_t stream) {
   if (rows.count <= 0) return cudaSuccess;
-  if (!recurrent && d == 128 && nmax <= kStageTok)
+  if (!recurrent && d == 128 && nmax <= kStageTok &&
+      decode_stream_pays(rows.count * P.Hv, variant, dtype))
     return launch_decode_stream(P, rows, io, variant, dtype, stream);
   TokenIO io2 = io;
   io2.lmax = flush_len;

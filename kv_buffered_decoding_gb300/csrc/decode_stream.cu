@@ -357,32 +357,57 @@ __global__ void __launch_bounds__(kStreamThreads, 4)
   }
 }
 
+// Resident CTAs of the kernel on this device (its persistent grid), once.
 template <typename KT, int VARIANT>
-cudaError_t run_stream(const PoolView &P, const RowBatch &rows, const TokenIO &io,
-                       cudaStream_t stream) {
-  constexpr size_t smem = kTileF4 * sizeof(float4) + 2 * sizeof(Stage<KT>);
-  static int grid_cap = 0;
-  if (grid_cap == 0) {
+int stream_ctas() {
+  static int ctas = -1;
+  if (ctas < 0) {
+    constexpr size_t smem = kTileF4 * sizeof(float4) + 2 * sizeof(Stage<KT>);
+    int dev = 0, sms = 0, per_sm = 0;
     cudaError_t e = cudaFuncSetAttribute(decode_stream_kernel<KT, VARIANT>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    int dev = 0, sms = 0, per_sm = 0;
     if (e == cudaSuccess) e = cudaGetDevice(&dev);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e == cudaSuccess)
       e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_stream_kernel<KT, VARIANT>,
                                                         kStreamThreads, smem);
-    if (e != cudaSuccess) return e;
-    if (per_sm < 1) return kUnsupported;
-    grid_cap = sms * per_sm;
+    ctas = e == cudaSuccess ? sms * per_sm : 0;
   }
+  return ctas;
+}
+
+template <typename KT, int VARIANT>
+cudaError_t run_stream(const PoolView &P, const RowBatch &rows, const TokenIO &io,
+                       cudaStream_t stream) {
+  constexpr size_t smem = kTileF4 * sizeof(float4) + 2 * sizeof(Stage<KT>);
+  const int cap = stream_ctas<KT, VARIANT>();
+  if (cap <= 0) return kUnsupported;
   const int units = rows.count * P.Hv;
-  const int grid = units < grid_cap ? units : grid_cap;
+  const int grid = units < cap ? units : cap;
   decode_stream_kernel<KT, VARIANT><<<grid, kStreamThreads, smem, stream>>>(
       P, rows, io, units, make_fastdiv((uint32_t)P.Hv));
   return cudaGetLastError();
 }
 
+template <typename KT>
+int ctas_for(int variant) {
+  switch (variant) {
+    case kPlain: return stream_ctas<KT, kPlain>();
+    case kGated: return stream_ctas<KT, kGated>();
+    case kGatedDelta: return stream_ctas<KT, kGatedDelta>();
+  }
+  return 0;
+}
+
 }  // namespace
+
+bool decode_stream_pays(int units, int variant, int dtype) {
+  // each resident CTA should get at least 8 units: fewer leave its pipeline
+  // prologue and the last partial round of units unamortized
+  const int cap = dtype == 1 ? ctas_for<__nv_bfloat16>(variant)
+                             : dtype == 0 ? ctas_for<float>(variant) : 0;
+  return cap > 0 && units >= 8 * cap;
+}
 
 cudaError_t launch_decode_stream(const PoolView &P, const RowBatch &rows, const TokenIO &io,
                                  int variant, int dtype, cudaStream_t stream) {

@@ -131,6 +131,8 @@ cudaError_t launch_accept_tempstate_static(const PoolView &P, const RowBatch &ro
 // persistent pipelined kernel.
 cudaError_t launch_decode_stream(const PoolView &P, const RowBatch &rows, const TokenIO &io,
                                  int variant, int dtype, cudaStream_t stream);
+// Whether a launch of `units` (row, value head) pairs is large enough for it.
+bool decode_stream_pays(int units, int variant, int dtype);
 // Chunked prefill of rows.r[i].n prompt tokens per row (io.T = padded length).
 cudaError_t launch_prefill(const PoolView &P, const RowBatch &rows, const TokenIO &io,
                            int variant, int dtype, int d, cudaStream_t stream);
