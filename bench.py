@@ -84,6 +84,21 @@ def hbm_peak():
     return FALLBACK_HBM_GBS, "of fallback (6.8 TB/s, no MEASURED_PEAKS.json)"
 
 
+def tensor_peak_bf16():
+    """Dense bf16 tensor peak (TFLOP/s): the measured cuBLAS burst rate, else the fallback."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        try:
+            with open(path) as f:
+                d = json.load(f)
+            for key in ("bf16_tflops", "bf16_TFLOPs", "bf16"):
+                if key in d and isinstance(d[key], (int, float)):
+                    return float(d[key]), "of measured (MEASURED_PEAKS.json bf16_tflops)"
+        except (OSError, ValueError):
+            pass
+    return FALLBACK_BF16_TFLOPS, "of fallback (1.9 PFLOP/s bf16)"
+
+
 def tensor_peak_tf32():
     """Dense tf32 tensor peak (TFLOP/s): the measured bf16 GEMM burst rate times the
     nominal tf32/bf16 ratio, or the fallback bf16 figure times the same ratio."""
@@ -473,9 +488,10 @@ def measure_paths(kvb, torch, dev, peak):
         "buffer-only decode, no state; buffer reads dominate")
     pool.close()
 
-    # chunked prefill: 1024-token prompts from S = 0, 32 requests, both layers; bound by
-    # the tensor cores (tf32 mma.sync), reported against the tf32 peak and HBM
-    tf_peak, tf_src = tensor_peak_tf32()
+    # chunked prefill: 1024-token prompts from S = 0, 32 requests, both layers; the bf16
+    # products run as tcgen05 MMAs (bf16 hi/lo parts, fp32 accumulation in TMEM),
+    # reported against the bf16 tensor peak and HBM
+    tf_peak, tf_src = tensor_peak_bf16()
     for L, tag in ((I.GATED_LAYER, "prefill_gated_B32_L1024"),
                    (I.GDN_LAYER, "prefill_gated_delta_B32_L1024")):
         B, Lp = 32, 1024
@@ -493,7 +509,7 @@ def measure_paths(kvb, torch, dev, peak):
                     "tensor_frac": tflops / tf_peak, "tensor_peak_tflops": tf_peak,
                     "tensor_peak_source": tf_src, "gbs": nbytes / us / 1e3,
                     "frac": nbytes / us / 1e3 / peak, "bytes": nbytes, "flops": flops,
-                    "note": "chunk 64, tf32 mma.sync with hi/lo splits (fp32-accurate); "
+                    "note": "chunk 64, tcgen05 bf16 MMAs with hi/lo parts, TMEM accumulators; "
                             "algorithmic flops of the chunked form"}
         del o_buf, prompt
         pool.close()

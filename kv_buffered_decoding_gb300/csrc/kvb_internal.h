@@ -91,7 +91,7 @@ struct TokenIO {
   int lmax;  // most tokens any row of the launch stages in shared memory
 };
 
-enum ErrKind : int32_t { kErrNone = 0, kErrBlockRange = 1 };
+enum ErrKind : int32_t { kErrNone = 0, kErrBlockRange = 1, kErrTimeout = 2 };
 
 // Launchers (kernels.cu).  `dtype` is KVB_F32 / KVB_BF16; `d` is d_k == d_v.
 // Return cudaSuccess or the launch error; kUnsupported for a missing instance.
@@ -133,6 +133,9 @@ cudaError_t launch_decode_stream(const PoolView &P, const RowBatch &rows, const 
                                  int variant, int dtype, cudaStream_t stream);
 // Whether a launch of `units` (row, value head) pairs is large enough for it.
 bool decode_stream_pays(int units, int variant, int dtype);
+// Chunked prefill on tcgen05 / TMEM (bf16 inputs, d = 128).
+cudaError_t launch_prefill_tc(const PoolView &P, const RowBatch &rows, const TokenIO &io,
+                              int variant, cudaStream_t stream);
 // Chunked prefill of rows.r[i].n prompt tokens per row (io.T = padded length).
 cudaError_t launch_prefill(const PoolView &P, const RowBatch &rows, const TokenIO &io,
                            int variant, int dtype, int d, cudaStream_t stream);

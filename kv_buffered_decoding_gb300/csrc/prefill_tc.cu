@@ -1,0 +1,557 @@
+// Chunked prefill on the fifth-generation tensor cores (tcgen05, TMEM), for
+// bf16 inputs at d = 128.
+//
+// Same chunk algebra as prefill.cu ("KVBuffer: IO-aware Serving for Linear
+// Attention", abstract: chunkwise computation; the delta-rule chunk form with
+// the UT transform), chunk C = 64, per (request, value head) CTA:
+//   Y = [Q; K] S,  Mq = scale e^{A_i-A_j} q_i.k_j (j <= i),  Mk = beta_i e^{A_i-A_j} k_i.k_j (j < i)
+//   (I + Mk) U = R,  R_i = beta_i (v_i - e^{A_i} S^T k_i)       (U = V unless the delta rule)
+//   O = e^{A} scale Y_q + Mq U,   S <- e^{A_{C-1}} S + K^T diag(w) U
+// Layout: thread t of the 128 owns TMEM lane t.  The state lives in TMEM
+// transposed (lane = value column c, columns = key rows), so that
+//   Y^T = S^T X^T          (A: S^T from TMEM as bf16 hi/lo parts, B: X = [Q;K] from smem)
+//   G   = X K^T            (A: X, B: the K rows of X; exact for bf16 inputs)
+//   O^T = e^A Y_q^T + U^T Mq^T   (A: U^T parts from TMEM, B: Mq parts from smem)
+//   S^T <- e^{A_C} S^T + (wU)^T K   (A: (wU)^T parts from TMEM, B: K^T from smem)
+// leave every per-column quantity (R, the substitution, U, the output column,
+// the state column) in the registers of the thread that owns that column: the
+// forward substitution runs one column per thread with no data exchange.
+// Operands that are not exact in bf16 (S, U, wU, Mq) enter as hi + lo bf16
+// parts (about 16 significant bits; the lo x lo product is dropped), with fp32
+// accumulation in TMEM.  Single-thread MMA issue, completion via tcgen05.commit
+// on an mbarrier; every wait is bounded and a timeout sets the error word.
+#include "kvb_device.cuh"
+
+namespace kvb {
+namespace {
+
+constexpr int kC = 64, kD = 128, kThreads = 256;  // two warpgroups share every TMEM lane
+// TMEM columns
+constexpr uint32_t kColS = 0;     // S^T fp32            [128 lanes x 128]
+constexpr uint32_t kColP = 128;   // A parts: S^T hi/lo (64 + 64), later U^T hi/lo, (wU)^T hi/lo (32 each)
+constexpr uint32_t kColY = 256;   // Y^T fp32 (tokens: 0..63 q, 64..127 k); O^T in 0..63
+constexpr uint32_t kColG = 384;   // G fp32 (lane = token of [Q;K], column = key token)
+constexpr uint32_t kTmemCols = 512;
+// shared memory (bytes)
+constexpr int kXBytes = 2 * kC * kD * 2;        // [Q;K] bf16, core-matrix K-major (32 KB)
+constexpr int kVBytes = kC * kD * 2;            // V bf16 [token][column] (16 KB)
+constexpr int kGBytes = 2 * kC * 4;             // log-gate, beta
+constexpr int kStage = (kXBytes + kVBytes + kGBytes + 1023) / 1024 * 1024;
+constexpr int kKtBytes = kD * kC * 2;           // K^T bf16, core-matrix K-major (16 KB)
+constexpr int kMqBytes = kC * kC * 2;           // one bf16 part of Mq (8 KB)
+constexpr int kLdMk = kC + 4;                   // fp32 rows of Mk
+constexpr int kMkBytes = kC * kLdMk * 4;
+constexpr int kOffKt = 2 * kStage;
+constexpr int kOffMq = kOffKt + kKtBytes;       // [2 parts]
+constexpr int kOffMk = kOffMq + 2 * kMqBytes;
+constexpr int kOffR = kOffMk + kMkBytes;        // R of tokens 32..63, fp32 [32][128]
+constexpr int kRBytes = 32 * kD * 4;
+constexpr int kOffA = kOffR + kRBytes;          // Acum, e^A, w: [3][C]
+constexpr int kSmemBytes = kOffA + 3 * kC * 4;
+// core-matrix strides (bytes): 8 rows x 16 bytes per core matrix, k groups adjacent
+constexpr uint32_t kLbo = 128;
+constexpr uint32_t kSboX = (kD / 8) * 128;      // X: 128 dk per row group
+constexpr uint32_t kSboKt = (kC / 8) * 128;     // K^T and Mq: 64 tokens per row group
+static_assert(kSmemBytes <= 227 * 1024, "one CTA's shared memory");
+static_assert(kStage % 1024 == 0 && kKtBytes % 1024 == 0 && kMqBytes % 1024 == 0, "alignment");
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+// shared-memory matrix descriptor: K-major, no swizzle (core matrices of 8 rows x
+// 16 bytes; lbo = distance between k groups, sbo = distance between row groups)
+__device__ __forceinline__ uint64_t sdesc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+  return (uint64_t)((addr >> 4) & 0x3FFF) | ((uint64_t)((lbo >> 4) & 0x3FFF) << 16) |
+         ((uint64_t)((sbo >> 4) & 0x3FFF) << 32) | ((uint64_t)1 << 46);
+}
+// instruction descriptor: bf16 x bf16 -> fp32, both K-major, M x N
+__host__ __device__ constexpr uint32_t idesc_bf16(int m, int n) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
+}
+__device__ __forceinline__ void mma_ss(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+  asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+               "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+               ::"r"(d), "l"(a), "l"(b), "r"(idesc), "r"(acc));
+}
+__device__ __forceinline__ void mma_ts(uint32_t d, uint32_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+  asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+               "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}"
+               ::"r"(d), "r"(a), "l"(b), "r"(idesc), "r"(acc));
+}
+__device__ __forceinline__ void mma_commit(uint32_t mbar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(mbar));
+}
+// bounded wait on an mbarrier phase; false on timeout (about 50 ms)
+__device__ __forceinline__ bool mbar_wait(uint32_t mbar, uint32_t parity) {
+  for (int it = 0; it < (1 << 20); ++it) {
+    uint32_t done;
+    asm volatile("{\n\t.reg .pred p;\n\tmbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+                 "selp.u32 %0, 1, 0, p;\n\t}"
+                 : "=r"(done) : "r"(mbar), "r"(parity));
+    if (done) return true;
+    __nanosleep(32);
+  }
+  return false;
+}
+__device__ __forceinline__ void fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+// 32 consecutive TMEM columns of this thread's lane
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};"
+      ::"r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+        "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]),
+        "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]),
+        "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+      : "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// x = hi + lo, both bf16 (hi = round(x), lo = round(x - hi))
+__device__ __forceinline__ void split_bf16(float x, uint16_t &hi, uint16_t &lo) {
+  const __nv_bfloat16 h = __float2bfloat16_rn(x);
+  hi = __bfloat16_as_ushort(h);
+  lo = __bfloat16_as_ushort(__float2bfloat16_rn(x - __bfloat162float(h)));
+}
+__device__ __forceinline__ uint32_t pack2(uint16_t a, uint16_t b) { return (uint32_t)a | ((uint32_t)b << 16); }
+
+// 64 fp32 values -> bf16 hi and lo parts packed in pairs (32 words each)
+__device__ __forceinline__ void split64(const float (&x)[64], uint32_t (&hi)[32], uint32_t (&lo)[32]) {
+#pragma unroll
+  for (int j = 0; j < 32; ++j) {
+    uint16_t h0, l0, h1, l1;
+    split_bf16(x[2 * j], h0, l0);
+    split_bf16(x[2 * j + 1], h1, l1);
+    hi[j] = pack2(h0, h1);
+    lo[j] = pack2(l0, l1);
+  }
+}
+
+__device__ __forceinline__ void split32(const float (&x)[32], uint32_t (&hi)[16], uint32_t (&lo)[16]) {
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    uint16_t h0, l0, h1, l1;
+    split_bf16(x[2 * j], h0, l0);
+    split_bf16(x[2 * j + 1], h1, l1);
+    hi[j] = pack2(h0, h1);
+    lo[j] = pack2(l0, l1);
+  }
+}
+__device__ __forceinline__ void cp16(uint32_t dst, const void *src, bool valid) {
+  const int n = valid ? 16 : 0;
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src), "r"(n) : "memory");
+}
+__device__ __forceinline__ void cp4(uint32_t dst, const void *src, bool valid) {
+  const int n = valid ? 4 : 0;
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;\n" ::"r"(dst), "l"(src), "r"(n) : "memory");
+}
+
+template <int VARIANT>
+__global__ void __launch_bounds__(kThreads, 1)
+    prefill_tc_kernel(const PoolView P, const __grid_constant__ RowBatch rows, const TokenIO io) {
+  using KT = __nv_bfloat16;
+  constexpr bool DELTA = VARIANT == kGatedDelta, GATED = VARIANT != kPlain;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  __shared__ uint64_t mbar_s;
+  __shared__ uint32_t tmem_s;
+  float *Acum = reinterpret_cast<float *>(smem + kOffA);
+  float *eA = Acum + kC, *wL = eA + kC;
+  float *Mk = reinterpret_cast<float *>(smem + kOffMk);
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int h = blockIdx.x;
+  const RowDesc &d = rows.r[blockIdx.y];
+  const size_t b = (size_t)rows.row0 + blockIdx.y;
+  const int hq = h / (P.Hv / P.Hk);
+  const int L = d.n;
+  const bool from_zero = (d.flags & kFlagFromZero) != 0;
+  if (L == 0 && !from_zero) return;  // nothing to do: the state stays as it is
+  const int Tp = io.T;
+  const int nchunks = (L + kC - 1) / kC;
+  float *Sg = P.state + ((size_t)d.slot * P.Hv + h) * kD * kD;
+  const uint32_t mbar = smem_u32(&mbar_s);
+  const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;  // this warp's TMEM lanes
+
+  if (tid == 0) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(mbar));
+    asm volatile("fence.mbarrier_init.release.cluster;");
+  }
+  if (warp == 0) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&tmem_s)),
+                 "r"(kTmemCols));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+  }
+
+  const KT *qg = static_cast<const KT *>(io.q);
+  const KT *kg = static_cast<const KT *>(io.k);
+  const KT *vg = static_cast<const KT *>(io.v);
+  // stage chunk c: q and k rows into X (core-matrix layout), v rows, gates
+  auto issue = [&](int c) {
+    uint8_t *st = smem + (c & 1) * kStage;
+    const uint32_t xs = smem_u32(st), vs = xs + kXBytes, gs = vs + kVBytes;
+    const int t0 = c * kC;
+    for (int idx = tid; idx < 2 * kC * 16; idx += kThreads) {  // 128 rows x 16 pieces of 8
+      const int i = idx >> 4, p = idx & 15;
+      const int tok = t0 + (i & (kC - 1));
+      const bool ok = tok < L;
+      const size_t row = b * Tp + (ok ? tok : L - 1);
+      const KT *src = (i < kC ? qg : kg) + (row * P.Hk + hq) * kD + p * 8;
+      cp16(xs + (i >> 3) * kSboX + p * kLbo + (i & 7) * 16, src, ok);
+    }
+    for (int idx = tid; idx < kC * 16; idx += kThreads) {
+      const int j = idx >> 4, p = idx & 15;
+      const bool ok = t0 + j < L;
+      const size_t row = b * Tp + (ok ? t0 + j : L - 1);
+      cp16(vs + j * kD * 2 + p * 16, vg + (row * P.Hv + h) * kD + p * 8, ok);
+    }
+    if (tid < kC) {
+      const bool ok = t0 + tid < L;
+      const size_t row = b * Tp + (ok ? t0 + tid : L - 1);
+      if (GATED) cp4(gs + tid * 4, io.log_g + row * P.Hv + h, ok);
+      if (DELTA) cp4(gs + (kC + tid) * 4, io.beta + row * P.Hv + h, ok);
+    }
+    asm volatile("cp.async.commit_group;\n" ::: "memory");
+  };
+  if (nchunks > 0) issue(0);
+
+  fence_before();
+  __syncthreads();
+  fence_after();
+  const uint32_t tmem = tmem_s;
+  const int lt = tid & 127;              // this thread's TMEM lane
+  const int wg = tid >> 7;               // warpgroup: which half of each lane's columns
+  const uint32_t my = tmem + lane_base;  // this thread's lane, column 0
+  const int c = lt;                      // as a state column
+  bool ok = true;
+  uint32_t phase = 0;
+  float *Rb = reinterpret_cast<float *>(smem + kOffR);
+
+  // 64 state rows (this warpgroup's half) of column c: fp32 into S^T, bf16 parts
+  auto put_half = [&](const float (&col)[64]) {
+    uint32_t w[32];
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+#pragma unroll
+      for (int j = 0; j < 32; ++j) w[j] = __float_as_uint(col[q * 32 + j]);
+      tmem_st32(my + kColS + wg * 64 + q * 32, w);
+    }
+  };
+  auto put_parts = [&](const float (&col)[64]) {
+    uint32_t hi[32], lo[32];
+    split64(col, hi, lo);
+    tmem_st32(my + kColP + wg * 32, hi);
+    tmem_st32(my + kColP + 64 + wg * 32, lo);
+  };
+  {
+    float col[64];
+#pragma unroll
+    for (int r = 0; r < 64; ++r) col[r] = from_zero ? 0.f : Sg[(size_t)(wg * 64 + r) * kD + c];
+    put_half(col);
+    put_parts(col);
+    tmem_wait_st();
+  }
+
+  for (int ch = 0; ch < nchunks && ok; ++ch) {
+    uint8_t *st = smem + (ch & 1) * kStage;
+    const uint32_t xs = smem_u32(st);
+    const KT *vs = reinterpret_cast<const KT *>(st + kXBytes);
+    const float *gs = reinterpret_cast<const float *>(st + kXBytes + kVBytes);
+    const float *bs = gs + kC;
+    const int t0 = ch * kC;
+    asm volatile("cp.async.wait_group 0;\n" ::: "memory");
+    fence_async_smem();
+    fence_before();
+    __syncthreads();  // chunk staged; the previous chunk's MMAs are done
+    fence_after();
+    if (ch + 1 < nchunks) issue(ch + 1);  // the other stage is free
+
+    // K^T (B of the state update) from the K rows of X, token groups split by
+    // warpgroup; cumulative gates (warp 3)
+    {
+      uint8_t *kt = smem + kOffKt;
+      const int r = lt;  // key row (d_k index)
+#pragma unroll
+      for (int q4 = 0; q4 < 4; ++q4) {
+        const int jg = wg * 4 + q4;
+        uint16_t e[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          const int i = kC + jg * 8 + q;  // X row of the key of token jg*8+q
+          e[q] = *reinterpret_cast<const uint16_t *>(st + (i >> 3) * kSboX + (r >> 3) * kLbo + (i & 7) * 16 +
+                                                     (r & 7) * 2);
+        }
+        *reinterpret_cast<uint4 *>(kt + (r >> 3) * kSboKt + jg * kLbo + (r & 7) * 16) =
+            make_uint4(pack2(e[0], e[1]), pack2(e[2], e[3]), pack2(e[4], e[5]), pack2(e[6], e[7]));
+      }
+    }
+    if (warp == 3) {
+      float a0 = GATED ? gs[lane] : 0.f, a1 = GATED ? gs[lane + 32] : 0.f;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const float y0 = __shfl_up_sync(kFull, a0, off), y1 = __shfl_up_sync(kFull, a1, off);
+        if (lane >= off) {
+          a0 += y0;
+          a1 += y1;
+        }
+      }
+      a1 += __shfl_sync(kFull, a0, 31);
+      const float AL = __shfl_sync(kFull, a1, 31);
+      Acum[lane] = a0;
+      Acum[lane + 32] = a1;
+      eA[lane] = expf(a0);
+      eA[lane + 32] = expf(a1);
+      wL[lane] = expf(AL - a0);
+      wL[lane + 32] = expf(AL - a1);
+    }
+    fence_async_smem();
+    fence_before();
+    __syncthreads();
+    fence_after();
+
+    // MMAs 1: G = X K^T (exact) and Y^T = S^T X^T (S^T as hi + lo parts)
+    if (tid == 0) {
+      const uint32_t idG = idesc_bf16(128, kC), idY = idesc_bf16(128, 2 * kC);
+#pragma unroll
+      for (int k0 = 0; k0 < kD; k0 += 16) {
+        const uint64_t a = sdesc(xs + (k0 / 8) * kLbo, kLbo, kSboX);
+        const uint64_t bk = sdesc(xs + (kC / 8) * kSboX + (k0 / 8) * kLbo, kLbo, kSboX);
+        mma_ss(tmem + kColG, a, bk, idG, k0 > 0);
+      }
+#pragma unroll
+      for (int part = 0; part < 2; ++part)
+#pragma unroll
+        for (int k0 = 0; k0 < kD; k0 += 16) {
+          const uint64_t bx = sdesc(xs + (k0 / 8) * kLbo, kLbo, kSboX);
+          mma_ts(tmem + kColY, tmem + kColP + part * 64 + k0 / 2, bx, idY, part > 0 || k0 > 0);
+        }
+      mma_commit(mbar);
+    }
+    ok = __syncthreads_and(mbar_wait(mbar, phase)) != 0;  // CTA-uniform
+    phase ^= 1;
+    fence_after();
+    if (!ok) break;
+
+    // Gram rows, key tokens split by warpgroup: thread (i, wg) builds entries
+    // j = 32 wg .. 32 wg + 31 of row i of Mq (parts, smem) or Mk (fp32)
+    {
+      const int i = lt, j0 = wg * 32;
+      float gr[32];
+      {
+        uint32_t w[32];
+        tmem_ld32(my + kColG + j0, w);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) gr[j] = __uint_as_float(w[j]);
+      }
+      if (i < kC) {  // Mq[i][j] = scale e^{A_i-A_j} q_i.k_j, j <= i
+        const float Ai = Acum[i];
+        float x[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) x[j] = j0 + j <= i ? P.scale * expf(Ai - Acum[j0 + j]) * gr[j] : 0.f;
+        uint32_t hi[16], lo[16];
+        split32(x, hi, lo);
+        uint8_t *mq = smem + kOffMq;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int off = (i >> 3) * kSboKt + (wg * 4 + q) * kLbo + (i & 7) * 16;
+          *reinterpret_cast<uint4 *>(mq + off) = make_uint4(hi[4 * q], hi[4 * q + 1], hi[4 * q + 2], hi[4 * q + 3]);
+          *reinterpret_cast<uint4 *>(mq + kMqBytes + off) =
+              make_uint4(lo[4 * q], lo[4 * q + 1], lo[4 * q + 2], lo[4 * q + 3]);
+        }
+      } else if (DELTA) {  // Mk[i'][j] = beta_i' e^{A_i'-A_j} k_i'.k_j, j < i'
+        const int ip = i - kC;
+        const float Ai = Acum[ip], bi = bs[ip];
+#pragma unroll
+        for (int j = 0; j < 32; j += 4) {
+          const int jj = j0 + j;
+          float4 m4;
+          m4.x = jj < ip ? bi * expf(Ai - Acum[jj]) * gr[j] : 0.f;
+          m4.y = jj + 1 < ip ? bi * expf(Ai - Acum[jj + 1]) * gr[j + 1] : 0.f;
+          m4.z = jj + 2 < ip ? bi * expf(Ai - Acum[jj + 2]) * gr[j + 2] : 0.f;
+          m4.w = jj + 3 < ip ? bi * expf(Ai - Acum[jj + 3]) * gr[j + 3] : 0.f;
+          *reinterpret_cast<float4 *>(&Mk[ip * kLdMk + jj]) = m4;
+        }
+      }
+    }
+    // column c of R (delta rule) for tokens 32 wg .. 32 wg + 31: warpgroup 0 keeps
+    // its half in registers, warpgroup 1 passes its half through shared memory
+    float u[kC];
+    if (DELTA) {
+      uint32_t w[32];
+      tmem_ld32(my + kColY + kC + wg * 32, w);
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        const int jj = wg * 32 + j;
+        const float r = bs[jj] * (__bfloat162float(vs[jj * kD + c]) - eA[jj] * __uint_as_float(w[j]));
+        if (wg == 0) u[j] = r;
+        else Rb[j * kD + c] = r;
+      }
+    }
+    fence_async_smem();
+    __syncthreads();  // Mk, Mq and R complete
+
+    if (wg == 0) {
+      // forward substitution (I + Mk) U = R, one column per thread
+      if (DELTA) {
+#pragma unroll
+        for (int j = 32; j < kC; ++j) u[j] = Rb[(j - 32) * kD + c];
+#pragma unroll
+        for (int i = 1; i < kC; ++i) {
+          float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+#pragma unroll
+          for (int j = 0; j + 3 < i; j += 4) {
+            const float4 x = *reinterpret_cast<const float4 *>(&Mk[i * kLdMk + j]);
+            s0 = fmaf(x.x, u[j], s0);
+            s1 = fmaf(x.y, u[j + 1], s1);
+            s2 = fmaf(x.z, u[j + 2], s2);
+            s3 = fmaf(x.w, u[j + 3], s3);
+          }
+#pragma unroll
+          for (int j = i & ~3; j < i; ++j) s0 = fmaf(Mk[i * kLdMk + j], u[j], s0);
+          u[i] -= (s0 + s1) + (s2 + s3);
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < kC; ++j) u[j] = __bfloat162float(vs[j * kD + c]);
+      }
+      // U^T and (wU)^T parts into TMEM (A operands of the second MMAs)
+      uint32_t hi[32], lo[32];
+      split64(u, hi, lo);
+      tmem_st32(my + kColP, hi);
+      tmem_st32(my + kColP + 32, lo);
+#pragma unroll
+      for (int j = 0; j < kC; ++j) u[j] *= wL[j];
+      split64(u, hi, lo);
+      tmem_st32(my + kColP + 64, hi);
+      tmem_st32(my + kColP + 96, lo);
+    } else {
+      // meanwhile: e^A scale Y_q^T (the output accumulator) and e^{A_C} S^T
+      uint32_t w[32];
+#pragma unroll
+      for (int q = 0; q < 2; ++q) {
+        tmem_ld32(my + kColY + q * 32, w);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) w[j] = __float_as_uint(P.scale * eA[q * 32 + j] * __uint_as_float(w[j]));
+        tmem_st32(my + kColY + q * 32, w);
+      }
+      const float eL = eA[kC - 1];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        tmem_ld32(my + kColS + q * 32, w);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) w[j] = __float_as_uint(eL * __uint_as_float(w[j]));
+        tmem_st32(my + kColS + q * 32, w);
+      }
+    }
+    tmem_wait_st();
+    fence_before();
+    __syncthreads();
+    fence_after();
+
+    // MMAs 2: O^T += U^T Mq^T (three part products), S^T += (wU)^T K
+    if (tid == 0) {
+      const uint32_t idO = idesc_bf16(128, kC), idS = idesc_bf16(128, kD);
+      const uint32_t mq = smem_u32(smem + kOffMq), kt = smem_u32(smem + kOffKt);
+#pragma unroll
+      for (int combo = 0; combo < 3; ++combo) {
+        const int ua = combo == 2 ? 32 : 0;                    // U^T hi, hi, lo
+        const uint32_t mb = mq + (combo == 1 ? kMqBytes : 0);  // Mq hi, lo, hi
+#pragma unroll
+        for (int k0 = 0; k0 < kC; k0 += 16)
+          mma_ts(tmem + kColY, tmem + kColP + ua + k0 / 2, sdesc(mb + (k0 / 8) * kLbo, kLbo, kSboKt),
+                 idO, 1);
+      }
+#pragma unroll
+      for (int part = 0; part < 2; ++part)
+#pragma unroll
+        for (int k0 = 0; k0 < kC; k0 += 16)
+          mma_ts(tmem + kColS, tmem + kColP + 64 + part * 32 + k0 / 2,
+                 sdesc(kt + (k0 / 8) * kLbo, kLbo, kSboKt), idS, 1);
+      mma_commit(mbar);
+    }
+    ok = __syncthreads_and(mbar_wait(mbar, phase)) != 0;  // CTA-uniform
+    phase ^= 1;
+    fence_after();
+    if (!ok) break;
+
+    // outputs (tokens 32 wg .. 32 wg + 31 of column c) and the next chunk's S^T
+    // parts (state rows 64 wg .. 64 wg + 63)
+    {
+      uint32_t w[32];
+      tmem_ld32(my + kColY + wg * 32, w);
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        const int i = wg * 32 + j;
+        if (t0 + i < L) io.o[((b * Tp + t0 + i) * P.Hv + h) * kD + c] = __uint_as_float(w[j]);
+      }
+      if (ch + 1 < nchunks) {
+        float col[64];
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+          tmem_ld32(my + kColS + wg * 64 + q * 32, w);
+#pragma unroll
+          for (int j = 0; j < 32; ++j) col[q * 32 + j] = __uint_as_float(w[j]);
+        }
+        put_parts(col);
+        tmem_wait_st();
+      }
+    }
+  }
+
+  if (ok) {
+    // this warpgroup's half of the state column back to global memory
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+      uint32_t w[32];
+      tmem_ld32(my + kColS + wg * 64 + q * 32, w);
+#pragma unroll
+      for (int j = 0; j < 32; ++j) Sg[(size_t)(wg * 64 + q * 32 + j) * kD + c] = __uint_as_float(w[j]);
+    }
+  } else if (tid == 0) {
+    record_error(P.err, kErrTimeout, d.req, h);
+  }
+  asm volatile("cp.async.wait_group 0;\n" ::: "memory");
+  fence_before();
+  __syncthreads();
+  fence_after();
+  if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols));
+}
+
+}  // namespace
+
+cudaError_t launch_prefill_tc(const PoolView &P, const RowBatch &rows, const TokenIO &io,
+                              int variant, cudaStream_t stream) {
+  if (rows.count <= 0) return cudaSuccess;
+  dim3 grid(P.Hv, rows.count);
+  auto run = [&](auto kernel) -> cudaError_t {
+    static bool configured[3] = {false, false, false};
+    if (!configured[variant]) {
+      cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+      if (e != cudaSuccess) return e;
+      configured[variant] = true;
+    }
+    kernel<<<grid, kThreads, kSmemBytes, stream>>>(P, rows, io);
+    return cudaGetLastError();
+  };
+  switch (variant) {
+    case kPlain: return run(prefill_tc_kernel<kPlain>);
+    case kGated: return run(prefill_tc_kernel<kGated>);
+    case kGatedDelta: return run(prefill_tc_kernel<kGatedDelta>);
+  }
+  return kUnsupported;
+}
+
+}  // namespace kvb
