@@ -15,7 +15,8 @@
 //   S^T <- e^{A_C} S^T + (wU)^T K   (A: (wU)^T parts from TMEM, B: K^T from smem)
 // leave every per-column quantity (R, the substitution, U, the output column,
 // the state column) in the registers of the thread that owns that column: the
-// forward substitution runs one column per thread with no data exchange.
+// UT transform T = (I + Mk)^{-1} is built in 16 x 16 blocks by all threads and
+// applied as one more tensor-core product, U^T = R^T T^T.
 // Operands that are not exact in bf16 (S, U, wU, Mq) enter as hi + lo bf16
 // parts (about 16 significant bits; the lo x lo product is dropped), with fp32
 // accumulation in TMEM.  Single-thread MMA issue, completion via tcgen05.commit
@@ -30,7 +31,7 @@ constexpr int kC = 64, kD = 128, kThreads = 256;  // two warpgroups share every 
 constexpr uint32_t kColS = 0;     // S^T fp32            [128 lanes x 128]
 constexpr uint32_t kColP = 128;   // A parts: S^T hi/lo (64 + 64), later U^T hi/lo, (wU)^T hi/lo (32 each)
 constexpr uint32_t kColY = 256;   // Y^T fp32 (tokens: 0..63 q, 64..127 k); O^T in 0..63
-constexpr uint32_t kColG = 384;   // G fp32 (lane = token of [Q;K], column = key token)
+constexpr uint32_t kColG = 384;   // G fp32 (lane = token of [Q;K], column = key token); then U^T
 constexpr uint32_t kTmemCols = 512;
 // shared memory (bytes)
 constexpr int kXBytes = 2 * kC * kD * 2;        // [Q;K] bf16, core-matrix K-major (32 KB)
@@ -44,9 +45,11 @@ constexpr int kMkBytes = kC * kLdMk * 4;
 constexpr int kOffKt = 2 * kStage;
 constexpr int kOffMq = kOffKt + kKtBytes;       // [2 parts]
 constexpr int kOffMk = kOffMq + 2 * kMqBytes;
-constexpr int kOffR = kOffMk + kMkBytes;        // R of tokens 32..63, fp32 [32][128]
-constexpr int kRBytes = 32 * kD * 4;
-constexpr int kOffA = kOffR + kRBytes;          // Acum, e^A, w: [3][C]
+constexpr int kOffR = kOffMk + kMkBytes;        // scratch for the block products, fp32 [3][16][16]
+constexpr int kRBytes = 3 * 16 * 16 * 4;
+constexpr int kOffTf = kOffR + kRBytes;         // T = (I + Mk)^-1, fp32 [64][68]
+constexpr int kOffTp = kOffTf + kMkBytes;       // T as bf16 hi / lo parts, core-matrix K-major
+constexpr int kOffA = kOffTp + 2 * kMqBytes;    // Acum, e^A, w: [3][C]
 constexpr int kSmemBytes = kOffA + 3 * kC * 4;
 // core-matrix strides (bytes): 8 rows x 16 bytes per core matrix, k groups adjacent
 constexpr uint32_t kLbo = 128;
@@ -151,6 +154,61 @@ __device__ __forceinline__ void split32(const float (&x)[32], uint32_t (&hi)[16]
     lo[j] = pack2(l0, l1);
   }
 }
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};"
+      ::"r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+        "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+      : "memory");
+}
+
+// T = (I + Mk)^{-1} for the strictly lower 64 x 64 Mk (fp32, row stride kLdMk),
+// in 16 x 16 blocks: T_aa = (I + Mk_aa)^{-1} by forward substitution (one
+// column per thread), then T_ab = -T_aa sum_{b<=c<a} Mk_ac T_cb level by level
+// (a - b = 1, 2, 3), one block entry per thread and step.  Writes T (zero above
+// the diagonal) to Tf; P is scratch for three 16 x 16 blocks.  All 256 threads.
+__device__ __forceinline__ void ut_inverse(const float *Mk, float *Tf, float *Pb, int tid) {
+  if (tid < 64) {  // diagonal blocks: block a, column j
+    const int a = tid >> 4, j = tid & 15, o = a * 16;
+    float t[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      float acc = i == j ? 1.f : 0.f;
+#pragma unroll
+      for (int l = 0; l < i; ++l) acc = fmaf(-Mk[(o + i) * kLdMk + o + l], t[l], acc);
+      t[i] = i < j ? 0.f : acc;
+    }
+#pragma unroll
+    for (int i = 0; i < 16; ++i) Tf[(o + i) * kLdMk + o + j] = t[i];
+  }
+  __syncthreads();
+  // level d: blocks (a, a - d), a = d .. 3; P = sum_c Mk_ac T_c,a-d, then T = -T_aa P
+  for (int dlev = 1; dlev <= 3; ++dlev) {
+    const int nblk = 4 - dlev;
+    for (int e = tid; e < nblk * 256; e += kThreads) {
+      const int blk = e >> 8, i = (e >> 4) & 15, j = e & 15;
+      const int a = blk + dlev, bcol = a - dlev;
+      float acc = 0.f;
+      for (int cb = bcol; cb < a; ++cb)
+#pragma unroll
+        for (int l = 0; l < 16; ++l)
+          acc = fmaf(Mk[(a * 16 + i) * kLdMk + cb * 16 + l], Tf[(cb * 16 + l) * kLdMk + bcol * 16 + j], acc);
+      Pb[blk * 256 + i * 16 + j] = acc;
+    }
+    __syncthreads();
+    for (int e = tid; e < nblk * 256; e += kThreads) {
+      const int blk = e >> 8, i = (e >> 4) & 15, j = e & 15;
+      const int a = blk + dlev, bcol = a - dlev;
+      float acc = 0.f;
+#pragma unroll
+      for (int l = 0; l < 16; ++l)
+        acc = fmaf(Tf[(a * 16 + i) * kLdMk + a * 16 + l], Pb[blk * 256 + l * 16 + j], acc);
+      Tf[(a * 16 + i) * kLdMk + bcol * 16 + j] = -acc;
+    }
+    __syncthreads();
+  }
+}
+
 __device__ __forceinline__ void cp16(uint32_t dst, const void *src, bool valid) {
   const int n = valid ? 16 : 0;
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src), "r"(n) : "memory");
@@ -238,7 +296,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int c = lt;                      // as a state column
   bool ok = true;
   uint32_t phase = 0;
-  float *Rb = reinterpret_cast<float *>(smem + kOffR);
 
   // 64 state rows (this warpgroup's half) of column c: fp32 into S^T, bf16 parts
   auto put_half = [&](const float (&col)[64]) {
@@ -386,42 +443,84 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
-    // column c of R (delta rule) for tokens 32 wg .. 32 wg + 31: warpgroup 0 keeps
-    // its half in registers, warpgroup 1 passes its half through shared memory
-    float u[kC];
+    // column c of R (delta rule), tokens 32 wg .. 32 wg + 31, as bf16 parts into
+    // TMEM: the A operand (R^T) of U^T = R^T T^T
     if (DELTA) {
       uint32_t w[32];
       tmem_ld32(my + kColY + kC + wg * 32, w);
+      float r[32];
 #pragma unroll
       for (int j = 0; j < 32; ++j) {
         const int jj = wg * 32 + j;
-        const float r = bs[jj] * (__bfloat162float(vs[jj * kD + c]) - eA[jj] * __uint_as_float(w[j]));
-        if (wg == 0) u[j] = r;
-        else Rb[j * kD + c] = r;
+        r[j] = bs[jj] * (__bfloat162float(vs[jj * kD + c]) - eA[jj] * __uint_as_float(w[j]));
       }
+      uint32_t hi[16], lo[16];
+      split32(r, hi, lo);
+      tmem_st16(my + kColP + wg * 16, hi);
+      tmem_st16(my + kColP + 32 + wg * 16, lo);
+      tmem_wait_st();
     }
     fence_async_smem();
+    fence_before();
     __syncthreads();  // Mk, Mq and R complete
+    fence_after();
+
+    // the UT transform: T = (I + Mk)^{-1} in blocks, its bf16 parts (B operand,
+    // rows i, k = j), then U^T = R^T T^T on the tensor cores into the G columns
+    float u[kC];
+    if (DELTA) {
+      float *Tf = reinterpret_cast<float *>(smem + kOffTf);
+      ut_inverse(Mk, Tf, reinterpret_cast<float *>(smem + kOffR), tid);
+      {
+        const int i = tid >> 2, jq = (tid & 3) * 16;  // row i, 16 columns
+        float x[16];
+#pragma unroll
+        for (int q = 0; q < 16; ++q) x[q] = jq + q <= i ? Tf[i * kLdMk + jq + q] : 0.f;
+        uint8_t *tp = smem + kOffTp;
+#pragma unroll
+        for (int g2 = 0; g2 < 2; ++g2) {
+          uint16_t hh[8], ll[8];
+#pragma unroll
+          for (int q = 0; q < 8; ++q) split_bf16(x[g2 * 8 + q], hh[q], ll[q]);
+          const int off = (i >> 3) * kSboKt + (jq / 8 + g2) * kLbo + (i & 7) * 16;
+          *reinterpret_cast<uint4 *>(tp + off) =
+              make_uint4(pack2(hh[0], hh[1]), pack2(hh[2], hh[3]), pack2(hh[4], hh[5]), pack2(hh[6], hh[7]));
+          *reinterpret_cast<uint4 *>(tp + kMqBytes + off) =
+              make_uint4(pack2(ll[0], ll[1]), pack2(ll[2], ll[3]), pack2(ll[4], ll[5]), pack2(ll[6], ll[7]));
+        }
+      }
+      fence_async_smem();
+      fence_before();
+      __syncthreads();
+      fence_after();
+      if (tid == 0) {
+        const uint32_t idU = idesc_bf16(128, kC), tpa = smem_u32(smem + kOffTp);
+#pragma unroll
+        for (int combo = 0; combo < 3; ++combo) {
+          const int ra = combo == 2 ? 32 : 0;                   // R^T hi, hi, lo
+          const uint32_t tb = tpa + (combo == 1 ? kMqBytes : 0);  // T hi, lo, hi
+#pragma unroll
+          for (int k0 = 0; k0 < kC; k0 += 16)
+            mma_ts(tmem + kColG, tmem + kColP + ra + k0 / 2, sdesc(tb + (k0 / 8) * kLbo, kLbo, kSboKt), idU,
+                   combo > 0 || k0 > 0);
+        }
+        mma_commit(mbar);
+      }
+      ok = __syncthreads_and(mbar_wait(mbar, phase)) != 0;  // CTA-uniform
+      phase ^= 1;
+      fence_after();
+      if (!ok) break;
+    }
 
     if (wg == 0) {
-      // forward substitution (I + Mk) U = R, one column per thread
+      // column c of U: from the UT product (delta rule) or V
       if (DELTA) {
 #pragma unroll
-        for (int j = 32; j < kC; ++j) u[j] = Rb[(j - 32) * kD + c];
+        for (int q = 0; q < 2; ++q) {
+          uint32_t w[32];
+          tmem_ld32(my + kColG + q * 32, w);
 #pragma unroll
-        for (int i = 1; i < kC; ++i) {
-          float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
-#pragma unroll
-          for (int j = 0; j + 3 < i; j += 4) {
-            const float4 x = *reinterpret_cast<const float4 *>(&Mk[i * kLdMk + j]);
-            s0 = fmaf(x.x, u[j], s0);
-            s1 = fmaf(x.y, u[j + 1], s1);
-            s2 = fmaf(x.z, u[j + 2], s2);
-            s3 = fmaf(x.w, u[j + 3], s3);
-          }
-#pragma unroll
-          for (int j = i & ~3; j < i; ++j) s0 = fmaf(Mk[i * kLdMk + j], u[j], s0);
-          u[i] -= (s0 + s1) + (s2 + s3);
+          for (int j = 0; j < 32; ++j) u[q * 32 + j] = __uint_as_float(w[j]);
         }
       } else {
 #pragma unroll
