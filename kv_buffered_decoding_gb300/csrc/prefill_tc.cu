@@ -132,16 +132,30 @@ __device__ __forceinline__ void split_bf16(float x, uint16_t &hi, uint16_t &lo) 
 }
 __device__ __forceinline__ uint32_t pack2(uint16_t a, uint16_t b) { return (uint32_t)a | ((uint32_t)b << 16); }
 
-// 64 fp32 values -> bf16 hi and lo parts packed in pairs (32 words each)
-__device__ __forceinline__ void split64(const float (&x)[64], uint32_t (&hi)[32], uint32_t (&lo)[32]) {
+// 16 fp32 values -> bf16 hi and lo parts packed in pairs (8 words each)
+__device__ __forceinline__ void split16(const float (&x)[16], uint32_t (&hi)[8], uint32_t (&lo)[8]) {
 #pragma unroll
-  for (int j = 0; j < 32; ++j) {
+  for (int j = 0; j < 8; ++j) {
     uint16_t h0, l0, h1, l1;
     split_bf16(x[2 * j], h0, l0);
     split_bf16(x[2 * j + 1], h1, l1);
     hi[j] = pack2(h0, h1);
     lo[j] = pack2(l0, l1);
   }
+}
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&r)[8]) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};"
+               ::"r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]),
+                 "r"(r[7])
+               : "memory");
 }
 
 __device__ __forceinline__ void split32(const float (&x)[32], uint32_t (&hi)[16], uint32_t (&lo)[16]) {
@@ -297,30 +311,29 @@ __global__ void __launch_bounds__(kThreads, 1)
   bool ok = true;
   uint32_t phase = 0;
 
-  // 64 state rows (this warpgroup's half) of column c: fp32 into S^T, bf16 parts
-  auto put_half = [&](const float (&col)[64]) {
-    uint32_t w[32];
+  // bf16 hi / lo parts of 16 state rows (16 r0 .. 16 r0 + 15) of column c into the
+  // A region (the operand of Y^T = S^T X^T)
+  auto put_parts16 = [&](const float (&x)[16], int r0) {
+    uint32_t hi[8], lo[8];
+    split16(x, hi, lo);
+    tmem_st8(my + kColP + r0 * 8, hi);
+    tmem_st8(my + kColP + 64 + r0 * 8, lo);
+  };
+  // this warpgroup's 64 state rows of column c: fp32 into S^T, and their parts
+#pragma unroll 1
+  for (int q = 0; q < 4; ++q) {
+    const int r0 = wg * 4 + q;  // 16-row piece
+    float x[16];
+    uint32_t w[16];
 #pragma unroll
-    for (int q = 0; q < 2; ++q) {
-#pragma unroll
-      for (int j = 0; j < 32; ++j) w[j] = __float_as_uint(col[q * 32 + j]);
-      tmem_st32(my + kColS + wg * 64 + q * 32, w);
+    for (int j = 0; j < 16; ++j) {
+      x[j] = from_zero ? 0.f : Sg[(size_t)(r0 * 16 + j) * kD + c];
+      w[j] = __float_as_uint(x[j]);
     }
-  };
-  auto put_parts = [&](const float (&col)[64]) {
-    uint32_t hi[32], lo[32];
-    split64(col, hi, lo);
-    tmem_st32(my + kColP + wg * 32, hi);
-    tmem_st32(my + kColP + 64 + wg * 32, lo);
-  };
-  {
-    float col[64];
-#pragma unroll
-    for (int r = 0; r < 64; ++r) col[r] = from_zero ? 0.f : Sg[(size_t)(wg * 64 + r) * kD + c];
-    put_half(col);
-    put_parts(col);
-    tmem_wait_st();
+    tmem_st16(my + kColS + r0 * 16, w);
+    put_parts16(x, r0);
   }
+  tmem_wait_st();
 
   for (int ch = 0; ch < nchunks && ok; ++ch) {
     uint8_t *st = smem + (ch & 1) * kStage;
@@ -467,7 +480,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     // the UT transform: T = (I + Mk)^{-1} in blocks, its bf16 parts (B operand,
     // rows i, k = j), then U^T = R^T T^T on the tensor cores into the G columns
-    float u[kC];
     if (DELTA) {
       float *Tf = reinterpret_cast<float *>(smem + kOffTf);
       ut_inverse(Mk, Tf, reinterpret_cast<float *>(smem + kOffR), tid);
@@ -513,33 +525,34 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 
     if (wg == 0) {
-      // column c of U: from the UT product (delta rule) or V
-      if (DELTA) {
+      // column c of U (from the UT product, or V), 16 tokens at a time: U^T and
+      // (wU)^T parts into TMEM, the A operands of the second MMAs
+#pragma unroll 1
+      for (int q = 0; q < 4; ++q) {
+        float x[16];
+        if (DELTA) {
+          uint32_t w[16];
+          tmem_ld16(my + kColG + q * 16, w);
 #pragma unroll
-        for (int q = 0; q < 2; ++q) {
-          uint32_t w[32];
-          tmem_ld32(my + kColG + q * 32, w);
+          for (int j = 0; j < 16; ++j) x[j] = __uint_as_float(w[j]);
+        } else {
 #pragma unroll
-          for (int j = 0; j < 32; ++j) u[q * 32 + j] = __uint_as_float(w[j]);
+          for (int j = 0; j < 16; ++j) x[j] = __bfloat162float(vs[(q * 16 + j) * kD + c]);
         }
-      } else {
+        uint32_t hi[8], lo[8];
+        split16(x, hi, lo);
+        tmem_st8(my + kColP + q * 8, hi);
+        tmem_st8(my + kColP + 32 + q * 8, lo);
 #pragma unroll
-        for (int j = 0; j < kC; ++j) u[j] = __bfloat162float(vs[j * kD + c]);
+        for (int j = 0; j < 16; ++j) x[j] *= wL[q * 16 + j];
+        split16(x, hi, lo);
+        tmem_st8(my + kColP + 64 + q * 8, hi);
+        tmem_st8(my + kColP + 96 + q * 8, lo);
       }
-      // U^T and (wU)^T parts into TMEM (A operands of the second MMAs)
-      uint32_t hi[32], lo[32];
-      split64(u, hi, lo);
-      tmem_st32(my + kColP, hi);
-      tmem_st32(my + kColP + 32, lo);
-#pragma unroll
-      for (int j = 0; j < kC; ++j) u[j] *= wL[j];
-      split64(u, hi, lo);
-      tmem_st32(my + kColP + 64, hi);
-      tmem_st32(my + kColP + 96, lo);
     } else {
       // meanwhile: e^A scale Y_q^T (the output accumulator) and e^{A_C} S^T
       uint32_t w[32];
-#pragma unroll
+#pragma unroll 1
       for (int q = 0; q < 2; ++q) {
         tmem_ld32(my + kColY + q * 32, w);
 #pragma unroll
@@ -547,7 +560,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_st32(my + kColY + q * 32, w);
       }
       const float eL = eA[kC - 1];
-#pragma unroll
+#pragma unroll 1
       for (int q = 0; q < 4; ++q) {
         tmem_ld32(my + kColS + q * 32, w);
 #pragma unroll
@@ -597,14 +610,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (t0 + i < L) io.o[((b * Tp + t0 + i) * P.Hv + h) * kD + c] = __uint_as_float(w[j]);
       }
       if (ch + 1 < nchunks) {
-        float col[64];
+#pragma unroll 1
+        for (int q = 0; q < 4; ++q) {
+          const int r0 = wg * 4 + q;
+          uint32_t w16[16];
+          tmem_ld16(my + kColS + r0 * 16, w16);
+          float x[16];
 #pragma unroll
-        for (int q = 0; q < 2; ++q) {
-          tmem_ld32(my + kColS + wg * 64 + q * 32, w);
-#pragma unroll
-          for (int j = 0; j < 32; ++j) col[q * 32 + j] = __uint_as_float(w[j]);
+          for (int j = 0; j < 16; ++j) x[j] = __uint_as_float(w16[j]);
+          put_parts16(x, r0);
         }
-        put_parts(col);
         tmem_wait_st();
       }
     }
