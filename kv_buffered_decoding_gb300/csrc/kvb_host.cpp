@@ -191,8 +191,10 @@ int decode_like(kvb_pool *p, int32_t B, const int32_t *req_ids, const void *q, c
         if (d.n + 1 > lmax) lmax = d.n + 1;
       }
     }
+    kvb::TokenIO io_short = io;
+    io_short.lmax = nmax;  // most buffered tokens any row stages
     cudaError_t e = mode == kShort
-                        ? kvb::launch_short(p->view, p->rows, io, c.variant, c.kv_dtype, c.d_k, stream)
+                        ? kvb::launch_short(p->view, p->rows, io_short, c.variant, c.kv_dtype, c.d_k, stream)
                         : kvb::launch_decode(p->view, p->rows, io, c.variant, c.kv_dtype, c.d_k,
                                              recurrent, lmax, nmax, stream);
     if (e != cudaSuccess) return cuda_status(e);

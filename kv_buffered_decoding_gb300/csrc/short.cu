@@ -6,29 +6,55 @@
 //   u_t = v_t                                                 plain / gated
 //   u_t = beta_t (v_t - sum_{i<t} e^{A_t-A_i} (k_t.k_i) u_i)   gated delta rule
 //   o_t = sum_{i<t} e^{A_t-A_i} (q_t.k_i) u_i + (q_t.k_t) u_t
-// One CTA of four warps per (batch row, value head).  Warp w takes buffered
-// tokens w, w+4, w+8, ... in register chunks, issuing the next chunk's loads
-// before computing the current one, reduces each chunk's dot products with one
+// One CTA of four warps per (batch row, value head).  Every buffered token's
+// key, u (or v) and gate reaches shared memory in one cp.async burst, so the row
+// pays one memory round trip instead of one per chunk of tokens; then warp w
+// takes tokens w, w+4, w+8, ..., reduces each group's dot products with one
 // butterfly, and accumulates e^{A_t-A_i} s_i u_i for its lane's columns; the
 // four warps' partial sums are added once through shared memory.
+#include <type_traits>
+
 #include "kvb_device.cuh"
 
 namespace kvb {
 
+__device__ __forceinline__ void scp16(void *smem, const void *gmem) {
+  const unsigned s = static_cast<unsigned>(__cvta_generic_to_shared(smem));
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(s), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void scp4(void *smem, const void *gmem) {
+  const unsigned s = static_cast<unsigned>(__cvta_generic_to_shared(smem));
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;\n" ::"r"(s), "l"(gmem) : "memory");
+}
+
+// Shared-memory bytes for rows holding up to `nmax` buffered tokens.
 template <typename KT, int VARIANT, int D>
-__global__ void __launch_bounds__(128) short_kernel(const PoolView P, const RowBatch rows,
+constexpr size_t short_smem(int nmax) {
+  constexpr size_t usz = VARIANT == kGatedDelta ? sizeof(float) : sizeof(KT);
+  return (size_t)nmax * D * (sizeof(KT) + usz) + (size_t)((nmax + 3) & ~3) * sizeof(float);
+}
+
+template <typename KT, int VARIANT, int D>
+__global__ void __launch_bounds__(128) short_kernel(const PoolView P,
+                                                     const __grid_constant__ RowBatch rows,
                                                      const TokenIO io) {
   constexpr int NT = 128, NW = 4, E = D / 32;
   constexpr bool DELTA = VARIANT == kGatedDelta, GATED = VARIANT != kPlain;
-  constexpr int C = DELTA ? 2 : 4;  // tokens per chunk (one butterfly of four sums)
+  using UT = typename std::conditional<DELTA, float, KT>::type;  // stored u (or v)
+  constexpr int C = DELTA ? 2 : 4;  // tokens per butterfly (four sums)
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int h = blockIdx.x;
-  const RowDesc d = rows.r[blockIdx.y];
+  const RowDesc &d = rows.r[blockIdx.y];
   const size_t b = (size_t)rows.row0 + blockIdx.y;
   const int group = P.Hv / P.Hk;
   const int hq = h / group;
   const int n = d.n;  // buffered tokens; the current token goes to slot n
+  const int nmax = io.lmax;
 
+  extern __shared__ float4 dyn_smem[];
+  KT *ks = reinterpret_cast<KT *>(dyn_smem);                     // [nmax][D] keys
+  UT *usm = reinterpret_cast<UT *>(ks + (size_t)nmax * D);        // [nmax][D] u / v
+  float *As = reinterpret_cast<float *>(usm + (size_t)nmax * D);  // [nmax] gates
   __shared__ __align__(16) float qs[D];
   __shared__ __align__(16) float kts[D];
   __shared__ __align__(16) float part_o[NW][D];
@@ -37,7 +63,7 @@ __global__ void __launch_bounds__(128) short_kernel(const PoolView P, const RowB
   __shared__ float s_t_s;
   __shared__ int bad;
 
-  // 1. where tokens 0..n live; q (scaled) and k_t to shared
+  // 1. where tokens 0..n live (warp 0); q (scaled) and k_t to shared
   if (warp == 0) {
     int anybad = 0;
     for (int i = lane; i <= n; i += 32) {
@@ -63,7 +89,27 @@ __global__ void __launch_bounds__(128) short_kernel(const PoolView P, const RowB
   __syncthreads();
   if (bad) return;  // CTA-uniform
 
-  const float A_t = (GATED && n > 0 ? P.gbuf[voff[n - 1]] : 0.f) + a_t;
+  // 2. every buffered token's key, u / v and gate into shared memory in one burst
+  {
+    constexpr int KP = D * (int)sizeof(KT) / 16, UP = D * (int)sizeof(UT) / 16;
+    constexpr int KE = 16 / (int)sizeof(KT), UE = 16 / (int)sizeof(UT);
+    for (int c = tid; c < n * KP; c += NT) {
+      const int i = c / KP, p = c - i * KP;
+      scp16(ks + (size_t)i * D + p * KE, static_cast<const KT *>(P.kbuf) + koff[i] + p * KE);
+    }
+    const UT *ub = DELTA ? reinterpret_cast<const UT *>(P.ubuf) : static_cast<const UT *>(P.vbuf);
+    for (int c = tid; c < n * UP; c += NT) {
+      const int i = c / UP, p = c - i * UP;
+      scp16(usm + (size_t)i * D + p * UE, ub + voff[i] * D + p * UE);
+    }
+    if (GATED)
+      for (int i = tid; i < n; i += NT) scp4(As + i, P.gbuf + voff[i]);
+    asm volatile("cp.async.commit_group;\n" ::: "memory");
+    asm volatile("cp.async.wait_group 0;\n" ::: "memory");
+  }
+  __syncthreads();
+
+  const float A_t = (GATED && n > 0 ? As[n - 1] : 0.f) + a_t;
   float qv[E], tv[E];
   load_smem<E>(qs + lane * E, qv);
   load_smem<E>(kts + lane * E, tv);
@@ -75,35 +121,25 @@ __global__ void __launch_bounds__(128) short_kernel(const PoolView P, const RowB
     if (lane == 0) s_t_s = st;
   }
 
-  // 2. this warp's buffered tokens, chunk by chunk with the next chunk in flight
+  // 3. this warp's buffered tokens (w, w + 4, ...), C per butterfly
   float po[E], pc[E];
 #pragma unroll
   for (int e = 0; e < E; ++e) po[e] = pc[e] = 0.f;
-  float kc[C][E], uc[C][E], ac[C];
-  auto load_chunk = [&](int i0, float (&kk)[C][E], float (&uu)[C][E], float (&aa)[C]) {
+  for (int i0 = warp; i0 < n; i0 += NW * C) {
+    float kc[C][E], uc[C][E], ac[C];
 #pragma unroll
     for (int x = 0; x < C; ++x) {
       const int i = i0 + NW * x;
       if (i < n) {
-        load_row<E>(static_cast<const KT *>(P.kbuf) + koff[i] + lane * E, kk[x]);
-        if (DELTA)
-          load_row<E>(P.ubuf + voff[i] * D + lane * E, uu[x]);
-        else
-          load_row<E>(static_cast<const KT *>(P.vbuf) + voff[i] * D + lane * E, uu[x]);
-        aa[x] = GATED ? P.gbuf[voff[i]] : 0.f;
+        load_row<E>(ks + (size_t)i * D + lane * E, kc[x]);
+        load_row<E>(usm + (size_t)i * D + lane * E, uc[x]);
+        ac[x] = GATED ? As[i] : 0.f;
       } else {
 #pragma unroll
-        for (int e = 0; e < E; ++e) kk[x][e] = uu[x][e] = 0.f;
-        aa[x] = A_t;
+        for (int e = 0; e < E; ++e) kc[x][e] = uc[x][e] = 0.f;
+        ac[x] = A_t;
       }
     }
-  };
-  const int stride = NW * C;  // tokens between this warp's chunks
-  if (warp < n) load_chunk(warp, kc, uc, ac);
-  for (int i0 = warp; i0 < n; i0 += stride) {
-    float kn[C][E], un[C][E], an[C];
-    const bool more = i0 + stride < n;
-    if (more) load_chunk(i0 + stride, kn, un, an);
     float sums[4];
 #pragma unroll
     for (int x = 0; x < C; ++x) {
@@ -134,17 +170,6 @@ __global__ void __launch_bounds__(128) short_kernel(const PoolView P, const RowB
         if (DELTA) pc[e] = fmaf(wc, uc[x][e], pc[e]);
       }
     }
-    if (more) {
-#pragma unroll
-      for (int x = 0; x < C; ++x) {
-        ac[x] = an[x];
-#pragma unroll
-        for (int e = 0; e < E; ++e) {
-          kc[x][e] = kn[x][e];
-          uc[x][e] = un[x][e];
-        }
-      }
-    }
   }
 #pragma unroll
   for (int e = 0; e < E; ++e) {
@@ -153,7 +178,7 @@ __global__ void __launch_bounds__(128) short_kernel(const PoolView P, const RowB
   }
   __syncthreads();
 
-  // 3. one thread per column: the current token's u and the output; append
+  // 4. one thread per column: the current token's u and the output; append
   const KT *vg = static_cast<const KT *>(io.v) + (b * P.Hv + h) * D;
   for (int c = tid; c < D; c += NT) {
     float o = 0.f, pcs = 0.f;
@@ -180,14 +205,28 @@ __global__ void __launch_bounds__(128) short_kernel(const PoolView P, const RowB
   }
 }
 
+template <typename KT, int VARIANT, int D>
+static cudaError_t run_short(const PoolView &P, const RowBatch &rows, const TokenIO &io,
+                             cudaStream_t s) {
+  static bool configured = false;
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(short_kernel<KT, VARIANT, D>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)short_smem<KT, VARIANT, D>(KVB_MAX_CAPACITY));
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  dim3 grid(P.Hv, rows.count);
+  short_kernel<KT, VARIANT, D><<<grid, 128, short_smem<KT, VARIANT, D>(io.lmax), s>>>(P, rows, io);
+  return cudaGetLastError();
+}
+
 template <typename KT, int VARIANT>
 static cudaError_t short_d(const PoolView &P, const RowBatch &rows, const TokenIO &io, int d,
                            cudaStream_t s) {
-  dim3 grid(P.Hv, rows.count);
-  if (d == 128) short_kernel<KT, VARIANT, 128><<<grid, 128, 0, s>>>(P, rows, io);
-  else if (d == 64) short_kernel<KT, VARIANT, 64><<<grid, 128, 0, s>>>(P, rows, io);
-  else return kUnsupported;
-  return cudaGetLastError();
+  if (d == 128) return run_short<KT, VARIANT, 128>(P, rows, io, s);
+  if (d == 64) return run_short<KT, VARIANT, 64>(P, rows, io, s);
+  return kUnsupported;
 }
 
 template <typename KT>
