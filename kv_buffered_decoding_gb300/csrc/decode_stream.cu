@@ -357,6 +357,195 @@ __global__ void __launch_bounds__(kStreamThreads, 4)
   }
 }
 
+// ------------------------------------------------------------------ flush
+// The standalone fold (kvb_flush, and kvb_accept when the buffer fills) with the
+// same streaming: S <- e^{A_L} S0 + sum_{i<=L} e^{A_L-A_i} k_i u_i^T for the L
+// buffered tokens (L <= kStageTok), each unit's two column halves passing
+// through the tile buffer while the staged keys, u / v rows and gates of the
+// next unit arrive.  Rows flagged kFlagFromZero start from S = 0.
+template <typename KT>
+struct alignas(16) FStage {
+  KT keys[kStageTok][kD];   // buffered keys (raw)
+  float uv[kStageTok][kD];  // buffered u (gated delta) / v rows
+  float A[kStageTok];       // buffered cumulative log-gates
+  int bad;
+};
+
+template <typename KT, int VARIANT>
+__global__ void __launch_bounds__(kStreamThreads, 4)
+    flush_stream_kernel(const PoolView P, const __grid_constant__ RowBatch rows, int units,
+                        FastDiv hv_div) {
+  constexpr bool DELTA = VARIANT == kGatedDelta, GATED = VARIANT != kPlain;
+  constexpr int RPT = 16;
+  constexpr int VEC = 16 / (int)sizeof(KT);
+  constexpr int NQ = kD / VEC;
+  constexpr int NU = DELTA ? kD / 4 : kD / VEC;
+  using St = FStage<KT>;
+  extern __shared__ float4 dyn_smem[];
+  float4 *tile = dyn_smem;
+  St *stages = reinterpret_cast<St *>(dyn_smem + kTileF4);
+  __shared__ float wt[kStageTok];
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int rsub = lane >> 2, row0 = rsub * RPT;
+  const int chunk = warp * 4 + (lane & 3), colL = chunk * 4;
+  const int group = P.Hv / P.Hk;
+
+  auto issue_tile = [&](int u, int part) {
+    const int y = fast_div(u, hv_div), h = u - y * P.Hv;
+    const float *Sp = P.state + ((size_t)rows.r[y].slot * P.Hv + h) * kD * kD + part * kCW;
+    for (int i = tid; i < kTileF4; i += kStreamThreads) {
+      const int r = i >> 4, ch = i & 15;
+      cp16(&tile[tile_slot(r, ch)], Sp + (size_t)r * kD + ch * 4);
+    }
+  };
+  auto issue_small = [&](int u, int st) {
+    St &S = stages[st];
+    const int y = fast_div(u, hv_div), h = u - y * P.Hv;
+    const RowDesc &d = rows.r[y];
+    const int hq = h / group, L = d.n;
+    size_t ko = 0, vo = 0;
+    int anybad = 0;
+    if (lane < L) {
+      const int g = buffer_row(P, d, lane);
+      anybad = g < 0;
+      if (g >= 0) {
+        ko = kv_row(P, g, hq, P.Hk) * kD;
+        vo = kv_row(P, g, h, P.Hv);
+      }
+    }
+    anybad = __any_sync(kFull, anybad);
+    if (warp == 3 && lane == 0) S.bad = anybad;
+    if (!anybad) {
+      const int l2 = (warp & 1) * 32 + lane;
+      if (warp < 2) {
+        const KT *kb = static_cast<const KT *>(P.kbuf);
+        for (int c0 = 0; c0 < L * NQ; c0 += 64) {
+          const int c = c0 + l2;
+          const bool ok = c < L * NQ;
+          const int i = ok ? c / NQ : 0, p = c - i * NQ;
+          const size_t off = __shfl_sync(kFull, ko, i);
+          if (ok) cp16(&S.keys[i][p * VEC], kb + off + p * VEC);
+        }
+      } else {
+        for (int c0 = 0; c0 < L * NU; c0 += 64) {
+          const int c = c0 + l2;
+          const bool ok = c < L * NU;
+          const int i = ok ? c / NU : 0, p = c - i * NU;
+          const size_t row = __shfl_sync(kFull, vo, i) * kD;
+          if (!ok) continue;
+          if (DELTA)
+            cp16(&S.uv[i][p * 4], P.ubuf + row + p * 4);
+          else
+            cp16(reinterpret_cast<KT *>(S.uv[i]) + p * VEC, static_cast<const KT *>(P.vbuf) + row + p * VEC);
+        }
+        if (GATED && warp == 3 && lane < L) cp4(&S.A[lane], P.gbuf + vo);
+      }
+    }
+  };
+  // the unit's state half, scaled by e^{A_L} (zero for rows that start from S = 0)
+  auto tile_to_regs = [&](float4 (&s)[RPT], bool zero, float eL) {
+#pragma unroll
+    for (int j = 0; j < RPT; ++j) s[j] = zero ? f4(0.f) : mul4(eL, tile[tile_slot(row0 + j, chunk)]);
+  };
+  auto fold_half = [&](float4 (&s)[RPT], const St &S, int part, int y, int h) {
+    const RowDesc &d = rows.r[y];
+    const int L = d.n, col0 = part * kCW + colL;
+    for (int i = 0; i < L; ++i) {
+      const float4 u = mul4(wt[i], DELTA ? *reinterpret_cast<const float4 *>(&S.uv[i][col0])
+                                         : raw4(reinterpret_cast<const KT *>(S.uv[i]) + col0));
+#pragma unroll
+      for (int j = 0; j < RPT; j += 4) {
+        const float4 k4 = raw4(&S.keys[i][row0 + j]);
+        fma4(s[j], k4.x, u);
+        fma4(s[j + 1], k4.y, u);
+        fma4(s[j + 2], k4.z, u);
+        fma4(s[j + 3], k4.w, u);
+      }
+    }
+    float *Sp = P.state + ((size_t)d.slot * P.Hv + h) * kD * kD;
+#pragma unroll
+    for (int j = 0; j < RPT; ++j) st_stream4(Sp + (size_t)(row0 + j) * kD + col0, s[j]);
+  };
+
+  int u = blockIdx.x, st = 0;
+  if (u < units) {
+    issue_tile(u, 0);
+    issue_small(u, 0);
+    cp_commit();
+  }
+  for (; u < units; u += gridDim.x, st ^= 1) {
+    const int y = fast_div(u, hv_div), h = u - y * P.Hv;
+    const St &S = stages[st];
+    float4 s[RPT];
+    cp_wait_all();
+    __syncthreads();  // first half and the unit's tokens staged; previous unit done
+    const bool bad = S.bad != 0, zero = (rows.r[y].flags & kFlagFromZero) != 0;
+    const int L = rows.r[y].n;
+    const float AL = GATED && L > 0 && !bad ? S.A[L - 1] : 0.f;
+    const float eL = GATED ? expf(AL) : 1.f;
+    if (warp == 1 && lane < L) wt[lane] = GATED && !bad ? expf(AL - S.A[lane]) : 1.f;
+    tile_to_regs(s, zero, eL);
+    __syncthreads();  // the tile buffer is free; weights ready
+    issue_tile(u, 1);
+    cp_commit();
+    if (!bad) fold_half(s, S, 0, y, h);
+    cp_wait_all();
+    __syncthreads();
+    tile_to_regs(s, zero, eL);
+    __syncthreads();
+    if (u + (int)gridDim.x < units) {
+      issue_tile(u + gridDim.x, 0);
+      issue_small(u + gridDim.x, st ^ 1);
+      cp_commit();
+    }
+    if (!bad) {
+      fold_half(s, S, 1, y, h);
+      if (h == 0 && tid == 0) P.dlen[rows.r[y].req] = 0;
+    }
+  }
+}
+
+template <typename KT, int VARIANT>
+int flush_ctas() {
+  static int ctas = -1;
+  if (ctas < 0) {
+    constexpr size_t smem = kTileF4 * sizeof(float4) + 2 * sizeof(FStage<KT>);
+    int dev = 0, sms = 0, per_sm = 0;
+    cudaError_t e = cudaFuncSetAttribute(flush_stream_kernel<KT, VARIANT>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e == cudaSuccess) e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e == cudaSuccess)
+      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, flush_stream_kernel<KT, VARIANT>,
+                                                        kStreamThreads, smem);
+    ctas = e == cudaSuccess ? sms * per_sm : 0;
+  }
+  return ctas;
+}
+
+template <typename KT, int VARIANT>
+cudaError_t run_flush_stream(const PoolView &P, const RowBatch &rows, cudaStream_t stream) {
+  constexpr size_t smem = kTileF4 * sizeof(float4) + 2 * sizeof(FStage<KT>);
+  const int cap = flush_ctas<KT, VARIANT>();
+  if (cap <= 0) return kUnsupported;
+  const int units = rows.count * P.Hv;
+  const int grid = units < cap ? units : cap;
+  flush_stream_kernel<KT, VARIANT><<<grid, kStreamThreads, smem, stream>>>(
+      P, rows, units, make_fastdiv((uint32_t)P.Hv));
+  return cudaGetLastError();
+}
+
+template <typename KT>
+int fctas_for(int variant) {
+  switch (variant) {
+    case kPlain: return flush_ctas<KT, kPlain>();
+    case kGated: return flush_ctas<KT, kGated>();
+    case kGatedDelta: return flush_ctas<KT, kGatedDelta>();
+  }
+  return 0;
+}
+
 // Resident CTAs of the kernel on this device (its persistent grid), once.
 template <typename KT, int VARIANT>
 int stream_ctas() {
@@ -400,6 +589,31 @@ int ctas_for(int variant) {
 }
 
 }  // namespace
+
+bool flush_stream_pays(int units, int variant, int dtype) {
+  const int cap = dtype == 1 ? fctas_for<__nv_bfloat16>(variant)
+                             : dtype == 0 ? fctas_for<float>(variant) : 0;
+  return cap > 0 && units >= 8 * cap;
+}
+
+cudaError_t launch_flush_stream(const PoolView &P, const RowBatch &rows, int variant, int dtype,
+                                cudaStream_t stream) {
+  if (rows.count <= 0) return cudaSuccess;
+  if (dtype == 1) {
+    switch (variant) {
+      case kPlain: return run_flush_stream<__nv_bfloat16, kPlain>(P, rows, stream);
+      case kGated: return run_flush_stream<__nv_bfloat16, kGated>(P, rows, stream);
+      case kGatedDelta: return run_flush_stream<__nv_bfloat16, kGatedDelta>(P, rows, stream);
+    }
+  } else if (dtype == 0) {
+    switch (variant) {
+      case kPlain: return run_flush_stream<float, kPlain>(P, rows, stream);
+      case kGated: return run_flush_stream<float, kGated>(P, rows, stream);
+      case kGatedDelta: return run_flush_stream<float, kGatedDelta>(P, rows, stream);
+    }
+  }
+  return kUnsupported;
+}
 
 bool decode_stream_pays(int units, int variant, int dtype) {
   // each resident CTA should get at least 8 units: fewer leave its pipeline

@@ -156,6 +156,8 @@ static cudaError_t flush_variant(const PoolView &P, const RowBatch &rows, int va
 cudaError_t launch_flush(const PoolView &P, const RowBatch &rows, int variant, int dtype, int d,
                          int max_len, cudaStream_t stream) {
   if (rows.count <= 0) return cudaSuccess;
+  if (d == 128 && max_len <= kStageTok && flush_stream_pays(rows.count * P.Hv, variant, dtype))
+    return launch_flush_stream(P, rows, variant, dtype, stream);
   if (dtype == 0) return flush_variant<float>(P, rows, variant, d, max_len, stream);
   if (dtype == 1) return flush_variant<__nv_bfloat16>(P, rows, variant, d, max_len, stream);
   return kUnsupported;

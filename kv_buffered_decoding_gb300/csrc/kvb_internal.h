@@ -133,6 +133,11 @@ cudaError_t launch_decode_stream(const PoolView &P, const RowBatch &rows, const 
                                  int variant, int dtype, cudaStream_t stream);
 // Whether a launch of `units` (row, value head) pairs is large enough for it.
 bool decode_stream_pays(int units, int variant, int dtype);
+// The fold (kvb_flush and accepts that fill the buffer) with the same streaming,
+// for rows of at most kStageTok tokens at d = 128, and its size rule.
+bool flush_stream_pays(int units, int variant, int dtype);
+cudaError_t launch_flush_stream(const PoolView &P, const RowBatch &rows, int variant, int dtype,
+                                cudaStream_t stream);
 // Chunked prefill on tcgen05 / TMEM (bf16 inputs, d = 128).
 cudaError_t launch_prefill_tc(const PoolView &P, const RowBatch &rows, const TokenIO &io,
                               int variant, cudaStream_t stream);

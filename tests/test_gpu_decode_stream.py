@@ -1,4 +1,4 @@
-"""GPU parity: the persistent buffered decode (launches large enough for it).
+"""GPU parity: the persistent buffered decode and fold (launches large enough for them).
 
 Batches of 200 requests x 32 value heads (6400 units, at least 8 per resident
 CTA on a 152-SM part) take the persistent kernel; the staggered warm-up
@@ -79,4 +79,71 @@ def test_persistent_decode(layer, m):
         last_fold = total - int(n[r]) - 1
         assert rel_err(st[r], states[last_fold]) <= tol, r
     assert np.array_equal(pool.get_device_lengths(), n)
+    assert pool.get_error() is None
+
+
+@pytest.mark.parametrize("layer,promote", [
+    (I.Layer(I.GATED_DELTA, 8, 32, 128, 128, "bf16", qk_dist="l2norm"), False),
+    (I.Layer(I.GATED, 16, 32, 128, 128, "f32"), False),
+    (I.Layer(I.PLAIN, 32, 32, 128, 128, "bf16"), False),
+    (I.Layer(I.GATED_DELTA, 8, 32, 128, 128, "bf16", qk_dist="l2norm"), True),
+    (I.Layer(I.GATED, 16, 32, 128, 128, "bf16"), True),
+], ids=["flush_gated_delta_bf16", "flush_gated_f32", "flush_plain_bf16",
+        "promote_gated_delta_bf16", "promote_gated_bf16"])
+def test_persistent_fold(layer, promote):
+    """Flush (or promote) of 200 requests x 32 heads holding 0..8 buffered tokens.
+
+    With every row at most 8 tokens long and at least 8 units per resident CTA
+    the fold takes the streaming kernel.  Promotion starts from S = 0 whatever
+    the slot held (the slots are filled with NaN first)."""
+    B, bs, m = 200, 8, 9
+    rng = np.random.default_rng(720 + layer.variant + 10 * promote)
+    pool = make_pool(layer, m, B, 2, bs, num_blocks=2 * B + 8, num_slots=B + 1)
+    perm = rng.permutation(2 * B + 8)
+    S0 = np.zeros((B, layer.n_v_heads, layer.d_k, layer.d_v), dtype=np.float32)
+    if not promote:
+        S0 = I.draw_state(rng, layer, B)
+        pool.state[:B].copy_(torch.from_numpy(S0))
+    for r in range(B):
+        pool.set_request(r, -1 if promote else r, [int(x) for x in perm[2 * r:2 * r + 2]])
+    lengths = rng.integers(0, 9, size=B)
+    lengths[:3] = [0, 8, 1]
+    hist = [[] for _ in range(B)]
+    for t in range(8):
+        rows = np.nonzero(lengths > t)[0]
+        tok = I.draw_tokens(rng, layer, (len(rows),))
+        args = token_tensors(tok, layer, slice(None))
+        if promote:
+            pool.short_ctx(rows, *args)
+        else:
+            pool.decode(rows, *args)
+        for i, r in enumerate(rows):
+            hist[r].append({key: (None if val is None else val[i:i + 1])
+                            for key, val in tok.items()})
+    assert np.array_equal(pool.get_lengths(), lengths)
+    req = np.arange(B)
+    slots = rng.permutation(B) if promote else req
+    if promote:
+        pool.state.fill_(float("nan"))
+        pool.promote(req, slots)
+    else:
+        pool.flush(req)
+    torch.cuda.synchronize()
+    st = pool.state.cpu().numpy()
+    tol = tol_for(layer)
+    for r in list(range(0, B, 7)) + [1, 2, B - 1]:
+        if lengths[r] == 0:
+            if promote:
+                assert np.all(st[slots[r]] == 0.0), r
+            else:
+                assert np.array_equal(st[r], S0[r]), r
+            continue
+        seq = {key: (None if hist[r][0][key] is None
+                     else np.concatenate([h[key] for h in hist[r]])) for key in hist[r][0]}
+        _, S_ref, _ = oracle.decode_sequence(S0[r], seq, layer.variant)
+        assert rel_err(st[slots[r]], S_ref) <= tol, r
+    if promote:
+        assert np.all(np.isnan(st[B]))
+    assert np.array_equal(pool.get_lengths(), np.zeros(B))
+    assert np.array_equal(pool.get_device_lengths(), np.zeros(B))
     assert pool.get_error() is None
