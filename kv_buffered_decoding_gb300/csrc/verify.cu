@@ -21,6 +21,8 @@
 // are reduced over the row lanes by one three-level transpose-reduction; the
 // score dot products use butterfly reductions; the forward substitution is
 // done per lane for its four columns without any cross-lane reduction.
+#include <type_traits>
+
 #include "kvb_device.cuh"
 
 namespace kvb {
@@ -311,62 +313,125 @@ __global__ void __launch_bounds__(2 * D / NSPLIT, 512 / (2 * D / NSPLIT))
 }
 
 // ------------------------------------------------------------------ tensor-core verify
-// The 2T mat-vecs as one small matrix product per head on the tensor cores:
-// Y^T = X^T S0 with X = [q_0..q_{T-1}, k_0..k_{T-1}] (d_k x V, V = 2T for the
-// delta rule, T otherwise, padded to 16) and S0 the d_k x d_v state.  Each warp
-// owns 32 state columns and walks the 128 rows in k-steps of 8 with
-// mma.sync.m16n8k8 (tf32 in, fp32 accumulate).  A lane (g = lane/4, t = lane%4)
-// loads rows 8ks+t and 8ks+t+4 of its columns 32w+4g..32w+4g+3 as two
-// coalesced 128-bit loads; element i of each becomes the B fragment of n-tile
-// i (n-tile i covers columns 32w+4p+i, p = 0..7), so no data moves between
-// lanes and the sum over rows happens inside the MMA.  The state is rounded to
-// tf32 (cvt.rna, relative error <= 2^-11 per element, about 2^-12 in the
-// outputs); q and k come from bf16 and are exact in tf32.  Used for bf16
-// pools at d = 128; the fp32 path keeps verify_kernel.
+// bf16 pools at d = 128.  One CTA of four warps per (batch row, value head):
+//  0. each lane starts streaming its first quarter of state rows into registers,
+//     and warp 0 locates the chunk's tokens;
+//  1. every small operand (draft q, k, v, betas, log-gates; buffered keys, u / v
+//     and cumulative gates) reaches shared memory in one cp.async burst, raw;
+//  2. the 2T mat-vecs and every score dot product are one pass of tensor-core
+//     products over d_k: Y^T = X^T [S0 | K^T], X = [q_0..q_{T-1}, k_0..k_{T-1}]
+//     (d_k x V, V = 2T for the delta rule, T otherwise, padded to 16) and K the
+//     chunk's keys (buffered, then drafts).  Warp w owns state columns
+//     32w..32w+31 and the key tiles w, w+4; each k-step of 8 is one
+//     mma.sync.m16n8k8 per n-tile (tf32 in, fp32 accumulate).  A lane (g, t)
+//     holds rows 8ks+t and 8ks+t+4 of its state columns 32w+4g..+3 (two
+//     coalesced 128-bit loads); element i of each is the B fragment of state
+//     n-tile i, so no data moves between lanes.  The state is rounded to tf32
+//     (cvt.rna, relative error <= 2^-11 per element); q and k are bf16 and exact
+//     in tf32, so the score dots are exact products with fp32 sums;
+//  3. decay weights e^{A_j - A_l} on the scores (one entry per thread);
+//  4. per draft, in order, one column per thread: u (the forward substitution of
+//     the delta rule) and o;
+//  5. the drafts' entries go to the buffer.
+// The fp32 path and d = 64 keep verify_kernel.
+
+__device__ __forceinline__ void vcp16(void *smem, const void *gmem) {
+  const unsigned s = static_cast<unsigned>(__cvta_generic_to_shared(smem));
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(s), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void vcp4(void *smem, const void *gmem) {
+  const unsigned s = static_cast<unsigned>(__cvta_generic_to_shared(smem));
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;\n" ::"r"(s), "l"(gmem) : "memory");
+}
+// bf16 -> the fp32 (and tf32) bit pattern of the same value
+__device__ __forceinline__ uint32_t bf_bits(__nv_bfloat16 x) {
+  return (uint32_t)__bfloat16_as_ushort(x) << 16;
+}
+
+constexpr int kVXS = 128 + 8;  // bf16 row stride of the staged vectors and keys (272 B)
+constexpr int kVMaxTiles = 8;  // key tiles of 8 (two per warp): chunks of up to 64 tokens
+
+// Byte offsets of the verify CTA's shared-memory arrays (16-byte aligned each).
+struct VLayout {
+  size_t xr, kr, us, vs, y, sc, sw, cw, acum, lg, bt, koff, voff, total;
+};
+__host__ __device__ inline VLayout verify_layout(int variant, int T, int LM) {
+  const bool delta = variant == kGatedDelta;
+  const size_t V = delta ? 2 * T : T, VP = (V + 15) / 16 * 16, LP = (LM + 7) / 8 * 8;
+  auto up = [](size_t x) { return (x + 15) & ~(size_t)15; };
+  VLayout l;
+  l.xr = 0;
+  l.kr = l.xr + up(VP * kVXS * 2);
+  l.us = l.kr + up(LP * kVXS * 2);
+  l.vs = l.us + up((size_t)LM * 128 * (delta ? 4 : 2));
+  l.y = l.vs + (delta ? up((size_t)T * 128 * 2) : 0);
+  l.sc = l.y + up(V * 128 * 4);
+  l.sw = l.sc + up(V * LP * 4);
+  l.cw = l.sw + up((size_t)T * LM * 4);
+  l.acum = l.cw + (delta ? up((size_t)T * LM * 4) : 0);
+  l.lg = l.acum + up((size_t)LM * 4);
+  l.bt = l.lg + up((size_t)T * 4);
+  l.koff = l.bt + up((size_t)T * 4);
+  l.voff = l.koff + up((size_t)LM * 8);
+  l.total = l.voff + up((size_t)LM * 8);
+  return l;
+}
 
 template <int VARIANT, bool TREE>
 __global__ void __launch_bounds__(128, 4)
-    verify_mma_kernel(const PoolView P, const RowBatch rows, const TokenIO io,
+    verify_mma_kernel(const PoolView P, const __grid_constant__ RowBatch rows, const TokenIO io,
                       const __grid_constant__ TreeArg<TREE> tree) {
   using KT = __nv_bfloat16;
-  constexpr int D = 128, DK = D, DV = D, NT = 128, NW = 4, E = 4;
+  constexpr int D = 128, DK = D, DV = D, NT = 128, XS = kVXS;
   constexpr bool DELTA = VARIANT == kGatedDelta, GATED = VARIANT != kPlain;
+  using UT = typename std::conditional<DELTA, float, KT>::type;  // stored u (or v)
+  constexpr int UE = 16 / (int)sizeof(UT), UC = DV / UE;        // per 16-byte chunk, per row
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int g = lane >> 2, t = lane & 3;
   const int h = blockIdx.x;
-  const RowDesc d = rows.r[blockIdx.y];
+  const RowDesc &d = rows.r[blockIdx.y];
   const size_t b = (size_t)rows.row0 + blockIdx.y;
   const int group = P.Hv / P.Hk;
   const int hq = h / group;
   const bool has_state = d.slot >= 0;
   const int n = d.n, T = io.T, L = n + T;
-  const int LM = io.lmax;
-  const int V = DELTA ? 2 * T : T;     // mat-vec vectors
-  const int MT = (V + 15) / 16;        // 16-vector m-tiles
-  const int VP = MT * 16;
+  const int LM = io.lmax;  // >= L for every row of the launch
+  const int V = DELTA ? 2 * T : T, MT = (V + 15) / 16, LP = (LM + 7) / 8 * 8, NS = LP / 8;
 
-  // shared: Xs[VP][DK] vectors (q scaled, then k; zero padding); ks[LM][DK] chunk
-  // keys; us[LM][DV] chunk u's; Y[V][DV] mat-vec results; vs[T][DV] draft values;
-  // sw/cw[T][LM]; Acum[LM]; bt[T]; koff/voff[LM]
   extern __shared__ float4 dyn_smem[];
-  float *Xs = reinterpret_cast<float *>(dyn_smem);
-  float *ks = Xs + (size_t)VP * DK;
-  float *us = ks + (size_t)LM * DK;
-  float *Y = us + (size_t)LM * DV;
-  float *vs = Y + (size_t)V * DV;
-  float *sw = vs + (size_t)T * DV;
-  float *cw = sw + (size_t)T * LM;
-  float *Acum = cw + (size_t)T * LM;
-  float *bt = Acum + ((LM + 1) & ~1);
-  size_t *koff = reinterpret_cast<size_t *>(bt + ((T + 1) & ~1));
-  size_t *voff = koff + LM;
+  const VLayout lay = verify_layout(VARIANT, T, LM);
+  char *base = reinterpret_cast<char *>(dyn_smem);
+  KT *Xr = reinterpret_cast<KT *>(base + lay.xr);     // [VP][XS] vectors, raw
+  KT *Kr = reinterpret_cast<KT *>(base + lay.kr);     // [LP][XS] chunk keys, raw
+  UT *us = reinterpret_cast<UT *>(base + lay.us);     // [LM][DV] chunk u's (or v's)
+  KT *vs = reinterpret_cast<KT *>(base + lay.vs);     // [T][DV] draft values (delta rule)
+  float *Y = reinterpret_cast<float *>(base + lay.y);  // [V][DV] mat-vecs
+  float *Sc = reinterpret_cast<float *>(base + lay.sc);  // [V][LP] dot products
+  float *sw = reinterpret_cast<float *>(base + lay.sw);  // [T][LM] weighted q.k
+  float *cw = reinterpret_cast<float *>(base + lay.cw);  // [T][LM] weighted k.k
+  float *Acum = reinterpret_cast<float *>(base + lay.acum);
+  float *lgr = reinterpret_cast<float *>(base + lay.lg);
+  float *bt = reinterpret_cast<float *>(base + lay.bt);
+  size_t *koff = reinterpret_cast<size_t *>(base + lay.koff);
+  size_t *voff = reinterpret_cast<size_t *>(base + lay.voff);
   __shared__ int bad;
   __shared__ unsigned long long anc[KVB_MAX_DRAFTS];  // draft trees: ancestor sets
 
   const float *Sp = P.state + (has_state ? ((size_t)d.slot * P.Hv + h) * DK * DV : 0);
-  const int cbase = warp * 32 + 4 * g;  // this lane's four columns
+  const int cbase = warp * 32 + 4 * g;  // this lane's four state columns
+  // rows 32q + 8i + t and + 4 (i = 0..3) of this lane's columns: quarter q of its rows
+  float4 snx[8];
+  auto load_quarter = [&](int q) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int r0 = q * 32 + i * 8 + t;
+      snx[2 * i] = ld_stream4(Sp + (size_t)r0 * DV + cbase);
+      snx[2 * i + 1] = ld_stream4(Sp + (size_t)(r0 + 4) * DV + cbase);
+    }
+  };
+  if (has_state) load_quarter(0);
 
-  // 1. where the chunk's tokens live; vectors, draft keys, values, betas to shared
+  // 0. where the chunk's tokens live
   if (warp == 0) {
     int anybad = 0;
     for (int i = lane; i < L; i += 32) {
@@ -380,45 +445,63 @@ __global__ void __launch_bounds__(128, 4)
     anybad = __any_sync(kFull, anybad);
     if (lane == 0) bad = anybad;
   }
-  const KT *qg = static_cast<const KT *>(io.q) + b * T * P.Hk * DK;
-  const KT *kg = static_cast<const KT *>(io.k) + b * T * P.Hk * DK;
-  for (int idx = tid; idx < VP * (DK / 4); idx += NT) {
-    const int m = idx / (DK / 4), c = (idx % (DK / 4)) * 4;
-    float4 x = f4(0.f);
-    if (m < T) {
-      x = mul4(P.scale, ld4(qg + ((size_t)m * P.Hk + hq) * DK + c));
-    } else if (DELTA && m < 2 * T) {
-      x = ld4(kg + ((size_t)(m - T) * P.Hk + hq) * DK + c);
-    }
-    *reinterpret_cast<float4 *>(&Xs[m * DK + c]) = x;
-  }
-  for (int idx = tid; idx < T * (DK / 4); idx += NT) {
-    const int j = idx / (DK / 4), c = (idx % (DK / 4)) * 4;
-    *reinterpret_cast<float4 *>(&ks[(n + j) * DK + c]) = ld4(kg + ((size_t)j * P.Hk + hq) * DK + c);
-  }
-  const KT *vg = static_cast<const KT *>(io.v) + b * T * P.Hv * DV;
-  for (int idx = tid; idx < T * (DV / 4); idx += NT) {
-    const int j = idx / (DV / 4), c = (idx % (DV / 4)) * 4;
-    *reinterpret_cast<float4 *>(&vs[j * DV + c]) = ld4(vg + ((size_t)j * P.Hv + h) * DV + c);
-  }
-  if (DELTA)
-    for (int j = tid; j < T; j += NT) bt[j] = io.beta[(b * T + j) * P.Hv + h];
   __syncthreads();
   if (bad) return;  // CTA-uniform
 
-  // 2. cumulative gates; buffered keys and u's to shared
+  // 1. the small operands, raw, in one burst
+  {
+    const KT *qg = static_cast<const KT *>(io.q) + b * T * P.Hk * DK;
+    const KT *kg = static_cast<const KT *>(io.k) + b * T * P.Hk * DK;
+    const KT *vg = static_cast<const KT *>(io.v) + b * T * P.Hv * DV;
+    for (int c = tid; c < V * 16; c += NT) {  // q_j, then k_j (delta rule)
+      const int m = c >> 4, p = c & 15;
+      const KT *src = m < T ? qg + ((size_t)m * P.Hk + hq) * DK
+                            : kg + ((size_t)(m - T) * P.Hk + hq) * DK;
+      vcp16(Xr + m * XS + p * 8, src + p * 8);
+    }
+    for (int c = tid; c < L * 16; c += NT) {  // the chunk's keys: buffered, then drafts
+      const int i = c >> 4, p = c & 15;
+      const KT *src = i < n ? static_cast<const KT *>(P.kbuf) + koff[i]
+                            : kg + ((size_t)(i - n) * P.Hk + hq) * DK;
+      vcp16(Kr + i * XS + p * 8, src + p * 8);
+    }
+    // buffered u's (delta rule) or v's; without the delta rule the drafts' v's follow
+    const int urows = DELTA ? n : L;
+    const UT *ub = DELTA ? reinterpret_cast<const UT *>(P.ubuf) : static_cast<const UT *>(P.vbuf);
+    for (int c = tid; c < urows * UC; c += NT) {
+      const int i = c / UC, p = c - i * UC;
+      const UT *src = i < n ? ub + voff[i] * DV
+                            : reinterpret_cast<const UT *>(vg + ((size_t)(i - n) * P.Hv + h) * DV);
+      vcp16(us + (size_t)i * DV + p * UE, src + p * UE);
+    }
+    if (DELTA)
+      for (int c = tid; c < T * 16; c += NT) {
+        const int j = c >> 4, p = c & 15;
+        vcp16(vs + j * DV + p * 8, vg + ((size_t)j * P.Hv + h) * DV + p * 8);
+      }
+    if (GATED) {
+      for (int i = tid; i < n; i += NT) vcp4(Acum + i, P.gbuf + voff[i]);
+      if (io.log_g)
+        for (int j = tid; j < T; j += NT) vcp4(lgr + j, io.log_g + (b * T + j) * P.Hv + h);
+    }
+    if (DELTA)
+      for (int j = tid; j < T; j += NT) vcp4(bt + j, io.beta + (b * T + j) * P.Hv + h);
+    asm volatile("cp.async.commit_group;\n" ::: "memory");
+    asm volatile("cp.async.wait_group 0;\n" ::: "memory");
+  }
+  __syncthreads();
+
+  // cumulative gates of the drafts (warp 0; along each draft's path for trees)
   if (GATED) {
     if (warp == 0) {
-      const float *lg = io.log_g;
-      for (int i = lane; i < n; i += 32) Acum[i] = P.gbuf[voff[i]];
-      const float A_prev = n > 0 ? P.gbuf[voff[n - 1]] : 0.f;
-      if constexpr (TREE) {  // cumulative along each draft's path
-        for (int j = lane; j < T; j += 32) Acum[n + j] = lg ? lg[(b * T + j) * P.Hv + h] : 0.f;
+      const float A_prev = n > 0 ? Acum[n - 1] : 0.f;
+      const bool lg = io.log_g != nullptr;
+      if constexpr (TREE) {
+        for (int j = lane; j < T; j += 32) Acum[n + j] = lg ? lgr[j] : 0.f;
         __syncwarp();
         if (lane == 0) tree_walk(tree.p[blockIdx.y], T, A_prev, Acum + n, anc);
       } else {
-        warp_prefix(
-            T, [&](int j) { return lg ? lg[(b * T + j) * P.Hv + h] : 0.f; }, Acum + n, lane);
+        warp_prefix(T, [&](int j) { return lg ? lgr[j] : 0.f; }, Acum + n, lane);
         __syncwarp();
         for (int j = lane; j < T; j += 32) Acum[n + j] += A_prev;
       }
@@ -429,46 +512,50 @@ __global__ void __launch_bounds__(128, 4)
       if (tid == 0) tree_walk(tree.p[blockIdx.y], T, 0.f, nullptr, anc);
     }
   }
-  for (int idx = tid; idx < n * (DK / 4); idx += NT) {
-    const int i = idx / (DK / 4), c = (idx % (DK / 4)) * 4;
-    *reinterpret_cast<float4 *>(&ks[i * DK + c]) = ld4(static_cast<const KT *>(P.kbuf) + koff[i] + c);
-  }
-  for (int idx = tid; idx < n * (DV / 4); idx += NT) {
-    const int i = idx / (DV / 4), c = (idx % (DV / 4)) * 4;
-    float4 u;
-    if (DELTA)
-      u = ld4(P.ubuf + voff[i] * DV + c);
-    else
-      u = ld4(static_cast<const KT *>(P.vbuf) + voff[i] * DV + c);
-    *reinterpret_cast<float4 *>(&us[i * DV + c]) = u;
-  }
-  __syncthreads();
 
-  // 3. the mat-vecs on the tensor cores (each m-tile: 16 vectors x 32 columns per warp)
+  // 2. mat-vecs and score dots on the tensor cores
+  const int ntile = warp < NS ? (warp + 4 < NS ? 2 : 1) : 0;  // this warp's key tiles
   for (int mt = 0; mt < MT; ++mt) {
-    float acc[4][4];
+    float acc[4][4], sacc[2][4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
-    if (has_state) {
-      const float *xa = Xs + (size_t)(mt * 16 + g) * DK;
-      const float *xb = xa + 8 * DK;
-#pragma unroll 4
-      for (int kstep = 0; kstep < DK / 8; ++kstep) {
-        const int r0 = kstep * 8 + t;
-        const float4 s0 = ld_stream4(Sp + (size_t)r0 * DV + cbase);
-        const float4 s1 = ld_stream4(Sp + (size_t)(r0 + 4) * DV + cbase);
-        const uint32_t a[4] = {__float_as_uint(xa[r0]), __float_as_uint(xb[r0]),
-                               __float_as_uint(xa[r0 + 4]), __float_as_uint(xb[r0 + 4])};
-        mma_tf32(acc[0], a, to_tf32(s0.x), to_tf32(s1.x));
-        mma_tf32(acc[1], a, to_tf32(s0.y), to_tf32(s1.y));
-        mma_tf32(acc[2], a, to_tf32(s0.z), to_tf32(s1.z));
-        mma_tf32(acc[3], a, to_tf32(s0.w), to_tf32(s1.w));
+#pragma unroll
+    for (int i = 0; i < 2; ++i) sacc[i][0] = sacc[i][1] = sacc[i][2] = sacc[i][3] = 0.f;
+    const KT *xa = Xr + (mt * 16 + g) * XS;
+    const KT *xb = xa + 8 * XS;
+    if (mt > 0 && has_state) load_quarter(0);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      float4 cur[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) cur[i] = snx[i];
+      if (q < 3 && has_state) load_quarter(q + 1);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int k0 = q * 32 + i * 8;
+        const uint32_t a[4] = {bf_bits(xa[k0 + t]), bf_bits(xb[k0 + t]), bf_bits(xa[k0 + t + 4]),
+                               bf_bits(xb[k0 + t + 4])};
+        if (has_state) {
+          const float4 s0 = cur[2 * i], s1 = cur[2 * i + 1];
+          mma_tf32(acc[0], a, to_tf32(s0.x), to_tf32(s1.x));
+          mma_tf32(acc[1], a, to_tf32(s0.y), to_tf32(s1.y));
+          mma_tf32(acc[2], a, to_tf32(s0.z), to_tf32(s1.z));
+          mma_tf32(acc[3], a, to_tf32(s0.w), to_tf32(s1.w));
+        }
+        if (ntile > 0) {
+          const KT *kr = Kr + (warp * 8 + g) * XS + k0;
+          mma_tf32(sacc[0], a, bf_bits(kr[t]), bf_bits(kr[t + 4]));
+        }
+        if (ntile > 1) {
+          const KT *kr = Kr + ((warp + 4) * 8 + g) * XS + k0;
+          mma_tf32(sacc[1], a, bf_bits(kr[t]), bf_bits(kr[t + 4]));
+        }
       }
     }
-    // D[m][p] of n-tile i is vector m at column warp*32 + 4p + i
+    // state n-tile i: D[m][p] is vector m at column warp*32 + 4p + i
+    const int m0 = mt * 16 + g, m1 = m0 + 8;
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      const int m0 = mt * 16 + g, m1 = m0 + 8;
       const int c0 = warp * 32 + 8 * t + i, c1 = c0 + 4;
       if (m0 < V) {
         Y[m0 * DV + c0] = acc[i][0];
@@ -479,92 +566,85 @@ __global__ void __launch_bounds__(128, 4)
         Y[m1 * DV + c1] = acc[i][3];
       }
     }
-  }
-
-  // 4. decay-weighted scores, two pairs per warp pass (as in verify_kernel)
-  const int npairs = T * (n + 1) + T * (T - 1) / 2;
-  const float *qsv = Xs;  // scaled draft queries are vectors 0..T-1
-  for (int p0 = 2 * warp; p0 < npairs; p0 += 2 * NW) {
-    int ja, la, jb = 0, lb = 0;
-    pair_jl(p0, n, ja, la);
-    const bool has_b = p0 + 1 < npairs;
-    if (has_b) pair_jl(p0 + 1, n, jb, lb);
-    float q0[E], k0[E], x0[E], q1[E], k1[E], x1[E];
-    load_smem<E>(qsv + ja * DK + lane * E, q0);
-    load_smem<E>(ks + (n + ja) * DK + lane * E, k0);
-    load_smem<E>(ks + la * DK + lane * E, x0);
-    load_smem<E>(qsv + jb * DK + lane * E, q1);
-    load_smem<E>(ks + (n + jb) * DK + lane * E, k1);
-    load_smem<E>(ks + lb * DK + lane * E, x1);
-    float qa = 0.f, ka = 0.f, qb = 0.f, kb = 0.f;
+    // key tile s: D[m][p] is vector m against key 8s + p
 #pragma unroll
-    for (int e = 0; e < E; ++e) {
-      qa = fmaf(q0[e], x0[e], qa);
-      qb = fmaf(q1[e], x1[e], qb);
-      if (DELTA) {
-        ka = fmaf(k0[e], x0[e], ka);
-        kb = fmaf(k1[e], x1[e], kb);
+    for (int x = 0; x < 2; ++x)
+      if (x < ntile) {
+        const int l0 = (warp + 4 * x) * 8 + 2 * t;
+        if (m0 < V) {
+          Sc[m0 * LP + l0] = sacc[x][0];
+          Sc[m0 * LP + l0 + 1] = sacc[x][1];
+        }
+        if (m1 < V) {
+          Sc[m1 * LP + l0] = sacc[x][2];
+          Sc[m1 * LP + l0 + 1] = sacc[x][3];
+        }
       }
-    }
-    float r;
-    int which;
-    if (DELTA) {
-      r = butterfly4(qa, ka, qb, kb, lane);
-      which = lane >> 3;
-    } else {
-      r = butterfly2(qa, qb, lane);
-      which = (lane >> 4) * 2;
-    }
-    if ((lane & 7) == 0 && (DELTA || (lane & 15) == 0)) {
-      const bool second = which >= 2;
-      if (!second || has_b) {
-        const int j = second ? jb : ja, l = second ? lb : la;
-        // draft trees: a draft sees the buffer and its own path only
-        const bool on_path = !TREE || l < n || ((anc[j] >> (l - n)) & 1ull);
-        const float w = GATED && on_path ? expf(Acum[n + j] - Acum[l]) : 1.f;
-        if ((which & 1) == 0)
-          sw[j * LM + l] = on_path ? w * r : 0.f;
-        else
-          cw[j * LM + l] = (on_path && l < n + j) ? w * r : 0.f;
-      }
-    }
   }
   __syncthreads();
 
-  // 5. per draft, in order, one column per thread: u (forward substitution for the
+  // 3. decay-weighted scores; a tree draft sees the buffer and its own path only
+  for (int idx = tid; idx < T * LM; idx += NT) {
+    const int j = idx / LM, l = idx - j * LM;
+    float wq = 0.f, wk = 0.f;
+    if (l <= n + j) {
+      const bool on_path = !TREE || l < n || ((anc[j] >> (l - n)) & 1ull);
+      if (on_path) {
+        const float w = GATED ? expf(Acum[n + j] - Acum[l]) : 1.f;
+        wq = w * P.scale * Sc[j * LP + l];
+        if (DELTA && l < n + j) wk = w * Sc[(T + j) * LP + l];
+      }
+    }
+    sw[idx] = wq;
+    if (DELTA) cw[idx] = wk;
+  }
+  __syncthreads();
+
+  // 4. per draft, in order, one column per thread: u (forward substitution for the
   //    delta rule) and o
   const int c = tid;
   for (int j = 0; j < T; ++j) {
     const int tpos = n + j;
     const float e_j = GATED ? expf(Acum[tpos]) : 1.f;
-    float po = e_j * Y[j * DV + c];
+    float po = e_j * P.scale * Y[j * DV + c];
     float pc = DELTA ? e_j * Y[(T + j) * DV + c] : 0.f;
     for (int l = 0; l < tpos; ++l) {
-      const float u = us[l * DV + c];
+      const float u = to_float(us[l * DV + c]);
       po = fmaf(sw[j * LM + l], u, po);
       if (DELTA) pc = fmaf(cw[j * LM + l], u, pc);
     }
-    const float vt = vs[j * DV + c];
-    const float ut = DELTA ? bt[j] * (vt - pc) : vt;
+    float ut;
+    if constexpr (DELTA) {
+      ut = bt[j] * (to_float(vs[j * DV + c]) - pc);
+      us[tpos * DV + c] = ut;  // read later only by this thread
+    } else {
+      ut = to_float(us[tpos * DV + c]);
+    }
     po = fmaf(sw[j * LM + tpos], ut, po);
     __stcs(io.o + ((b * T + j) * P.Hv + h) * DV + c, po);
-    us[tpos * DV + c] = ut;  // read later only by this thread
   }
   __syncthreads();
 
-  // 6. drafts into the buffer: values and u's, keys (one value head per q/k head),
+  // 5. drafts into the buffer: values and u's, keys (one value head per q/k head),
   //    cumulative gates, betas
-  for (int idx = tid; idx < T * (DV / 4); idx += NT) {
-    const int j = idx / (DV / 4), cc4 = (idx % (DV / 4)) * 4;
-    const size_t dst = voff[n + j] * DV + cc4;
-    st4(static_cast<KT *>(P.vbuf) + dst, *reinterpret_cast<const float4 *>(&vs[j * DV + cc4]));
-    if (DELTA) st4(P.ubuf + dst, *reinterpret_cast<const float4 *>(&us[(n + j) * DV + cc4]));
+  for (int idx = tid; idx < T * 16; idx += NT) {
+    const int j = idx >> 4, p = idx & 15;
+    const KT *src = DELTA ? vs + j * DV : reinterpret_cast<const KT *>(us) + (size_t)(n + j) * DV;
+    *reinterpret_cast<uint4 *>(static_cast<KT *>(P.vbuf) + voff[n + j] * DV + p * 8) =
+        *reinterpret_cast<const uint4 *>(src + p * 8);
   }
+  if (DELTA)
+    for (int idx = tid; idx < T * 32; idx += NT) {
+      const int j = idx >> 5, p = idx & 31;
+      *reinterpret_cast<float4 *>(P.ubuf + voff[n + j] * DV + p * 4) =
+          *reinterpret_cast<const float4 *>(reinterpret_cast<const float *>(us) +
+                                            (size_t)(n + j) * DV + p * 4);
+    }
   if (h % group == 0)
-    for (int idx = tid; idx < T * (DK / 4); idx += NT) {
-      const int j = idx / (DK / 4), cc4 = (idx % (DK / 4)) * 4;
-      st4(static_cast<KT *>(P.kbuf) + koff[n + j] + cc4,
-          *reinterpret_cast<const float4 *>(&ks[(n + j) * DK + cc4]));
+    for (int idx = tid; idx < T * 16; idx += NT) {
+      const int j = idx >> 4, p = idx & 15;
+      *reinterpret_cast<uint4 *>(static_cast<KT *>(P.kbuf) + koff[n + j] + p * 8) =
+          *reinterpret_cast<const uint4 *>(Kr + (n + j) * XS + p * 8);
     }
   for (int j = tid; j < T; j += NT) {
     P.gbuf[voff[n + j]] = Acum[n + j];
@@ -573,12 +653,7 @@ __global__ void __launch_bounds__(128, 4)
 }
 
 static size_t verify_mma_smem(int variant, int T, int LM) {
-  const int D = 128;
-  const size_t V = variant == kGatedDelta ? 2 * T : T;
-  const size_t VP = (V + 15) / 16 * 16;
-  const size_t floats = VP * D + (size_t)LM * D + (size_t)LM * D + V * D + (size_t)T * D +
-                        2 * (size_t)T * LM + ((LM + 1) & ~1) + ((T + 1) & ~1);
-  return floats * sizeof(float) + 2 * (size_t)LM * sizeof(size_t);
+  return verify_layout(variant, T, LM).total;
 }
 
 template <int VARIANT, bool TREE>
@@ -649,7 +724,8 @@ static cudaError_t verify_dispatch(const PoolView &P, const RowBatch &rows, cons
   if (dtype == 0) return verify_variant<float, TREE>(P, rows, io, variant, d, tree, stream);
   if (dtype == 1) {
     // tensor-core path for bf16 pools at d = 128 when its shared memory fits
-    if (d == 128 && verify_mma_smem(variant, io.T, io.lmax) <= 227 * 1024 - 1024) {
+    if (d == 128 && io.lmax <= 8 * kVMaxTiles &&
+        verify_mma_smem(variant, io.T, io.lmax) <= 227 * 1024 - 1024) {
       switch (variant) {
         case kPlain: return run_verify_mma<kPlain, TREE>(P, rows, io, tree, stream);
         case kGated: return run_verify_mma<kGated, TREE>(P, rows, io, tree, stream);
