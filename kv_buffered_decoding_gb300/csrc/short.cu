@@ -7,8 +7,9 @@
 //   u_t = beta_t (v_t - sum_{i<t} e^{A_t-A_i} (k_t.k_i) u_i)   gated delta rule
 //   o_t = sum_{i<t} e^{A_t-A_i} (q_t.k_i) u_i + (q_t.k_t) u_t
 // One CTA of four warps per (batch row, value head).  Every buffered token's
-// key, u (or v) and gate reaches shared memory in one cp.async burst, so the row
-// pays one memory round trip instead of one per chunk of tokens; then warp w
+// key, u (or v) and gate, and the current token's q, k, v, gate and beta, reach
+// shared memory in one cp.async burst, so the row pays one memory round trip
+// instead of one per chunk of tokens; then warp w
 // takes tokens w, w+4, w+8, ..., reduces each group's dot products with one
 // butterfly, and accumulates e^{A_t-A_i} s_i u_i for its lane's columns; the
 // four warps' partial sums are added once through shared memory.
@@ -55,15 +56,17 @@ __global__ void __launch_bounds__(128) short_kernel(const PoolView P,
   KT *ks = reinterpret_cast<KT *>(dyn_smem);                     // [nmax][D] keys
   UT *usm = reinterpret_cast<UT *>(ks + (size_t)nmax * D);        // [nmax][D] u / v
   float *As = reinterpret_cast<float *>(usm + (size_t)nmax * D);  // [nmax] gates
-  __shared__ __align__(16) float qs[D];
-  __shared__ __align__(16) float kts[D];
+  __shared__ __align__(16) KT qraw[D];  // the current token's q, k, v (raw)
+  __shared__ __align__(16) KT kraw[D];
+  __shared__ __align__(16) KT vraw[D];
+  __shared__ float gate2[2];  // its log-gate and beta
   __shared__ __align__(16) float part_o[NW][D];
   __shared__ __align__(16) float part_c[NW][D];
   __shared__ size_t koff[kMaxTok], voff[kMaxTok];
   __shared__ float s_t_s;
   __shared__ int bad;
 
-  // 1. where tokens 0..n live (warp 0); q (scaled) and k_t to shared
+  // 1. where tokens 0..n live (warp 0)
   if (warp == 0) {
     int anybad = 0;
     for (int i = lane; i <= n; i += 32) {
@@ -77,22 +80,28 @@ __global__ void __launch_bounds__(128) short_kernel(const PoolView P,
     anybad = __any_sync(kFull, anybad);
     if (lane == 0) bad = anybad;
   }
-  const KT *qg = static_cast<const KT *>(io.q) + (b * P.Hk + hq) * D;
-  const KT *kg = static_cast<const KT *>(io.k) + (b * P.Hk + hq) * D;
-  for (int i = tid; i < D; i += NT) {
-    qs[i] = P.scale * to_float(qg[i]);
-    kts[i] = to_float(kg[i]);
+  if (tid == 32) {
+    if (!(GATED && io.log_g)) gate2[0] = 0.f;
+    if (!DELTA) gate2[1] = 0.f;
   }
-  float a_t = 0.f, beta_t = 0.f;
-  if (GATED && io.log_g) a_t = io.log_g[b * P.Hv + h];
-  if (DELTA) beta_t = io.beta[b * P.Hv + h];
   __syncthreads();
   if (bad) return;  // CTA-uniform
 
-  // 2. every buffered token's key, u / v and gate into shared memory in one burst
+  // 2. the current token's q, k, v, gate and beta, and every buffered token's key,
+  //    u / v and gate, into shared memory in one burst
   {
     constexpr int KP = D * (int)sizeof(KT) / 16, UP = D * (int)sizeof(UT) / 16;
     constexpr int KE = 16 / (int)sizeof(KT), UE = 16 / (int)sizeof(UT);
+    const KT *qg = static_cast<const KT *>(io.q) + (b * P.Hk + hq) * D;
+    const KT *kg = static_cast<const KT *>(io.k) + (b * P.Hk + hq) * D;
+    const KT *vg = static_cast<const KT *>(io.v) + (b * P.Hv + h) * D;
+    for (int c = tid; c < 3 * KP; c += NT) {
+      const int part = c / KP, p = c - part * KP;
+      scp16((part == 0 ? qraw : part == 1 ? kraw : vraw) + p * KE,
+            (part == 0 ? qg : part == 1 ? kg : vg) + p * KE);
+    }
+    if (tid == 0 && GATED && io.log_g) scp4(&gate2[0], io.log_g + b * P.Hv + h);
+    if (tid == 1 && DELTA) scp4(&gate2[1], io.beta + b * P.Hv + h);
     for (int c = tid; c < n * KP; c += NT) {
       const int i = c / KP, p = c - i * KP;
       scp16(ks + (size_t)i * D + p * KE, static_cast<const KT *>(P.kbuf) + koff[i] + p * KE);
@@ -109,10 +118,13 @@ __global__ void __launch_bounds__(128) short_kernel(const PoolView P,
   }
   __syncthreads();
 
+  const float a_t = gate2[0], beta_t = gate2[1];
   const float A_t = (GATED && n > 0 ? As[n - 1] : 0.f) + a_t;
   float qv[E], tv[E];
-  load_smem<E>(qs + lane * E, qv);
-  load_smem<E>(kts + lane * E, tv);
+  load_row<E>(qraw + lane * E, qv);
+#pragma unroll
+  for (int e = 0; e < E; ++e) qv[e] *= P.scale;
+  load_row<E>(kraw + lane * E, tv);
   if (warp == 0) {
     float st = 0.f;
 #pragma unroll
@@ -179,7 +191,6 @@ __global__ void __launch_bounds__(128) short_kernel(const PoolView P,
   __syncthreads();
 
   // 4. one thread per column: the current token's u and the output; append
-  const KT *vg = static_cast<const KT *>(io.v) + (b * P.Hv + h) * D;
   for (int c = tid; c < D; c += NT) {
     float o = 0.f, pcs = 0.f;
 #pragma unroll
@@ -187,17 +198,20 @@ __global__ void __launch_bounds__(128) short_kernel(const PoolView P,
       o += part_o[w][c];
       if (DELTA) pcs += part_c[w][c];
     }
-    const float vt = to_float(vg[c]);
+    const float vt = to_float(vraw[c]);
     float ut = vt;
     if (DELTA) ut = beta_t * (vt - pcs);
     o = fmaf(s_t_s, ut, o);
     io.o[(b * P.Hv + h) * D + c] = o;
-    static_cast<KT *>(P.vbuf)[voff[n] * D + c] = static_cast<KT>(vt);
+    static_cast<KT *>(P.vbuf)[voff[n] * D + c] = vraw[c];
     if (DELTA) P.ubuf[voff[n] * D + c] = ut;
   }
-  if (h % group == 0)
-    for (int c = tid; c < D / 4; c += NT)
-      st4(static_cast<KT *>(P.kbuf) + koff[n] + 4 * c, *reinterpret_cast<const float4 *>(&kts[4 * c]));
+  if (h % group == 0) {
+    constexpr int KP = D * (int)sizeof(KT) / 16, KE = 16 / (int)sizeof(KT);
+    for (int c = tid; c < KP; c += NT)
+      *reinterpret_cast<uint4 *>(static_cast<KT *>(P.kbuf) + koff[n] + c * KE) =
+          *reinterpret_cast<const uint4 *>(kraw + c * KE);
+  }
   if (tid == 0) {
     P.gbuf[voff[n]] = GATED ? A_t : 0.f;  // cumulative
     P.bbuf[voff[n]] = beta_t;

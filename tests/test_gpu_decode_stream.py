@@ -147,3 +147,48 @@ def test_persistent_fold(layer, promote):
     assert np.array_equal(pool.get_lengths(), np.zeros(B))
     assert np.array_equal(pool.get_device_lengths(), np.zeros(B))
     assert pool.get_error() is None
+
+
+def _stack(hist):
+    return {key: np.stack(val) for key, val in hist.items()}
+
+
+@pytest.mark.parametrize("layer,B", [
+    (I.Layer(I.GATED_DELTA, 8, 32, 128, 128, "bf16", qk_dist="l2norm"), 160),
+    (I.Layer(I.GATED, 16, 16, 128, 128, "f32"), 200),
+    (I.Layer(I.PLAIN, 16, 16, 128, 128, "bf16"), 200),
+    (I.Layer(I.GATED_DELTA, 16, 16, 128, 128, "f32", qk_dist="l2norm"), 120),
+], ids=["gated_delta_bf16", "gated_f32", "plain_bf16", "gated_delta_f32"])
+def test_short_ctx_large_batch(layer, B):
+    """Short-context decode of B requests (no state) growing to ragged lengths
+    1..64 in 64-slot buffers (block ids beyond the row descriptor's come from the
+    block table), launches from B rows down to a handful.  Sampled outputs against
+    the oracle's buffer-only decode, all lengths bit for bit."""
+    bs, nb = 8, 8
+    cap = nb * bs
+    rng = np.random.default_rng(740 + layer.variant + B)
+    pool = make_pool(layer, 8, B, nb, bs, num_blocks=B * nb + 8, num_slots=1)
+    blocks = rng.permutation(B * nb + 8)
+    for r in range(B):
+        pool.set_request(r, -1, [int(x) for x in blocks[r * nb:(r + 1) * nb]])
+    lengths = rng.integers(1, cap + 1, size=B)
+    lengths[:2] = [cap, 1]
+    sample = [0, 1, 5, 77, B - 1]
+    hist = {r: {} for r in sample}
+    tol = tol_for(layer)
+    for t in range(cap):
+        rows = np.nonzero(lengths > t)[0]
+        tok = I.draw_tokens(rng, layer, (len(rows),))
+        o = pool.short_ctx(rows, *token_tensors(tok, layer, slice(None))).cpu().numpy()
+        for i, r in enumerate(rows):
+            if r in hist:
+                for key, val in tok.items():
+                    if val is not None:
+                        hist[r].setdefault(key, []).append(val[i])
+                if t in (0, 9, 31, 47, cap - 1) or t == lengths[r] - 1:
+                    o_ref = oracle.short_context(_stack(hist[r]), layer.variant, layer.d_k,
+                                                 layer.d_v)
+                    assert rel_err(o[i], o_ref[-1]) <= tol, (t, r)
+        assert np.array_equal(pool.get_lengths(), np.minimum(lengths, t + 1)), t
+    assert np.array_equal(pool.get_device_lengths(), lengths)
+    assert pool.get_error() is None
