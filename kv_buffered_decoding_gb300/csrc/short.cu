@@ -219,6 +219,226 @@ __global__ void __launch_bounds__(128) short_kernel(const PoolView P,
   }
 }
 
+// ------------------------------------------------------------------ tensor-core scores
+// bf16 pools at d = 128.  Same arithmetic; the score dots of every buffered
+// token and the current one (q.k_i, and k_t.k_i for the delta rule) are one
+// pass of mma.sync.m16n8k16 (bf16 in, fp32 accumulate, exact products): A holds
+// q in row 0 and k_t in row 1 (the other rows zero), B the chunk's keys (tokens
+// 0..n-1 buffered, token n the current one), warp w the key tiles w, w+4, ...
+// The lanes holding a token's dots turn them into its decay-weighted scores
+// (one e^{A_t-A_i} per token instead of one per lane), and the warps then
+// accumulate sum_i ws_i u_i (and sum_i wc_i u_i) over their tokens with FMAs.
+constexpr int kSXS = 128 + 8;  // bf16 key row stride (272 B): fragment loads hit distinct banks
+
+__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a2, uint32_t b0,
+                                               uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(0u), "r"(a2), "r"(0u), "r"(b0), "r"(b1));
+}
+
+template <int VARIANT>
+constexpr size_t short_mma_smem(int nmax) {
+  constexpr size_t usz = VARIANT == kGatedDelta ? sizeof(float) : sizeof(__nv_bfloat16);
+  return (size_t)((nmax + 1 + 7) & ~7) * kSXS * 2 + (size_t)nmax * 128 * usz +
+         (size_t)((nmax + 3) & ~3) * sizeof(float);
+}
+
+template <int VARIANT>
+__global__ void __launch_bounds__(128) short_mma_kernel(const PoolView P,
+                                                         const __grid_constant__ RowBatch rows,
+                                                         const TokenIO io) {
+  using KT = __nv_bfloat16;
+  constexpr int D = 128, NT = 128, NW = 4, E = D / 32, XS = kSXS;
+  constexpr bool DELTA = VARIANT == kGatedDelta, GATED = VARIANT != kPlain;
+  using UT = typename std::conditional<DELTA, float, KT>::type;  // stored u (or v)
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int g = lane >> 2, t = lane & 3;
+  const int h = blockIdx.x;
+  const RowDesc &d = rows.r[blockIdx.y];
+  const size_t b = (size_t)rows.row0 + blockIdx.y;
+  const int group = P.Hv / P.Hk;
+  const int hq = h / group;
+  const int n = d.n;  // buffered tokens; the current token goes to slot n
+  const int nmax = io.lmax;
+
+  extern __shared__ float4 dyn_smem[];
+  KT *Kr = reinterpret_cast<KT *>(dyn_smem);  // [tiles * 8][XS] keys; row n = k_t
+  UT *usm = reinterpret_cast<UT *>(Kr + (size_t)((nmax + 1 + 7) & ~7) * XS);  // [nmax][D]
+  float *As = reinterpret_cast<float *>(usm + (size_t)nmax * D);              // [nmax] gates
+  __shared__ __align__(16) KT qraw[D];  // the current token's q and v (raw)
+  __shared__ __align__(16) KT vraw[D];
+  __shared__ float gate2[2];  // its log-gate and beta
+  __shared__ float ws[kMaxTok], wc[kMaxTok];  // decay-weighted scores per buffered token
+  __shared__ __align__(16) float part_o[NW][D];
+  __shared__ __align__(16) float part_c[NW][D];
+  __shared__ size_t koff[kMaxTok], voff[kMaxTok];
+  __shared__ float s_t_s;
+  __shared__ int bad;
+
+  // 1. where tokens 0..n live (warp 0)
+  if (warp == 0) {
+    int anybad = 0;
+    for (int i = lane; i <= n; i += 32) {
+      const int gr = buffer_row(P, d, i);
+      anybad |= (gr < 0);
+      if (gr >= 0) {
+        koff[i] = kv_row(P, gr, hq, P.Hk) * D;
+        voff[i] = kv_row(P, gr, h, P.Hv);
+      }
+    }
+    anybad = __any_sync(kFull, anybad);
+    if (lane == 0) bad = anybad;
+  }
+  if (tid == 32) {
+    if (!(GATED && io.log_g)) gate2[0] = 0.f;
+    if (!DELTA) gate2[1] = 0.f;
+  }
+  __syncthreads();
+  if (bad) return;  // CTA-uniform
+
+  // 2. the current token's q, k, v, gate and beta, and every buffered token's key,
+  //    u / v and gate, in one burst
+  {
+    const KT *qg = static_cast<const KT *>(io.q) + (b * P.Hk + hq) * D;
+    const KT *kg = static_cast<const KT *>(io.k) + (b * P.Hk + hq) * D;
+    const KT *vg = static_cast<const KT *>(io.v) + (b * P.Hv + h) * D;
+    for (int c = tid; c < 3 * 16; c += NT) {
+      const int part = c >> 4, p = c & 15;
+      KT *dst = part == 0 ? qraw : part == 1 ? Kr + (size_t)n * XS : vraw;
+      scp16(dst + p * 8, (part == 0 ? qg : part == 1 ? kg : vg) + p * 8);
+    }
+    if (tid == 0 && GATED && io.log_g) scp4(&gate2[0], io.log_g + b * P.Hv + h);
+    if (tid == 1 && DELTA) scp4(&gate2[1], io.beta + b * P.Hv + h);
+    for (int c = tid; c < n * 16; c += NT) {
+      const int i = c >> 4, p = c & 15;
+      scp16(Kr + (size_t)i * XS + p * 8, static_cast<const KT *>(P.kbuf) + koff[i] + p * 8);
+    }
+    constexpr int UP = D * (int)sizeof(UT) / 16, UE = 16 / (int)sizeof(UT);
+    const UT *ub = DELTA ? reinterpret_cast<const UT *>(P.ubuf) : static_cast<const UT *>(P.vbuf);
+    for (int c = tid; c < n * UP; c += NT) {
+      const int i = c / UP, p = c - i * UP;
+      scp16(usm + (size_t)i * D + p * UE, ub + voff[i] * D + p * UE);
+    }
+    if (GATED)
+      for (int i = tid; i < n; i += NT) scp4(As + i, P.gbuf + voff[i]);
+    asm volatile("cp.async.commit_group;\n" ::: "memory");
+    asm volatile("cp.async.wait_group 0;\n" ::: "memory");
+  }
+  __syncthreads();
+
+  const float a_t = gate2[0], beta_t = gate2[1];
+  const float A_t = (GATED && n > 0 ? As[n - 1] : 0.f) + a_t;
+
+  // 3. score dots on the tensor cores; each token's weighted scores
+  {
+    const KT *arow = g == 0 ? qraw : Kr + (size_t)n * XS;  // row 0: q; row 1: k_t
+    const bool has_a = g == 0 || (DELTA && g == 1);
+    uint32_t af[8][2];
+#pragma unroll
+    for (int ks = 0; ks < 8; ++ks) {
+      af[ks][0] = has_a ? *reinterpret_cast<const uint32_t *>(arow + 16 * ks + 2 * t) : 0u;
+      af[ks][1] = has_a ? *reinterpret_cast<const uint32_t *>(arow + 16 * ks + 2 * t + 8) : 0u;
+    }
+    const int tiles = (n + 1 + 7) >> 3;
+    for (int tile = warp; tile < tiles; tile += NW) {
+      float acc[4] = {0.f, 0.f, 0.f, 0.f};
+      const KT *kr = Kr + (size_t)(tile * 8 + g) * XS;
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks) {
+        const uint32_t b0 = *reinterpret_cast<const uint32_t *>(kr + 16 * ks + 2 * t);
+        const uint32_t b1 = *reinterpret_cast<const uint32_t *>(kr + 16 * ks + 2 * t + 8);
+        mma_bf16_16816(acc, af[ks][0], af[ks][1], b0, b1);
+      }
+      // row g of D: tokens tile*8 + 2t and + 1 (rows 8..15 are zero)
+      if (g < 2) {
+#pragma unroll
+        for (int x = 0; x < 2; ++x) {
+          const int i = tile * 8 + 2 * t + x;
+          if (i < n) {
+            const float w = GATED ? expf(A_t - As[i]) : 1.f;
+            if (g == 0) ws[i] = P.scale * w * acc[x];
+            else wc[i] = w * acc[x];
+          } else if (i == n && g == 0) {
+            s_t_s = P.scale * acc[x];
+          }
+        }
+      }
+    }
+  }
+  __syncthreads();
+
+  // 4. this warp's buffered tokens (w, w + 4, ...): partial o (and the delta rule's
+  //    correction) for the lane's E columns
+  {
+    float po[E], pc[E];
+#pragma unroll
+    for (int e = 0; e < E; ++e) po[e] = pc[e] = 0.f;
+#pragma unroll 4
+    for (int i = warp; i < n; i += NW) {
+      float u[E];
+      load_row<E>(usm + (size_t)i * D + lane * E, u);
+      const float a = ws[i];
+      const float cc = DELTA ? wc[i] : 0.f;
+#pragma unroll
+      for (int e = 0; e < E; ++e) {
+        po[e] = fmaf(a, u[e], po[e]);
+        if (DELTA) pc[e] = fmaf(cc, u[e], pc[e]);
+      }
+    }
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+      part_o[warp][lane * E + e] = po[e];
+      part_c[warp][lane * E + e] = pc[e];
+    }
+  }
+  __syncthreads();
+
+  // 5. one thread per column: the current token's u and the output; append
+  {
+    const int c = tid;
+    float o = 0.f, pcs = 0.f;
+#pragma unroll
+    for (int w = 0; w < NW; ++w) {
+      o += part_o[w][c];
+      if (DELTA) pcs += part_c[w][c];
+    }
+    const float vt = to_float(vraw[c]);
+    float ut = vt;
+    if (DELTA) ut = beta_t * (vt - pcs);
+    o = fmaf(s_t_s, ut, o);
+    io.o[(b * P.Hv + h) * D + c] = o;
+    static_cast<KT *>(P.vbuf)[voff[n] * D + c] = vraw[c];
+    if (DELTA) P.ubuf[voff[n] * D + c] = ut;
+  }
+  if (h % group == 0)
+    for (int c = tid; c < 16; c += NT)
+      *reinterpret_cast<uint4 *>(static_cast<KT *>(P.kbuf) + koff[n] + c * 8) =
+          *reinterpret_cast<const uint4 *>(Kr + (size_t)n * XS + c * 8);
+  if (tid == 0) {
+    P.gbuf[voff[n]] = GATED ? A_t : 0.f;  // cumulative
+    P.bbuf[voff[n]] = beta_t;
+    if (h == 0) P.dlen[d.req] = n + 1;
+  }
+}
+
+template <int VARIANT>
+static cudaError_t run_short_mma(const PoolView &P, const RowBatch &rows, const TokenIO &io,
+                                 cudaStream_t s) {
+  static bool configured = false;
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(short_mma_kernel<VARIANT>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)short_mma_smem<VARIANT>(KVB_MAX_CAPACITY));
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  dim3 grid(P.Hv, rows.count);
+  short_mma_kernel<VARIANT><<<grid, 128, short_mma_smem<VARIANT>(io.lmax), s>>>(P, rows, io);
+  return cudaGetLastError();
+}
+
 template <typename KT, int VARIANT, int D>
 static cudaError_t run_short(const PoolView &P, const RowBatch &rows, const TokenIO &io,
                              cudaStream_t s) {
@@ -257,6 +477,13 @@ static cudaError_t short_variant(const PoolView &P, const RowBatch &rows, const 
 cudaError_t launch_short(const PoolView &P, const RowBatch &rows, const TokenIO &io, int variant,
                          int dtype, int d, cudaStream_t stream) {
   if (rows.count <= 0) return cudaSuccess;
+  if (dtype == 1 && d == 128) {
+    switch (variant) {
+      case kPlain: return run_short_mma<kPlain>(P, rows, io, stream);
+      case kGated: return run_short_mma<kGated>(P, rows, io, stream);
+      case kGatedDelta: return run_short_mma<kGatedDelta>(P, rows, io, stream);
+    }
+  }
   if (dtype == 0) return short_variant<float>(P, rows, io, variant, d, stream);
   if (dtype == 1) return short_variant<__nv_bfloat16>(P, rows, io, variant, d, stream);
   return kUnsupported;
