@@ -634,8 +634,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int j = 0; j < 32; ++j) Sg[(size_t)(wg * 64 + q * 32 + j) * kD + c] = __uint_as_float(w[j]);
     }
-  } else if (tid == 0) {
-    record_error(P.err, kErrTimeout, d.req, h);
+  } else {
+    if (tid == 0) record_error(P.err, kErrTimeout, d.req, h);
+    // the products that timed out may still be running: one more bounded wait on
+    // their commit (phase already advanced) before TMEM is released
+    mbar_wait(mbar, phase ^ 1);
   }
   asm volatile("cp.async.wait_group 0;\n" ::: "memory");
   fence_before();
