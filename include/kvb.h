@@ -21,8 +21,13 @@
  *
  * Conventions for every call:
  *  - All device memory (state, buffer, metadata, inputs, outputs) is allocated
- *    by the caller and borrowed; the library never allocates device memory.
- *    The library owns only the small host-side pool handle.
+ *    by the caller and borrowed; no call allocates device memory.  The one
+ *    piece of device memory the library holds itself is the fixed
+ *    KVB_STATIC_TEMP_BYTES array of kvb_verify_tempstate_static, a file-scope
+ *    device array that every GPU loading the library keeps until the process
+ *    exits.  The library owns the small host-side pool handle.
+ *  - A process may drive several GPUs (one pool per GPU): every call works on
+ *    the current device, and per-device launch set-up is done once per device.
  *  - Pointers named q, k, v, log_g, beta, o are DEVICE pointers, contiguous,
  *    16-byte aligned.  Pointers named req_ids, block_ids, n_accepted and
  *    host_out are HOST pointers.
@@ -293,7 +298,9 @@ int kvb_accept_tempstate(kvb_pool *pool, int32_t B, int32_t T, const int32_t *re
    may be NULL) applies kvb_accept_tempstate in the same call: request
    req_ids[b] takes the state after its first n_accepted[b] drafts.
    The first call on a device looks up the array's device address; make it
-   before any stream capture.  All calls share the array and it keeps the last
+   before any stream capture.  The address is kept for the process, so a
+   cudaDeviceReset() after that first call is not supported (the array would
+   then be reached through a stale address).  All calls share the array and it keeps the last
    call's contents (every temporary state is written before it is read, so
    nothing needs clearing); calls whose GPU work overlaps, from other streams or
    threads, race on it.  Calls no allocator. */
@@ -313,8 +320,25 @@ int kvb_get_device_lengths(kvb_pool *pool, int32_t *host_out, kvb_stream_t strea
 
 /* Synchronize `stream` and read the device error word.  Returns KVB_OK, or
    KVB_E_DEVICE with detail[0..2] = {kind, request, value} when detail is not
-   NULL, and clears the word.  kind 1 = block id out of range. */
+   NULL, and clears the word.  Kinds:
+     1  block id out of range (value = the id); the row was skipped;
+     2  a bounded wait of the tensor-core prefill gave up (value = head); the
+        CTA released its tensor memory and returned: every output and state of
+        that kvb_prefill launch is invalid;
+     3  as 2, and the wait for the products still in flight gave up too, so the
+        tensor memory was released while they may still have been running:
+        treat the device as unreliable for that stream. */
 int kvb_get_error(kvb_pool *pool, kvb_stream_t stream, int32_t *detail);
+
+/* Testing hook for the device-side failure path (host only, process-wide).
+   The tensor-core prefill (bf16, d = 128) waits for its tensor-core products
+   with bounded polls.  This caps the first such wait of every CTA of later
+   kvb_prefill launches at `polls` polls (0 restores the default bound, about
+   2^20 polls), so a test can make that wait run out without any fault: the CTA
+   records kind 2 in the error word, waits with the full bound for the products
+   still in flight, releases its tensor memory and returns, and the context
+   stays usable.  KVB_E_ARG for polls < 0. */
+int kvb_set_prefill_wait_limit(int32_t polls);
 
 /* Name of a status code (static string). */
 const char *kvb_strerror(int status);
@@ -324,7 +348,7 @@ const char *kvb_strerror(int status);
    the achievable HBM bandwidth in the same run as the decode benchmark. */
 int kvb_copy_probe(const void *src, void *dst, size_t bytes, kvb_stream_t stream);
 
-/* Library version, e.g. "libkvb 0.1 sm_103a". */
+/* Library version, e.g. "libkvb 0.2 sm_103a". */
 const char *kvb_version(void);
 
 #ifdef __cplusplus

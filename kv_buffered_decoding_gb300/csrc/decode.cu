@@ -305,14 +305,8 @@ static cudaError_t run_decode(const PoolView &P, const RowBatch &rows, const Tok
                               cudaStream_t stream) {
   constexpr int NS = (D == 128) ? KVB_DECODE_SPLIT : 1;
   const size_t smem = (size_t)io.lmax * 2 * D * sizeof(float);
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(decode_kernel<KT, VARIANT, D, REC, NS>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         kMaxTok * 2 * D * (int)sizeof(float));
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
+  cudaError_t e = ensure_smem((const void *)decode_kernel<KT, VARIANT, D, REC, NS>, smem);
+  if (e != cudaSuccess) return e;
   dim3 grid(P.Hv * NS, rows.count);
   decode_kernel<KT, VARIANT, D, REC, NS><<<grid, 2 * D / NS, smem, stream>>>(P, rows, io);
   return cudaGetLastError();
@@ -365,10 +359,8 @@ cudaError_t launch_set_lengths(const PoolView &P, const RowBatch &rows, cudaStre
 }
 
 cudaError_t launch_copy_probe(const void *src, void *dst, size_t bytes, cudaStream_t stream) {
-  int dev = 0, sms = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  int sms = 0;
+  cudaError_t e = sm_count(&sms);
   if (e != cudaSuccess) return e;
   const size_t n16 = bytes / 16;
   copy_probe_kernel<<<sms * 4, 256, 0, stream>>>(static_cast<const float4 *>(src),

@@ -506,22 +506,13 @@ __global__ void __launch_bounds__(kStreamThreads, 4)
   }
 }
 
+// Resident CTAs of the kernel on the current device (its persistent grid).
 template <typename KT, int VARIANT>
 int flush_ctas() {
-  static int ctas = -1;
-  if (ctas < 0) {
-    constexpr size_t smem = kTileF4 * sizeof(float4) + 2 * sizeof(FStage<KT>);
-    int dev = 0, sms = 0, per_sm = 0;
-    cudaError_t e = cudaFuncSetAttribute(flush_stream_kernel<KT, VARIANT>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e == cudaSuccess) e = cudaGetDevice(&dev);
-    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    if (e == cudaSuccess)
-      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, flush_stream_kernel<KT, VARIANT>,
-                                                        kStreamThreads, smem);
-    ctas = e == cudaSuccess ? sms * per_sm : 0;
-  }
-  return ctas;
+  constexpr size_t smem = kTileF4 * sizeof(float4) + 2 * sizeof(FStage<KT>);
+  int ctas = 0;
+  return resident_ctas((const void *)flush_stream_kernel<KT, VARIANT>, kStreamThreads, smem,
+                       &ctas) == cudaSuccess ? ctas : 0;
 }
 
 template <typename KT, int VARIANT>
@@ -546,23 +537,13 @@ int fctas_for(int variant) {
   return 0;
 }
 
-// Resident CTAs of the kernel on this device (its persistent grid), once.
+// Resident CTAs of the kernel on the current device (its persistent grid).
 template <typename KT, int VARIANT>
 int stream_ctas() {
-  static int ctas = -1;
-  if (ctas < 0) {
-    constexpr size_t smem = kTileF4 * sizeof(float4) + 2 * sizeof(Stage<KT>);
-    int dev = 0, sms = 0, per_sm = 0;
-    cudaError_t e = cudaFuncSetAttribute(decode_stream_kernel<KT, VARIANT>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e == cudaSuccess) e = cudaGetDevice(&dev);
-    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    if (e == cudaSuccess)
-      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_stream_kernel<KT, VARIANT>,
-                                                        kStreamThreads, smem);
-    ctas = e == cudaSuccess ? sms * per_sm : 0;
-  }
-  return ctas;
+  constexpr size_t smem = kTileF4 * sizeof(float4) + 2 * sizeof(Stage<KT>);
+  int ctas = 0;
+  return resident_ctas((const void *)decode_stream_kernel<KT, VARIANT>, kStreamThreads, smem,
+                       &ctas) == cudaSuccess ? ctas : 0;
 }
 
 template <typename KT, int VARIANT>

@@ -1,0 +1,76 @@
+// Per-device launch set-up shared by every launcher.
+//
+// A kernel's dynamic shared-memory limit (cudaFuncSetAttribute) and its
+// occupancy are properties of one device: a process that drives several GPUs,
+// one pool per GPU, has to configure each of them.  Both helpers act on the
+// current device and cache their answer per (device, kernel) behind one mutex,
+// so launches from several host threads are safe and each device is configured
+// once.
+#include <atomic>
+#include <map>
+#include <mutex>
+#include <utility>
+
+#include <cuda_runtime_api.h>
+
+#include "kvb_internal.h"
+
+namespace kvb {
+namespace {
+
+std::mutex g_mu;
+std::map<std::pair<int, const void *>, size_t> g_smem;  // configured dynamic smem bytes
+std::map<std::pair<std::pair<int, const void *>, std::pair<int, size_t>>, int> g_ctas;
+std::atomic<int> g_prefill_polls{0};
+
+}  // namespace
+
+cudaError_t ensure_smem(const void *kernel, size_t bytes) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lock(g_mu);
+  size_t &have = g_smem[{dev, kernel}];
+  if (bytes <= have) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+  if (e != cudaSuccess) return e;
+  have = bytes;
+  return cudaSuccess;
+}
+
+cudaError_t resident_ctas(const void *kernel, int threads, size_t smem, int *out) {
+  *out = 0;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  {
+    std::lock_guard<std::mutex> lock(g_mu);
+    auto it = g_ctas.find({{dev, kernel}, {threads, smem}});
+    if (it != g_ctas.end()) {
+      *out = it->second;
+      return cudaSuccess;
+    }
+  }
+  if ((e = ensure_smem(kernel, smem)) != cudaSuccess) return e;
+  int sms = 0, per_sm = 0;
+  if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+  if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, smem)) != cudaSuccess)
+    return e;
+  std::lock_guard<std::mutex> lock(g_mu);
+  g_ctas[{{dev, kernel}, {threads, smem}}] = sms * per_sm;
+  *out = sms * per_sm;
+  return cudaSuccess;
+}
+
+cudaError_t sm_count(int *out) {
+  *out = 0;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  return cudaDeviceGetAttribute(out, cudaDevAttrMultiProcessorCount, dev);
+}
+
+int prefill_first_wait_polls() { return g_prefill_polls.load(std::memory_order_relaxed); }
+void set_prefill_first_wait_polls(int polls) { g_prefill_polls.store(polls, std::memory_order_relaxed); }
+
+}  // namespace kvb

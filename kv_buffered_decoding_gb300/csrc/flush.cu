@@ -120,15 +120,9 @@ template <typename KT, int VARIANT, int D>
 static cudaError_t run_flush(const PoolView &P, const RowBatch &rows, int max_len,
                              cudaStream_t stream) {
   constexpr int NS = D == 128 ? 2 : 1;
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(flush_kernel<KT, VARIANT, D, NS>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (kMaxTok - 1) * 2 * D * (int)sizeof(float));
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
   const size_t smem = (size_t)max_len * (D + D / NS) * sizeof(float);
+  cudaError_t e = ensure_smem((const void *)flush_kernel<KT, VARIANT, D, NS>, smem);
+  if (e != cudaSuccess) return e;
   dim3 grid(P.Hv * NS, rows.count);
   flush_kernel<KT, VARIANT, D, NS><<<grid, 2 * D / NS, smem, stream>>>(P, rows);
   return cudaGetLastError();

@@ -788,6 +788,12 @@ int kvb_copy_probe(const void *src, void *dst, size_t bytes, kvb_stream_t stream
   return cuda_status(kvb::launch_copy_probe(src, dst, bytes, reinterpret_cast<cudaStream_t>(stream)));
 }
 
-const char *kvb_version(void) { return "libkvb 0.1 sm_103a"; }
+int kvb_set_prefill_wait_limit(int32_t polls) {
+  if (polls < 0) return KVB_E_ARG;
+  kvb::set_prefill_first_wait_polls(polls);
+  return KVB_OK;
+}
+
+const char *kvb_version(void) { return "libkvb 0.2 sm_103a"; }
 
 }  // extern "C"

@@ -91,7 +91,26 @@ struct TokenIO {
   int lmax;  // most tokens any row of the launch stages in shared memory
 };
 
-enum ErrKind : int32_t { kErrNone = 0, kErrBlockRange = 1, kErrTimeout = 2 };
+// kErrTimeout: a bounded wait on the tensor cores gave up (the launch's outputs
+// and states are invalid); kErrTimeoutDrain: the wait that follows, for the
+// products still in flight before TMEM is released, gave up as well.
+enum ErrKind : int32_t { kErrNone = 0, kErrBlockRange = 1, kErrTimeout = 2, kErrTimeoutDrain = 3 };
+
+// Per-device launch set-up (device_setup.cpp).  A kernel's dynamic
+// shared-memory limit and its occupancy belong to one device, so both helpers
+// act on the current device and cache per (device, kernel); they are safe to
+// call from several host threads.
+// Raise `kernel`'s dynamic shared-memory limit on the current device to >= bytes.
+cudaError_t ensure_smem(const void *kernel, size_t bytes);
+// CTAs of `kernel` (threads, dynamic smem) resident on the whole current device
+// (SM count x CTAs per SM), the grid of a persistent launch; 0 if none fit.
+cudaError_t resident_ctas(const void *kernel, int threads, size_t smem, int *out);
+// SM count of the current device.
+cudaError_t sm_count(int *out);
+// Poll bound of the first completion wait of every tensor-core prefill CTA
+// (0 = the default bound); set by kvb_set_prefill_wait_limit.
+int prefill_first_wait_polls();
+void set_prefill_first_wait_polls(int polls);
 
 // Launchers (kernels.cu).  `dtype` is KVB_F32 / KVB_BF16; `d` is d_k == d_v.
 // Return cudaSuccess or the launch error; kUnsupported for a missing instance.

@@ -479,13 +479,8 @@ template <typename KT, int VARIANT, int D>
 cudaError_t run_prefill(const PoolView &P, const RowBatch &rows, const TokenIO &io,
                         cudaStream_t stream) {
   using Sh = PrefillShape<KT, D>;
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(prefill_kernel<KT, VARIANT, D>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Sh::BYTES);
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
+  cudaError_t e = ensure_smem((const void *)prefill_kernel<KT, VARIANT, D>, Sh::BYTES);
+  if (e != cudaSuccess) return e;
   dim3 grid(P.Hv, rows.count);
   prefill_kernel<KT, VARIANT, D><<<grid, kPrefillThreads, Sh::BYTES, stream>>>(P, rows, io);
   return cudaGetLastError();

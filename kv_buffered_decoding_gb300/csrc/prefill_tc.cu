@@ -84,9 +84,11 @@ __device__ __forceinline__ void mma_ts(uint32_t d, uint32_t a, uint64_t b, uint3
 __device__ __forceinline__ void mma_commit(uint32_t mbar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(mbar));
 }
-// bounded wait on an mbarrier phase; false on timeout (about 50 ms)
-__device__ __forceinline__ bool mbar_wait(uint32_t mbar, uint32_t parity) {
-  for (int it = 0; it < (1 << 20); ++it) {
+// Bounded wait on an mbarrier phase: at most `polls` polls (the default is about
+// 50 ms); false on timeout.
+constexpr int kWaitPolls = 1 << 20;
+__device__ __forceinline__ bool mbar_wait(uint32_t mbar, uint32_t parity, int polls = kWaitPolls) {
+  for (int it = 0; it < polls; ++it) {
     uint32_t done;
     asm volatile("{\n\t.reg .pred p;\n\tmbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
                  "selp.u32 %0, 1, 0, p;\n\t}"
@@ -234,7 +236,8 @@ __device__ __forceinline__ void cp4(uint32_t dst, const void *src, bool valid) {
 
 template <int VARIANT>
 __global__ void __launch_bounds__(kThreads, 1)
-    prefill_tc_kernel(const PoolView P, const __grid_constant__ RowBatch rows, const TokenIO io) {
+    prefill_tc_kernel(const PoolView P, const __grid_constant__ RowBatch rows, const TokenIO io,
+                      int first_polls) {
   using KT = __nv_bfloat16;
   constexpr bool DELTA = VARIANT == kGatedDelta, GATED = VARIANT != kPlain;
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -310,6 +313,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int c = lt;                      // as a state column
   bool ok = true;
   uint32_t phase = 0;
+  // poll bound of the next completion wait: the first one may be capped by the
+  // failure-path test hook (first_polls > 0), every later one has the default
+  int polls = first_polls > 0 ? first_polls : kWaitPolls;
 
   // bf16 hi / lo parts of 16 state rows (16 r0 .. 16 r0 + 15) of column c into the
   // A region (the operand of Y^T = S^T X^T)
@@ -410,7 +416,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       mma_commit(mbar);
     }
-    ok = __syncthreads_and(mbar_wait(mbar, phase)) != 0;  // CTA-uniform
+    ok = __syncthreads_and(mbar_wait(mbar, phase, polls)) != 0;  // CTA-uniform
+    polls = kWaitPolls;
     phase ^= 1;
     fence_after();
     if (!ok) break;
@@ -518,7 +525,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mma_commit(mbar);
       }
-      ok = __syncthreads_and(mbar_wait(mbar, phase)) != 0;  // CTA-uniform
+      ok = __syncthreads_and(mbar_wait(mbar, phase, polls)) != 0;  // CTA-uniform
+      polls = kWaitPolls;
       phase ^= 1;
       fence_after();
       if (!ok) break;
@@ -594,7 +602,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                  sdesc(kt + (k0 / 8) * kLbo, kLbo, kSboKt), idS, 1);
       mma_commit(mbar);
     }
-    ok = __syncthreads_and(mbar_wait(mbar, phase)) != 0;  // CTA-uniform
+    ok = __syncthreads_and(mbar_wait(mbar, phase, polls)) != 0;  // CTA-uniform
+    polls = kWaitPolls;
     phase ^= 1;
     fence_after();
     if (!ok) break;
@@ -637,8 +646,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     if (tid == 0) record_error(P.err, kErrTimeout, d.req, h);
     // the products that timed out may still be running: one more bounded wait on
-    // their commit (phase already advanced) before TMEM is released
-    mbar_wait(mbar, phase ^ 1);
+    // their commit (phase already advanced) before TMEM is released; if that
+    // gives up too, the more severe kind replaces the first one
+    const bool drained = mbar_wait(mbar, phase ^ 1);
+    if (!drained && tid == 0) {
+      atomicExch(&P.err[0], (int32_t)kErrTimeoutDrain);
+      P.err[1] = d.req;
+      P.err[2] = h;
+    }
   }
   asm volatile("cp.async.wait_group 0;\n" ::: "memory");
   fence_before();
@@ -654,13 +669,9 @@ cudaError_t launch_prefill_tc(const PoolView &P, const RowBatch &rows, const Tok
   if (rows.count <= 0) return cudaSuccess;
   dim3 grid(P.Hv, rows.count);
   auto run = [&](auto kernel) -> cudaError_t {
-    static bool configured[3] = {false, false, false};
-    if (!configured[variant]) {
-      cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-      if (e != cudaSuccess) return e;
-      configured[variant] = true;
-    }
-    kernel<<<grid, kThreads, kSmemBytes, stream>>>(P, rows, io);
+    cudaError_t e = ensure_smem((const void *)kernel, kSmemBytes);
+    if (e != cudaSuccess) return e;
+    kernel<<<grid, kThreads, kSmemBytes, stream>>>(P, rows, io, prefill_first_wait_polls());
     return cudaGetLastError();
   };
   switch (variant) {

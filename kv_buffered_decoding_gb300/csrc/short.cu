@@ -426,14 +426,9 @@ __global__ void __launch_bounds__(128) short_mma_kernel(const PoolView P,
 template <int VARIANT>
 static cudaError_t run_short_mma(const PoolView &P, const RowBatch &rows, const TokenIO &io,
                                  cudaStream_t s) {
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(short_mma_kernel<VARIANT>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)short_mma_smem<VARIANT>(KVB_MAX_CAPACITY));
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
+  cudaError_t e = ensure_smem((const void *)short_mma_kernel<VARIANT>,
+                              short_mma_smem<VARIANT>(io.lmax));
+  if (e != cudaSuccess) return e;
   dim3 grid(P.Hv, rows.count);
   short_mma_kernel<VARIANT><<<grid, 128, short_mma_smem<VARIANT>(io.lmax), s>>>(P, rows, io);
   return cudaGetLastError();
@@ -442,14 +437,9 @@ static cudaError_t run_short_mma(const PoolView &P, const RowBatch &rows, const 
 template <typename KT, int VARIANT, int D>
 static cudaError_t run_short(const PoolView &P, const RowBatch &rows, const TokenIO &io,
                              cudaStream_t s) {
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(short_kernel<KT, VARIANT, D>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)short_smem<KT, VARIANT, D>(KVB_MAX_CAPACITY));
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
+  cudaError_t e = ensure_smem((const void *)short_kernel<KT, VARIANT, D>,
+                              short_smem<KT, VARIANT, D>(io.lmax));
+  if (e != cudaSuccess) return e;
   dim3 grid(P.Hv, rows.count);
   short_kernel<KT, VARIANT, D><<<grid, 128, short_smem<KT, VARIANT, D>(io.lmax), s>>>(P, rows, io);
   return cudaGetLastError();

@@ -660,13 +660,8 @@ template <int VARIANT, bool TREE>
 static cudaError_t run_verify_mma(const PoolView &P, const RowBatch &rows, const TokenIO &io,
                                   const TreeArg<TREE> &tree, cudaStream_t stream) {
   const size_t smem = verify_mma_smem(VARIANT, io.T, io.lmax);
-  static size_t configured = 0;
-  if (smem > configured) {
-    cudaError_t e = cudaFuncSetAttribute(verify_mma_kernel<VARIANT, TREE>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    configured = smem;
-  }
+  cudaError_t e = ensure_smem((const void *)verify_mma_kernel<VARIANT, TREE>, smem);
+  if (e != cudaSuccess) return e;
   dim3 grid(P.Hv, rows.count);
   verify_mma_kernel<VARIANT, TREE><<<grid, 128, smem, stream>>>(P, rows, io, tree);
   return cudaGetLastError();
@@ -684,15 +679,9 @@ template <typename KT, int VARIANT, int D, bool TREE>
 static cudaError_t run_verify(const PoolView &P, const RowBatch &rows, const TokenIO &io,
                               const TreeArg<TREE> &tree, cudaStream_t stream) {
   constexpr int NS = D == 128 ? 2 : 1;
-  static bool configured = false;
-  if (!configured) {
-    const size_t most = verify_smem(D, NS, kMaxTok - 1, kMaxTok - 1);
-    cudaError_t e = cudaFuncSetAttribute(verify_kernel<KT, VARIANT, D, NS, TREE>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)most);
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
   const size_t smem = verify_smem(D, NS, io.T, io.lmax);
+  cudaError_t e = ensure_smem((const void *)verify_kernel<KT, VARIANT, D, NS, TREE>, smem);
+  if (e != cudaSuccess) return e;
   dim3 grid(P.Hv * NS, rows.count);
   verify_kernel<KT, VARIANT, D, NS, TREE><<<grid, 2 * D / NS, smem, stream>>>(P, rows, io, tree);
   return cudaGetLastError();

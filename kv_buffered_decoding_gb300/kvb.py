@@ -36,7 +36,7 @@ EXPORTS = ("kvb_pool_layout", "kvb_alloc_pool", "kvb_free_pool", "kvb_set_reques
            "kvb_accept", "kvb_verify_tree", "kvb_accept_tree", "kvb_verify_tempstate",
            "kvb_accept_tempstate",
            "kvb_verify_tempstate_static", "kvb_get_lengths", "kvb_get_device_lengths", "kvb_get_error",
-           "kvb_strerror", "kvb_copy_probe", "kvb_version")
+           "kvb_strerror", "kvb_set_prefill_wait_limit", "kvb_copy_probe", "kvb_version")
 
 
 class KvbConfig(ctypes.Structure):
@@ -102,6 +102,7 @@ def load_library(path: str = LIB_PATH):
         "kvb_get_device_lengths": (ctypes.c_int, [_P, _I32P, _P]),
         "kvb_get_error": (ctypes.c_int, [_P, _P, _I32P]),
         "kvb_strerror": (ctypes.c_char_p, [ctypes.c_int]),
+        "kvb_set_prefill_wait_limit": (ctypes.c_int, [_I32]),
         "kvb_copy_probe": (ctypes.c_int, [_P, _P, ctypes.c_size_t, _P]),
         "kvb_version": (ctypes.c_char_p, []),
     }
@@ -119,6 +120,11 @@ def kvb_strerror(status: int) -> str:
 
 def kvb_version() -> str:
     return load_library().kvb_version().decode()
+
+
+def set_prefill_wait_limit(polls: int):
+    """Cap the first bounded wait of every tensor-core prefill CTA (0 = default)."""
+    _check(load_library().kvb_set_prefill_wait_limit(int(polls)), "kvb_set_prefill_wait_limit")
 
 
 def _check(status: int, where: str):

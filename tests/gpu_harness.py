@@ -19,12 +19,22 @@ def tol_for(layer):
     return TOL_F32 if layer.kv_dtype == "f32" else TOL_BF16
 
 
-def rel_err(x, ref) -> float:
-    """max_i |x_i - r_i| / max_i |r_i| (normwise, well defined near zeros)."""
+def rel_err(x, ref, tail: int = 2) -> float:
+    """Worst per-tensor error: max_i |x_i - r_i| / max_i |r_i| (normwise, well defined
+    near zeros) over every tensor made of the trailing ``tail`` axes, the worst over
+    the leading axes (steps, requests, drafts).
+
+    With tail = 2 a tensor is one output o_t of one request ([Hv, d_v]) or one value
+    head's state ([d_k, d_v]), so stacked runs are never pooled into one error."""
     x = np.asarray(x, dtype=np.float64)
     r = np.asarray(ref, dtype=np.float64)
     assert x.shape == r.shape, (x.shape, r.shape)
-    return float(np.abs(x - r).max() / max(np.abs(r).max(), 1e-30))
+    if r.ndim <= tail:
+        return float(np.abs(x - r).max() / max(np.abs(r).max(), 1e-30))
+    axes = tuple(range(r.ndim - tail, r.ndim))
+    num = np.abs(x - r).max(axis=axes)
+    den = np.maximum(np.abs(r).max(axis=axes), 1e-30)
+    return float((num / den).max())
 
 
 def kvb_mod():
@@ -33,7 +43,7 @@ def kvb_mod():
 
 
 def make_pool(layer, m, n_req, blocks_per_req, block_size=8, num_blocks=None, num_slots=None,
-              max_blocks=None):
+              max_blocks=None, scale=1.0):
     kvb = kvb_mod()
     variant = layer.variant
     dtype = kvb.KVB_BF16 if layer.kv_dtype == "bf16" else kvb.KVB_F32
@@ -41,7 +51,7 @@ def make_pool(layer, m, n_req, blocks_per_req, block_size=8, num_blocks=None, nu
     num_slots = n_req if num_slots is None else num_slots
     max_blocks = blocks_per_req if max_blocks is None else max_blocks
     cfg = kvb.make_config(variant, dtype, layer.n_qk_heads, layer.n_v_heads, layer.d_k, layer.d_v,
-                          m, block_size, num_blocks, num_slots, n_req, max(max_blocks, 1))
+                          m, block_size, num_blocks, num_slots, n_req, max(max_blocks, 1), scale)
     return kvb.Pool(cfg)
 
 

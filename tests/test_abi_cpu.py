@@ -141,3 +141,10 @@ def test_two_rank_timing_gloo():
     for rank, worst, rate in res:
         assert worst == 25.0
         assert rate == pytest.approx(2 * 256 * 100 / 0.025)
+
+
+def test_prefill_wait_limit_hook(kvb):
+    lib = kvb.load_library()
+    assert lib.kvb_set_prefill_wait_limit(-1) == kvb.KVB_E_ARG
+    assert lib.kvb_set_prefill_wait_limit(5) == kvb.KVB_OK
+    assert lib.kvb_set_prefill_wait_limit(0) == kvb.KVB_OK

@@ -121,3 +121,38 @@ def test_prefill_errors():
     pool.flush([2])
     pool.prefill([2], *args)
     assert pool.get_error() is None
+
+
+def test_prefill_wait_timeout_reports_and_recovers():
+    """The tensor-core prefill waits for its tensor-core products with bounded polls.
+    A test hook caps the first wait of every CTA at one poll, so it runs out while
+    the products are still in flight: each CTA records a timeout (kind 2) in the
+    error word, waits with the full bound for those products, releases its tensor
+    memory and returns; nothing faults.  The same context then runs a normal
+    prefill that matches the recurrence."""
+    kvb = kvb_mod()
+    layer = I.Layer(I.GATED_DELTA, 2, 4, 128, 128, "bf16", qk_dist="l2norm")
+    B, L = 2, 70
+    rng = np.random.default_rng(333)
+    pool = make_pool(layer, 8, B, 1, 8)
+    for r in range(B):
+        pool.set_request(r, r, [r])
+    tok = I.draw_tokens(rng, layer, (B, L))
+    kvb.set_prefill_wait_limit(1)
+    try:
+        pool.prefill(np.arange(B), *token_tensors(tok, layer, slice(None)), from_zero=True)
+        err = pool.get_error()
+    finally:
+        kvb.set_prefill_wait_limit(0)
+    assert err is not None and err[0] == 2, err
+    assert 0 <= err[1] < B and 0 <= err[2] < layer.n_v_heads
+    o = pool.prefill(np.arange(B), *token_tensors(tok, layer, slice(None)), from_zero=True)
+    torch.cuda.synchronize()
+    o = o.cpu().numpy()
+    st = pool.state.cpu().numpy()
+    zero = np.zeros((layer.n_v_heads, layer.d_k, layer.d_v))
+    for r in range(B):
+        o_ref, S_r, _ = oracle.decode_sequence(zero, _prompt(tok, r, L), layer.variant)
+        assert rel_err(o[r], o_ref) <= tol_for(layer), r
+        assert rel_err(st[r], S_r) <= tol_for(layer), r
+    assert pool.get_error() is None

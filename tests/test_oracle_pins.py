@@ -93,6 +93,46 @@ def pin_plain_exact_rational(orc):
             assert S_T[0, i, c] == float(S[i][c])
 
 
+def pin_scale_exact_rational(orc):
+    """The output scale multiplies the output once: o_t = s * S_t^T q_t, exactly.
+
+    Integer inputs and s = 3/8 make every oracle value an exact binary fraction,
+    so the oracle must agree bit for bit with rational arithmetic.  s = 3/8 is
+    not a power of two and not 1, so applying it twice (9/64), not at all, or to
+    the state update instead of the output, all differ from the exact value.
+    """
+    rng = np.random.default_rng(16)
+    T, dk, dv = 6, 3, 2
+    s = Fraction(3, 8)
+    qi = rng.integers(-3, 4, size=(T, 1, dk))
+    ki = rng.integers(-3, 4, size=(T, 1, dk))
+    vi = rng.integers(-3, 4, size=(T, 1, dv))
+    S0i = rng.integers(-3, 4, size=(1, dk, dv))
+    o, S_T, _ = orc.recurrent_scan(S0i.astype(float), qi.astype(float), ki.astype(float),
+                                   vi.astype(float), variant=PLAIN, scale=float(s))
+    S = [[Fraction(int(S0i[0, i, c])) for c in range(dv)] for i in range(dk)]
+    for t in range(T):
+        for i in range(dk):
+            for c in range(dv):
+                S[i][c] += Fraction(int(ki[t, 0, i])) * Fraction(int(vi[t, 0, c]))
+        for c in range(dv):
+            exact = s * sum(S[i][c] * Fraction(int(qi[t, 0, i])) for i in range(dk))
+            assert o[t, 0, c] == float(exact), (t, c)
+    for i in range(dk):
+        for c in range(dv):
+            assert S_T[0, i, c] == float(S[i][c])  # the state carries no scale
+    # the delta rule with the same scale: s times the unscaled outputs, and the
+    # same states (the scale touches only the output)
+    tok = _tokens(rng, 5, 1, 1, 1, 4, 3, GATED_DELTA)
+    S0 = _rand(rng, 1, 1, 4, 3)
+    o1, S1, _ = orc.recurrent_scan(S0, tok["q"], tok["k"], tok["v"], tok["log_g"], tok["beta"],
+                                   variant=GATED_DELTA)
+    o2, S2, _ = orc.recurrent_scan(S0, tok["q"], tok["k"], tok["v"], tok["log_g"], tok["beta"],
+                                   variant=GATED_DELTA, scale=0.375)
+    assert np.array_equal(S1, S2)
+    assert np.abs(o2 - 0.375 * o1).max() <= 1e-15 * max(1.0, np.abs(o1).max())
+
+
 def pin_gated_constant_gate(orc):
     rng = np.random.default_rng(13)
     T, dk, dv = 10, 4, 3
@@ -438,7 +478,8 @@ def pin_buffered_tree_equals_recurrent(orc):
             assert np.abs(head.current_state() - S_acc[0]).max() <= 1e-10
 
 
-PINS = [pin_plain_closed_form, pin_plain_exact_rational, pin_gated_constant_gate,
+PINS = [pin_plain_closed_form, pin_plain_exact_rational, pin_scale_exact_rational,
+        pin_gated_constant_gate,
         pin_gated_product_of_gates, pin_gated_unit_gate_is_plain, pin_delta_beta_zero_decay,
         pin_delta_overwrite, pin_delta_gradient_step, pin_delta_ut_chunk_form,
         pin_buffered_equals_recurrent, pin_verify_accept, pin_short_context, pin_gqa_mapping,
@@ -504,6 +545,20 @@ def _mut_output_not_transposed(S, q, k, v, log_g, beta, variant, scale=1.0):
     return S_new, scale * np.einsum("...ij,...j->...i", S_new, qq)
 
 
+def _mut_scale_twice(S, q, k, v, log_g, beta, variant, scale=1.0):
+    S_new, o = _ORIG_STEP(S, q, k, v, log_g, beta, variant, scale)
+    return S_new, scale * o
+
+
+def _mut_scale_dropped(S, q, k, v, log_g, beta, variant, scale=1.0):
+    return _ORIG_STEP(S, q, k, v, log_g, beta, variant, 1.0)
+
+
+def _mut_scale_on_key(S, q, k, v, log_g, beta, variant, scale=1.0):
+    S_new, _ = _ORIG_STEP(S, q, scale * np.asarray(k, float), v, log_g, beta, variant, 1.0)
+    return S_new, np.einsum("...ij,...i->...j", S_new, np.asarray(q, float))
+
+
 def _mut_gqa_modulo(x, n_v_heads):
     x = np.asarray(x, float)
     hk = x.shape[-2]
@@ -529,6 +584,9 @@ MUTANTS = {
     "gate_after_write": ("recurrent_step", _mut_gate_after_write),
     "output_not_transposed": ("recurrent_step", _mut_output_not_transposed),
     "gqa_modulo": ("expand_qk", _mut_gqa_modulo),
+    "scale_twice": ("recurrent_step", _mut_scale_twice),
+    "scale_dropped": ("recurrent_step", _mut_scale_dropped),
+    "scale_on_key": ("recurrent_step", _mut_scale_on_key),
     "tree_path_without_node": ("tree_path", _mut_tree_path_without_node),
     "tree_path_leaf_first": ("tree_path", _mut_tree_path_leaf_first),
 }
