@@ -336,6 +336,14 @@ def measure_paths(kvb, torch, dev, peak):
     out = {}
     stream = torch.cuda.current_stream(dev)
 
+    def checked_close(p):
+        """Release a pool after reading its device error word: a timing taken while
+        a kernel reported an error is not a result."""
+        err = p.get_error()
+        p.close()
+        if err is not None:
+            raise RuntimeError(f"device error during the path timings: {err}")
+
     def timed(fn, reps):
         """GPU time per call of `reps` back-to-back calls.  A sleep kernel holds the
         stream while the host enqueues them, so the host's per-call work (argument
@@ -420,7 +428,7 @@ def measure_paths(kvb, torch, dev, peak):
         nbytes = B * (S + T * (q + 2 * e + o) + n0 * e)
         rec(tag, us, nbytes, "verify + accept(0) per round; state %d MiB%s" % (
             B * S >> 20, " (L2-resident)" if B * S < 100 * 2 ** 20 else ""))
-        pool.close()
+        checked_close(pool)
 
     # draft tree: 8 drafts as a binary tree of depth 4 (every request the same shape)
     # against a chain of 8, gated delta layer at B=256; accept(-1 / 0) keeps the buffer
@@ -455,7 +463,7 @@ def measure_paths(kvb, torch, dev, peak):
         "of 128 rows")
     out["verify_tree_gated_delta_B256_T8"]["chain_T8_us"] = us_chain
     del o_t
-    pool.close()
+    checked_close(pool)
 
     # verify latency against the number of drafts: buffered verify vs the recurrent
     # temporary-state baseline (Figure 2), gated delta layer at B=256, plus the memory
@@ -487,8 +495,8 @@ def measure_paths(kvb, torch, dev, peak):
                        "buffered_bytes_per_request": S + (8 - 1 + T) * slot_bytes,
                        "tempstate_bytes_per_request": (1 + T) * S}
         del temp
-        pool.close()
-        base.close()
+        checked_close(pool)
+        checked_close(base)
     out["verify_vs_tempstate_gated_delta_B256"] = cmp
 
     # Figure 3 of the page: decode latency averaged over a full buffer cycle
@@ -506,7 +514,7 @@ def measure_paths(kvb, torch, dev, peak):
             cycle = max(m, 1)
             us = timed(lambda: pool.decode(req, *toks), 8 * cycle)
             sweep[str(m)] = us
-            pool.close()
+            checked_close(pool)
         out["fig3_gated_B%d" % B] = {
             "us_per_step": sweep,
             "normalised_to_m0": {m_: v / sweep["0"] for m_, v in sweep.items()},
@@ -535,7 +543,7 @@ def measure_paths(kvb, torch, dev, peak):
         times.append(a.elapsed_time(b) * 1e3)
     us = statistics.median(times[2:])
     rec("flush_gated_delta_B256_L8", us, B * (2 * S + 8 * e), "one kvb_flush of 8 tokens per request")
-    pool.close()
+    checked_close(pool)
 
     # short context: buffer-only decode, gated layer, B=256 requests holding 32..44 tokens
     L, B = I.GATED_LAYER, 256
@@ -553,7 +561,7 @@ def measure_paths(kvb, torch, dev, peak):
     e = _entry_bytes(L)
     rec("short_ctx_gated_B256_n32to44", us, int(B * (q + 2 * e + o + mean_n * e)),
         "buffer-only decode, no state; buffer reads dominate; each call after an L2 flush")
-    pool.close()
+    checked_close(pool)
 
     # chunked prefill: 1024-token prompts from S = 0, 32 requests, both layers; the bf16
     # products run as tcgen05 MMAs (bf16 hi/lo parts, fp32 accumulation in TMEM),
@@ -579,7 +587,7 @@ def measure_paths(kvb, torch, dev, peak):
                     "note": "chunk 64, tcgen05 bf16 MMAs with hi/lo parts, TMEM accumulators; "
                             "algorithmic flops of the chunked form"}
         del o_buf, prompt
-        pool.close()
+        checked_close(pool)
     return out
 
 

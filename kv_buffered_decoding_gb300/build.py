@@ -21,7 +21,8 @@ INCLUDE = os.path.join(ROOT, "include")
 OUT_DIR = os.path.join(PKG, "_lib")
 LIB = os.path.join(OUT_DIR, "libkvb.so")
 
-CU_SOURCES = ["decode.cu", "decode_stream.cu", "short.cu", "verify.cu", "flush.cu", "baseline.cu", "prefill.cu", "prefill_tc.cu"]
+CU_SOURCES = ["decode.cu", "decode_stream.cu", "short.cu", "verify.cu", "verify_tc.cu", "flush.cu",
+              "baseline.cu", "prefill.cu", "prefill_tc.cu"]
 CPP_SOURCES = ["kvb_host.cpp", "device_setup.cpp"]
 HEADERS = ["kvb_internal.h", "kvb_device.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

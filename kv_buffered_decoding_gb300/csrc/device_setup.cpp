@@ -11,6 +11,8 @@
 #include <mutex>
 #include <utility>
 
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime_api.h>
 
 #include "kvb_internal.h"
@@ -68,6 +70,29 @@ cudaError_t sm_count(int *out) {
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   return cudaDeviceGetAttribute(out, cudaDevAttrMultiProcessorCount, dev);
+}
+
+cudaError_t encode_state_map(StateMap *out, float *state, uint64_t rows) {
+  static_assert(sizeof(StateMap) == sizeof(CUtensorMap) && alignof(StateMap) >= 64, "tensor map");
+  static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  if (!encode || !state || rows == 0 || rows > (1ull << 31)) return cudaErrorNotSupported;
+  const cuuint64_t dims[2] = {128, rows};
+  const cuuint64_t strides[1] = {128 * sizeof(float)};
+  const cuuint32_t box[2] = {32, 128};
+  const cuuint32_t elem[2] = {1, 1};
+  CUresult r = encode(reinterpret_cast<CUtensorMap *>(out), CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, state, dims,
+                      strides, box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B_ATOM_32B,
+                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorNotSupported;
 }
 
 int prefill_first_wait_polls() { return g_prefill_polls.load(std::memory_order_relaxed); }

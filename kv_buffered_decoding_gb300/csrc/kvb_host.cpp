@@ -103,6 +103,10 @@ struct kvb_pool {
   std::vector<int8_t> tree_host;
   std::vector<uint8_t> pending_tree;
   kvb::TreeArg<true> tree_arg;
+  // TMA map of the state region (d = 128 pools with a state pool), for the
+  // tensor-core verify; has_map is false when it could not be encoded
+  kvb::StateMap state_map;
+  bool has_map = false;
 
   int capacity(int r) const { return nblk[r] * cfg.block_size; }
 };
@@ -298,6 +302,10 @@ int kvb_alloc_pool(const kvb_config *cfg, void *state_mem, void *kv_mem, void *m
     delete p;
     return KVB_E_CUDA;
   }
+  if (cfg->d_k == 128 && cfg->kv_dtype == KVB_BF16 && cfg->num_state_slots > 0)
+    p->has_map = kvb::encode_state_map(&p->state_map, v.state,
+                                       (uint64_t)cfg->num_state_slots * cfg->n_v_heads * cfg->d_k) ==
+                 cudaSuccess;
   *out = p;
   return KVB_OK;
 }
@@ -492,7 +500,8 @@ int verify_impl(kvb_pool *p, int32_t B, int32_t T, const int32_t *req_ids,
           p->tree_arg.p[i][j] = static_cast<int8_t>(parents[(size_t)(base + i) * T + j]);
     }
     cudaError_t e = kvb::launch_verify(p->view, p->rows, io, c.variant, c.kv_dtype, c.d_k, lmax,
-                                       stream, parents ? &p->tree_arg : nullptr);
+                                       stream, parents ? &p->tree_arg : nullptr,
+                                       p->has_map ? &p->state_map : nullptr);
     if (e != cudaSuccess) return cuda_status(e);
     for (int32_t i = 0; i < cnt; ++i) {
       const int32_t r = req_ids[base + i];

@@ -82,6 +82,16 @@ struct TreeArg<true> {
   int8_t p[kTreeRows][KVB_MAX_DRAFTS];
 };
 
+// A TMA tensor map (the driver's CUtensorMap: 128 bytes, 64-byte aligned) of a
+// pool's state region viewed as a 2D fp32 array {d_v columns, slots * Hv * d_k
+// rows}, copied in {32 x 128} boxes with the 128-byte swizzle of 32-byte atoms:
+// the layout the tensor cores read as an MN-major tf32 operand.
+struct alignas(64) StateMap {
+  uint64_t opaque[16];
+};
+// Encode the map of `rows` state rows of 128 fp32 at `state` (d = 128 pools).
+cudaError_t encode_state_map(StateMap *out, float *state, uint64_t rows);
+
 // Input / output pointers of a decode or verify launch (device).
 struct TokenIO {
   const void *q, *k, *v;  // kv dtype
@@ -123,9 +133,17 @@ cudaError_t launch_decode(const PoolView &P, const RowBatch &rows, const TokenIO
                           cudaStream_t stream);
 cudaError_t launch_short(const PoolView &P, const RowBatch &rows, const TokenIO &io, int variant,
                          int dtype, int d, cudaStream_t stream);
+// smap: the pool's state map, or nullptr when it has none (the tensor-core
+// verify then falls back to the mma.sync kernel).
 cudaError_t launch_verify(const PoolView &P, const RowBatch &rows, const TokenIO &io, int variant,
                           int dtype, int d, int max_len, cudaStream_t stream,
-                          const TreeArg<true> *tree = nullptr);
+                          const TreeArg<true> *tree = nullptr, const StateMap *smap = nullptr);
+// The tcgen05 / TMA verify (bf16, d = 128): whether a launch of T drafts and
+// chunks of at most lmax tokens fits it, and the launch itself.
+bool verify_tc_fits(int variant, int T, int lmax);
+template <bool TREE>
+cudaError_t launch_verify_tc(const PoolView &P, const RowBatch &rows, const TokenIO &io, int variant,
+                             const TreeArg<TREE> &tree, const StateMap &smap, cudaStream_t stream);
 // Move each row's accepted draft path to the front of its draft slots: row i
 // (RowDesc.n = length before the drafts, RowDesc.flags = path length) copies
 // the entry of draft path.p[i][l] into slot n + l, l in path order.

@@ -709,9 +709,12 @@ static cudaError_t verify_variant(const PoolView &P, const RowBatch &rows, const
 template <bool TREE>
 static cudaError_t verify_dispatch(const PoolView &P, const RowBatch &rows, const TokenIO &io,
                                    int variant, int dtype, int d, const TreeArg<TREE> &tree,
-                                   cudaStream_t stream) {
+                                   const StateMap *smap, cudaStream_t stream) {
   if (dtype == 0) return verify_variant<float, TREE>(P, rows, io, variant, d, tree, stream);
   if (dtype == 1) {
+    // tcgen05 path (state by TMA, mat-vecs on the fifth-generation tensor cores)
+    if (d == 128 && smap && verify_tc_fits(variant, io.T, io.lmax))
+      return launch_verify_tc<TREE>(P, rows, io, variant, tree, *smap, stream);
     // tensor-core path for bf16 pools at d = 128 when its shared memory fits
     if (d == 128 && io.lmax <= 8 * kVMaxTiles &&
         verify_mma_smem(variant, io.T, io.lmax) <= 227 * 1024 - 1024) {
@@ -728,15 +731,15 @@ static cudaError_t verify_dispatch(const PoolView &P, const RowBatch &rows, cons
 
 cudaError_t launch_verify(const PoolView &P, const RowBatch &rows, const TokenIO &io, int variant,
                           int dtype, int d, int max_len, cudaStream_t stream,
-                          const TreeArg<true> *tree) {
+                          const TreeArg<true> *tree, const StateMap *smap) {
   if (rows.count <= 0) return cudaSuccess;
   TokenIO io2 = io;
   io2.lmax = max_len;
   if (tree) {
     if (rows.count > kTreeRows) return kUnsupported;
-    return verify_dispatch<true>(P, rows, io2, variant, dtype, d, *tree, stream);
+    return verify_dispatch<true>(P, rows, io2, variant, dtype, d, *tree, smap, stream);
   }
-  return verify_dispatch<false>(P, rows, io2, variant, dtype, d, TreeArg<false>{}, stream);
+  return verify_dispatch<false>(P, rows, io2, variant, dtype, d, TreeArg<false>{}, smap, stream);
 }
 
 // ------------------------------------------------------------------ tree accept

@@ -19,7 +19,7 @@ import pytest
 import oracle
 from kv_buffered_decoding_gb300 import inputs as I
 from tests import oracle_pool
-from tests.gpu_harness import blocks_needed, dev, make_pool, rel_err, tol_for
+from tests.gpu_harness import blocks_needed, dev, make_pool, rel_err, token_tensors, tol_for
 
 pytestmark = pytest.mark.gpu
 torch = pytest.importorskip("torch")
@@ -172,3 +172,95 @@ def test_verify_gated_delta_d128(T):
     torch.cuda.synchronize()
     assert oracle_pool.rel_err_rows(pool.state.cpu().numpy(), S_hist, 1).max() <= tol
     assert pool.get_error() is None
+
+
+GDN_SMALL = I.Layer(I.GATED_DELTA, 2, 4, 128, 128, "bf16", qk_dist="l2norm")
+
+
+@pytest.mark.parametrize("T", [1, 4, 8, 12])
+def test_verify_tc_shapes(T):
+    """The tensor-core verify (the state tile by TMA, the mat-vecs as one tcgen05
+    product; chunks of at most 16 tokens and 2T <= 16 vectors for the delta rule) and,
+    past those limits (T = 12), the mma.sync kernel: ragged buffers of 0..7 tokens,
+    stateless (short-context) requests verifying against S = 0, and more (row, head)
+    units than the persistent grid holds, so every CTA walks several.  Every draft
+    output and, after accept and a closing flush, every state."""
+    layer = GDN_SMALL
+    B, n_short, m, bs = 100, 10, 8, 8
+    n_long = B - n_short
+    nb = blocks_needed(m - 1 + T, bs)
+    rng = np.random.default_rng(60 + T)
+    pool = make_pool(layer, m, B, nb, bs, num_slots=n_long)
+    S0 = I.draw_state(rng, layer, n_long)
+    pool.state.copy_(torch.from_numpy(S0))
+    perm = rng.permutation(B * nb)
+    for r in range(B):
+        pool.set_request(r, r if r < n_long else -1, perm[r * nb:(r + 1) * nb])
+    occ = np.arange(B) % m
+    wtok = I.draw_tokens(rng, layer, (m - 1, B))
+    for s in range(m - 1):
+        rows = np.nonzero(occ > s)[0]
+        lrows, srows = rows[rows < n_long], rows[rows >= n_long]
+        if len(lrows):
+            pool.decode(lrows, *token_tensors(wtok, layer, (s, lrows)))
+        if len(srows):
+            pool.short_ctx(srows, *token_tensors(wtok, layer, (s, srows)))
+    assert np.array_equal(pool.get_lengths(), occ.astype(np.int32))
+    req = np.arange(B)
+    tok = I.draw_tokens(rng, layer, (B, T))
+    o = pool.verify(req, *token_tensors(tok, layer, slice(None))).cpu().numpy()
+    j = rng.integers(0, T + 1, size=B)
+    pool.accept(req, j)
+    tol = tol_for(layer)
+    zero = np.zeros((layer.n_v_heads, layer.d_k, layer.d_v))
+    S_acc = []
+    for r in range(B):
+        hist = {key: (None if tok[key] is None else
+                      np.concatenate([wtok[key][:occ[r], r], tok[key][r]]))
+                for key in tok}
+        start = S0[r].astype(np.float64) if r < n_long else zero
+        o_ref, _, states = oracle.decode_sequence(start, hist, layer.variant,
+                                                  keep_states=range(occ[r] + T))
+        assert rel_err(o[r], o_ref[occ[r]:]) <= tol, r
+        S_acc.append(states[occ[r] + j[r] - 1] if occ[r] + j[r] > 0 else start)
+    expect = occ + j
+    expect[(expect >= m) & (req < n_long)] = 0
+    assert np.array_equal(pool.get_lengths(), expect.astype(np.int32))
+    pool.flush(req[:n_long])
+    torch.cuda.synchronize()
+    st = pool.state.cpu().numpy()
+    for r in range(n_long):
+        assert rel_err(st[r], S_acc[r]) <= tol, r
+    assert pool.get_error() is None
+
+
+def test_verify_tc_corrupt_table():
+    """Two-slot blocks put the drafts' slots past the row descriptor's first four
+    blocks, so the tensor-core verify reads them from the device block table.  A
+    corrupted entry there is caught by the kernel's own check: the unit records
+    (kind 1, request, value) and writes nothing, and the other request verifies
+    normally."""
+    layer = GDN_SMALL
+    rng = np.random.default_rng(71)
+    pool = make_pool(layer, 16, 2, 8, 2)
+    S0 = I.draw_state(rng, layer, 2)
+    pool.state.copy_(torch.from_numpy(S0))
+    pool.set_request(0, 0, list(range(8)))
+    pool.set_request(1, 1, list(range(8, 16)))
+    pre = I.draw_tokens(rng, layer, (10, 2))
+    for t in range(10):
+        pool.decode([0, 1], *token_tensors(pre, layer, t))
+    torch.cuda.synchronize()
+    # the block table is the first region of the metadata: request 0, block 5 (slots 10, 11)
+    bad = torch.tensor([12345], dtype=torch.int32).view(torch.uint8).cuda()
+    pool._meta_mem[20:24].copy_(bad)
+    tok = I.draw_tokens(rng, layer, (2, 4))
+    o = torch.full((2, 4, layer.n_v_heads, layer.d_v), float("nan"), device="cuda")
+    pool.verify([0, 1], *token_tensors(tok, layer, slice(None)), o=o)
+    o = o.cpu().numpy()
+    assert pool.get_error() == (1, 0, 12345)
+    assert np.all(np.isnan(o[0]))
+    hist = {key: (None if tok[key] is None else np.concatenate([pre[key][:, 1], tok[key][1]]))
+            for key in tok}
+    o_ref, _, _ = oracle.decode_sequence(S0[1], hist, layer.variant)
+    assert rel_err(o[1], o_ref[10:]) <= tol_for(layer)
