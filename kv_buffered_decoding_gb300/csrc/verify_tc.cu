@@ -22,21 +22,30 @@
 // hardware truncates S0 to tf32 (relative error < 2^-10 per element); q and k
 // are bf16 and exact.
 //
-// Each CTA is persistent (one per SM) and walks units u, u + grid, ...  Two
-// producer warps run ahead of the consumers:
-//  * warp 4 streams the state tiles through a ring of up to three 64 KB stages
-//    by TMA, refilling a stage as soon as the tensor cores have read it;
-//  * warp 5 stages each unit's small operands (draft q, k, v; buffered keys,
-//    u / v and gates; draft gates and betas) into one of two stages with
-//    16-byte (rows) and 4-byte (gates) cp.async copies spread over its lanes,
-//    with no register round trip: one bulk copy per row was slower, the
-//    bulk-copy engine taking hundreds of small copies per unit one at a time.
-// Warps 0-3 (thread c owns state column c and TMEM lane c) build X in the
-// canonical K-major layout, issue the product (one elected thread), run the
-// score dots q_j.k_l and k_j.k_l as one mma.sync pass (exact bf16 products),
-// form the decay-weighted scores, read their column of Y^T from TMEM, run the
-// forward substitution over the drafts and write the outputs and the drafts'
-// buffer entries.
+// Each CTA is persistent (one per SM) and walks units u, u + grid, ...; unit k
+// of a CTA belongs to consumer group g = k mod G (G = 2 when shared memory
+// allows).  The roles form a pipeline, every hand-off an mbarrier:
+//  * the TMA warp streams the state tiles through a ring of 64 KB stages,
+//    refilling a stage as soon as the tensor cores have read it;
+//  * one staging warp per group copies each unit's small operands (draft q, k,
+//    v; buffered keys, u / v and gates; draft gates and betas) into one of the
+//    group's small stages: rows by bulk copies (one per lane), gates by 4-byte
+//    cp.async, so no register round trip;
+//  * one builder group (4 warps) per group turns a unit's staged q and k into
+//    X (fp32, canonical K-major layout) in one of two X buffers, then forms the
+//    drafts' cumulative gates and, with one mma.sync pass, the score dots
+//    q_j.k_l, k_j.k_l and their decay weights in one of two weight buffers;
+//  * one MMA warp per group issues the unit's product into one of the group's
+//    two TMEM accumulators once its tile has landed and its X is built;
+//  * the consumer group (4 warps; thread c owns state column c and TMEM lane
+//    c) reads its column of Y^T, runs the forward substitution over the drafts
+//    and writes the outputs and the drafts' buffer entries.
+// With two buffers of X, weights and accumulator per group, the builder and the
+// tensor cores work on unit k + 2G while the consumers finish unit k.  A
+// single warp issuing every product, with the consumers building X between
+// their own phases, kept the tensor cores and the consumers waiting on each
+// other: the product of one tile (16 MMAs) took about as long to issue as the
+// HBM share of a tile.
 //
 // Every wait is bounded: a timeout records the error word (kErrTimeout), stops
 // every role, waits (bounded) for the copies and products still in flight,
@@ -50,17 +59,18 @@
 namespace kvb {
 namespace {
 
-constexpr int kVtCons = 128;               // threads of one consumer group (4 warps)
-constexpr int kVtMaxGroups = 3;            // consumer groups, each on its own unit
-constexpr int kVtStagers = 1;              // staging warps per consumer group (two measured slower)
-constexpr int kVtMaxThreads = kVtMaxGroups * (kVtCons + 32 * kVtStagers) + 64;  // + the TMA, MMA warps
+constexpr int kVtCons = 128;               // threads of one consumer (or builder) group
+constexpr int kVtMaxGroups = 2;            // unit pipelines per CTA
+// per group: consumers, builders, its MMA warp and staging warp; + the TMA warp
+constexpr int kVtGroupThreads = 2 * kVtCons + 64;
+constexpr int kVtMaxThreads = kVtMaxGroups * kVtGroupThreads + 32;
 constexpr int kVtXS = 128 + 8;             // bf16 row stride of staged vectors and keys (272 B)
 constexpr int kVtMaxL = 16;                // chunk tokens (buffered + drafts)
 constexpr int kVtMaxV = 16;                // vectors of the product (its N)
 constexpr int kVtMaxStages = 3;            // state tiles in flight
 constexpr int kVtPolls = 1 << 16;          // try_wait bound of every wait (each up to ~a microsecond)
 constexpr uint32_t kTileBytes = 128 * 128 * 4;
-constexpr uint32_t kTmemCols = 128;  // 32 columns per consumer group
+constexpr uint32_t kTmemCols = 128;  // per group two accumulators of up to 16 columns
 constexpr uint32_t kVtSmemMax = 227 * 1024 - 10 * 1024;  // dynamic bytes (9 KB static aside)
 
 // Byte offsets of one small stage (16-byte aligned parts).
@@ -87,35 +97,38 @@ __host__ __device__ inline VtStage vt_stage(int variant, int T, int LM) {
   s.bytes = s.meta + 32;
   return s;
 }
-// Whole dynamic shared memory: `ns` state tiles (1024-aligned); per consumer
-// group two X buffers (fp32, K-major core matrices, 16 vectors), weights and
-// e^{A_j}; `nst` small stages per group.
+// Whole dynamic shared memory: `ns` state tiles (1024-aligned); per group two
+// X buffers (fp32, K-major core matrices, VP = V rounded up to 8 vectors) and
+// two weight buffers (weighted q.k, weighted k.k, e^{A_j}); `nst` small stages
+// per group.
 struct VtLayout {
-  uint32_t tile, grp, xf, sw, cw, ea, grp_bytes, stage, stage_bytes, total;
+  uint32_t tile, grp, xf, xbuf, sw, cw, ea, wbuf, grp_bytes, stage, stage_bytes, total;
 };
 __host__ __device__ inline VtLayout vt_layout(int variant, int T, int LM, int ns, int groups, int nst) {
   VtLayout l;
+  const uint32_t V = (uint32_t)(variant == kGatedDelta ? 2 * T : T);
+  const uint32_t VP = (V + 7) & ~7u;
   const uint32_t TP = (uint32_t)(T + 3) & ~3u;   // weight row stride (float4 reads)
   l.tile = 0;
   l.grp = (uint32_t)ns * kTileBytes;              // group parts, group g at grp + g * grp_bytes
-  l.xf = 0;                                       // 2 x (16 x 128 fp32), 8 KB each
-  l.sw = 2 * kVtMaxV * 128 * 4;                   // [LM][TP] weighted q.k, token-major
-  l.cw = l.sw + (uint32_t)LM * TP * 4;            // [LM][TP] weighted k.k
-  l.ea = l.cw + (uint32_t)LM * TP * 4;            // 2 x [TP] e^{A_j}
-  l.grp_bytes = (l.ea + 2 * TP * 4 + 127) / 128 * 128;
+  l.xf = 0;                                       // X buffer b at xf + b * xbuf
+  l.xbuf = VP * 128 * 4;
+  l.sw = 2 * l.xbuf;                              // weight buffer b at + b * wbuf:
+  l.cw = l.sw + (uint32_t)LM * TP * 4;            //   [LM][TP] weighted q.k, token-major,
+  l.ea = l.cw + (uint32_t)LM * TP * 4;            //   [LM][TP] weighted k.k, [TP] e^{A_j}
+  l.wbuf = (2 * (uint32_t)LM + 1) * TP * 4;
+  l.grp_bytes = (l.sw + 2 * l.wbuf + 127) / 128 * 128;
   l.stage = l.grp + (uint32_t)groups * l.grp_bytes;  // small stage s at stage + s * stage_bytes
   l.stage_bytes = (vt_stage(variant, T, LM).bytes + 127) / 128 * 128;
   l.total = l.stage + (uint32_t)(nst * groups) * l.stage_bytes;
   return l;
 }
-// The launch shape: consumer groups, state stages and small stages per group.
-// Two groups measured faster than three (three share the SM's issue slots and
-// instruction fetch with the producer warps); then the most small stages (the
-// staging warp of a group runs that many units ahead), then the most state
-// stages that fit (false: none fits).
-constexpr int kVtPreferredGroups = 2;
+// The launch shape: groups, state stages and small stages per group.  Two
+// groups first (one leaves the SM idle between its phases); then the most
+// small stages (with three the staging warp and the builders run a unit ahead
+// of the consumers), then the most state stages that fit (false: none fits).
 __host__ __device__ inline bool vt_shape(int variant, int T, int LM, int &groups, int &ns, int &nst) {
-  for (groups = kVtPreferredGroups; groups >= 1; --groups)
+  for (groups = kVtMaxGroups; groups >= 1; --groups)
     for (nst = 3; nst >= 2; --nst)
       for (ns = kVtMaxStages; ns >= 2; --ns)
         if (vt_layout(variant, T, LM, ns, groups, nst).total <= kVtSmemMax) return true;
@@ -150,6 +163,19 @@ __device__ __forceinline__ bool vt_wait(uint32_t mbar, uint32_t parity) {
   }
   return false;
 }
+// The same wait, given up early once another role has stopped the CTA (*abort
+// set): 1 = the phase completed, 0 = timed out, -1 = stopped.
+__device__ __forceinline__ int vt_wait_ab(uint32_t mbar, uint32_t parity, const int *abort) {
+  for (int it = 0; it < kVtPolls; ++it) {
+    uint32_t done;
+    asm volatile("{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+                 "selp.u32 %0, 1, 0, p;\n\t}"
+                 : "=r"(done) : "r"(mbar), "r"(parity) : "memory");
+    if (done) return 1;
+    if ((it & 15) == 15 && *(const volatile int *)abort) return -1;
+  }
+  return 0;
+}
 __device__ __forceinline__ void vt_arrive(uint32_t mbar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(mbar) : "memory");
 }
@@ -165,9 +191,6 @@ __device__ __forceinline__ void vt_bulk(uint32_t dst, const void *src, uint32_t 
 // thread's earlier cp.async copies (its pending count rises by one until they land)
 __device__ __forceinline__ void vt_cp4(uint32_t dst, const void *src) {
   asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
-}
-__device__ __forceinline__ void vt_cp16(uint32_t dst, const void *src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
 }
 __device__ __forceinline__ void vt_cp_arrive(uint32_t mbar) {
   asm volatile("cp.async.mbarrier.arrive.shared.b64 [%0];" ::"r"(mbar) : "memory");
@@ -225,17 +248,21 @@ __global__ void __launch_bounds__(kVtMaxThreads, 1)
   constexpr int JMAX = DELTA ? 8 : 16;                            // most drafts per unit
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int T = io.T, LM = io.lmax;
-  const int V = DELTA ? 2 * T : T;
+  const int V = DELTA ? 2 * T : T, VP = (V + 7) & ~7;
+  const int TP = (T + 3) & ~3;
   const int group = P.Hv / P.Hk;
   const int NSM = NST * G;  // small stages; unit k uses stage k % NSM
   const VtLayout lay = vt_layout(VARIANT, T, LM, NS, G, NST);
   const VtStage sl = vt_stage(VARIANT, T, LM);
-  // warps: 4 G consumers, then the TMA warp, the MMA warp and kVtStagers G staging warps
-  const int w_tma = 4 * G, w_mma = w_tma + 1, w_stage = w_tma + 2;
+  // warps: 4 G consumers, 4 G builders, the TMA warp, G MMA warps, G staging warps
+  const int w_bld = 4 * G, w_tma = 8 * G, w_mma = w_tma + 1, w_stage = w_mma + G;
 
   extern __shared__ __align__(1024) uint8_t smem[];
-  __shared__ uint64_t bar_full[kVtMaxStages], bar_empty[kVtMaxStages], bar_mma[kVtMaxGroups],
-      bar_xready[kVtMaxGroups], bar_sfull[3 * kVtMaxGroups], bar_sempty[3 * kVtMaxGroups];
+  // per group g and buffer b (index 2 g + b): X built, weights built, product
+  // done, accumulator and X buffer free again, weight buffer free again
+  __shared__ uint64_t bar_full[kVtMaxStages], bar_empty[kVtMaxStages], bar_sfull[3 * kVtMaxGroups],
+      bar_sempty[3 * kVtMaxGroups], bar_xready[2 * kVtMaxGroups], bar_wready[2 * kVtMaxGroups],
+      bar_mmad[2 * kVtMaxGroups], bar_afree[2 * kVtMaxGroups], bar_wfree[2 * kVtMaxGroups];
   __shared__ uint32_t tmem_s;
   __shared__ int s_abort;
   __shared__ unsigned long long anc[kVtMaxGroups][kVtMaxL];  // draft trees: ancestor sets
@@ -244,20 +271,23 @@ __global__ void __launch_bounds__(kVtMaxThreads, 1)
   // barriers (8 bytes apart within each array) and stage memory
   auto bar = [](uint64_t *b, int i) { return su32(b) + 8u * (uint32_t)i; };
   auto stage_base = [&](int s) { return smem + lay.stage + (uint32_t)s * lay.stage_bytes; };
+  auto group_base = [&](int g) { return smem + lay.grp + (uint32_t)g * lay.grp_bytes; };
 
   if (tid == 0) {
-    for (int i = 0; i < kVtMaxStages; ++i) {
-      asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bar(bar_full, i)));
-      asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bar(bar_empty, i)));
-    }
-    for (int i = 0; i < kVtMaxGroups; ++i) {
-      asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bar(bar_mma, i)));
-      asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bar(bar_xready, i)));
-    }
-    for (int i = 0; i < 3 * kVtMaxGroups; ++i) {
-      asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bar(bar_sfull, i)));
-      asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bar(bar_sempty, i)));
-    }
+    // one arrival completes a phase, except where each consumer warp arrives
+    auto init = [&](uint64_t *b, int n, uint32_t count) {
+      for (int i = 0; i < n; ++i)
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar(b, i)), "r"(count));
+    };
+    init(bar_full, kVtMaxStages, 1);
+    init(bar_empty, kVtMaxStages, 1);
+    init(bar_sfull, 3 * kVtMaxGroups, 1);
+    init(bar_sempty, 3 * kVtMaxGroups, kVtCons / 32);
+    init(bar_xready, 2 * kVtMaxGroups, 1);
+    init(bar_wready, 2 * kVtMaxGroups, 1);
+    init(bar_mmad, 2 * kVtMaxGroups, 1);
+    init(bar_afree, 2 * kVtMaxGroups, kVtCons / 32);
+    init(bar_wfree, 2 * kVtMaxGroups, kVtCons / 32);
     s_abort = 0;
     asm volatile("fence.mbarrier_init.release.cluster;");
   }
@@ -271,6 +301,10 @@ __global__ void __launch_bounds__(kVtMaxThreads, 1)
   __syncthreads();
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
   const uint32_t tmem = tmem_s;
+  auto stop = [&](int kind, int req, int value) {
+    record_error(P.err, kind, req, value);
+    s_abort = 1;
+  };
 
   if (warp == w_tma) {
     // ------------------------------------------------------------- state tiles
@@ -280,10 +314,12 @@ __global__ void __launch_bounds__(kVtMaxThreads, 1)
         const int u = blockIdx.x + k * gridDim.x;
         if (u >= units || *(volatile int *)&s_abort) break;
         const int ks = k % NS;
-        if (k >= NS && !vt_wait(bar(bar_empty, ks), ((k / NS) - 1) & 1)) {  // read by unit k - NS
-          record_error(P.err, kErrTimeout, -1, 10);
-          s_abort = 1;
-          break;
+        if (k >= NS) {  // the tile of unit k - NS has been read
+          const int w = vt_wait_ab(bar(bar_empty, ks), ((k / NS) - 1) & 1, &s_abort);
+          if (w <= 0) {
+            if (w == 0) stop(kErrTimeout, -1, 10);
+            break;
+          }
         }
         const int y = fast_div(u, hv_div), h = u - y * P.Hv;
         const int slot = rs[y].slot;
@@ -299,33 +335,26 @@ __global__ void __launch_bounds__(kVtMaxThreads, 1)
         armed |= 1u << ks;
         phases = (phases & ~(1u << ks)) | ((uint32_t)((k / NS) & 1) << ks);
       }
-      // tiles still in flight (only after an abort) land before the CTA exits
-      for (int ks = 0; ks < NS; ++ks)
-        if (armed & (1u << ks)) vt_wait(bar(bar_full, ks), (phases >> ks) & 1u);
+      // tiles still in flight (only after a stop) land before the CTA exits
+      if (*(volatile int *)&s_abort)
+        for (int ks = 0; ks < NS; ++ks)
+          if (armed & (1u << ks)) vt_wait(bar(bar_full, ks), (phases >> ks) & 1u);
     }
   } else if (warp >= w_stage) {
     // ------------------------------------------------------------- small operands
-    // staging warp (gs, ws) stages the units k = gs + G (ws + kVtStagers j) of
-    // consumer group gs into the group's stages
-    const int gs = (warp - w_stage) % G, ws = (warp - w_stage) / G;
+    // staging warp g stages the units k = g + G i of group g
+    const int gs = warp - w_stage;
     uint32_t armed = 0u, phases = 0u;  // lane 0: bit s: stage armed; its phase parity
-    bool aborted = false;
-    for (int k = gs + G * ws;; k += G * kVtStagers) {
+    for (int k = gs;; k += G) {
       const int u = blockIdx.x + k * gridDim.x;
-      const int ab = __shfl_sync(kFull, *(volatile int *)&s_abort, 0);  // warp-uniform
-      aborted = ab != 0;
-      if (u >= units || ab) break;
+      if (u >= units || __shfl_sync(kFull, *(volatile int *)&s_abort, 0)) break;
       const int s = k % NSM;
       uint8_t *st = stage_base(s);
       if (k >= NSM) {  // unit k - NSM has released this stage
-        bool ok = lane == 0 ? vt_wait(bar(bar_sempty, s), ((k / NSM) - 1) & 1) : true;
-        ok = __shfl_sync(kFull, ok, 0);
-        if (!ok) {
-          if (lane == 0) {
-            record_error(P.err, kErrTimeout, -1, 11);
-            s_abort = 1;
-          }
-          aborted = true;
+        int w = lane == 0 ? vt_wait_ab(bar(bar_sempty, s), ((k / NSM) - 1) & 1, &s_abort) : 0;
+        w = __shfl_sync(kFull, w, 0);
+        if (w <= 0) {
+          if (lane == 0 && w == 0) stop(kErrTimeout, -1, 11);
           break;
         }
       }
@@ -414,50 +443,49 @@ __global__ void __launch_bounds__(kVtMaxThreads, 1)
         }
       } else {
         __syncwarp();
-        if (lane == 0) vt_arrive(bar(bar_sfull, s));  // with a bad block id the consumers skip the unit
+        if (lane == 0) vt_arrive(bar(bar_sfull, s));  // with a bad block id the unit is skipped
       }
       if (lane == 0) {
         armed |= 1u << s;
         phases = (phases & ~(1u << s)) | ((uint32_t)((k / NSM) & 1) << s);
       }
     }
-    // after an abort, copies still in flight land before the CTA exits (without
-    // one, the consumers have waited for every stage; and a stage this warp armed
-    // may since have been re-armed by the group's other staging warp, so its
-    // recorded parity would no longer be the latest)
-    if (lane == 0 && aborted)
-      for (int s = 0; s < NSM; ++s)
+    // after a stop, copies still in flight land before the CTA exits (without
+    // one, the consumers have waited for every stage)
+    if (lane == 0 && *(volatile int *)&s_abort)
+      for (int s = gs; s < NSM; s += G)
         if (armed & (1u << s)) vt_wait(bar(bar_sfull, s), (phases >> s) & 1u);
-  } else if (warp == w_mma) {
+  } else if (warp >= w_mma) {
     // ------------------------------------------------------------- products
-    // Y^T = S0^T X for unit k, in order, once its tile has landed and its
-    // consumer group has built X; the commits free the tile's stage and tell
-    // the group.  Group g accumulates into TMEM columns 32 g .. 32 g + 15.
+    // MMA warp g: Y^T = S0^T X for the units k = g + G i of its group, each once
+    // its tile has landed and its X is built, into accumulator i & 1 (TMEM
+    // columns 32 g + 16 (i & 1) ...); the commits free the tile's stage and tell
+    // the consumers
+    const int g = warp - w_mma;
     if (lane == 0) {
-      uint32_t pending = 0u, phases = 0u;  // bit g: a product in flight; its parity
-      for (int k = 0;; ++k) {
+      uint32_t pending = 0u, phases = 0u;  // bit b: a product in flight into accumulator b; its parity
+      const uint32_t id = vt_idesc(128, VP);
+      for (int i = 0;; ++i) {
+        const int k = g + i * G;
         const int u = blockIdx.x + k * gridDim.x;
         if (u >= units || *(volatile int *)&s_abort) break;
-        const int ks = k % NS, g = k % G, i = k / G;
+        const int ks = k % NS, bb = i & 1;
         const int *meta = reinterpret_cast<const int *>(stage_base(k % NSM) + sl.meta);
-        const bool ready = vt_wait(bar(bar_xready, g), i & 1);
-        const bool landed = ready && vt_wait(bar(bar_full, ks), (k / NS) & 1);
-        if (!landed) {
-          record_error(P.err, kErrTimeout, -1, 30);
-          s_abort = 1;
+        int w = vt_wait_ab(bar(bar_xready, 2 * g + bb), (i >> 1) & 1, &s_abort);
+        if (w > 0) w = vt_wait_ab(bar(bar_full, ks), (k / NS) & 1, &s_abort);
+        if (w <= 0) {
+          if (w == 0) stop(kErrTimeout, -1, 30);
           break;
         }
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
         if (meta[4] >= 0 && !meta[3]) {  // a state, and the unit's tokens located
-          const uint32_t id = vt_idesc(128, 16);
           const uint32_t ta = su32(smem + lay.tile) + (uint32_t)ks * kTileBytes;
-          const uint32_t xa = su32(smem + lay.grp + (uint32_t)g * lay.grp_bytes + lay.xf) +
-                              (uint32_t)(i & 1) * (kVtMaxV * 128 * 4);
-          const uint32_t dt = tmem + 32u * (uint32_t)g;
+          const uint32_t xa = su32(group_base(g) + lay.xf) + (uint32_t)bb * lay.xbuf;
+          const uint32_t dt = tmem + 32u * (uint32_t)g + 16u * (uint32_t)bb;
           // K steps of 8 rows: A advances 1024 bytes (8 rows of 128), B 256 (two
           // core matrices); the start-address field counts 16-byte units.  A
           // rolled loop keeps this warp's code small: unrolled, its instruction
-          // fetches competed with the consumers' and issue took twice as long.
+          // fetches competed with the other roles' and issue took twice as long.
           uint64_t adesc = vt_desc(ta, 16384, 512, 1), bdesc = vt_desc(xa, 128, 4096, 0);
 #pragma unroll 1
           for (int kk = 0; kk < 16; ++kk) {
@@ -471,65 +499,50 @@ __global__ void __launch_bounds__(kVtMaxThreads, 1)
         asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
                      ::"r"(bar(bar_empty, ks)) : "memory");
         asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
-                     ::"r"(bar(bar_mma, g)) : "memory");
-        pending |= 1u << g;
-        phases = (phases & ~(1u << g)) | ((uint32_t)(i & 1) << g);
+                     ::"r"(bar(bar_mmad, 2 * g + bb)) : "memory");
+        pending |= 1u << bb;
+        phases = (phases & ~(1u << bb)) | ((uint32_t)((i >> 1) & 1) << bb);
       }
-      // products still in flight (only after an abort) finish before TMEM is released
-      for (int g = 0; g < G; ++g)
-        if (pending & (1u << g)) vt_wait(bar(bar_mma, g), (phases >> g) & 1u);
+      // products still in flight (only after a stop) finish before TMEM is released
+      if (*(volatile int *)&s_abort)
+        for (int bb = 0; bb < 2; ++bb)
+          if (pending & (1u << bb)) vt_wait(bar(bar_mmad, 2 * g + bb), (phases >> bb) & 1u);
     }
-  } else if (warp < 4 * G) {
-    // ------------------------------------------------------------- consumers
-    // Group gi takes units k = gi, gi + G, ...  For each one: the score dots and
-    // decay weights, then (once its product is done) its column of Y^T; then X of
-    // the group's next unit is built into the other X buffer, so that product
-    // runs while this unit's forward substitution, outputs and buffer entries
-    // are written.
-    const int gi = warp >> 2;        // this group
-    const int bid = 1 + gi;          // its named barrier
-    const int c = tid & 127;         // state column, TMEM lane
-    const int qw = warp & 3;         // warp within the group
-    const int g = lane >> 2, t = lane & 3;
-    const uint32_t my_tmem = tmem + 32u * (uint32_t)gi + ((uint32_t)(qw * 32) << 16);
-    const int TP = (T + 3) & ~3;
-    uint8_t *gp = smem + lay.grp + (uint32_t)gi * lay.grp_bytes;
-    float *sw = reinterpret_cast<float *>(gp + lay.sw);
-    float *cw = reinterpret_cast<float *>(gp + lay.cw);
-    unsigned long long *ancg = anc[gi];
-
-    // wait for unit k's operands (uniform over the group); false: stop
-    auto staged_ok = [&](int k) -> bool {
-      const int s = k % NSM;
-      const bool ok = vt_wait(bar(bar_sfull, s), (k / NSM) & 1);
-      if (!cons_and(bid, ok && !*(volatile int *)&s_abort)) {
-        if (c == 0 && !ok) {
-          record_error(P.err, kErrTimeout, -1, 20);
-          s_abort = 1;
-        }
-        return false;
+  } else if (warp >= w_bld) {
+    // ------------------------------------------------------------- builders
+    // Builder group g, for the units k = g + G i of its group: X into X buffer
+    // i & 1 once unit i - 2 has read its product (the MMA warp may then issue
+    // the product); then, once unit i - 2 is finished, the drafts' cumulative
+    // gates, e^{A_j} and the decay-weighted scores into weight buffer i & 1.
+    const int g = (warp - w_bld) >> 2;
+    const int bid = 1 + G + g;     // the group's named barrier
+    const int c = tid & 127;
+    const int qw = warp & 3;       // warp within the group
+    const int gq = lane >> 2, t = lane & 3;
+    uint8_t *gp = group_base(g);
+    unsigned long long *ancg = anc[g];
+    for (int i = 0;; ++i) {
+      const int k = g + i * G;
+      if (blockIdx.x + k * gridDim.x >= units) break;
+      const int bb = i & 1, s = k % NSM;
+      int w = 1;
+      if (i >= 2) w = vt_wait_ab(bar(bar_afree, 2 * g + bb), ((i >> 1) - 1) & 1, &s_abort);
+      if (w > 0) w = vt_wait_ab(bar(bar_sfull, s), (k / NSM) & 1, &s_abort);
+      if (!cons_and(bid, w > 0)) {
+        if (c == 0 && w == 0) stop(kErrTimeout, -1, 40);
+        break;
       }
-      return true;
-    };
-    // X of unit k into X buffer (k / G) & 1, the drafts' cumulative gates and
-    // e^{A_j} (the group's first warp), then hand X to the MMA warp
-    auto prepare = [&](int k) {
-      const uint8_t *st = stage_base(k % NSM);
+      uint8_t *st = stage_base(s);
       const int *meta = reinterpret_cast<const int *>(st + sl.meta);
       const int y = meta[0], n = meta[2], bad = meta[3], L = n + T;
-      const int buf = (k / G) & 1;
       const KT *Xr = reinterpret_cast<const KT *>(st + sl.xr);
       const KT *Kr = reinterpret_cast<const KT *>(st + sl.kr);
-      float *Acum = reinterpret_cast<float *>(stage_base(k % NSM) + sl.acum);
-      const float *lgs = reinterpret_cast<const float *>(st + sl.lg);
-      uint8_t *Xf = gp + lay.xf + buf * (kVtMaxV * 128 * 4);
-      float *eA = reinterpret_cast<float *>(gp + lay.ea) + buf * TP;
       // K-major core matrices (8 vectors x 16 bytes), vector v at
       // (v / 8) * 4096 + (r / 4) * 128 + (v % 8) * 16; consecutive threads take
       // consecutive vectors of a core matrix, so a warp's stores cover 512
       // contiguous bytes
       if (!bad) {
-        const int VP = (V + 7) & ~7;
+        uint8_t *Xf = gp + lay.xf + (uint32_t)bb * lay.xbuf;
         for (int idx = c; idx < VP * 32; idx += kVtCons) {
           const int v = (idx & 7) | ((idx >> 8) << 3), c4 = (idx >> 3) & 31;
           if (v >= V) continue;
@@ -537,7 +550,25 @@ __global__ void __launch_bounds__(kVtMaxThreads, 1)
           *reinterpret_cast<float4 *>(Xf + (v >> 3) * 4096 + c4 * 128 + (v & 7) * 16) = ld4(src + c4 * 4);
         }
       }
-      // cumulative gates along each draft's path for trees
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // X for the tensor cores
+      cons_sync(bid);
+      if (c == 0) vt_arrive(bar(bar_xready, 2 * g + bb));
+
+      // weight buffer bb: free once unit i - 2 is finished
+      w = 1;
+      if (i >= 2) w = vt_wait_ab(bar(bar_wfree, 2 * g + bb), ((i >> 1) - 1) & 1, &s_abort);
+      if (!cons_and(bid, w > 0)) {
+        if (c == 0 && w == 0) stop(kErrTimeout, -1, 41);
+        break;
+      }
+      float *Acum = reinterpret_cast<float *>(st + sl.acum);
+      const float *lgs = reinterpret_cast<const float *>(st + sl.lg);
+      uint8_t *wb = gp + (uint32_t)bb * lay.wbuf;
+      float *sw = reinterpret_cast<float *>(wb + lay.sw);
+      float *cw = reinterpret_cast<float *>(wb + lay.cw);
+      float *eA = reinterpret_cast<float *>(wb + lay.ea);
+      // cumulative gates of the drafts (the group's first warp): along each
+      // draft's path for trees, else a prefix over the chain
       if (qw == 0 && !bad) {
         const float A_prev = GATED && n > 0 ? Acum[n - 1] : 0.f;
         if constexpr (TREE) {
@@ -545,183 +576,190 @@ __global__ void __launch_bounds__(kVtMaxThreads, 1)
           __syncwarp();
           if (lane == 0) tree_walk(tree.p[y], T, GATED ? A_prev : 0.f, GATED ? Acum + n : nullptr, ancg);
           __syncwarp();
-        } else if (GATED) {
-          warp_prefix(T, [&](int j) { return lgs[j]; }, Acum + n, lane);
-          __syncwarp();
-          for (int j = lane; j < T; j += 32) Acum[n + j] += A_prev;
+          for (int j = lane; j < T; j += 32) eA[j] = GATED ? expf(Acum[n + j]) : 1.f;
+        } else {
+          for (int j = lane; j < T; j += 32) {
+            float a = 0.f;
+            for (int i2 = 0; i2 <= j; ++i2) a += lgs[i2];
+            a += A_prev;
+            if (GATED) Acum[n + j] = a;
+            eA[j] = GATED ? expf(a) : 1.f;
+          }
         }
         if (!GATED)
           for (int j = lane; j < L; j += 32) Acum[j] = 0.f;
-        __syncwarp();
-        for (int j = lane; j < T; j += 32) eA[j] = GATED ? expf(Acum[n + j]) : 1.f;
       }
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // X for the tensor cores
-      asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+      cons_sync(bid);  // the gates (and tree paths) for the score warps
+
+      // score dots q_j.k_l, k_j.k_l as one mma.sync pass (warps 0, 1: key tiles
+      // 0, 1); the lanes holding them write the decay-weighted scores,
+      // token-major: sw[l][j] = scale e^{A_{n+j}-A_l} q_j.k_l (l <= n+j),
+      // cw[l][j] = e^{A_{n+j}-A_l} k_{n+j}.k_l (l < n+j); a tree draft sees the
+      // buffer and its own path only
+      const int LP = (L + 7) >> 3;
+      if (!bad && qw < LP) {
+        auto arow = [&](int v) -> const KT * {
+          return v < T ? Xr + v * XS : (v < V ? Kr + (n + v - T) * XS : nullptr);
+        };
+        const KT *a0 = arow(gq), *a1 = arow(gq + 8);
+        const KT *kr = Kr + (qw * 8 + gq) * XS;
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int ks2 = 0; ks2 < 8; ++ks2) {
+          const int o = ks2 * 16 + 2 * t;
+          const uint32_t a[4] = {a0 ? *reinterpret_cast<const uint32_t *>(a0 + o) : 0u,
+                                 a1 ? *reinterpret_cast<const uint32_t *>(a1 + o) : 0u,
+                                 a0 ? *reinterpret_cast<const uint32_t *>(a0 + o + 8) : 0u,
+                                 a1 ? *reinterpret_cast<const uint32_t *>(a1 + o + 8) : 0u};
+          mma_bf16(acc, a, *reinterpret_cast<const uint32_t *>(kr + o),
+                   *reinterpret_cast<const uint32_t *>(kr + o + 8));
+        }
+        // acc[2 hi + x]: vector gq + 8 hi against key l = tile * 8 + 2t + x
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int v = gq + 8 * (e >> 1), l = qw * 8 + 2 * t + (e & 1);
+          if (v >= V || l >= LM) continue;
+          const bool isq = v < T;
+          const int j = isq ? v : v - T;
+          float wgt = 0.f;
+          const bool inside = isq ? l <= n + j : l < n + j;
+          const bool on_path = !TREE || l < n || ((ancg[j] >> (l - n)) & 1ull);
+          if (l < L && inside && on_path) wgt = (GATED ? expf(Acum[n + j] - Acum[l]) : 1.f) * acc[e];
+          if (isq)
+            sw[l * TP + j] = P.scale * wgt;
+          else
+            cw[l * TP + j] = wgt;
+        }
+      }
       cons_sync(bid);
-      if (c == 0) vt_arrive(bar(bar_xready, gi));  // the MMA warp may issue the product
-    };
+      if (c == 0) vt_arrive(bar(bar_wready, 2 * g + bb));
+    }
+  } else {
+    // ------------------------------------------------------------- consumers
+    // Consumer group g, for the units k = g + G i of its group: once the weights
+    // and the product are ready, this column of Y^T from accumulator i & 1 (the
+    // accumulator is then released), the forward substitution over the drafts,
+    // the outputs and the drafts' buffer entries; then the stage and the weight
+    // buffer are released.
+    const int g = warp >> 2;
+    const int bid = 1 + g;     // the group's named barrier
+    const int c = tid & 127;   // state column, TMEM lane
+    const int qw = warp & 3;   // warp within the group
+    const uint32_t my_tmem = tmem + 32u * (uint32_t)g + ((uint32_t)(qw * 32) << 16);
+    uint8_t *gp = group_base(g);
+    for (int i = 0;; ++i) {
+      const int k = g + i * G;
+      if (blockIdx.x + k * gridDim.x >= units) break;
+      const int bb = i & 1, s = k % NSM;
+      int w = vt_wait_ab(bar(bar_wready, 2 * g + bb), (i >> 1) & 1, &s_abort);
+      if (w > 0) w = vt_wait_ab(bar(bar_sfull, s), (k / NSM) & 1, &s_abort);
+      if (w > 0) w = vt_wait_ab(bar(bar_mmad, 2 * g + bb), (i >> 1) & 1, &s_abort);
+      const bool go = cons_and(bid, w > 0);  // uniform over the group
+      asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+      if (!go) {
+        if (c == 0 && w == 0) stop(kErrTimeout, -1, 50);
+        break;
+      }
+      const uint8_t *st = stage_base(s);
+      const int *meta = reinterpret_cast<const int *>(st + sl.meta);
+      const int y = meta[0], h = meta[1], n = meta[2], bad = meta[3], slot = meta[4];
+      const size_t b = (size_t)rows.row0 + y;
+      const bool has_state = slot >= 0 && !bad;
+      const KT *Kr = reinterpret_cast<const KT *>(st + sl.kr);
+      const UT *us = reinterpret_cast<const UT *>(st + sl.us);
+      const float *Acum = reinterpret_cast<const float *>(st + sl.acum);
+      const float *bts = reinterpret_cast<const float *>(st + sl.bt);
+      const size_t *koff = reinterpret_cast<const size_t *>(st + sl.koff);
+      const size_t *voff = reinterpret_cast<const size_t *>(st + sl.voff);
+      const uint8_t *wb = gp + (uint32_t)bb * lay.wbuf;
+      const float *sw = reinterpret_cast<const float *>(wb + lay.sw);
+      const float *cw = reinterpret_cast<const float *>(wb + lay.cw);
+      const float *eA = reinterpret_cast<const float *>(wb + lay.ea);
 
-    int k = gi;
-    if (blockIdx.x + k * gridDim.x < units && staged_ok(k)) {
-      prepare(k);
-      for (;; k += G) {
-        const int s = k % NSM, i = k / G;
-        const uint8_t *st = stage_base(s);
-        const int *meta = reinterpret_cast<const int *>(st + sl.meta);
-        const int y = meta[0], h = meta[1], n = meta[2], bad = meta[3], slot = meta[4], req = meta[5];
-        const size_t b = (size_t)rows.row0 + y;
-        const bool has_state = slot >= 0 && !bad;
-        const int L = n + T;
-        const KT *Xr = reinterpret_cast<const KT *>(st + sl.xr);
-        const KT *Kr = reinterpret_cast<const KT *>(st + sl.kr);
-        const UT *us = reinterpret_cast<const UT *>(st + sl.us);
-        const float *Acum = reinterpret_cast<const float *>(st + sl.acum);
-        const float *bts = reinterpret_cast<const float *>(st + sl.bt);
-        const size_t *koff = reinterpret_cast<const size_t *>(st + sl.koff);
-        const size_t *voff = reinterpret_cast<const size_t *>(st + sl.voff);
-        const float *eA = reinterpret_cast<const float *>(gp + lay.ea) + (i & 1) * TP;
+      float po[JMAX], pc[DELTA ? JMAX : 1];
+      if (has_state) {
+        tmem_ldn<JMAX>(my_tmem + 16u * (uint32_t)bb, po);
+        if constexpr (DELTA) tmem_ldn<JMAX>(my_tmem + 16u * (uint32_t)bb + (uint32_t)T, pc);
+      } else {
+#pragma unroll
+        for (int j = 0; j < JMAX; ++j) {
+          po[j] = 0.f;
+          if constexpr (DELTA) pc[j] = 0.f;
+        }
+      }
+      // this warp is done with accumulator bb (and so with X buffer bb): the
+      // builders and the tensor cores may take unit i + 2
+      asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+      __syncwarp();
+      if (lane == 0) vt_arrive(bar(bar_afree, 2 * g + bb));
 
-        // score dots q_j.k_l, k_j.k_l as one mma.sync pass (the group's warps 0,
-        // 1: key tiles 0, 1); the lanes holding them write the decay-weighted
-        // scores, token-major: sw[l][j] = scale e^{A_{n+j}-A_l} q_j.k_l (l <= n+j),
-        // cw[l][j] = e^{A_{n+j}-A_l} k_{n+j}.k_l (l < n+j); a tree draft sees the
-        // buffer and its own path only
-        const int LP = (L + 7) >> 3;
-        if (!bad && qw < LP) {
-          auto arow = [&](int v) -> const KT * {
-            return v < T ? Xr + v * XS : (v < V ? Kr + (n + v - T) * XS : nullptr);
-          };
-          const KT *a0 = arow(g), *a1 = arow(g + 8);
-          const KT *kr = Kr + (qw * 8 + g) * XS;
-          float acc[4] = {0.f, 0.f, 0.f, 0.f};
+      // per draft in order: u (the delta rule's forward substitution) and o,
+      // and the drafts' buffer entries for this column
+      if (!bad) {
 #pragma unroll
-          for (int ks2 = 0; ks2 < 8; ++ks2) {
-            const int o = ks2 * 16 + 2 * t;
-            const uint32_t a[4] = {a0 ? *reinterpret_cast<const uint32_t *>(a0 + o) : 0u,
-                                   a1 ? *reinterpret_cast<const uint32_t *>(a1 + o) : 0u,
-                                   a0 ? *reinterpret_cast<const uint32_t *>(a0 + o + 8) : 0u,
-                                   a1 ? *reinterpret_cast<const uint32_t *>(a1 + o + 8) : 0u};
-            mma_bf16(acc, a, *reinterpret_cast<const uint32_t *>(kr + o),
-                     *reinterpret_cast<const uint32_t *>(kr + o + 8));
-          }
-          // acc[2 hi + x]: vector g + 8 hi against key l = tile * 8 + 2t + x
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int v = g + 8 * (e >> 1), l = qw * 8 + 2 * t + (e & 1);
-            if (v >= V || l >= LM) continue;
-            const bool isq = v < T;
-            const int j = isq ? v : v - T;
-            float w = 0.f;
-            const bool inside = isq ? l <= n + j : l < n + j;
-            const bool on_path = !TREE || l < n || ((ancg[j] >> (l - n)) & 1ull);
-            if (l < L && inside && on_path) w = (GATED ? expf(Acum[n + j] - Acum[l]) : 1.f) * acc[e];
-            if (isq)
-              sw[l * TP + j] = P.scale * w;
-            else
-              cw[l * TP + j] = w;
+        for (int j = 0; j < JMAX; ++j) {
+          if (j < T) {
+            po[j] *= eA[j] * P.scale;
+            if constexpr (DELTA) pc[j] *= eA[j];
           }
         }
-        cons_sync(bid);
-
-        // this column of Y^T once the product is done
-        const bool done = vt_wait(bar(bar_mma, gi), i & 1);
-        const bool go = cons_and(bid, done && !*(volatile int *)&s_abort);  // uniform over the group
-        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-        if (!go) {
-          if (c == 0 && !done) {
-            record_error(P.err, kErrTimeout, req, h);
-            s_abort = 1;
-          }
-          break;
-        }
-        float po[JMAX], pc[DELTA ? JMAX : 1];
-        if (has_state) {
-          tmem_ldn<JMAX>(my_tmem, po);
-          if constexpr (DELTA) tmem_ldn<JMAX>(my_tmem + (uint32_t)T, pc);
-        } else {
+        // the buffered tokens, for all drafts at once
+        for (int l = 0; l < n; ++l) {
+          const float ul = to_float(us[l * D + c]);
 #pragma unroll
-          for (int j = 0; j < JMAX; ++j) {
-            po[j] = 0.f;
-            if constexpr (DELTA) pc[j] = 0.f;
-          }
-        }
-        // the group's next unit: its X, so its product runs during this unit's
-        // substitution (the product reads the other X buffer and overwrites this
-        // group's accumulator only after the reads above)
-        const int k2 = k + G;
-        const bool more = blockIdx.x + k2 * gridDim.x < units;
-        bool next_ok = false;
-        if (more) {
-          asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-          next_ok = staged_ok(k2);
-          if (next_ok) prepare(k2);
-        }
-
-        // per draft in order: u (the delta rule's forward substitution) and o,
-        // and the drafts' buffer entries for this column
-        if (!bad) {
-#pragma unroll
-          for (int j = 0; j < JMAX; ++j) {
-            if (j < T) {
-              po[j] *= eA[j] * P.scale;
-              if constexpr (DELTA) pc[j] *= eA[j];
-            }
-          }
-          // the buffered tokens, for all drafts at once
-          for (int l = 0; l < n; ++l) {
-            const float ul = to_float(us[l * D + c]);
-#pragma unroll
-            for (int j4 = 0; j4 < JMAX; j4 += 4) {
-              if (j4 >= T) break;
-              const float4 wq = *reinterpret_cast<const float4 *>(sw + l * TP + j4);
-              po[j4] = fmaf(wq.x, ul, po[j4]);
-              po[j4 + 1] = fmaf(wq.y, ul, po[j4 + 1]);
-              po[j4 + 2] = fmaf(wq.z, ul, po[j4 + 2]);
-              po[j4 + 3] = fmaf(wq.w, ul, po[j4 + 3]);
-              if constexpr (DELTA) {
-                const float4 wk = *reinterpret_cast<const float4 *>(cw + l * TP + j4);
-                pc[j4] = fmaf(wk.x, ul, pc[j4]);
-                pc[j4 + 1] = fmaf(wk.y, ul, pc[j4 + 1]);
-                pc[j4 + 2] = fmaf(wk.z, ul, pc[j4 + 2]);
-                pc[j4 + 3] = fmaf(wk.w, ul, pc[j4 + 3]);
-              }
-            }
-          }
-          // the drafts in order; each one's u goes into the later drafts' sums
-          const KT *vdr = DELTA ? reinterpret_cast<const KT *>(st + sl.vs)
-                                : reinterpret_cast<const KT *>(us) + (size_t)n * D;
-          const bool keys = h % group == 0;
-#pragma unroll
-          for (int j = 0; j < JMAX; ++j) {
-            if (j >= T) break;
-            const int tp = n + j;
-            const KT vraw = vdr[j * D + c];
-            float ut = to_float(vraw);
-            if constexpr (DELTA) ut = bts[j] * (ut - pc[j]);
-            const float *swr = sw + tp * TP;
-            const float *cwr = cw + tp * TP;
-            __stcs(io.o + ((b * T + j) * P.Hv + h) * D + c, fmaf(swr[j], ut, po[j]));
-#pragma unroll
-            for (int j2 = j + 1; j2 < JMAX; ++j2) {
-              if (j2 < T) {
-                po[j2] = fmaf(swr[j2], ut, po[j2]);
-                if constexpr (DELTA) pc[j2] = fmaf(cwr[j2], ut, pc[j2]);
-              }
-            }
-            const size_t vo = voff[tp];
-            static_cast<KT *>(P.vbuf)[vo * D + c] = vraw;
-            if constexpr (DELTA) P.ubuf[vo * D + c] = ut;
-            if (keys) static_cast<KT *>(P.kbuf)[koff[tp] + c] = Kr[tp * XS + c];
-            if (c == j) {
-              P.gbuf[vo] = Acum[tp];  // cumulative since the last fold
-              P.bbuf[vo] = DELTA ? bts[j] : 0.f;
+          for (int j4 = 0; j4 < JMAX; j4 += 4) {
+            if (j4 >= T) break;
+            const float4 wq = *reinterpret_cast<const float4 *>(sw + l * TP + j4);
+            po[j4] = fmaf(wq.x, ul, po[j4]);
+            po[j4 + 1] = fmaf(wq.y, ul, po[j4 + 1]);
+            po[j4 + 2] = fmaf(wq.z, ul, po[j4 + 2]);
+            po[j4 + 3] = fmaf(wq.w, ul, po[j4 + 3]);
+            if constexpr (DELTA) {
+              const float4 wk = *reinterpret_cast<const float4 *>(cw + l * TP + j4);
+              pc[j4] = fmaf(wk.x, ul, pc[j4]);
+              pc[j4 + 1] = fmaf(wk.y, ul, pc[j4 + 1]);
+              pc[j4 + 2] = fmaf(wk.z, ul, pc[j4 + 2]);
+              pc[j4 + 3] = fmaf(wk.w, ul, pc[j4 + 3]);
             }
           }
         }
-        // (the stage is refilled by cp.async, the generic proxy: no proxy fence)
-        cons_sync(bid);
-        if (c == 0) vt_arrive(bar(bar_sempty, s));  // the staging warp may refill this stage
-        if (!more || !next_ok) break;
+        // the drafts in order; each one's u goes into the later drafts' sums
+        const KT *vdr = DELTA ? reinterpret_cast<const KT *>(st + sl.vs)
+                              : reinterpret_cast<const KT *>(us) + (size_t)n * D;
+        const bool keys = h % group == 0;
+#pragma unroll
+        for (int j = 0; j < JMAX; ++j) {
+          if (j >= T) break;
+          const int tp = n + j;
+          const KT vraw = vdr[j * D + c];
+          float ut = to_float(vraw);
+          if constexpr (DELTA) ut = bts[j] * (ut - pc[j]);
+          const float *swr = sw + tp * TP;
+          const float *cwr = cw + tp * TP;
+          __stcs(io.o + ((b * T + j) * P.Hv + h) * D + c, fmaf(swr[j], ut, po[j]));
+#pragma unroll
+          for (int j2 = j + 1; j2 < JMAX; ++j2) {
+            if (j2 < T) {
+              po[j2] = fmaf(swr[j2], ut, po[j2]);
+              if constexpr (DELTA) pc[j2] = fmaf(cwr[j2], ut, pc[j2]);
+            }
+          }
+          const size_t vo = voff[tp];
+          static_cast<KT *>(P.vbuf)[vo * D + c] = vraw;
+          if constexpr (DELTA) P.ubuf[vo * D + c] = ut;
+          if (keys) static_cast<KT *>(P.kbuf)[koff[tp] + c] = Kr[tp * XS + c];
+          if (c == j) {
+            P.gbuf[vo] = Acum[tp];  // cumulative since the last fold
+            P.bbuf[vo] = DELTA ? bts[j] : 0.f;
+          }
+        }
+      }
+      // this warp is done with the stage and weight buffer bb (the stage is
+      // refilled by copies that need no proxy fence after generic reads)
+      __syncwarp();
+      if (lane == 0) {
+        vt_arrive(bar(bar_sempty, s));
+        vt_arrive(bar(bar_wfree, 2 * g + bb));
       }
     }
   }
@@ -738,7 +776,7 @@ cudaError_t run_verify_tc(const PoolView &P, const RowBatch &rows, const TokenIO
   int groups = 0, ns = 0, nst = 0;
   if (!vt_shape(VARIANT, io.T, io.lmax, groups, ns, nst)) return kUnsupported;
   const size_t smem = vt_layout(VARIANT, io.T, io.lmax, ns, groups, nst).total;
-  const int threads = groups * (kVtCons + 32 * kVtStagers) + 64;
+  const int threads = groups * kVtGroupThreads + 32;
   const void *fn = (const void *)verify_tc_kernel<VARIANT, TREE>;
   int cap = 0;
   cudaError_t e = resident_ctas(fn, threads, smem, &cap);
