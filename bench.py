@@ -459,8 +459,8 @@ def measure_paths(kvb, torch, dev, peak):
     e = _entry_bytes(L)
     nbytes = B * (S + T * (q + 2 * e + o) + n0 * e)
     rec("verify_tree_gated_delta_B256_T8", us_tree, nbytes,
-        "binary draft tree of depth 4 (8 drafts) + accept_tree(-1) per round; two launches "
-        "of 128 rows")
+        "binary draft tree of depth 4 (8 drafts) + accept_tree(-1) per round; one launch "
+        "of 256 rows")
     out["verify_tree_gated_delta_B256_T8"]["chain_T8_us"] = us_chain
     del o_t
     checked_close(pool)

@@ -74,7 +74,7 @@ constexpr int kStageTok = 8;
 // of the launch and draft j, p[i][j] is the parent draft (-1: the last
 // accepted token), always < j.  Accept reuses it for the accepted path (the
 // draft index at each path position).  Chain launches pass the empty form.
-constexpr int kTreeRows = 128;  // rows per tree launch
+constexpr int kTreeRows = kMaxRows;  // rows per tree launch (16 KB of parents: within the 32 KB parameter block)
 template <bool TREE>
 struct TreeArg {};
 template <>
