@@ -9,10 +9,13 @@
 // One CTA of four warps per (batch row, value head).  Every buffered token's
 // key, u (or v) and gate, and the current token's q, k, v, gate and beta, reach
 // shared memory in one cp.async burst, so the row pays one memory round trip
-// instead of one per chunk of tokens; then warp w
-// takes tokens w, w+4, w+8, ..., reduces each group's dot products with one
-// butterfly, and accumulates e^{A_t-A_i} s_i u_i for its lane's columns; the
-// four warps' partial sums are added once through shared memory.
+// instead of one per chunk of tokens.  bf16 pools at d = 128 then run the sums
+// on the tensor cores: short_tc_kernel (plain and gated: scores and the output
+// sum both as mma.sync passes) and short_mma_kernel (delta rule: the scores as
+// an mma.sync pass, the sums with FMAs).  short_kernel (fp32 pools, d = 64):
+// warp w takes tokens w, w+4, w+8, ..., reduces each group's dot products with
+// one butterfly, and accumulates e^{A_t-A_i} s_i u_i for its lane's columns;
+// the four warps' partial sums are added once through shared memory.
 #include <type_traits>
 
 #include "kvb_device.cuh"
@@ -423,6 +426,203 @@ __global__ void __launch_bounds__(128) short_mma_kernel(const PoolView P,
   }
 }
 
+// ------------------------------------------------------------------ tensor-core output
+// bf16 pools at d = 128 without the delta rule (u = v): one CTA of four warps
+// per (batch row, value head), both sums on the tensor cores.  The chunk
+// (tokens 0..n-1 buffered, token n the current one) arrives by 16-byte cp.async
+// copies in padded rows; the score dots q.k_i are one mma.sync pass with q in
+// row 0 of A and the keys as B (warp w: key tiles w, w + 4, ...); the output
+// o = sum_{i<=n} w_i v_i, w_i = scale e^{A_t-A_i} q.k_i, is a second pass with
+// the weights in A (w = hi + lo, bf16 parts in rows 0 and 8: about 16
+// significant bits) and V^T as B, read from the row-major value rows by
+// ldmatrix.trans; warp w owns output columns 32w .. 32w + 31, so no partial sums
+// cross warps.  Rows are padded to multiples of 16 tokens (the product's K);
+// the padded value rows are zeroed and their weights are 0.
+struct ShortTcLayout {
+  uint32_t kr, vr, as, ws, koff, voff, qrow, bytes;
+};
+__host__ __device__ inline ShortTcLayout short_tc_layout(int nmax) {
+  const uint32_t LP = (uint32_t)(nmax + 1 + 15) & ~15u;
+  ShortTcLayout l;
+  l.kr = 0;                           // [LP][XS] bf16 keys (row n: k_t)
+  l.vr = l.kr + LP * kSXS * 2;        // [LP][XS] bf16 values (row n: v_t)
+  l.as = l.vr + LP * kSXS * 2;        // [LP] cumulative log-gates
+  l.ws = l.as + LP * 4;               // [LP] weights
+  l.koff = l.ws + LP * 4;             // [LP] key row offsets (elements)
+  l.voff = l.koff + LP * 8;           // [LP] value row indices
+  l.qrow = l.voff + LP * 8;           // q (bf16)
+  l.bytes = l.qrow + 128 * 2;
+  return l;
+}
+
+__device__ __forceinline__ void mma_bf16_full(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                              uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+// bf16 pair {x.x, x.y} (x.x in the low half) and the pair of remainders
+__device__ __forceinline__ void split_bf16x2(float2 x, uint32_t &hi, uint32_t &lo) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(x.x, x.y);
+  const float2 hf = __bfloat1622float2(h);
+  const __nv_bfloat162 l = __floats2bfloat162_rn(x.x - hf.x, x.y - hf.y);
+  hi = *reinterpret_cast<const uint32_t *>(&h);
+  lo = *reinterpret_cast<const uint32_t *>(&l);
+}
+
+template <int VARIANT>
+__global__ void __launch_bounds__(128) short_tc_kernel(const PoolView P,
+                                                        const __grid_constant__ RowBatch rows,
+                                                        const TokenIO io, FastDiv hv_div) {
+  static_assert(VARIANT != kGatedDelta, "the delta rule keeps short_mma_kernel");
+  using KT = __nv_bfloat16;
+  constexpr int D = 128, XS = kSXS, NW = 4;
+  constexpr bool GATED = VARIANT != kPlain;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int g = lane >> 2, t = lane & 3;
+  const int u = blockIdx.x;
+  const int y = fast_div(u, hv_div), h = u - y * P.Hv;
+  const RowDesc &d = rows.r[y];
+  const size_t b = (size_t)rows.row0 + y;
+  const int group = P.Hv / P.Hk, hq = h / group;
+  const int n = d.n, L = n + 1;  // buffered tokens; the current token goes to slot n
+  const ShortTcLayout lay = short_tc_layout(io.lmax);
+  const int LP = (io.lmax + 1 + 15) & ~15;
+
+  extern __shared__ __align__(16) uint8_t sm[];
+  KT *Kr = reinterpret_cast<KT *>(sm + lay.kr);
+  KT *Vr = reinterpret_cast<KT *>(sm + lay.vr);
+  float *As = reinterpret_cast<float *>(sm + lay.as);
+  float *ws = reinterpret_cast<float *>(sm + lay.ws);
+  size_t *koff = reinterpret_cast<size_t *>(sm + lay.koff);
+  size_t *voff = reinterpret_cast<size_t *>(sm + lay.voff);
+  KT *qs = reinterpret_cast<KT *>(sm + lay.qrow);
+
+  // 1. where tokens 0..n live (one thread per token)
+  int bad = 0;
+  if (tid < L) {
+    const int gr = buffer_row(P, d, tid);
+    bad = gr < 0;
+    koff[tid] = gr >= 0 ? kv_row(P, gr, hq, P.Hk) * D : 0;
+    voff[tid] = gr >= 0 ? kv_row(P, gr, h, P.Hv) : 0;
+  }
+  if (__syncthreads_or(bad)) return;  // recorded in the error word; CTA-uniform
+
+  // 2. the chunk in one burst: buffered keys, values and gates; the current
+  //    token's q, k (row n) and v (row n)
+  const KT *kb = static_cast<const KT *>(P.kbuf);
+  const KT *vb = static_cast<const KT *>(P.vbuf);
+  for (int c = tid; c < n * 16; c += 128) {
+    const int i = c >> 4, p = (c & 15) * 8;
+    scp16(Kr + i * XS + p, kb + koff[i] + p);
+    scp16(Vr + i * XS + p, vb + voff[i] * D + p);
+  }
+  if (tid < 48) {
+    const int part = tid >> 4, p = (tid & 15) * 8;
+    if (part == 0) scp16(qs + p, static_cast<const KT *>(io.q) + (b * P.Hk + hq) * D + p);
+    else if (part == 1) scp16(Kr + n * XS + p, static_cast<const KT *>(io.k) + (b * P.Hk + hq) * D + p);
+    else scp16(Vr + n * XS + p, static_cast<const KT *>(io.v) + (b * P.Hv + h) * D + p);
+  }
+  if (GATED && tid >= 64 && tid - 64 < n) scp4(As + tid - 64, P.gbuf + voff[tid - 64]);
+  asm volatile("cp.async.commit_group;\n" ::: "memory");
+  // meanwhile: zero the padded value rows (the output product reads them) and
+  // the padded tokens' weights
+  for (int c = tid; c < (LP - L) * 16; c += 128)
+    *reinterpret_cast<uint4 *>(Vr + (L + (c >> 4)) * XS + (c & 15) * 8) = make_uint4(0u, 0u, 0u, 0u);
+  if (tid >= L && tid < LP) ws[tid] = 0.f;
+  const float a_t = GATED && io.log_g ? io.log_g[b * P.Hv + h] : 0.f;
+  asm volatile("cp.async.wait_group 0;\n" ::: "memory");
+  __syncthreads();
+  const float A_t = (GATED && n > 0 ? As[n - 1] : 0.f) + a_t;
+
+  // 3. score dots q.k_i of tokens 0..n (warp w: key tiles w, w + 4, ...); the
+  //    lanes holding them (row 0 of D) write the weights w_i (token n: A_n = A_t)
+  {
+    uint32_t af[8][2];
+#pragma unroll
+    for (int ks = 0; ks < 8; ++ks) {
+      af[ks][0] = g == 0 ? *reinterpret_cast<const uint32_t *>(qs + 16 * ks + 2 * t) : 0u;
+      af[ks][1] = g == 0 ? *reinterpret_cast<const uint32_t *>(qs + 16 * ks + 2 * t + 8) : 0u;
+    }
+    const int tiles = (L + 7) >> 3;
+    for (int tile = warp; tile < tiles; tile += NW) {
+      float acc[4] = {0.f, 0.f, 0.f, 0.f};
+      const KT *kr = Kr + (tile * 8 + g) * XS;
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks)
+        mma_bf16_16816(acc, af[ks][0], af[ks][1], *reinterpret_cast<const uint32_t *>(kr + 16 * ks + 2 * t),
+                       *reinterpret_cast<const uint32_t *>(kr + 16 * ks + 2 * t + 8));
+      if (g == 0) {
+#pragma unroll
+        for (int x = 0; x < 2; ++x) {
+          const int i = tile * 8 + 2 * t + x;
+          if (i < L) {
+            const float Ai = i < n ? As[i] : A_t;
+            ws[i] = P.scale * (GATED ? expf(A_t - Ai) : 1.f) * acc[x];
+          }
+        }
+      }
+    }
+  }
+  __syncthreads();
+
+  // 4. o = sum_i w_i v_i for this warp's 32 columns: A = weights (hi in row 0,
+  //    lo in row 8), B = V^T by ldmatrix.trans, two column tiles of 8 per load
+  float oc[4][4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) oc[j][0] = oc[j][1] = oc[j][2] = oc[j][3] = 0.f;
+  const uint32_t vbase = static_cast<uint32_t>(__cvta_generic_to_shared(Vr)) +
+                         (uint32_t)((lane & 15) * XS * 2 + (4 * warp + (lane >> 4)) * 16);
+  for (int kk = 0; kk < LP / 16; ++kk) {
+    uint32_t a0 = 0u, a1 = 0u, a2 = 0u, a3 = 0u;
+    if (g == 0) {
+      split_bf16x2(*reinterpret_cast<const float2 *>(ws + 16 * kk + 2 * t), a0, a1);
+      split_bf16x2(*reinterpret_cast<const float2 *>(ws + 16 * kk + 2 * t + 8), a2, a3);
+    }
+    const uint32_t vrow = vbase + (uint32_t)(16 * kk * XS * 2);
+#pragma unroll
+    for (int np = 0; np < 2; ++np) {
+      uint32_t r0, r1, r2, r3;
+      asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+                   : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(vrow + np * 32));
+      mma_bf16_full(oc[2 * np], a0, a1, a2, a3, r0, r1);
+      mma_bf16_full(oc[2 * np + 1], a0, a1, a2, a3, r2, r3);
+    }
+  }
+
+  // 5. the output (row 0 hi + row 8 lo of column tile j: lanes 0..3 hold
+  //    columns 32w + 8j + 2t, + 1) and the current token's buffer entry
+  if (g == 0) {
+    float *orow = io.o + (b * P.Hv + h) * D + 32 * warp + 2 * t;
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      __stcs(reinterpret_cast<float2 *>(orow + 8 * j), make_float2(oc[j][0] + oc[j][2], oc[j][1] + oc[j][3]));
+  }
+  if (tid < 16) {
+    *reinterpret_cast<uint4 *>(static_cast<KT *>(P.vbuf) + voff[n] * D + tid * 8) =
+        *reinterpret_cast<const uint4 *>(Vr + n * XS + tid * 8);
+  } else if (tid < 32 && h % group == 0) {
+    *reinterpret_cast<uint4 *>(static_cast<KT *>(P.kbuf) + koff[n] + (tid - 16) * 8) =
+        *reinterpret_cast<const uint4 *>(Kr + n * XS + (tid - 16) * 8);
+  } else if (tid == 32) {
+    P.gbuf[voff[n]] = GATED ? A_t : 0.f;  // cumulative
+    P.bbuf[voff[n]] = 0.f;
+    if (h == 0) P.dlen[d.req] = n + 1;
+  }
+}
+
+template <int VARIANT>
+static cudaError_t run_short_tc(const PoolView &P, const RowBatch &rows, const TokenIO &io,
+                                cudaStream_t s) {
+  const size_t smem = short_tc_layout(io.lmax).bytes;
+  cudaError_t e = ensure_smem((const void *)short_tc_kernel<VARIANT>, smem);
+  if (e != cudaSuccess) return e;
+  short_tc_kernel<VARIANT><<<rows.count * P.Hv, 128, smem, s>>>(P, rows, io,
+                                                                 make_fastdiv((uint32_t)P.Hv));
+  return cudaGetLastError();
+}
+
 template <int VARIANT>
 static cudaError_t run_short_mma(const PoolView &P, const RowBatch &rows, const TokenIO &io,
                                  cudaStream_t s) {
@@ -469,8 +669,8 @@ cudaError_t launch_short(const PoolView &P, const RowBatch &rows, const TokenIO 
   if (rows.count <= 0) return cudaSuccess;
   if (dtype == 1 && d == 128) {
     switch (variant) {
-      case kPlain: return run_short_mma<kPlain>(P, rows, io, stream);
-      case kGated: return run_short_mma<kGated>(P, rows, io, stream);
+      case kPlain: return run_short_tc<kPlain>(P, rows, io, stream);
+      case kGated: return run_short_tc<kGated>(P, rows, io, stream);
       case kGatedDelta: return run_short_mma<kGatedDelta>(P, rows, io, stream);
     }
   }
