@@ -430,14 +430,16 @@ __global__ void __launch_bounds__(128) short_mma_kernel(const PoolView P,
 // bf16 pools at d = 128 without the delta rule (u = v): one CTA of four warps
 // per (batch row, value head), both sums on the tensor cores.  The chunk
 // (tokens 0..n-1 buffered, token n the current one) arrives by 16-byte cp.async
-// copies in padded rows; the score dots q.k_i are one mma.sync pass with q in
-// row 0 of A and the keys as B (warp w: key tiles w, w + 4, ...); the output
-// o = sum_{i<=n} w_i v_i, w_i = scale e^{A_t-A_i} q.k_i, is a second pass with
-// the weights in A (w = hi + lo, bf16 parts in rows 0 and 8: about 16
-// significant bits) and V^T as B, read from the row-major value rows by
-// ldmatrix.trans; warp w owns output columns 32w .. 32w + 31, so no partial sums
-// cross warps.  Rows are padded to multiples of 16 tokens (the product's K);
-// the padded value rows are zeroed and their weights are 0.
+// copies in padded rows.  The score dots q.k_i are one mma.sync pass with the
+// keys as A (16 tokens per tile, fragments by ldmatrix; warp w: tiles w, w + 4)
+// and q as column 0 of B; the lanes holding a token's dot form its weight
+// w_i = scale e^{A_t-A_i} q.k_i and store it as bf16 hi and lo parts (w = hi +
+// lo to about 16 significant bits).  The output is a second pass,
+// o^T = V^T [w_hi w_lo], with V^T as A read from the row-major value rows by
+// ldmatrix.trans and the two weight columns as B; warp w owns output columns
+// 32w .. 32w + 31, so no partial sums cross warps.  Rows are padded to
+// multiples of 16 tokens (the products' M and K); the padded value rows are
+// zeroed and their weights are 0.
 struct ShortTcLayout {
   uint32_t kr, vr, as, ws, koff, voff, qrow, bytes;
 };
@@ -447,7 +449,7 @@ __host__ __device__ inline ShortTcLayout short_tc_layout(int nmax) {
   l.kr = 0;                           // [LP][XS] bf16 keys (row n: k_t)
   l.vr = l.kr + LP * kSXS * 2;        // [LP][XS] bf16 values (row n: v_t)
   l.as = l.vr + LP * kSXS * 2;        // [LP] cumulative log-gates
-  l.ws = l.as + LP * 4;               // [LP] weights
+  l.ws = l.as + LP * 4;               // [LP] weights, bf16 hi parts then [LP] lo parts
   l.koff = l.ws + LP * 4;             // [LP] key row offsets (elements)
   l.voff = l.koff + LP * 8;           // [LP] value row indices
   l.qrow = l.voff + LP * 8;           // q (bf16)
@@ -462,15 +464,6 @@ __device__ __forceinline__ void mma_bf16_full(float (&d)[4], uint32_t a0, uint32
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
-// bf16 pair {x.x, x.y} (x.x in the low half) and the pair of remainders
-__device__ __forceinline__ void split_bf16x2(float2 x, uint32_t &hi, uint32_t &lo) {
-  const __nv_bfloat162 h = __floats2bfloat162_rn(x.x, x.y);
-  const float2 hf = __bfloat1622float2(h);
-  const __nv_bfloat162 l = __floats2bfloat162_rn(x.x - hf.x, x.y - hf.y);
-  hi = *reinterpret_cast<const uint32_t *>(&h);
-  lo = *reinterpret_cast<const uint32_t *>(&l);
-}
-
 template <int VARIANT>
 __global__ void __launch_bounds__(128) short_tc_kernel(const PoolView P,
                                                         const __grid_constant__ RowBatch rows,
@@ -494,7 +487,8 @@ __global__ void __launch_bounds__(128) short_tc_kernel(const PoolView P,
   KT *Kr = reinterpret_cast<KT *>(sm + lay.kr);
   KT *Vr = reinterpret_cast<KT *>(sm + lay.vr);
   float *As = reinterpret_cast<float *>(sm + lay.as);
-  float *ws = reinterpret_cast<float *>(sm + lay.ws);
+  KT *whi = reinterpret_cast<KT *>(sm + lay.ws);
+  KT *wlo = whi + LP;
   size_t *koff = reinterpret_cast<size_t *>(sm + lay.koff);
   size_t *voff = reinterpret_cast<size_t *>(sm + lay.voff);
   KT *qs = reinterpret_cast<KT *>(sm + lay.qrow);
@@ -530,36 +524,46 @@ __global__ void __launch_bounds__(128) short_tc_kernel(const PoolView P,
   // the padded tokens' weights
   for (int c = tid; c < (LP - L) * 16; c += 128)
     *reinterpret_cast<uint4 *>(Vr + (L + (c >> 4)) * XS + (c & 15) * 8) = make_uint4(0u, 0u, 0u, 0u);
-  if (tid >= L && tid < LP) ws[tid] = 0.f;
+  if (tid >= L && tid < LP) whi[tid] = wlo[tid] = __float2bfloat16_rn(0.f);
   const float a_t = GATED && io.log_g ? io.log_g[b * P.Hv + h] : 0.f;
   asm volatile("cp.async.wait_group 0;\n" ::: "memory");
   __syncthreads();
   const float A_t = (GATED && n > 0 ? As[n - 1] : 0.f) + a_t;
 
-  // 3. score dots q.k_i of tokens 0..n (warp w: key tiles w, w + 4, ...); the
-  //    lanes holding them (row 0 of D) write the weights w_i (token n: A_n = A_t)
+  // 3. score dots q.k_i of tokens 0..n: A = the keys (16 tokens per tile, by
+  //    ldmatrix; warp w: tiles w, w + 4), B = q in column 0.  Lanes t == 0 hold
+  //    tokens 16 mt + g and + 8 and write their weights w_i (token n: A_n = A_t)
+  //    as bf16 hi and lo parts, w = hi + lo to about 16 significant bits
   {
-    uint32_t af[8][2];
+    uint32_t bq[8][2];
 #pragma unroll
     for (int ks = 0; ks < 8; ++ks) {
-      af[ks][0] = g == 0 ? *reinterpret_cast<const uint32_t *>(qs + 16 * ks + 2 * t) : 0u;
-      af[ks][1] = g == 0 ? *reinterpret_cast<const uint32_t *>(qs + 16 * ks + 2 * t + 8) : 0u;
+      bq[ks][0] = g == 0 ? *reinterpret_cast<const uint32_t *>(qs + 16 * ks + 2 * t) : 0u;
+      bq[ks][1] = g == 0 ? *reinterpret_cast<const uint32_t *>(qs + 16 * ks + 2 * t + 8) : 0u;
     }
-    const int tiles = (L + 7) >> 3;
-    for (int tile = warp; tile < tiles; tile += NW) {
+    const int mtiles = (L + 15) >> 4;
+    const uint32_t kaddr = static_cast<uint32_t>(__cvta_generic_to_shared(Kr)) +
+                           (uint32_t)((lane & 15) * XS * 2 + (lane >> 4) * 16);
+    for (int mt = warp; mt < mtiles; mt += NW) {
       float acc[4] = {0.f, 0.f, 0.f, 0.f};
-      const KT *kr = Kr + (tile * 8 + g) * XS;
+      const uint32_t ka = kaddr + (uint32_t)(mt * 16 * XS * 2);
 #pragma unroll
-      for (int ks = 0; ks < 8; ++ks)
-        mma_bf16_16816(acc, af[ks][0], af[ks][1], *reinterpret_cast<const uint32_t *>(kr + 16 * ks + 2 * t),
-                       *reinterpret_cast<const uint32_t *>(kr + 16 * ks + 2 * t + 8));
-      if (g == 0) {
+      for (int ks = 0; ks < 8; ++ks) {
+        uint32_t a0, a1, a2, a3;
+        asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                     : "=r"(a0), "=r"(a1), "=r"(a2), "=r"(a3) : "r"(ka + ks * 32));
+        mma_bf16_full(acc, a0, a1, a2, a3, bq[ks][0], bq[ks][1]);
+      }
+      if (t == 0) {
 #pragma unroll
         for (int x = 0; x < 2; ++x) {
-          const int i = tile * 8 + 2 * t + x;
+          const int i = 16 * mt + g + 8 * x;
           if (i < L) {
             const float Ai = i < n ? As[i] : A_t;
-            ws[i] = P.scale * (GATED ? expf(A_t - Ai) : 1.f) * acc[x];
+            const float w = P.scale * (GATED ? expf(A_t - Ai) : 1.f) * acc[2 * x];
+            const KT hi = __float2bfloat16_rn(w);
+            whi[i] = hi;
+            wlo[i] = __float2bfloat16_rn(w - __bfloat162float(hi));
           }
         }
       }
@@ -567,37 +571,38 @@ __global__ void __launch_bounds__(128) short_tc_kernel(const PoolView P,
   }
   __syncthreads();
 
-  // 4. o = sum_i w_i v_i for this warp's 32 columns: A = weights (hi in row 0,
-  //    lo in row 8), B = V^T by ldmatrix.trans, two column tiles of 8 per load
-  float oc[4][4];
+  // 4. o^T = V^T w for this warp's 32 columns (two tiles of 16): A = V^T by
+  //    ldmatrix.trans from the row-major value rows, B = the weights (column 0:
+  //    hi parts, column 1: lo parts, the others zero)
+  float oc[2][4];
 #pragma unroll
-  for (int j = 0; j < 4; ++j) oc[j][0] = oc[j][1] = oc[j][2] = oc[j][3] = 0.f;
-  const uint32_t vbase = static_cast<uint32_t>(__cvta_generic_to_shared(Vr)) +
-                         (uint32_t)((lane & 15) * XS * 2 + (4 * warp + (lane >> 4)) * 16);
+  for (int mt = 0; mt < 2; ++mt) oc[mt][0] = oc[mt][1] = oc[mt][2] = oc[mt][3] = 0.f;
+  const uint32_t vaddr = static_cast<uint32_t>(__cvta_generic_to_shared(Vr)) +
+                         (uint32_t)((((lane & 7) + ((lane >> 4) << 3)) * XS * 2) +
+                                    (4 * warp + ((lane >> 3) & 1)) * 16);
+  const KT *wsrc = g == 0 ? whi : wlo;
   for (int kk = 0; kk < LP / 16; ++kk) {
-    uint32_t a0 = 0u, a1 = 0u, a2 = 0u, a3 = 0u;
-    if (g == 0) {
-      split_bf16x2(*reinterpret_cast<const float2 *>(ws + 16 * kk + 2 * t), a0, a1);
-      split_bf16x2(*reinterpret_cast<const float2 *>(ws + 16 * kk + 2 * t + 8), a2, a3);
-    }
-    const uint32_t vrow = vbase + (uint32_t)(16 * kk * XS * 2);
+    const uint32_t b0 = g < 2 ? *reinterpret_cast<const uint32_t *>(wsrc + 16 * kk + 2 * t) : 0u;
+    const uint32_t b1 = g < 2 ? *reinterpret_cast<const uint32_t *>(wsrc + 16 * kk + 2 * t + 8) : 0u;
+    const uint32_t va = vaddr + (uint32_t)(16 * kk * XS * 2);
 #pragma unroll
-    for (int np = 0; np < 2; ++np) {
-      uint32_t r0, r1, r2, r3;
+    for (int mt = 0; mt < 2; ++mt) {
+      uint32_t a0, a1, a2, a3;
       asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
-                   : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(vrow + np * 32));
-      mma_bf16_full(oc[2 * np], a0, a1, a2, a3, r0, r1);
-      mma_bf16_full(oc[2 * np + 1], a0, a1, a2, a3, r2, r3);
+                   : "=r"(a0), "=r"(a1), "=r"(a2), "=r"(a3) : "r"(va + mt * 32));
+      mma_bf16_full(oc[mt], a0, a1, a2, a3, b0, b1);
     }
   }
 
-  // 5. the output (row 0 hi + row 8 lo of column tile j: lanes 0..3 hold
-  //    columns 32w + 8j + 2t, + 1) and the current token's buffer entry
-  if (g == 0) {
-    float *orow = io.o + (b * P.Hv + h) * D + 32 * warp + 2 * t;
+  // 5. the output (lanes t == 0: hi + lo sums of columns 32w + 16mt + g and + 8)
+  //    and the current token's buffer entry
+  if (t == 0) {
+    float *orow = io.o + (b * P.Hv + h) * D + 32 * warp + g;
 #pragma unroll
-    for (int j = 0; j < 4; ++j)
-      __stcs(reinterpret_cast<float2 *>(orow + 8 * j), make_float2(oc[j][0] + oc[j][2], oc[j][1] + oc[j][3]));
+    for (int mt = 0; mt < 2; ++mt) {
+      __stcs(orow + 16 * mt, oc[mt][0] + oc[mt][1]);
+      __stcs(orow + 16 * mt + 8, oc[mt][2] + oc[mt][3]);
+    }
   }
   if (tid < 16) {
     *reinterpret_cast<uint4 *>(static_cast<KT *>(P.vbuf) + voff[n] * D + tid * 8) =
