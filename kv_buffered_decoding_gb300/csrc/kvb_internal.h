@@ -17,7 +17,7 @@ constexpr int kMaxRows = 256;
 // Leading block ids of each request carried in its row descriptor, so the
 // kernels find the first kRowBlocks * block_size buffer slots without a
 // dependent load of the block table.
-constexpr int kRowBlocks = 4;
+constexpr int kRowBlocks = 8;
 
 // Device view of a pool: raw pointers into the caller's regions plus shapes.
 struct PoolView {

@@ -71,7 +71,7 @@ constexpr int kVtMaxStages = 3;            // state tiles in flight
 constexpr int kVtPolls = 1 << 16;          // try_wait bound of every wait (each up to ~a microsecond)
 constexpr uint32_t kTileBytes = 128 * 128 * 4;
 constexpr uint32_t kTmemCols = 128;  // per group two accumulators of up to 16 columns
-constexpr uint32_t kVtSmemMax = 227 * 1024 - 10 * 1024;  // dynamic bytes (9 KB static aside)
+constexpr uint32_t kVtSmemMax = 227 * 1024 - 10 * 1024;  // dynamic bytes (1 KB static aside, and margin)
 
 // Byte offsets of one small stage (16-byte aligned parts).
 struct VtStage {
@@ -266,7 +266,6 @@ __global__ void __launch_bounds__(kVtMaxThreads, 1)
   __shared__ uint32_t tmem_s;
   __shared__ int s_abort;
   __shared__ unsigned long long anc[kVtMaxGroups][kVtMaxL];  // draft trees: ancestor sets
-  __shared__ RowDesc rs[kMaxRows];  // the launch's row descriptors (read with dynamic indices)
 
   // barriers (8 bytes apart within each array) and stage memory
   auto bar = [](uint64_t *b, int i) { return su32(b) + 8u * (uint32_t)i; };
@@ -291,7 +290,6 @@ __global__ void __launch_bounds__(kVtMaxThreads, 1)
     s_abort = 0;
     asm volatile("fence.mbarrier_init.release.cluster;");
   }
-  for (int r = tid; r < rows.count; r += blockDim.x) rs[r] = rows.r[r];
   if (warp == 0) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(su32(&tmem_s)),
                  "r"(kTmemCols));
@@ -322,7 +320,7 @@ __global__ void __launch_bounds__(kVtMaxThreads, 1)
           }
         }
         const int y = fast_div(u, hv_div), h = u - y * P.Hv;
-        const int slot = rs[y].slot;
+        const int slot = rows.r[y].slot;  // the parameter block, read in place
         if (slot >= 0) {
           vt_arrive_tx(bar(bar_full, ks), kTileBytes);
           const uint32_t dst = su32(smem + lay.tile) + (uint32_t)ks * kTileBytes;
@@ -359,7 +357,7 @@ __global__ void __launch_bounds__(kVtMaxThreads, 1)
         }
       }
       const int y = fast_div(u, hv_div), h = u - y * P.Hv;
-      const RowDesc &d = rs[y];
+      const RowDesc &d = rows.r[y];
       const size_t b = (size_t)rows.row0 + y;
       const int hq = h / group, n = d.n, L = n + T;
       size_t *koff = reinterpret_cast<size_t *>(st + sl.koff);

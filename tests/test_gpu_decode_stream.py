@@ -164,7 +164,7 @@ def test_short_ctx_large_batch(layer, B):
     1..64 in 64-slot buffers (block ids beyond the row descriptor's come from the
     block table), launches from B rows down to a handful.  Sampled outputs against
     the oracle's buffer-only decode, all lengths bit for bit."""
-    bs, nb = 8, 8
+    bs, nb = 4, 16  # blocks 8..15 come from the block table
     cap = nb * bs
     rng = np.random.default_rng(740 + layer.variant + B)
     pool = make_pool(layer, 8, B, nb, bs, num_blocks=B * nb + 8, num_slots=1)

@@ -146,19 +146,19 @@ def test_gdn_d64_grouped_heads_all_calls():
 def test_device_error_word_on_corrupt_table():
     """A block id corrupted in the device block table is caught by the kernel's own check:
     the CTA records (kind=1, request, value) and returns before using it; nothing faults.
-    The first blocks of a request travel in the launch's row descriptors, so the
-    corrupted entry is the fifth block (slots 16..19 at 4 slots per block)."""
+    The first eight blocks of a request travel in the launch's row descriptors, so the
+    corrupted entry is the ninth block (slots 16, 17 at 2 slots per block)."""
     layer = I.GATED_LAYER
-    pool = make_pool(layer, 4, 2, 8, 4, num_slots=1)
-    pool.set_request(0, -1, list(range(8)))
-    pool.set_request(1, -1, list(range(8, 16)))
+    pool = make_pool(layer, 4, 2, 16, 2, num_slots=1)
+    pool.set_request(0, -1, list(range(16)))
+    pool.set_request(1, -1, list(range(16, 32)))
     rng = np.random.default_rng(3)
     tok = I.draw_tokens(rng, layer, (17, 2))
     outs = [pool.short_ctx([0, 1], *token_tensors(tok, layer, t)).cpu().numpy() for t in range(16)]
     torch.cuda.synchronize()
-    # the block table is the first region of the metadata: request 0, block 4
+    # the block table is the first region of the metadata: request 0, block 8
     bad = torch.tensor([12345], dtype=torch.int32).view(torch.uint8).cuda()
-    pool._meta_mem[16:20].copy_(bad)
+    pool._meta_mem[32:36].copy_(bad)
     outs.append(pool.short_ctx([0, 1], *token_tensors(tok, layer, 16)).cpu().numpy())
     err = pool.get_error()
     assert err == (1, 0, 12345)

@@ -235,25 +235,25 @@ def test_verify_tc_shapes(T):
 
 
 def test_verify_tc_corrupt_table():
-    """Two-slot blocks put the drafts' slots past the row descriptor's first four
+    """One-slot blocks put the drafts' slots past the row descriptor's first eight
     blocks, so the tensor-core verify reads them from the device block table.  A
     corrupted entry there is caught by the kernel's own check: the unit records
     (kind 1, request, value) and writes nothing, and the other request verifies
     normally."""
     layer = GDN_SMALL
     rng = np.random.default_rng(71)
-    pool = make_pool(layer, 16, 2, 8, 2)
+    pool = make_pool(layer, 16, 2, 16, 1)
     S0 = I.draw_state(rng, layer, 2)
     pool.state.copy_(torch.from_numpy(S0))
-    pool.set_request(0, 0, list(range(8)))
-    pool.set_request(1, 1, list(range(8, 16)))
+    pool.set_request(0, 0, list(range(16)))
+    pool.set_request(1, 1, list(range(16, 32)))
     pre = I.draw_tokens(rng, layer, (10, 2))
     for t in range(10):
         pool.decode([0, 1], *token_tensors(pre, layer, t))
     torch.cuda.synchronize()
-    # the block table is the first region of the metadata: request 0, block 5 (slots 10, 11)
+    # the block table is the first region of the metadata: request 0, block 10 (slot 10)
     bad = torch.tensor([12345], dtype=torch.int32).view(torch.uint8).cuda()
-    pool._meta_mem[20:24].copy_(bad)
+    pool._meta_mem[40:44].copy_(bad)
     tok = I.draw_tokens(rng, layer, (2, 4))
     o = torch.full((2, 4, layer.n_v_heads, layer.d_v), float("nan"), device="cuda")
     pool.verify([0, 1], *token_tensors(tok, layer, slice(None)), o=o)
