@@ -574,9 +574,9 @@ def measure_paths(kvb, torch, dev, peak):
 
     # the same calls queued back to back (each after the flush): the difference to
     # the flushes alone, per call; fresh pools so that each sequence covers 32..44
-    # tokens again; median of three
+    # tokens again; median of five
     piped = []
-    for _ in range(3):
+    for _ in range(5):
         p2 = pool_for(L, B, 8, 8, slots=False)
         for _ in range(32):
             p2.short_ctx(req, *toks)
@@ -592,7 +592,7 @@ def measure_paths(kvb, torch, dev, peak):
     rec("short_ctx_gated_B256_n32to44", us, int(B * (q + 2 * e + o + mean_n * e)),
         "buffer-only decode, no state; buffer reads dominate; cold L2: each call after an "
         "L2 flush, calls and flushes queued back to back, the flushes' own time subtracted "
-        "(median of three sequences of 13)")
+        "(median of five sequences of 13)")
     out["short_ctx_gated_B256_n32to44"]["us_single_call"] = us_single
     out["short_ctx_gated_B256_n32to44"]["single_call_note"] = (
         "one call between two events after a sleep kernel: adds the event and launch floor, "

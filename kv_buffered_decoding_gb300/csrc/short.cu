@@ -507,18 +507,27 @@ __global__ void __launch_bounds__(128) short_tc_kernel(const PoolView P,
   //    token's q, k (row n) and v (row n)
   const KT *kb = static_cast<const KT *>(P.kbuf);
   const KT *vb = static_cast<const KT *>(P.vbuf);
+  // first group: what the score pass needs (keys, q, gates); second: the values,
+  // still in flight while the scores are formed
   for (int c = tid; c < n * 16; c += 128) {
     const int i = c >> 4, p = (c & 15) * 8;
     scp16(Kr + i * XS + p, kb + koff[i] + p);
-    scp16(Vr + i * XS + p, vb + voff[i] * D + p);
   }
-  if (tid < 48) {
-    const int part = tid >> 4, p = (tid & 15) * 8;
-    if (part == 0) scp16(qs + p, static_cast<const KT *>(io.q) + (b * P.Hk + hq) * D + p);
-    else if (part == 1) scp16(Kr + n * XS + p, static_cast<const KT *>(io.k) + (b * P.Hk + hq) * D + p);
-    else scp16(Vr + n * XS + p, static_cast<const KT *>(io.v) + (b * P.Hv + h) * D + p);
+  if (tid < 32) {
+    const int p = (tid & 15) * 8;
+    if (tid < 16) scp16(qs + p, static_cast<const KT *>(io.q) + (b * P.Hk + hq) * D + p);
+    else scp16(Kr + n * XS + p, static_cast<const KT *>(io.k) + (b * P.Hk + hq) * D + p);
   }
   if (GATED && tid >= 64 && tid - 64 < n) scp4(As + tid - 64, P.gbuf + voff[tid - 64]);
+  asm volatile("cp.async.commit_group;\n" ::: "memory");
+  for (int c = tid; c < n * 16; c += 128) {
+    const int i = c >> 4, p = (c & 15) * 8;
+    scp16(Vr + i * XS + p, vb + voff[i] * D + p);
+  }
+  if (tid >= 32 && tid < 48) {
+    const int p = (tid & 15) * 8;
+    scp16(Vr + n * XS + p, static_cast<const KT *>(io.v) + (b * P.Hv + h) * D + p);
+  }
   asm volatile("cp.async.commit_group;\n" ::: "memory");
   // meanwhile: zero the padded value rows (the output product reads them) and
   // the padded tokens' weights
@@ -526,7 +535,7 @@ __global__ void __launch_bounds__(128) short_tc_kernel(const PoolView P,
     *reinterpret_cast<uint4 *>(Vr + (L + (c >> 4)) * XS + (c & 15) * 8) = make_uint4(0u, 0u, 0u, 0u);
   if (tid >= L && tid < LP) whi[tid] = wlo[tid] = __float2bfloat16_rn(0.f);
   const float a_t = GATED && io.log_g ? io.log_g[b * P.Hv + h] : 0.f;
-  asm volatile("cp.async.wait_group 0;\n" ::: "memory");
+  asm volatile("cp.async.wait_group 1;\n" ::: "memory");  // keys, q and gates
   __syncthreads();
   const float A_t = (GATED && n > 0 ? As[n - 1] : 0.f) + a_t;
 
@@ -545,15 +554,21 @@ __global__ void __launch_bounds__(128) short_tc_kernel(const PoolView P,
     const uint32_t kaddr = static_cast<uint32_t>(__cvta_generic_to_shared(Kr)) +
                            (uint32_t)((lane & 15) * XS * 2 + (lane >> 4) * 16);
     for (int mt = warp; mt < mtiles; mt += NW) {
-      float acc[4] = {0.f, 0.f, 0.f, 0.f};
+      // two accumulator chains (even and odd k-steps) halve the dependent MMA chain
+      float acc[4] = {0.f, 0.f, 0.f, 0.f}, acc2[4] = {0.f, 0.f, 0.f, 0.f};
       const uint32_t ka = kaddr + (uint32_t)(mt * 16 * XS * 2);
 #pragma unroll
-      for (int ks = 0; ks < 8; ++ks) {
-        uint32_t a0, a1, a2, a3;
+      for (int ks = 0; ks < 8; ks += 2) {
+        uint32_t a0, a1, a2, a3, c0, c1, c2, c3;
         asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
                      : "=r"(a0), "=r"(a1), "=r"(a2), "=r"(a3) : "r"(ka + ks * 32));
+        asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                     : "=r"(c0), "=r"(c1), "=r"(c2), "=r"(c3) : "r"(ka + ks * 32 + 32));
         mma_bf16_full(acc, a0, a1, a2, a3, bq[ks][0], bq[ks][1]);
+        mma_bf16_full(acc2, c0, c1, c2, c3, bq[ks + 1][0], bq[ks + 1][1]);
       }
+#pragma unroll
+      for (int x = 0; x < 4; ++x) acc[x] += acc2[x];
       if (t == 0) {
 #pragma unroll
         for (int x = 0; x < 2; ++x) {
@@ -569,6 +584,7 @@ __global__ void __launch_bounds__(128) short_tc_kernel(const PoolView P,
       }
     }
   }
+  asm volatile("cp.async.wait_group 0;\n" ::: "memory");  // the values
   __syncthreads();
 
   // 4. o^T = V^T w for this warp's 32 columns (two tiles of 16): A = V^T by
