@@ -598,6 +598,58 @@ def measure_paths(kvb, torch, dev, peak):
         "one call between two events after a sleep kernel: adds the event and launch floor, "
         "about 4-6 us for an empty kernel on this GPU")
 
+    # Figure 5 of the pages: per-step latency against context length for KV-only
+    # decoding (short context: the buffer alone, no state), recurrent decoding
+    # (m = 0) and buffered decoding (m = 8, averaged over a whole cycle), gated layer,
+    # B = 256.  Every step runs on a cold L2, as one layer's step among a model's
+    # layers would: k steps, each after an L2 flush, queued back to back, minus the
+    # flushes alone.  KV-only contexts stop at 60..63 tokens (64-slot buffers); a
+    # request that outgrows them is promoted to a state (kvb_promote).
+    def cold_per_call(fn, k):
+        def seq(f):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda._sleep(2_000_000)
+            a.record(stream)
+            for _ in range(k):
+                l2_flush.fill_(1)
+                l2_clean.max()
+                if f is not None:
+                    f()
+            b.record(stream)
+            torch.cuda.synchronize()
+            return a.elapsed_time(b) * 1e3
+        return (seq(fn) - seq(None)) / k
+
+    L, B = I.GATED_LAYER, 256
+    req = np.arange(B, dtype=np.int32)
+    toks = tokens(L, (B,), 30)
+    kv_only = {}
+    for ctx in (16, 32, 48, 60):
+        vals = []
+        for _ in range(3):
+            pk = pool_for(L, B, 8, 8, slots=False)
+            for _ in range(ctx - 1):
+                pk.short_ctx(req, *toks)
+            vals.append(cold_per_call(lambda: pk.short_ctx(req, *toks), 4))  # contexts ctx .. ctx + 3
+            checked_close(pk)
+        kv_only[str(ctx)] = statistics.median(vals)
+    by_m = {}
+    for m_ in (0, 8):
+        vals = []
+        for _ in range(3):
+            pm = pool_for(L, B, m_, 1)
+            k_ = max(m_, 4)  # a whole cycle of occupancies 0..m-1 (the last step folds)
+            vals.append(cold_per_call(lambda: pm.decode(req, *toks), k_))
+            checked_close(pm)
+        by_m[m_] = statistics.median(vals)
+    out["fig5_context_gated_B256"] = {
+        "kv_only_us": kv_only, "recurrent_m0_us": by_m[0], "buffered_m8_us": by_m[8],
+        "kv_only_normalised_to_m0": {c: v / by_m[0] for c, v in kv_only.items()},
+        "buffered_m8_normalised_to_m0": by_m[8] / by_m[0],
+        "note": "per-step GPU time, each step after an L2 flush (flush time subtracted); KV-only at "
+                "context c averages contexts c..c+3; state %d MiB" % (
+                    B * L.n_v_heads * L.d_k * L.d_v * 4 >> 20)}
+
     # chunked prefill: 1024-token prompts from S = 0, 32 requests, both layers; the bf16
     # products run as tcgen05 MMAs (bf16 hi/lo parts, fp32 accumulation in TMEM),
     # reported against the bf16 tensor peak and HBM
