@@ -177,19 +177,25 @@ def test_verify_gated_delta_d128(T):
 GDN_SMALL = I.Layer(I.GATED_DELTA, 2, 4, 128, 128, "bf16", qk_dist="l2norm")
 
 
-@pytest.mark.parametrize("T", [1, 4, 8, 12])
-def test_verify_tc_shapes(T):
+GATED_SMALL = I.Layer(I.GATED, 2, 4, 128, 128, "bf16")
+
+
+@pytest.mark.parametrize("name,T,m", [("gdn", 1, 8), ("gdn", 4, 8), ("gdn", 8, 8), ("gdn", 12, 8),
+                                      ("gated", 9, 8), ("gated", 16, 1)])
+def test_verify_tc_shapes(name, T, m):
     """The tensor-core verify (the state tile by TMA, the mat-vecs as one tcgen05
-    product; chunks of at most 16 tokens and 2T <= 16 vectors for the delta rule) and,
-    past those limits (T = 12), the mma.sync kernel: ragged buffers of 0..7 tokens,
-    stateless (short-context) requests verifying against S = 0, and more (row, head)
-    units than the persistent grid holds, so every CTA walks several.  Every draft
-    output and, after accept and a closing flush, every state."""
-    layer = GDN_SMALL
-    B, n_short, m, bs = 100, 10, 8, 8
+    product; chunks of at most 16 tokens and at most 16 vectors: 2T for the delta rule,
+    T without it) and, past those limits (T = 12 with the delta rule), the mma.sync
+    kernel: ragged buffers of 0..m-1 tokens (empty at m = 1, so that 16 drafts make a
+    16-token chunk, the launch shape with one pipeline per CTA), stateless
+    (short-context) requests verifying against S = 0, and more (row, head) units than
+    the persistent grid holds, so every CTA walks several.  Every draft output and,
+    after accept and a closing flush, every state."""
+    layer = GDN_SMALL if name == "gdn" else GATED_SMALL
+    B, n_short, bs = 100, 10, 8
     n_long = B - n_short
     nb = blocks_needed(m - 1 + T, bs)
-    rng = np.random.default_rng(60 + T)
+    rng = np.random.default_rng(60 + T + 100 * layer.variant)
     pool = make_pool(layer, m, B, nb, bs, num_slots=n_long)
     S0 = I.draw_state(rng, layer, n_long)
     pool.state.copy_(torch.from_numpy(S0))
