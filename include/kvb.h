@@ -250,7 +250,7 @@ int kvb_accept(kvb_pool *pool, int32_t B, const int32_t *req_ids, const int32_t 
    on the path from the root to j.  As in kvb_verify, the drafts occupy buffer
    slots n .. n+T-1 and the state is only read; inputs and o are laid out as
    there.  A verify_tree must be followed by kvb_accept_tree (kvb_accept gives
-   KVB_E_STATE).  Launches carry at most 128 rows each. */
+   KVB_E_STATE).  Launches carry at most 256 rows each. */
 int kvb_verify_tree(kvb_pool *pool, int32_t B, int32_t T, const int32_t *req_ids,
                     const int32_t *parents, const void *q, const void *k, const void *v,
                     const float *log_g, const float *beta, float *o, kvb_stream_t stream);

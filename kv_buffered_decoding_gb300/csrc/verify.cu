@@ -14,6 +14,11 @@
 // The drafts' K, V, u, gates go to buffer slots n..n+T-1; kvb_accept later
 // keeps a prefix of them by length alone.
 //
+// bf16 pools at d = 128 run on the fifth-generation tensor cores
+// (verify_tc.cu) when the chunk and draft count fit that kernel; the rest run
+// here: verify_mma_kernel (bf16, d = 128: the mat-vecs and score dots as
+// mma.sync passes) and verify_kernel (fp32 pools, d = 64), described next.
+//
 // Two CTAs of 128 threads per (batch row, value head) at d = 128, with the
 // decode kernel's layout: warp w owns 16 state columns, each lane 16
 // consecutive rows of four of them, and the tile stays in registers.  The 2T
