@@ -7,7 +7,8 @@
 //   Y = [Q; K] S,  Mq = scale e^{A_i-A_j} q_i.k_j (j <= i),  Mk = beta_i e^{A_i-A_j} k_i.k_j (j < i)
 //   (I + Mk) U = R,  R_i = beta_i (v_i - e^{A_i} S^T k_i)       (U = V unless the delta rule)
 //   O = e^{A} scale Y_q + Mq U,   S <- e^{A_{C-1}} S + K^T diag(w) U
-// Layout: thread t of the 128 owns TMEM lane t.  The state lives in TMEM
+// Layout: four warpgroups of 128 threads; thread t of each owns TMEM lane t,
+// the warpgroups splitting its column ranges.  The state lives in TMEM
 // transposed (lane = value column c, columns = key rows), so that
 //   Y^T = S^T X^T          (A: S^T from TMEM as bf16 hi/lo parts, B: X = [Q;K] from smem)
 //   G   = X K^T            (A: X, B: the K rows of X; exact for bf16 inputs)
@@ -26,7 +27,7 @@
 namespace kvb {
 namespace {
 
-constexpr int kC = 64, kD = 128, kThreads = 256;  // two warpgroups share every TMEM lane
+constexpr int kC = 64, kD = 128, kThreads = 512;  // four warpgroups share every TMEM lane
 // TMEM columns
 constexpr uint32_t kColS = 0;     // S^T fp32            [128 lanes x 128]
 constexpr uint32_t kColP = 128;   // A parts: S^T hi/lo (64 + 64), later U^T hi/lo, (wU)^T hi/lo (32 each)
@@ -114,16 +115,6 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
       : "r"(taddr));
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
-__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
-      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};"
-      ::"r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
-        "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]),
-        "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]),
-        "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
-      : "memory");
-}
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 // x = hi + lo, both bf16 (hi = round(x), lo = round(x - hi))
@@ -160,16 +151,6 @@ __device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&r)[8])
                : "memory");
 }
 
-__device__ __forceinline__ void split32(const float (&x)[32], uint32_t (&hi)[16], uint32_t (&lo)[16]) {
-#pragma unroll
-  for (int j = 0; j < 16; ++j) {
-    uint16_t h0, l0, h1, l1;
-    split_bf16(x[2 * j], h0, l0);
-    split_bf16(x[2 * j + 1], h1, l1);
-    hi[j] = pack2(h0, h1);
-    lo[j] = pack2(l0, l1);
-  }
-}
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};"
@@ -182,7 +163,7 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16
 // in 16 x 16 blocks: T_aa = (I + Mk_aa)^{-1} by forward substitution (one
 // column per thread), then T_ab = -T_aa sum_{b<=c<a} Mk_ac T_cb level by level
 // (a - b = 1, 2, 3), one block entry per thread and step.  Writes T (zero above
-// the diagonal) to Tf; P is scratch for three 16 x 16 blocks.  All 256 threads.
+// the diagonal) to Tf; P is scratch for three 16 x 16 blocks.  All threads.
 __device__ __forceinline__ void ut_inverse(const float *Mk, float *Tf, float *Pb, int tid) {
   if (tid < 64) {  // diagonal blocks: block a, column j
     const int a = tid >> 4, j = tid & 15, o = a * 16;
@@ -308,7 +289,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   fence_after();
   const uint32_t tmem = tmem_s;
   const int lt = tid & 127;              // this thread's TMEM lane
-  const int wg = tid >> 7;               // warpgroup: which half of each lane's columns
+  const int wg = tid >> 7;               // warpgroup: which quarter of each lane's columns
   const uint32_t my = tmem + lane_base;  // this thread's lane, column 0
   const int c = lt;                      // as a state column
   bool ok = true;
@@ -325,10 +306,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_st8(my + kColP + r0 * 8, hi);
     tmem_st8(my + kColP + 64 + r0 * 8, lo);
   };
-  // this warpgroup's 64 state rows of column c: fp32 into S^T, and their parts
+  // this warpgroup's 32 state rows of column c: fp32 into S^T, and their parts
 #pragma unroll 1
-  for (int q = 0; q < 4; ++q) {
-    const int r0 = wg * 4 + q;  // 16-row piece
+  for (int q = 0; q < 2; ++q) {
+    const int r0 = wg * 2 + q;  // 16-row piece
     float x[16];
     uint32_t w[16];
 #pragma unroll
@@ -361,8 +342,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint8_t *kt = smem + kOffKt;
       const int r = lt;  // key row (d_k index)
 #pragma unroll
-      for (int q4 = 0; q4 < 4; ++q4) {
-        const int jg = wg * 4 + q4;
+      for (int q4 = 0; q4 < 2; ++q4) {
+        const int jg = wg * 2 + q4;
         uint16_t e[8];
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
@@ -423,27 +404,27 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (!ok) break;
 
     // Gram rows, key tokens split by warpgroup: thread (i, wg) builds entries
-    // j = 32 wg .. 32 wg + 31 of row i of Mq (parts, smem) or Mk (fp32)
+    // j = 16 wg .. 16 wg + 15 of row i of Mq (parts, smem) or Mk (fp32)
     {
-      const int i = lt, j0 = wg * 32;
-      float gr[32];
+      const int i = lt, j0 = wg * 16;
+      float gr[16];
       {
-        uint32_t w[32];
-        tmem_ld32(my + kColG + j0, w);
+        uint32_t w[16];
+        tmem_ld16(my + kColG + j0, w);
 #pragma unroll
-        for (int j = 0; j < 32; ++j) gr[j] = __uint_as_float(w[j]);
+        for (int j = 0; j < 16; ++j) gr[j] = __uint_as_float(w[j]);
       }
       if (i < kC) {  // Mq[i][j] = scale e^{A_i-A_j} q_i.k_j, j <= i
         const float Ai = Acum[i];
-        float x[32];
+        float x[16];
 #pragma unroll
-        for (int j = 0; j < 32; ++j) x[j] = j0 + j <= i ? P.scale * expf(Ai - Acum[j0 + j]) * gr[j] : 0.f;
-        uint32_t hi[16], lo[16];
-        split32(x, hi, lo);
+        for (int j = 0; j < 16; ++j) x[j] = j0 + j <= i ? P.scale * expf(Ai - Acum[j0 + j]) * gr[j] : 0.f;
+        uint32_t hi[8], lo[8];
+        split16(x, hi, lo);
         uint8_t *mq = smem + kOffMq;
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const int off = (i >> 3) * kSboKt + (wg * 4 + q) * kLbo + (i & 7) * 16;
+        for (int q = 0; q < 2; ++q) {
+          const int off = (i >> 3) * kSboKt + (wg * 2 + q) * kLbo + (i & 7) * 16;
           *reinterpret_cast<uint4 *>(mq + off) = make_uint4(hi[4 * q], hi[4 * q + 1], hi[4 * q + 2], hi[4 * q + 3]);
           *reinterpret_cast<uint4 *>(mq + kMqBytes + off) =
               make_uint4(lo[4 * q], lo[4 * q + 1], lo[4 * q + 2], lo[4 * q + 3]);
@@ -452,7 +433,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int ip = i - kC;
         const float Ai = Acum[ip], bi = bs[ip];
 #pragma unroll
-        for (int j = 0; j < 32; j += 4) {
+        for (int j = 0; j < 16; j += 4) {
           const int jj = j0 + j;
           float4 m4;
           m4.x = jj < ip ? bi * expf(Ai - Acum[jj]) * gr[j] : 0.f;
@@ -463,21 +444,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
-    // column c of R (delta rule), tokens 32 wg .. 32 wg + 31, as bf16 parts into
+    // column c of R (delta rule), tokens 16 wg .. 16 wg + 15, as bf16 parts into
     // TMEM: the A operand (R^T) of U^T = R^T T^T
     if (DELTA) {
-      uint32_t w[32];
-      tmem_ld32(my + kColY + kC + wg * 32, w);
-      float r[32];
+      uint32_t w[16];
+      tmem_ld16(my + kColY + kC + wg * 16, w);
+      float r[16];
 #pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        const int jj = wg * 32 + j;
+      for (int j = 0; j < 16; ++j) {
+        const int jj = wg * 16 + j;
         r[j] = bs[jj] * (__bfloat162float(vs[jj * kD + c]) - eA[jj] * __uint_as_float(w[j]));
       }
-      uint32_t hi[16], lo[16];
-      split32(r, hi, lo);
-      tmem_st16(my + kColP + wg * 16, hi);
-      tmem_st16(my + kColP + 32 + wg * 16, lo);
+      uint32_t hi[8], lo[8];
+      split16(r, hi, lo);
+      tmem_st8(my + kColP + wg * 8, hi);
+      tmem_st8(my + kColP + 32 + wg * 8, lo);
       tmem_wait_st();
     }
     fence_async_smem();
@@ -490,7 +471,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (DELTA) {
       float *Tf = reinterpret_cast<float *>(smem + kOffTf);
       ut_inverse(Mk, Tf, reinterpret_cast<float *>(smem + kOffR), tid);
-      {
+      if (tid < 4 * kC) {
         const int i = tid >> 2, jq = (tid & 3) * 16;  // row i, 16 columns
         float x[16];
 #pragma unroll
@@ -532,11 +513,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
     }
 
-    if (wg == 0) {
-      // column c of U (from the UT product, or V), 16 tokens at a time: U^T and
-      // (wU)^T parts into TMEM, the A operands of the second MMAs
+    if (wg < 2) {
+      // column c of U (from the UT product, or V), 16 tokens at a time (warpgroups
+      // 0 and 1: two each): U^T and (wU)^T parts into TMEM, the A operands of the
+      // second MMAs
 #pragma unroll 1
-      for (int q = 0; q < 4; ++q) {
+      for (int q = 2 * wg; q < 2 * wg + 2; ++q) {
         float x[16];
         if (DELTA) {
           uint32_t w[16];
@@ -557,23 +539,26 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_st8(my + kColP + 64 + q * 8, hi);
         tmem_st8(my + kColP + 96 + q * 8, lo);
       }
-    } else {
-      // meanwhile: e^A scale Y_q^T (the output accumulator) and e^{A_C} S^T
-      uint32_t w[32];
-#pragma unroll 1
-      for (int q = 0; q < 2; ++q) {
-        tmem_ld32(my + kColY + q * 32, w);
-#pragma unroll
-        for (int j = 0; j < 32; ++j) w[j] = __float_as_uint(P.scale * eA[q * 32 + j] * __uint_as_float(w[j]));
-        tmem_st32(my + kColY + q * 32, w);
-      }
-      const float eL = eA[kC - 1];
+    } else if (wg == 2) {
+      // meanwhile: e^A scale Y_q^T (the output accumulator)
+      uint32_t w[16];
 #pragma unroll 1
       for (int q = 0; q < 4; ++q) {
-        tmem_ld32(my + kColS + q * 32, w);
+        tmem_ld16(my + kColY + q * 16, w);
 #pragma unroll
-        for (int j = 0; j < 32; ++j) w[j] = __float_as_uint(eL * __uint_as_float(w[j]));
-        tmem_st32(my + kColS + q * 32, w);
+        for (int j = 0; j < 16; ++j) w[j] = __float_as_uint(P.scale * eA[q * 16 + j] * __uint_as_float(w[j]));
+        tmem_st16(my + kColY + q * 16, w);
+      }
+    } else {
+      // and e^{A_C} S^T
+      uint32_t w[16];
+      const float eL = eA[kC - 1];
+#pragma unroll 1
+      for (int q = 0; q < 8; ++q) {
+        tmem_ld16(my + kColS + q * 16, w);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) w[j] = __float_as_uint(eL * __uint_as_float(w[j]));
+        tmem_st16(my + kColS + q * 16, w);
       }
     }
     tmem_wait_st();
@@ -608,20 +593,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     fence_after();
     if (!ok) break;
 
-    // outputs (tokens 32 wg .. 32 wg + 31 of column c) and the next chunk's S^T
-    // parts (state rows 64 wg .. 64 wg + 63)
+    // outputs (tokens 16 wg .. 16 wg + 15 of column c) and the next chunk's S^T
+    // parts (state rows 32 wg .. 32 wg + 31)
     {
-      uint32_t w[32];
-      tmem_ld32(my + kColY + wg * 32, w);
+      uint32_t w[16];
+      tmem_ld16(my + kColY + wg * 16, w);
 #pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        const int i = wg * 32 + j;
+      for (int j = 0; j < 16; ++j) {
+        const int i = wg * 16 + j;
         if (t0 + i < L) io.o[((b * Tp + t0 + i) * P.Hv + h) * kD + c] = __uint_as_float(w[j]);
       }
       if (ch + 1 < nchunks) {
 #pragma unroll 1
-        for (int q = 0; q < 4; ++q) {
-          const int r0 = wg * 4 + q;
+        for (int q = 0; q < 2; ++q) {
+          const int r0 = wg * 2 + q;
           uint32_t w16[16];
           tmem_ld16(my + kColS + r0 * 16, w16);
           float x[16];
@@ -635,13 +620,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
   if (ok) {
-    // this warpgroup's half of the state column back to global memory
-#pragma unroll
-    for (int q = 0; q < 2; ++q) {
+    // this warpgroup's quarter of the state column back to global memory
+    {
       uint32_t w[32];
-      tmem_ld32(my + kColS + wg * 64 + q * 32, w);
+      tmem_ld32(my + kColS + wg * 32, w);
 #pragma unroll
-      for (int j = 0; j < 32; ++j) Sg[(size_t)(wg * 64 + q * 32 + j) * kD + c] = __uint_as_float(w[j]);
+      for (int j = 0; j < 32; ++j) Sg[(size_t)(wg * 32 + j) * kD + c] = __uint_as_float(w[j]);
     }
   } else {
     if (tid == 0) record_error(P.err, kErrTimeout, d.req, h);
