@@ -298,6 +298,29 @@ __global__ void __launch_bounds__(kThreads, 1)
   // failure-path test hook (first_polls > 0), every later one has the default
   int polls = first_polls > 0 ? first_polls : kWaitPolls;
 
+  // e^A scale Y_q^T (the output accumulator), and e^{A_C} S^T (the state before
+  // its update), for this thread's lane
+  // (16-column rounds q0 .. q1 - 1 of each)
+  auto scale_y = [&](const float *eAv, int q0, int q1) {
+    uint32_t w[16];
+#pragma unroll 1
+    for (int q = q0; q < q1; ++q) {
+      tmem_ld16(my + kColY + q * 16, w);
+#pragma unroll
+      for (int j = 0; j < 16; ++j) w[j] = __float_as_uint(P.scale * eAv[q * 16 + j] * __uint_as_float(w[j]));
+      tmem_st16(my + kColY + q * 16, w);
+    }
+  };
+  auto scale_s = [&](float eL, int q0, int q1) {
+    uint32_t w[16];
+#pragma unroll 1
+    for (int q = q0; q < q1; ++q) {
+      tmem_ld16(my + kColS + q * 16, w);
+#pragma unroll
+      for (int j = 0; j < 16; ++j) w[j] = __float_as_uint(eL * __uint_as_float(w[j]));
+      tmem_st16(my + kColS + q * 16, w);
+    }
+  };
   // bf16 hi / lo parts of 16 state rows (16 r0 .. 16 r0 + 15) of column c into the
   // A region (the operand of Y^T = S^T X^T)
   auto put_parts16 = [&](const float (&x)[16], int r0) {
@@ -334,7 +357,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     fence_before();
     __syncthreads();  // chunk staged; the previous chunk's MMAs are done
     fence_after();
-    if (ch + 1 < nchunks) issue(ch + 1);  // the other stage is free
 
     // K^T (B of the state update) from the K rows of X, token groups split by
     // warpgroup; cumulative gates (warp 3)
@@ -397,6 +419,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       mma_commit(mbar);
     }
+    // while the products run: the next chunk's copies (into the other stage, free
+    // since the previous chunk finished)
+    if (ch + 1 < nchunks) issue(ch + 1);
     ok = __syncthreads_and(mbar_wait(mbar, phase, polls)) != 0;  // CTA-uniform
     polls = kWaitPolls;
     phase ^= 1;
@@ -469,6 +494,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     // the UT transform: T = (I + Mk)^{-1} in blocks, its bf16 parts (B operand,
     // rows i, k = j), then U^T = R^T T^T on the tensor cores into the G columns
     if (DELTA) {
+      // meanwhile, while the first 64 threads invert the diagonal blocks:
+      // warpgroup 1 scales Y_q^T, warpgroups 2 and 3 the two halves of S^T
+      if (wg == 1) scale_y(eA, 0, 4);
+      if (wg >= 2) scale_s(eA[kC - 1], (wg - 2) * 4, (wg - 1) * 4);
+      if (wg >= 1) tmem_wait_st();
       float *Tf = reinterpret_cast<float *>(smem + kOffTf);
       ut_inverse(Mk, Tf, reinterpret_cast<float *>(smem + kOffR), tid);
       if (tid < 4 * kC) {
@@ -513,12 +543,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
     }
 
-    if (wg < 2) {
-      // column c of U (from the UT product, or V), 16 tokens at a time (warpgroups
-      // 0 and 1: two each): U^T and (wU)^T parts into TMEM, the A operands of the
-      // second MMAs
-#pragma unroll 1
-      for (int q = 2 * wg; q < 2 * wg + 2; ++q) {
+    {
+      // column c of U (from the UT product, or V), 16 tokens at a time: U^T and
+      // (wU)^T parts into TMEM, the A operands of the second MMAs; without the
+      // delta rule the scaling of Y_q^T and S^T (done during the inverse with it)
+      // shares these warpgroups: 4 U chunks + 4 Y rounds + 8 S rounds
+      auto u_parts = [&](int q) {
         float x[16];
         if (DELTA) {
           uint32_t w[16];
@@ -538,27 +568,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         split16(x, hi, lo);
         tmem_st8(my + kColP + 64 + q * 8, hi);
         tmem_st8(my + kColP + 96 + q * 8, lo);
-      }
-    } else if (wg == 2) {
-      // meanwhile: e^A scale Y_q^T (the output accumulator)
-      uint32_t w[16];
-#pragma unroll 1
-      for (int q = 0; q < 4; ++q) {
-        tmem_ld16(my + kColY + q * 16, w);
-#pragma unroll
-        for (int j = 0; j < 16; ++j) w[j] = __float_as_uint(P.scale * eA[q * 16 + j] * __uint_as_float(w[j]));
-        tmem_st16(my + kColY + q * 16, w);
-      }
-    } else {
-      // and e^{A_C} S^T
-      uint32_t w[16];
+      };
       const float eL = eA[kC - 1];
-#pragma unroll 1
-      for (int q = 0; q < 8; ++q) {
-        tmem_ld16(my + kColS + q * 16, w);
-#pragma unroll
-        for (int j = 0; j < 16; ++j) w[j] = __float_as_uint(eL * __uint_as_float(w[j]));
-        tmem_st16(my + kColS + q * 16, w);
+      if (DELTA) {
+        u_parts(wg);
+      } else if (wg < 2) {
+        u_parts(2 * wg);
+        u_parts(2 * wg + 1);
+        scale_s(eL, wg, wg + 1);
+      } else if (wg == 2) {
+        scale_y(eA, 0, 4);
+        scale_s(eL, 2, 3);
+      } else {
+        scale_s(eL, 3, 8);
       }
     }
     tmem_wait_st();

@@ -129,10 +129,12 @@ def test_prefill_wait_timeout_reports_and_recovers():
     the products are still in flight: each CTA records a timeout (kind 2) in the
     error word, waits with the full bound for those products, releases its tensor
     memory and returns; nothing faults.  The same context then runs a normal
-    prefill that matches the recurrence."""
+    prefill that matches the recurrence.  The prompt is one chunk, so the first wait
+    follows the products' issue directly (with a second chunk, the copies of that
+    chunk are issued in between, and the products may be done by then)."""
     kvb = kvb_mod()
     layer = I.Layer(I.GATED_DELTA, 2, 4, 128, 128, "bf16", qk_dist="l2norm")
-    B, L = 2, 70
+    B, L = 2, 50
     rng = np.random.default_rng(333)
     pool = make_pool(layer, 8, B, 1, 8)
     for r in range(B):
