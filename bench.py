@@ -335,6 +335,8 @@ def measure_paths(kvb, torch, dev, peak):
     """
     out = {}
     stream = torch.cuda.current_stream(dev)
+    # figures whose data fits in L2 are labelled L2-assisted; the size they fit in
+    out["l2_cache_bytes"] = int(getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 0))
 
     def checked_close(p):
         """Release a pool after reading its device error word: a timing taken while
@@ -427,7 +429,7 @@ def measure_paths(kvb, torch, dev, peak):
         e = _entry_bytes(L)
         nbytes = B * (S + T * (q + 2 * e + o) + n0 * e)
         rec(tag, us, nbytes, "verify + accept(0) per round; state %d MiB%s" % (
-            B * S >> 20, " (L2-resident)" if B * S < 100 * 2 ** 20 else ""))
+            B * S >> 20, " (L2-resident: L2-assisted)" if B * S < 100 * 2 ** 20 else ""))
         checked_close(pool)
 
     # draft tree: 8 drafts as a binary tree of depth 4 (every request the same shape)
@@ -519,7 +521,9 @@ def measure_paths(kvb, torch, dev, peak):
             "us_per_step": sweep,
             "normalised_to_m0": {m_: v / sweep["0"] for m_, v in sweep.items()},
             "note": "timed over whole cycles from a cycle-aligned start (every request folds "
-                    "on the same step); state %d MiB" % (B * L.n_v_heads * L.d_k * L.d_v * 4 >> 20)}
+                    "on the same step); state %d MiB%s" % (
+                        B * L.n_v_heads * L.d_k * L.d_v * 4 >> 20,
+                        " (L2-assisted)" if B * L.n_v_heads * L.d_k * L.d_v * 4 < 100 * 2 ** 20 else "")}
 
     # flush: 8 buffered tokens per request folded into the state (gated delta, B=256)
     L, B = I.GDN_LAYER, 256
