@@ -46,8 +46,9 @@ constexpr int kMkBytes = kC * kLdMk * 4;
 constexpr int kOffKt = 2 * kStage;
 constexpr int kOffMq = kOffKt + kKtBytes;       // [2 parts]
 constexpr int kOffMk = kOffMq + 2 * kMqBytes;
-constexpr int kOffR = kOffMk + kMkBytes;        // scratch for the block products, fp32 [3][16][16]
-constexpr int kRBytes = 3 * 16 * 16 * 4;
+constexpr int kLdP = 20;                        // fp32 row stride of the block-product scratch
+constexpr int kOffR = kOffMk + kMkBytes;        // scratch for the block products, fp32 [3][16][kLdP]
+constexpr int kRBytes = 3 * 16 * kLdP * 4;
 constexpr int kOffTf = kOffR + kRBytes;         // T = (I + Mk)^-1, fp32 [64][68]
 constexpr int kOffTp = kOffTf + kMkBytes;       // T as bf16 hi / lo parts, core-matrix K-major
 constexpr int kOffA = kOffTp + 2 * kMqBytes;    // Acum, e^A, w: [3][C]
@@ -159,10 +160,53 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16
       : "memory");
 }
 
+// Block products for the UT inverse on the tensor cores.  A fp32 value x enters
+// as bf16 hi + lo parts (x ~ hi + lo to about 16 significant bits); a product is
+// hi*hi + hi*lo + lo*hi with fp32 accumulation, the lo*lo term dropped, as the
+// chunk's other tensor-core products take their non-bf16 operands.
+__device__ __forceinline__ void split_pair(float x0, float x1, uint32_t &hi, uint32_t &lo) {
+  uint16_t h0, l0, h1, l1;
+  split_bf16(x0, h0, l0);
+  split_bf16(x1, h1, l1);
+  hi = pack2(h0, h1);
+  lo = pack2(l0, l1);
+}
+__device__ __forceinline__ void mma_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+// d += A B for the 16 x 16 block of A at (ar, ac) (row stride lda) and the 16 x 8
+// block of B at (br, bc) (row stride ldb), both fp32 in shared memory; lane
+// (g, t) = (lane / 4, lane % 4) holds rows g, g + 8 and columns 2t, 2t + 1 of d
+__device__ __forceinline__ void mma3_f32(float (&d)[4], const float *A, int lda, int ar, int ac,
+                                         const float *B, int ldb, int br, int bc, int lane) {
+  const int g = lane >> 2, t = lane & 3;
+  uint32_t ah[4], al[4], bh[2], bl[2];
+  const float *a0 = A + (ar + g) * lda + ac + 2 * t, *a1 = a0 + 8 * lda;
+  split_pair(a0[0], a0[1], ah[0], al[0]);
+  split_pair(a1[0], a1[1], ah[1], al[1]);
+  split_pair(a0[8], a0[9], ah[2], al[2]);
+  split_pair(a1[8], a1[9], ah[3], al[3]);
+  const float *b0 = B + (br + 2 * t) * ldb + bc + g;
+  split_pair(b0[0], b0[ldb], bh[0], bl[0]);
+  split_pair(b0[8 * ldb], b0[9 * ldb], bh[1], bl[1]);
+  mma_16816(d, ah, bh[0], bh[1]);
+  mma_16816(d, ah, bl[0], bl[1]);
+  mma_16816(d, al, bh[0], bh[1]);
+}
+// the 16 x 8 tile d (times s) into C at columns c0 .. c0 + 7 (row stride ldc)
+__device__ __forceinline__ void store_tile(float *C, int ldc, int c0, const float (&d)[4], float s, int lane) {
+  const int g = lane >> 2, t = lane & 3;
+  *reinterpret_cast<float2 *>(C + g * ldc + c0 + 2 * t) = make_float2(s * d[0], s * d[1]);
+  *reinterpret_cast<float2 *>(C + (g + 8) * ldc + c0 + 2 * t) = make_float2(s * d[2], s * d[3]);
+}
+
 // T = (I + Mk)^{-1} for the strictly lower 64 x 64 Mk (fp32, row stride kLdMk),
 // in 16 x 16 blocks: T_aa = (I + Mk_aa)^{-1} by forward substitution (one
 // column per thread), then T_ab = -T_aa sum_{b<=c<a} Mk_ac T_cb level by level
-// (a - b = 1, 2, 3), one block entry per thread and step.  Writes T (zero above
+// (a - b = 1, 2, 3) as tensor-core block products.  Writes T (zero above
 // the diagonal) to Tf; P is scratch for three 16 x 16 blocks.  All threads.
 __device__ __forceinline__ void ut_inverse(const float *Mk, float *Tf, float *Pb, int tid) {
   if (tid < 64) {  // diagonal blocks: block a, column j
@@ -179,28 +223,26 @@ __device__ __forceinline__ void ut_inverse(const float *Mk, float *Tf, float *Pb
     for (int i = 0; i < 16; ++i) Tf[(o + i) * kLdMk + o + j] = t[i];
   }
   __syncthreads();
-  // level d: blocks (a, a - d), a = d .. 3; P = sum_c Mk_ac T_c,a-d, then T = -T_aa P
+  // level d: blocks (a, a - d), a = d .. 3; P = sum_c Mk_ac T_c,a-d, then T = -T_aa P,
+  // each 16 x 16 block product as mma.sync passes: warp 2 blk + nh takes columns
+  // 8 nh .. 8 nh + 7 of block blk of the level
+  const int warp = tid >> 5;
   for (int dlev = 1; dlev <= 3; ++dlev) {
     const int nblk = 4 - dlev;
-    for (int e = tid; e < nblk * 256; e += kThreads) {
-      const int blk = e >> 8, i = (e >> 4) & 15, j = e & 15;
-      const int a = blk + dlev, bcol = a - dlev;
-      float acc = 0.f;
+    const bool mine = warp < 2 * nblk;
+    const int blk = warp >> 1, nh = warp & 1;
+    const int a = blk + dlev, bcol = a - dlev;
+    if (mine) {
+      float acc[4] = {0.f, 0.f, 0.f, 0.f};
       for (int cb = bcol; cb < a; ++cb)
-#pragma unroll
-        for (int l = 0; l < 16; ++l)
-          acc = fmaf(Mk[(a * 16 + i) * kLdMk + cb * 16 + l], Tf[(cb * 16 + l) * kLdMk + bcol * 16 + j], acc);
-      Pb[blk * 256 + i * 16 + j] = acc;
+        mma3_f32(acc, Mk, kLdMk, a * 16, cb * 16, Tf, kLdMk, cb * 16, bcol * 16 + 8 * nh, tid & 31);
+      store_tile(Pb + blk * 16 * kLdP, kLdP, 8 * nh, acc, 1.f, tid & 31);
     }
     __syncthreads();
-    for (int e = tid; e < nblk * 256; e += kThreads) {
-      const int blk = e >> 8, i = (e >> 4) & 15, j = e & 15;
-      const int a = blk + dlev, bcol = a - dlev;
-      float acc = 0.f;
-#pragma unroll
-      for (int l = 0; l < 16; ++l)
-        acc = fmaf(Tf[(a * 16 + i) * kLdMk + a * 16 + l], Pb[blk * 256 + l * 16 + j], acc);
-      Tf[(a * 16 + i) * kLdMk + bcol * 16 + j] = -acc;
+    if (mine) {
+      float acc[4] = {0.f, 0.f, 0.f, 0.f};
+      mma3_f32(acc, Tf, kLdMk, a * 16, a * 16, Pb + blk * 16 * kLdP, kLdP, 0, 8 * nh, tid & 31);
+      store_tile(Tf + a * 16 * kLdMk, kLdMk, bcol * 16 + 8 * nh, acc, -1.f, tid & 31);
     }
     __syncthreads();
   }
