@@ -400,23 +400,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();  // chunk staged; the previous chunk's MMAs are done
     fence_after();
 
-    // K^T (B of the state update) from the K rows of X, token groups split by
-    // warpgroup; cumulative gates (warp 3)
+    // K^T (B of the state update) from the K rows of X: the keys' core matrices
+    // (8 tokens x 8 dims, 16-byte rows) transposed into K^T's (8 dims x 8
+    // tokens) by ldmatrix.trans + stmatrix, four per warp instruction; warp w
+    // takes tiles 8 w .. 8 w + 7 (token group tile & 7, dim group tile >> 3).
+    // Cumulative gates (warp 3) follow.
     {
-      uint8_t *kt = smem + kOffKt;
-      const int r = lt;  // key row (d_k index)
+      const uint32_t xs_u = smem_u32(st), kt_u = smem_u32(smem + kOffKt);
 #pragma unroll
-      for (int q4 = 0; q4 < 2; ++q4) {
-        const int jg = wg * 2 + q4;
-        uint16_t e[8];
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          const int i = kC + jg * 8 + q;  // X row of the key of token jg*8+q
-          e[q] = *reinterpret_cast<const uint16_t *>(st + (i >> 3) * kSboX + (r >> 3) * kLbo + (i & 7) * 16 +
-                                                     (r & 7) * 2);
-        }
-        *reinterpret_cast<uint4 *>(kt + (r >> 3) * kSboKt + jg * kLbo + (r & 7) * 16) =
-            make_uint4(pack2(e[0], e[1]), pack2(e[2], e[3]), pack2(e[4], e[5]), pack2(e[6], e[7]));
+      for (int q = 0; q < 2; ++q) {
+        const int tile = warp * 8 + q * 4 + (lane >> 3), jg = tile & 7, dg = tile >> 3, row = lane & 7;
+        const uint32_t src = xs_u + ((kC >> 3) + jg) * kSboX + dg * kLbo + row * 16;
+        const uint32_t dst = kt_u + dg * kSboKt + jg * kLbo + row * 16;
+        uint32_t r0, r1, r2, r3;
+        asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+                     : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(src));
+        asm volatile("stmatrix.sync.aligned.m8n8.x4.shared.b16 [%0], {%1,%2,%3,%4};"
+                     ::"r"(dst), "r"(r0), "r"(r1), "r"(r2), "r"(r3) : "memory");
       }
     }
     if (warp == 3) {
