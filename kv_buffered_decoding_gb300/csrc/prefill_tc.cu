@@ -118,24 +118,18 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
 }
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
-// x = hi + lo, both bf16 (hi = round(x), lo = round(x - hi))
-__device__ __forceinline__ void split_bf16(float x, uint16_t &hi, uint16_t &lo) {
-  const __nv_bfloat16 h = __float2bfloat16_rn(x);
-  hi = __bfloat16_as_ushort(h);
-  lo = __bfloat16_as_ushort(__float2bfloat16_rn(x - __bfloat162float(h)));
+// x = hi + lo, both bf16 (hi = round(x), lo = round(x - hi), to nearest even), two
+// values at once: {x0, x1} (x0 in the low half) as hi and lo pairs
+__device__ __forceinline__ void split_pair(float x0, float x1, uint32_t &hi, uint32_t &lo) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
+  const float2 hf = __bfloat1622float2(h);
+  const __nv_bfloat162 l = __floats2bfloat162_rn(x0 - hf.x, x1 - hf.y);
+  hi = *reinterpret_cast<const uint32_t *>(&h);
+  lo = *reinterpret_cast<const uint32_t *>(&l);
 }
-__device__ __forceinline__ uint32_t pack2(uint16_t a, uint16_t b) { return (uint32_t)a | ((uint32_t)b << 16); }
-
-// 16 fp32 values -> bf16 hi and lo parts packed in pairs (8 words each)
 __device__ __forceinline__ void split16(const float (&x)[16], uint32_t (&hi)[8], uint32_t (&lo)[8]) {
 #pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    uint16_t h0, l0, h1, l1;
-    split_bf16(x[2 * j], h0, l0);
-    split_bf16(x[2 * j + 1], h1, l1);
-    hi[j] = pack2(h0, h1);
-    lo[j] = pack2(l0, l1);
-  }
+  for (int j = 0; j < 8; ++j) split_pair(x[2 * j], x[2 * j + 1], hi[j], lo[j]);
 }
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
   asm volatile(
@@ -164,13 +158,6 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16
 // as bf16 hi + lo parts (x ~ hi + lo to about 16 significant bits); a product is
 // hi*hi + hi*lo + lo*hi with fp32 accumulation, the lo*lo term dropped, as the
 // chunk's other tensor-core products take their non-bf16 operands.
-__device__ __forceinline__ void split_pair(float x0, float x1, uint32_t &hi, uint32_t &lo) {
-  uint16_t h0, l0, h1, l1;
-  split_bf16(x0, h0, l0);
-  split_bf16(x1, h1, l1);
-  hi = pack2(h0, h1);
-  lo = pack2(l0, l1);
-}
 __device__ __forceinline__ void mma_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
   asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
       "{%8,%9}, {%0,%1,%2,%3};"
@@ -549,16 +536,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int q = 0; q < 16; ++q) x[q] = jq + q <= i ? Tf[i * kLdMk + jq + q] : 0.f;
         uint8_t *tp = smem + kOffTp;
+        uint32_t hi[8], lo[8];
+        split16(x, hi, lo);
 #pragma unroll
         for (int g2 = 0; g2 < 2; ++g2) {
-          uint16_t hh[8], ll[8];
-#pragma unroll
-          for (int q = 0; q < 8; ++q) split_bf16(x[g2 * 8 + q], hh[q], ll[q]);
           const int off = (i >> 3) * kSboKt + (jq / 8 + g2) * kLbo + (i & 7) * 16;
-          *reinterpret_cast<uint4 *>(tp + off) =
-              make_uint4(pack2(hh[0], hh[1]), pack2(hh[2], hh[3]), pack2(hh[4], hh[5]), pack2(hh[6], hh[7]));
+          *reinterpret_cast<uint4 *>(tp + off) = make_uint4(hi[4 * g2], hi[4 * g2 + 1], hi[4 * g2 + 2], hi[4 * g2 + 3]);
           *reinterpret_cast<uint4 *>(tp + kMqBytes + off) =
-              make_uint4(pack2(ll[0], ll[1]), pack2(ll[2], ll[3]), pack2(ll[4], ll[5]), pack2(ll[6], ll[7]));
+              make_uint4(lo[4 * g2], lo[4 * g2 + 1], lo[4 * g2 + 2], lo[4 * g2 + 3]);
         }
       }
       fence_async_smem();
