@@ -7,6 +7,7 @@
 // so launches from several host threads are safe and each device is configured
 // once.
 #include <atomic>
+#include <cstdint>
 #include <map>
 #include <mutex>
 #include <utility>
@@ -72,8 +73,9 @@ cudaError_t sm_count(int *out) {
   return cudaDeviceGetAttribute(out, cudaDevAttrMultiProcessorCount, dev);
 }
 
-cudaError_t encode_state_map(StateMap *out, float *state, uint64_t rows) {
-  static_assert(sizeof(StateMap) == sizeof(CUtensorMap) && alignof(StateMap) >= 64, "tensor map");
+namespace {
+// the driver's tensor-map encoder, looked up once (null when unavailable)
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
   static std::once_flag once;
   std::call_once(once, [] {
@@ -84,6 +86,13 @@ cudaError_t encode_state_map(StateMap *out, float *state, uint64_t rows) {
         q == cudaDriverEntryPointSuccess)
       encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
   });
+  return encode;
+}
+}  // namespace
+
+cudaError_t encode_state_map(StateMap *out, float *state, uint64_t rows) {
+  static_assert(sizeof(StateMap) == sizeof(CUtensorMap) && alignof(StateMap) >= 64, "tensor map");
+  const PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
   if (!encode || !state || rows == 0 || rows > (1ull << 31)) return cudaErrorNotSupported;
   const cuuint64_t dims[2] = {128, rows};
   const cuuint64_t strides[1] = {128 * sizeof(float)};
@@ -93,6 +102,30 @@ cudaError_t encode_state_map(StateMap *out, float *state, uint64_t rows) {
                       strides, box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B_ATOM_32B,
                       CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorNotSupported;
+}
+
+cudaError_t encode_prefill_maps(PrefillMaps *out, const TokenIO &io, int Hk, int Hv) {
+  static_assert(sizeof(TmaMap) == sizeof(CUtensorMap) && alignof(TmaMap) >= 64, "tensor map");
+  const PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
+  const uint64_t tokens = (uint64_t)(io.nrows > 0 ? io.nrows : 0) * (uint64_t)(io.T > 0 ? io.T : 0);
+  if (!encode || tokens == 0 || tokens >= (1ull << 31) || Hk <= 0 || Hv <= 0) return cudaErrorNotSupported;
+  auto one = [&](TmaMap *m, const void *base, int heads, cuuint32_t box0, CUtensorMapSwizzle sw, bool f32) {
+    if (!base || (reinterpret_cast<uintptr_t>(base) & 15) != 0) return false;
+    const cuuint64_t esz = f32 ? 4 : 2;
+    const cuuint64_t dims[3] = {128, (cuuint64_t)heads, tokens};
+    const cuuint64_t strides[2] = {128 * esz, (cuuint64_t)heads * 128 * esz};  // bytes
+    const cuuint32_t box[3] = {box0, 1, 64};
+    const cuuint32_t elem[3] = {1, 1, 1};
+    return encode(reinterpret_cast<CUtensorMap *>(m),
+                  f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+                  const_cast<void *>(base), dims, strides, box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  };
+  const bool ok = one(&out->q, io.q, Hk, 64, CU_TENSOR_MAP_SWIZZLE_128B, false) &&
+                  one(&out->k, io.k, Hk, 64, CU_TENSOR_MAP_SWIZZLE_128B, false) &&
+                  one(&out->v, io.v, Hv, 128, CU_TENSOR_MAP_SWIZZLE_NONE, false) &&
+                  one(&out->o, io.o, Hv, 128, CU_TENSOR_MAP_SWIZZLE_NONE, true);
+  return ok ? cudaSuccess : cudaErrorNotSupported;
 }
 
 int prefill_first_wait_polls() { return g_prefill_polls.load(std::memory_order_relaxed); }

@@ -414,7 +414,7 @@ int kvb_prefill(kvb_pool *p, int32_t B, int32_t L, const int32_t *req_ids,
     if (lengths && (lengths[b] < 0 || lengths[b] > L)) return KVB_E_ARG;
   }
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  const kvb::TokenIO io{q, k, v, log_g, beta, o, L, 0};
+  const kvb::TokenIO io{q, k, v, log_g, beta, o, L, 0, B};
   const int32_t flags = from_zero ? kvb::kFlagFromZero : 0;
   for (int32_t base = 0; base < B; base += kvb::kMaxRows) {
     const int32_t cnt = B - base < kvb::kMaxRows ? B - base : kvb::kMaxRows;

@@ -99,7 +99,22 @@ struct TokenIO {
   float *o;
   int T;     // tokens per row (1 for decode)
   int lmax;  // most tokens any row of the launch stages in shared memory
+  int nrows = 0;  // rows of the token buffers (prefill: the whole batch), for tensor maps
 };
+
+// TMA tensor maps of a prefill's token buffers at d = 128, each viewed as {128
+// elements, heads, nrows * T tokens}: q and k (bf16) copied in {64, 1, 64}
+// boxes with the 128-byte swizzle (the K-major layout the tensor cores read), v
+// (bf16) in {128, 1, 64} boxes as plain rows, o (fp32, Hv heads) written in
+// {128, 1, 64} boxes.  Encoding fails (cudaErrorNotSupported) for buffers that
+// are not 16-byte aligned or too many tokens for the coordinates.
+struct alignas(64) TmaMap {
+  uint64_t opaque[16];
+};
+struct PrefillMaps {
+  TmaMap q, k, v, o;
+};
+cudaError_t encode_prefill_maps(PrefillMaps *out, const TokenIO &io, int Hk, int Hv);
 
 // kErrTimeout: a bounded wait on the tensor cores gave up (the launch's outputs
 // and states are invalid); kErrTimeoutDrain: the wait that follows, for the
@@ -177,7 +192,7 @@ cudaError_t launch_flush_stream(const PoolView &P, const RowBatch &rows, int var
                                 cudaStream_t stream);
 // Chunked prefill on tcgen05 / TMEM (bf16 inputs, d = 128).
 cudaError_t launch_prefill_tc(const PoolView &P, const RowBatch &rows, const TokenIO &io,
-                              int variant, cudaStream_t stream);
+                              const PrefillMaps &maps, int variant, cudaStream_t stream);
 // Chunked prefill of rows.r[i].n prompt tokens per row (io.T = padded length).
 cudaError_t launch_prefill(const PoolView &P, const RowBatch &rows, const TokenIO &io,
                            int variant, int dtype, int d, cudaStream_t stream);

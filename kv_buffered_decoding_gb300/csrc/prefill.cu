@@ -510,7 +510,13 @@ cudaError_t prefill_variant(const PoolView &P, const RowBatch &rows, const Token
 cudaError_t launch_prefill(const PoolView &P, const RowBatch &rows, const TokenIO &io,
                            int variant, int dtype, int d, cudaStream_t stream) {
   if (rows.count <= 0) return cudaSuccess;
-  if (dtype == 1 && d == 128) return launch_prefill_tc(P, rows, io, variant, stream);
+  if (dtype == 1 && d == 128 && (reinterpret_cast<uintptr_t>(io.o) & 15) == 0) {
+    // the tensor-core kernel moves its tiles by TMA: 16-byte aligned buffers
+    // only; others take the mma.sync kernel below
+    PrefillMaps maps;
+    if (encode_prefill_maps(&maps, io, P.Hk, P.Hv) == cudaSuccess)
+      return launch_prefill_tc(P, rows, io, maps, variant, stream);
+  }
   if (dtype == 0) return prefill_variant<float>(P, rows, io, variant, d, stream);
   if (dtype == 1) return prefill_variant<__nv_bfloat16>(P, rows, io, variant, d, stream);
   return kUnsupported;

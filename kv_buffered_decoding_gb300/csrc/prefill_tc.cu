@@ -2,8 +2,8 @@
 // bf16 inputs at d = 128.
 //
 // Same chunk algebra as prefill.cu ("KVBuffer: IO-aware Serving for Linear
-// Attention", abstract: chunkwise computation; the delta-rule chunk form with
-// the UT transform), chunk C = 64, per (request, value head) CTA:
+// Attention", abstract: chunkwise computation; the delta-rule chunk form),
+// chunk C = 64, per (request, value head) CTA:
 //   Y = [Q; K] S,  Mq = scale e^{A_i-A_j} q_i.k_j (j <= i),  Mk = beta_i e^{A_i-A_j} k_i.k_j (j < i)
 //   (I + Mk) U = R,  R_i = beta_i (v_i - e^{A_i} S^T k_i)       (U = V unless the delta rule)
 //   O = e^{A} scale Y_q + Mq U,   S <- e^{A_{C-1}} S + K^T diag(w) U
@@ -14,14 +14,16 @@
 //   G   = X K^T            (A: X, B: the K rows of X; exact for bf16 inputs)
 //   O^T = e^A Y_q^T + U^T Mq^T   (A: U^T parts from TMEM, B: Mq parts from smem)
 //   S^T <- e^{A_C} S^T + (wU)^T K   (A: (wU)^T parts from TMEM, B: K^T from smem)
-// leave every per-column quantity (R, the substitution, U, the output column,
-// the state column) in the registers of the thread that owns that column: the
-// UT transform T = (I + Mk)^{-1} is built in 16 x 16 blocks by all threads and
-// applied as one more tensor-core product, U^T = R^T T^T.
+// leave every per-column quantity (R, U, the output column, the state column)
+// with the threads that own that column: (I + Mk) U = R is solved in fp32 by a
+// blocked forward substitution, warpgroup a owning tokens 16 a .. 16 a + 15.
 // Operands that are not exact in bf16 (S, U, wU, Mq) enter as hi + lo bf16
 // parts (about 16 significant bits; the lo x lo product is dropped), with fp32
-// accumulation in TMEM.  Single-thread MMA issue, completion via tcgen05.commit
-// on an mbarrier; every wait is bounded and a timeout sets the error word.
+// accumulation in TMEM.  Q, K, V arrive by TMA (Q and K in the K-major layout
+// with the 128-byte swizzle), outputs leave by TMA from a staging tile.  MMAs
+// are issued by single threads, completion via tcgen05.commit on mbarriers;
+// every wait on the tensor cores or the copies is bounded and a timeout sets
+// the error word.
 #include "kvb_device.cuh"
 
 namespace kvb {
@@ -33,32 +35,36 @@ constexpr uint32_t kColS = 0;     // S^T fp32            [128 lanes x 128]
 constexpr uint32_t kColP = 128;   // A parts: S^T hi/lo (64 + 64), later U^T hi/lo, (wU)^T hi/lo (32 each)
 constexpr uint32_t kColY = 256;   // Y^T fp32 (tokens: 0..63 q, 64..127 k); O^T in 0..63
 constexpr uint32_t kColG = 384;   // G fp32 (lane = token of [Q;K], column = key token); then U^T
+constexpr uint32_t kColX = 448;   // a further 64-column accumulator (part products issued apart)
 constexpr uint32_t kTmemCols = 512;
 // shared memory (bytes)
-constexpr int kXBytes = 2 * kC * kD * 2;        // [Q;K] bf16, core-matrix K-major (32 KB)
+constexpr int kXBytes = 2 * kC * kD * 2;        // [Q;K] bf16, K-major, 128-byte swizzle (32 KB)
+constexpr int kXHalf = kXBytes / 2;             // X: [d_k half][token of [Q;K]][64 elements]
 constexpr int kVBytes = kC * kD * 2;            // V bf16 [token][column] (16 KB)
 constexpr int kGBytes = 2 * kC * 4;             // log-gate, beta
 constexpr int kStage = (kXBytes + kVBytes + kGBytes + 1023) / 1024 * 1024;
-constexpr int kKtBytes = kD * kC * 2;           // K^T bf16, core-matrix K-major (16 KB)
+constexpr int kKtBytes = kD * kC * 2;           // K^T bf16, core-matrix K-major (16 KB), two buffers
 constexpr int kMqBytes = kC * kC * 2;           // one bf16 part of Mq (8 KB)
 constexpr int kLdMk = kC + 4;                   // fp32 rows of Mk
 constexpr int kMkBytes = kC * kLdMk * 4;
 constexpr int kOffKt = 2 * kStage;
-constexpr int kOffMq = kOffKt + kKtBytes;       // [2 parts]
+constexpr int kOffMq = kOffKt + 2 * kKtBytes;   // [2 parts]
 constexpr int kOffMk = kOffMq + 2 * kMqBytes;
-constexpr int kLdP = 20;                        // fp32 row stride of the block-product scratch
-constexpr int kOffR = kOffMk + kMkBytes;        // scratch for the block products, fp32 [3][16][kLdP]
-constexpr int kRBytes = 3 * 16 * kLdP * 4;
-constexpr int kOffTf = kOffR + kRBytes;         // T = (I + Mk)^-1, fp32 [64][68]
-constexpr int kOffTp = kOffTf + kMkBytes;       // T as bf16 hi / lo parts, core-matrix K-major
-constexpr int kOffA = kOffTp + 2 * kMqBytes;    // Acum, e^A, w: [3][C]
-constexpr int kSmemBytes = kOffA + 3 * kC * 4;
+constexpr int kOffMkp = kOffMk + kMkBytes;      // Mk as bf16 hi / lo parts, core-matrix K-major
+constexpr int kOffA = kOffMkp + 2 * kMqBytes;   // gates per chunk parity: [2][Acum, e^A, w][C]
+constexpr int kSmemBytes = kOffA + 2 * 3 * kC * 4;
 // core-matrix strides (bytes): 8 rows x 16 bytes per core matrix, k groups adjacent
 constexpr uint32_t kLbo = 128;
-constexpr uint32_t kSboX = (kD / 8) * 128;      // X: 128 dk per row group
 constexpr uint32_t kSboKt = (kC / 8) * 128;     // K^T and Mq: 64 tokens per row group
 static_assert(kSmemBytes <= 227 * 1024, "one CTA's shared memory");
 static_assert(kStage % 1024 == 0 && kKtBytes % 1024 == 0 && kMqBytes % 1024 == 0, "alignment");
+// completion barriers, one completion each per chunk (so phase parity = chunk &
+// 1): G, Y (first products), O and S (second products), P + b (the delta rule's
+// products Mk_{.,b} U_b, b = 0 .. 2); then the two stages' landing barriers
+// (TMA bytes), one completion per use.  O completes on three commits (its part
+// products are issued by three threads into separate accumulators), the others
+// on one.
+constexpr int kBarG = 0, kBarY = 1, kBarO = 2, kBarS = 3, kBarP = 4, kBarF = 7, kBars = 9;
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -68,6 +74,13 @@ __device__ __forceinline__ uint32_t smem_u32(const void *p) {
 __device__ __forceinline__ uint64_t sdesc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
   return (uint64_t)((addr >> 4) & 0x3FFF) | ((uint64_t)((lbo >> 4) & 0x3FFF) << 16) |
          ((uint64_t)((sbo >> 4) & 0x3FFF) << 32) | ((uint64_t)1 << 46);
+}
+// K-major operand with the 128-byte swizzle (rows of 64 bf16 = 128 bytes, 8-row
+// atoms of 1024 bytes, atom-aligned): stride between row groups 1024, leading
+// offset unused; a K step of 16 elements advances the start by 32 bytes
+__device__ __forceinline__ uint64_t sdesc_sw128(uint32_t addr) {
+  return (uint64_t)((addr >> 4) & 0x3FFF) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
+         ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
 }
 // instruction descriptor: bf16 x bf16 -> fp32, both K-major, M x N
 __host__ __device__ constexpr uint32_t idesc_bf16(int m, int n) {
@@ -154,91 +167,36 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16
       : "memory");
 }
 
-// Block products for the UT inverse on the tensor cores.  A fp32 value x enters
-// as bf16 hi + lo parts (x ~ hi + lo to about 16 significant bits); a product is
-// hi*hi + hi*lo + lo*hi with fp32 accumulation, the lo*lo term dropped, as the
-// chunk's other tensor-core products take their non-bf16 operands.
-__device__ __forceinline__ void mma_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
-  asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
-      "{%8,%9}, {%0,%1,%2,%3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+// named barrier `id` over `n` threads (whole warps): arrive without waiting, or wait
+__device__ __forceinline__ void named_arrive(int id, int n) {
+  asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(n) : "memory");
 }
-// d += A B for the 16 x 16 block of A at (ar, ac) (row stride lda) and the 16 x 8
-// block of B at (br, bc) (row stride ldb), both fp32 in shared memory; lane
-// (g, t) = (lane / 4, lane % 4) holds rows g, g + 8 and columns 2t, 2t + 1 of d
-__device__ __forceinline__ void mma3_f32(float (&d)[4], const float *A, int lda, int ar, int ac,
-                                         const float *B, int ldb, int br, int bc, int lane) {
-  const int g = lane >> 2, t = lane & 3;
-  uint32_t ah[4], al[4], bh[2], bl[2];
-  const float *a0 = A + (ar + g) * lda + ac + 2 * t, *a1 = a0 + 8 * lda;
-  split_pair(a0[0], a0[1], ah[0], al[0]);
-  split_pair(a1[0], a1[1], ah[1], al[1]);
-  split_pair(a0[8], a0[9], ah[2], al[2]);
-  split_pair(a1[8], a1[9], ah[3], al[3]);
-  const float *b0 = B + (br + 2 * t) * ldb + bc + g;
-  split_pair(b0[0], b0[ldb], bh[0], bl[0]);
-  split_pair(b0[8 * ldb], b0[9 * ldb], bh[1], bl[1]);
-  mma_16816(d, ah, bh[0], bh[1]);
-  mma_16816(d, ah, bl[0], bl[1]);
-  mma_16816(d, al, bh[0], bh[1]);
-}
-// the 16 x 8 tile d (times s) into C at columns c0 .. c0 + 7 (row stride ldc)
-__device__ __forceinline__ void store_tile(float *C, int ldc, int c0, const float (&d)[4], float s, int lane) {
-  const int g = lane >> 2, t = lane & 3;
-  *reinterpret_cast<float2 *>(C + g * ldc + c0 + 2 * t) = make_float2(s * d[0], s * d[1]);
-  *reinterpret_cast<float2 *>(C + (g + 8) * ldc + c0 + 2 * t) = make_float2(s * d[2], s * d[3]);
-}
+__device__ __forceinline__ void named_sync(int id, int n) { asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory"); }
 
-// T = (I + Mk)^{-1} for the strictly lower 64 x 64 Mk (fp32, row stride kLdMk),
-// in 16 x 16 blocks: T_aa = (I + Mk_aa)^{-1} by forward substitution (one
-// column per thread), then T_ab = -T_aa sum_{b<=c<a} Mk_ac T_cb level by level
-// (a - b = 1, 2, 3) as tensor-core block products.  Writes T (zero above
-// the diagonal) to Tf; P is scratch for three 16 x 16 blocks.  All threads.
-__device__ __forceinline__ void ut_inverse(const float *Mk, float *Tf, float *Pb, int tid) {
-  if (tid < 64) {  // diagonal blocks: block a, column j
-    const int a = tid >> 4, j = tid & 15, o = a * 16;
-    float t[16];
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      float acc = i == j ? 1.f : 0.f;
-#pragma unroll
-      for (int l = 0; l < i; ++l) acc = fmaf(-Mk[(o + i) * kLdMk + o + l], t[l], acc);
-      t[i] = i < j ? 0.f : acc;
-    }
-#pragma unroll
-    for (int i = 0; i < 16; ++i) Tf[(o + i) * kLdMk + o + j] = t[i];
-  }
-  __syncthreads();
-  // level d: blocks (a, a - d), a = d .. 3; P = sum_c Mk_ac T_c,a-d, then T = -T_aa P,
-  // each 16 x 16 block product as mma.sync passes: warp 2 blk + nh takes columns
-  // 8 nh .. 8 nh + 7 of block blk of the level
-  const int warp = tid >> 5;
-  for (int dlev = 1; dlev <= 3; ++dlev) {
-    const int nblk = 4 - dlev;
-    const bool mine = warp < 2 * nblk;
-    const int blk = warp >> 1, nh = warp & 1;
-    const int a = blk + dlev, bcol = a - dlev;
-    if (mine) {
-      float acc[4] = {0.f, 0.f, 0.f, 0.f};
-      for (int cb = bcol; cb < a; ++cb)
-        mma3_f32(acc, Mk, kLdMk, a * 16, cb * 16, Tf, kLdMk, cb * 16, bcol * 16 + 8 * nh, tid & 31);
-      store_tile(Pb + blk * 16 * kLdP, kLdP, 8 * nh, acc, 1.f, tid & 31);
-    }
-    __syncthreads();
-    if (mine) {
-      float acc[4] = {0.f, 0.f, 0.f, 0.f};
-      mma3_f32(acc, Tf, kLdMk, a * 16, a * 16, Pb + blk * 16 * kLdP, kLdP, 0, 8 * nh, tid & 31);
-      store_tile(Tf + a * 16 * kLdMk, kLdMk, bcol * 16 + 8 * nh, acc, -1.f, tid & 31);
-    }
-    __syncthreads();
-  }
+// TMA: a 3D box of a tensor map into shared memory, completing its bytes on mbar
+__device__ __forceinline__ void tma3d(uint32_t dst, const void *map, int x, int y, int z, uint32_t mbar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];"
+      ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(mbar) : "memory");
 }
-
-__device__ __forceinline__ void cp16(uint32_t dst, const void *src, bool valid) {
-  const int n = valid ? 16 : 0;
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src), "r"(n) : "memory");
+__device__ __forceinline__ void arrive_tx(uint32_t mbar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(mbar), "r"(bytes) : "memory");
 }
+// bulk copy shared -> global (16-byte aligned addresses, 16-byte multiple size),
+// tracked in this thread's bulk groups
+__device__ __forceinline__ void bulk_store(void *dst, uint32_t src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(src), "r"(bytes)
+               : "memory");
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// TMA: a 3D box of shared memory out to a tensor map (bulk group of this thread)
+__device__ __forceinline__ void tma3d_store(const void *map, int x, int y, int z, uint32_t src) {
+  asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%1, %2, %3}], [%4];"
+               ::"l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(src) : "memory");
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 __device__ __forceinline__ void cp4(uint32_t dst, const void *src, bool valid) {
   const int n = valid ? 4 : 0;
   asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;\n" ::"r"(dst), "l"(src), "r"(n) : "memory");
@@ -247,14 +205,14 @@ __device__ __forceinline__ void cp4(uint32_t dst, const void *src, bool valid) {
 template <int VARIANT>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_tc_kernel(const PoolView P, const __grid_constant__ RowBatch rows, const TokenIO io,
-                      int first_polls) {
+                      const __grid_constant__ PrefillMaps maps, int first_polls) {
   using KT = __nv_bfloat16;
   constexpr bool DELTA = VARIANT == kGatedDelta, GATED = VARIANT != kPlain;
   extern __shared__ __align__(1024) uint8_t smem[];
-  __shared__ uint64_t mbar_s;
+  __shared__ uint64_t mbar_s[kBars];
   __shared__ uint32_t tmem_s;
-  float *Acum = reinterpret_cast<float *>(smem + kOffA);
-  float *eA = Acum + kC, *wL = eA + kC;
+  // cumulative log-gates A, e^A and w = e^{A_{C-1} - A} of chunk cc
+  auto gates = [&](int cc) { return reinterpret_cast<float *>(smem + kOffA) + (cc & 1) * 3 * kC; };
   float *Mk = reinterpret_cast<float *>(smem + kOffMk);
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -268,11 +226,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int Tp = io.T;
   const int nchunks = (L + kC - 1) / kC;
   float *Sg = P.state + ((size_t)d.slot * P.Hv + h) * kD * kD;
-  const uint32_t mbar = smem_u32(&mbar_s);
+  const uint32_t mbar0 = smem_u32(&mbar_s[0]);  // barrier k at mbar0 + 8 k
   const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;  // this warp's TMEM lanes
 
   if (tid == 0) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(mbar));
+#pragma unroll
+    for (int k = 0; k < kBars; ++k)
+      asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(mbar0 + 8 * k), "r"(k == kBarO ? 3 : 1));
     asm volatile("fence.mbarrier_init.release.cluster;");
   }
   if (warp == 0) {
@@ -281,75 +241,54 @@ __global__ void __launch_bounds__(kThreads, 1)
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
   }
 
-  const KT *qg = static_cast<const KT *>(io.q);
-  const KT *kg = static_cast<const KT *>(io.k);
-  const KT *vg = static_cast<const KT *>(io.v);
-  // stage chunk c: q and k rows into X (core-matrix layout), v rows, gates
-  auto issue = [&](int c) {
-    uint8_t *st = smem + (c & 1) * kStage;
-    const uint32_t xs = smem_u32(st), vs = xs + kXBytes, gs = vs + kVBytes;
-    const int t0 = c * kC;
-    for (int idx = tid; idx < 2 * kC * 16; idx += kThreads) {  // 128 rows x 16 pieces of 8
-      const int i = idx >> 4, p = idx & 15;
-      const int tok = t0 + (i & (kC - 1));
-      const bool ok = tok < L;
-      const size_t row = b * Tp + (ok ? tok : L - 1);
-      const KT *src = (i < kC ? qg : kg) + (row * P.Hk + hq) * kD + p * 8;
-      cp16(xs + (i >> 3) * kSboX + p * kLbo + (i & 7) * 16, src, ok);
+  // stage chunk cc: q and k rows of the chunk by TMA into X (two d_k halves of
+  // 64 elements, 128-byte swizzle), v rows into V, the landing barrier of the
+  // stage counting the bytes (thread 64, which also sends the outputs staged in
+  // X two chunks earlier: those must have left first); gates and beta as plain
+  // copies, zero past the prompt (warps 2 and 3)
+  auto issue = [&](int cc) {
+    const uint32_t st_u = smem_u32(smem + (cc & 1) * kStage);
+    if (tid == 64) {
+      bulk_wait_read();
+      const uint32_t full = mbar0 + 8 * (kBarF + (cc & 1));
+      const int z = (int)(b * Tp + (size_t)cc * kC);  // first token row of the chunk
+      arrive_tx(full, kXBytes + kVBytes);
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf) {
+        tma3d(st_u + hf * kXHalf, &maps.q, hf * 64, hq, z, full);
+        tma3d(st_u + hf * kXHalf + kC * 128, &maps.k, hf * 64, hq, z, full);
+      }
+      tma3d(st_u + kXBytes, &maps.v, 0, h, z, full);
     }
-    for (int idx = tid; idx < kC * 16; idx += kThreads) {
-      const int j = idx >> 4, p = idx & 15;
-      const bool ok = t0 + j < L;
-      const size_t row = b * Tp + (ok ? t0 + j : L - 1);
-      cp16(vs + j * kD * 2 + p * 16, vg + (row * P.Hv + h) * kD + p * 8, ok);
-    }
-    if (tid < kC) {
-      const bool ok = t0 + tid < L;
-      const size_t row = b * Tp + (ok ? t0 + tid : L - 1);
-      if (GATED) cp4(gs + tid * 4, io.log_g + row * P.Hv + h, ok);
-      if (DELTA) cp4(gs + (kC + tid) * 4, io.beta + row * P.Hv + h, ok);
+    if (tid >= 64 && tid < 64 + kC) {
+      const int j = tid - 64;
+      const bool ok = cc * kC + j < L;
+      const size_t row = b * Tp + (ok ? cc * kC + j : L - 1);
+      const uint32_t gs = st_u + kXBytes + kVBytes;
+      if (GATED) cp4(gs + j * 4, io.log_g + row * P.Hv + h, ok);
+      if (DELTA) cp4(gs + (kC + j) * 4, io.beta + row * P.Hv + h, ok);
     }
     asm volatile("cp.async.commit_group;\n" ::: "memory");
   };
-  if (nchunks > 0) issue(0);
 
   fence_before();
   __syncthreads();
   fence_after();
   const uint32_t tmem = tmem_s;
+  int pending = -1;  // the chunk whose copies are issued and not yet waited for
+  if (nchunks > 0) {
+    issue(0);
+    pending = 0;
+  }
   const int lt = tid & 127;              // this thread's TMEM lane
   const int wg = tid >> 7;               // warpgroup: which quarter of each lane's columns
   const uint32_t my = tmem + lane_base;  // this thread's lane, column 0
   const int c = lt;                      // as a state column
   bool ok = true;
-  uint32_t phase = 0;
   // poll bound of the next completion wait: the first one may be capped by the
   // failure-path test hook (first_polls > 0), every later one has the default
   int polls = first_polls > 0 ? first_polls : kWaitPolls;
 
-  // e^A scale Y_q^T (the output accumulator), and e^{A_C} S^T (the state before
-  // its update), for this thread's lane
-  // (16-column rounds q0 .. q1 - 1 of each)
-  auto scale_y = [&](const float *eAv, int q0, int q1) {
-    uint32_t w[16];
-#pragma unroll 1
-    for (int q = q0; q < q1; ++q) {
-      tmem_ld16(my + kColY + q * 16, w);
-#pragma unroll
-      for (int j = 0; j < 16; ++j) w[j] = __float_as_uint(P.scale * eAv[q * 16 + j] * __uint_as_float(w[j]));
-      tmem_st16(my + kColY + q * 16, w);
-    }
-  };
-  auto scale_s = [&](float eL, int q0, int q1) {
-    uint32_t w[16];
-#pragma unroll 1
-    for (int q = q0; q < q1; ++q) {
-      tmem_ld16(my + kColS + q * 16, w);
-#pragma unroll
-      for (int j = 0; j < 16; ++j) w[j] = __float_as_uint(eL * __uint_as_float(w[j]));
-      tmem_st16(my + kColS + q * 16, w);
-    }
-  };
   // bf16 hi / lo parts of 16 state rows (16 r0 .. 16 r0 + 15) of column c into the
   // A region (the operand of Y^T = S^T X^T)
   auto put_parts16 = [&](const float (&x)[16], int r0) {
@@ -358,56 +297,32 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_st8(my + kColP + r0 * 8, hi);
     tmem_st8(my + kColP + 64 + r0 * 8, lo);
   };
-  // this warpgroup's 32 state rows of column c: fp32 into S^T, and their parts
-#pragma unroll 1
-  for (int q = 0; q < 2; ++q) {
-    const int r0 = wg * 2 + q;  // 16-row piece
-    float x[16];
-    uint32_t w[16];
-#pragma unroll
-    for (int j = 0; j < 16; ++j) {
-      x[j] = from_zero ? 0.f : Sg[(size_t)(r0 * 16 + j) * kD + c];
-      w[j] = __float_as_uint(x[j]);
-    }
-    tmem_st16(my + kColS + r0 * 16, w);
-    put_parts16(x, r0);
-  }
-  tmem_wait_st();
 
-  for (int ch = 0; ch < nchunks && ok; ++ch) {
-    uint8_t *st = smem + (ch & 1) * kStage;
-    const uint32_t xs = smem_u32(st);
-    const KT *vs = reinterpret_cast<const KT *>(st + kXBytes);
-    const float *gs = reinterpret_cast<const float *>(st + kXBytes + kVBytes);
-    const float *bs = gs + kC;
-    const int t0 = ch * kC;
-    asm volatile("cp.async.wait_group 0;\n" ::: "memory");
-    fence_async_smem();
-    fence_before();
-    __syncthreads();  // chunk staged; the previous chunk's MMAs are done
-    fence_after();
-
-    // K^T (B of the state update) from the K rows of X: the keys' core matrices
-    // (8 tokens x 8 dims, 16-byte rows) transposed into K^T's (8 dims x 8
-    // tokens) by ldmatrix.trans + stmatrix, four per warp instruction; warp w
-    // takes tiles 8 w .. 8 w + 7 (token group tile & 7, dim group tile >> 3).
-    // Cumulative gates (warp 3) follow.
-    {
-      const uint32_t xs_u = smem_u32(st), kt_u = smem_u32(smem + kOffKt);
+  // K^T of chunk cc (the B operand of its state update) from the K rows of its
+  // staged X, and its cumulative gates.  K^T: 8 x 8 tiles of the keys (8 tokens
+  // x 8 dims, 16-byte pieces of the swizzled rows: piece p of row t sits at
+  // p ^ (t & 7)) transposed into K^T's core matrices (8 dims x 8 tokens) by
+  // ldmatrix.trans + stmatrix, four per warp instruction; warp w takes tiles
+  // 8 w .. 8 w + 7 (token group tile & 7, dim group tile >> 3).  Gates: warp 3.
+  auto prep = [&](int cc) {
+    const uint8_t *stc = smem + (cc & 1) * kStage;
+    const uint32_t xs_u = smem_u32(stc), kt_u = smem_u32(smem + kOffKt + (cc & 1) * kKtBytes);
 #pragma unroll
-      for (int q = 0; q < 2; ++q) {
-        const int tile = warp * 8 + q * 4 + (lane >> 3), jg = tile & 7, dg = tile >> 3, row = lane & 7;
-        const uint32_t src = xs_u + ((kC >> 3) + jg) * kSboX + dg * kLbo + row * 16;
-        const uint32_t dst = kt_u + dg * kSboKt + jg * kLbo + row * 16;
-        uint32_t r0, r1, r2, r3;
-        asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
-                     : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(src));
-        asm volatile("stmatrix.sync.aligned.m8n8.x4.shared.b16 [%0], {%1,%2,%3,%4};"
-                     ::"r"(dst), "r"(r0), "r"(r1), "r"(r2), "r"(r3) : "memory");
-      }
+    for (int q = 0; q < 2; ++q) {
+      const int tile = warp * 8 + q * 4 + (lane >> 3), jg = tile & 7, dg = tile >> 3, row = lane & 7;
+      const uint32_t src =
+          xs_u + (dg >> 3) * kXHalf + (kC + jg * 8 + row) * 128 + (uint32_t)(((dg & 7) ^ row) << 4);
+      const uint32_t dst = kt_u + dg * kSboKt + jg * kLbo + row * 16;
+      uint32_t r0, r1, r2, r3;
+      asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+                   : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(src));
+      asm volatile("stmatrix.sync.aligned.m8n8.x4.shared.b16 [%0], {%1,%2,%3,%4};"
+                   ::"r"(dst), "r"(r0), "r"(r1), "r"(r2), "r"(r3) : "memory");
     }
     if (warp == 3) {
-      float a0 = GATED ? gs[lane] : 0.f, a1 = GATED ? gs[lane + 32] : 0.f;
+      const float *gsc = reinterpret_cast<const float *>(stc + kXBytes + kVBytes);
+      float *Acum = gates(cc), *eA = Acum + kC, *wL = eA + kC;
+      float a0 = GATED ? gsc[lane] : 0.f, a1 = GATED ? gsc[lane + 32] : 0.f;
 #pragma unroll
       for (int off = 1; off < 32; off <<= 1) {
         const float y0 = __shfl_up_sync(kFull, a0, off), y1 = __shfl_up_sync(kFull, a1, off);
@@ -425,37 +340,112 @@ __global__ void __launch_bounds__(kThreads, 1)
       wL[lane] = expf(AL - a0);
       wL[lane + 32] = expf(AL - a1);
     }
-    fence_async_smem();
-    fence_before();
-    __syncthreads();
-    fence_after();
-
-    // MMAs 1: G = X K^T (exact) and Y^T = S^T X^T (S^T as hi + lo parts)
-    if (tid == 0) {
-      const uint32_t idG = idesc_bf16(128, kC), idY = idesc_bf16(128, 2 * kC);
-#pragma unroll
-      for (int k0 = 0; k0 < kD; k0 += 16) {
-        const uint64_t a = sdesc(xs + (k0 / 8) * kLbo, kLbo, kSboX);
-        const uint64_t bk = sdesc(xs + (kC / 8) * kSboX + (k0 / 8) * kLbo, kLbo, kSboX);
-        mma_ss(tmem + kColG, a, bk, idG, k0 > 0);
+  };
+  // CTA-uniform: chunk cc's copies landed (bounded wait on the TMA bytes, then
+  // this thread's plain copies), visible to all; the rows past the prompt of a
+  // last, partial chunk are zeroed (the TMA brought whatever follows it)
+  auto land = [&](int cc) -> bool {
+    asm volatile("cp.async.wait_group 0;\n" ::: "memory");
+    ok = __syncthreads_and(mbar_wait(mbar0 + 8 * (kBarF + (cc & 1)), (cc >> 1) & 1)) != 0;
+    if (!ok) return false;
+    pending = -1;
+    const int nv = L - cc * kC;  // valid tokens of the chunk
+    if (nv < kC) {
+      uint8_t *stc = smem + (cc & 1) * kStage;
+      // per padded token: 4 X rows of 128 bytes (2 halves x Q, K), 1 V row of 256
+      for (int idx = tid; idx < (kC - nv) * 48; idx += kThreads) {
+        const int t = nv + idx / 48, pc = idx % 48;
+        uint8_t *dst = pc < 32 ? stc + (pc >> 4) * kXHalf + ((pc >> 3) & 1) * (kC * 128) + t * 128 + (pc & 7) * 16
+                               : stc + kXBytes + t * 256 + (pc - 32) * 16;
+        *reinterpret_cast<uint4 *>(dst) = make_uint4(0u, 0u, 0u, 0u);
       }
+      __syncthreads();
+    }
+    return true;
+  };
+  if (nchunks > 0 && land(0)) prep(0);
+  // this warpgroup's 32 state rows of column c: their parts (the operand of the
+  // first Y^T), and e^{A_{C-1}} S^T in fp32, the state ready for chunk 0's
+  // update (each chunk's decay is applied when its predecessor's parts are made)
+  {
+    __syncthreads();  // chunk 0's gates
+    const float eL = nchunks > 0 ? gates(0)[kC + kC - 1] : 1.f;
+#pragma unroll 1
+    for (int q = 0; q < 2; ++q) {
+      const int r0 = wg * 2 + q;  // 16-row piece
+      float x[16];
+      uint32_t w[16];
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        x[j] = from_zero ? 0.f : Sg[(size_t)(r0 * 16 + j) * kD + c];
+        w[j] = __float_as_uint(eL * x[j]);
+      }
+      tmem_st16(my + kColS + r0 * 16, w);
+      put_parts16(x, r0);
+    }
+    tmem_wait_st();
+  }
+  fence_async_smem();
+  fence_before();
+  __syncthreads();
+  fence_after();
+
+  // the barriers committed in the current chunk (a timeout drains on each)
+  uint32_t cmask = 0;
+  int ch_at = 0;  // the chunk the loop is in
+  // CTA-uniform bounded wait on barrier k of chunk ch (parity ch & 1)
+  auto wait_bar = [&](int k, int chn) -> bool {
+    ok = __syncthreads_and(mbar_wait(mbar0 + 8 * k, chn & 1, polls)) != 0;
+    polls = kWaitPolls;
+    fence_after();
+    return ok;
+  };
+
+  for (int ch = 0; ch < nchunks && ok; ++ch) {
+    ch_at = ch;
+    uint8_t *st = smem + (ch & 1) * kStage;
+    const uint32_t xs = smem_u32(st);
+    const KT *vs = reinterpret_cast<const KT *>(st + kXBytes);
+    const float *gs = reinterpret_cast<const float *>(st + kXBytes + kVBytes);
+    const float *bs = gs + kC;
+    const float *Acum = gates(ch), *eA = Acum + kC, *wL = eA + kC;
+    const int t0 = ch * kC;
+    // (chunk ch staged, its K^T and gates built, S^T's parts in TMEM, S^T
+    // already decayed by e^{A_{C-1}})
+
+    // MMAs 1, from two issuing threads: G = X K^T (exact; thread 0) and Y^T =
+    // S^T X^T (S^T as hi + lo parts; thread 32)
+    if (tid == 0) {
+      const uint32_t idG = idesc_bf16(128, kC);
+#pragma unroll
+      for (int ks = 0; ks < kD / 16; ++ks) {  // X rows: tokens of [Q;K]; the keys from row kC
+        const uint32_t xk = xs + (ks >> 2) * kXHalf + (ks & 3) * 32;
+        mma_ss(tmem + kColG, sdesc_sw128(xk), sdesc_sw128(xk + kC * 128), idG, ks > 0);
+      }
+      mma_commit(mbar0 + 8 * kBarG);
+    } else if (tid == 32) {
+      const uint32_t idY = idesc_bf16(128, 2 * kC);
 #pragma unroll
       for (int part = 0; part < 2; ++part)
 #pragma unroll
-        for (int k0 = 0; k0 < kD; k0 += 16) {
-          const uint64_t bx = sdesc(xs + (k0 / 8) * kLbo, kLbo, kSboX);
-          mma_ts(tmem + kColY, tmem + kColP + part * 64 + k0 / 2, bx, idY, part > 0 || k0 > 0);
+        for (int ks = 0; ks < kD / 16; ++ks) {
+          const uint64_t bx = sdesc_sw128(xs + (ks >> 2) * kXHalf + (ks & 3) * 32);
+          mma_ts(tmem + kColY, tmem + kColP + part * 64 + ks * 8, bx, idY, part > 0 || ks > 0);
         }
-      mma_commit(mbar);
+      mma_commit(mbar0 + 8 * kBarY);
     }
+    cmask = (1u << kBarG) | (1u << kBarY);
     // while the products run: the next chunk's copies (into the other stage, free
     // since the previous chunk finished)
-    if (ch + 1 < nchunks) issue(ch + 1);
-    ok = __syncthreads_and(mbar_wait(mbar, phase, polls)) != 0;  // CTA-uniform
+    if (ch + 1 < nchunks) {
+      issue(ch + 1);
+      pending = ch + 1;
+    }
+    // G: each thread waits by itself and starts its Gram rows; the CTA-wide
+    // check of this wait comes with the one on Y
+    const bool okG = mbar_wait(mbar0 + 8 * kBarG, ch & 1, polls);
     polls = kWaitPolls;
-    phase ^= 1;
     fence_after();
-    if (!ok) break;
 
     // Gram rows, key tokens split by warpgroup: thread (i, wg) builds entries
     // j = 16 wg .. 16 wg + 15 of row i of Mq (parts, smem) or Mk (fp32)
@@ -472,7 +462,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float Ai = Acum[i];
         float x[16];
 #pragma unroll
-        for (int j = 0; j < 16; ++j) x[j] = j0 + j <= i ? P.scale * expf(Ai - Acum[j0 + j]) * gr[j] : 0.f;
+        for (int j = 0; j < 16; ++j) x[j] = j0 + j <= i ? P.scale * __expf(Ai - Acum[j0 + j]) * gr[j] : 0.f;
         uint32_t hi[8], lo[8];
         split16(x, hi, lo);
         uint8_t *mq = smem + kOffMq;
@@ -483,109 +473,37 @@ __global__ void __launch_bounds__(kThreads, 1)
           *reinterpret_cast<uint4 *>(mq + kMqBytes + off) =
               make_uint4(lo[4 * q], lo[4 * q + 1], lo[4 * q + 2], lo[4 * q + 3]);
         }
-      } else if (DELTA) {  // Mk[i'][j] = beta_i' e^{A_i'-A_j} k_i'.k_j, j < i'
+      } else if (DELTA) {  // Mk[i'][j] = beta_i' e^{A_i'-A_j} k_i'.k_j, j < i': fp32 and parts
         const int ip = i - kC;
         const float Ai = Acum[ip], bi = bs[ip];
-#pragma unroll
-        for (int j = 0; j < 16; j += 4) {
-          const int jj = j0 + j;
-          float4 m4;
-          m4.x = jj < ip ? bi * expf(Ai - Acum[jj]) * gr[j] : 0.f;
-          m4.y = jj + 1 < ip ? bi * expf(Ai - Acum[jj + 1]) * gr[j + 1] : 0.f;
-          m4.z = jj + 2 < ip ? bi * expf(Ai - Acum[jj + 2]) * gr[j + 2] : 0.f;
-          m4.w = jj + 3 < ip ? bi * expf(Ai - Acum[jj + 3]) * gr[j + 3] : 0.f;
-          *reinterpret_cast<float4 *>(&Mk[ip * kLdMk + jj]) = m4;
-        }
-      }
-    }
-    // column c of R (delta rule), tokens 16 wg .. 16 wg + 15, as bf16 parts into
-    // TMEM: the A operand (R^T) of U^T = R^T T^T
-    if (DELTA) {
-      uint32_t w[16];
-      tmem_ld16(my + kColY + kC + wg * 16, w);
-      float r[16];
-#pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        const int jj = wg * 16 + j;
-        r[j] = bs[jj] * (__bfloat162float(vs[jj * kD + c]) - eA[jj] * __uint_as_float(w[j]));
-      }
-      uint32_t hi[8], lo[8];
-      split16(r, hi, lo);
-      tmem_st8(my + kColP + wg * 8, hi);
-      tmem_st8(my + kColP + 32 + wg * 8, lo);
-      tmem_wait_st();
-    }
-    fence_async_smem();
-    fence_before();
-    __syncthreads();  // Mk, Mq and R complete
-    fence_after();
-
-    // the UT transform: T = (I + Mk)^{-1} in blocks, its bf16 parts (B operand,
-    // rows i, k = j), then U^T = R^T T^T on the tensor cores into the G columns
-    if (DELTA) {
-      // meanwhile, while the first 64 threads invert the diagonal blocks:
-      // warpgroup 1 scales Y_q^T, warpgroups 2 and 3 the two halves of S^T
-      if (wg == 1) scale_y(eA, 0, 4);
-      if (wg >= 2) scale_s(eA[kC - 1], (wg - 2) * 4, (wg - 1) * 4);
-      if (wg >= 1) tmem_wait_st();
-      float *Tf = reinterpret_cast<float *>(smem + kOffTf);
-      ut_inverse(Mk, Tf, reinterpret_cast<float *>(smem + kOffR), tid);
-      if (tid < 4 * kC) {
-        const int i = tid >> 2, jq = (tid & 3) * 16;  // row i, 16 columns
         float x[16];
 #pragma unroll
-        for (int q = 0; q < 16; ++q) x[q] = jq + q <= i ? Tf[i * kLdMk + jq + q] : 0.f;
-        uint8_t *tp = smem + kOffTp;
+        for (int j = 0; j < 16; ++j) x[j] = j0 + j < ip ? bi * __expf(Ai - Acum[j0 + j]) * gr[j] : 0.f;
+#pragma unroll
+        for (int j = 0; j < 16; j += 4)
+          *reinterpret_cast<float4 *>(&Mk[ip * kLdMk + j0 + j]) = make_float4(x[j], x[j + 1], x[j + 2], x[j + 3]);
         uint32_t hi[8], lo[8];
         split16(x, hi, lo);
+        uint8_t *mkp = smem + kOffMkp;
 #pragma unroll
-        for (int g2 = 0; g2 < 2; ++g2) {
-          const int off = (i >> 3) * kSboKt + (jq / 8 + g2) * kLbo + (i & 7) * 16;
-          *reinterpret_cast<uint4 *>(tp + off) = make_uint4(hi[4 * g2], hi[4 * g2 + 1], hi[4 * g2 + 2], hi[4 * g2 + 3]);
-          *reinterpret_cast<uint4 *>(tp + kMqBytes + off) =
-              make_uint4(lo[4 * g2], lo[4 * g2 + 1], lo[4 * g2 + 2], lo[4 * g2 + 3]);
+        for (int q = 0; q < 2; ++q) {
+          const int off = (ip >> 3) * kSboKt + (wg * 2 + q) * kLbo + (ip & 7) * 16;
+          *reinterpret_cast<uint4 *>(mkp + off) = make_uint4(hi[4 * q], hi[4 * q + 1], hi[4 * q + 2], hi[4 * q + 3]);
+          *reinterpret_cast<uint4 *>(mkp + kMqBytes + off) =
+              make_uint4(lo[4 * q], lo[4 * q + 1], lo[4 * q + 2], lo[4 * q + 3]);
         }
       }
-      fence_async_smem();
-      fence_before();
-      __syncthreads();
-      fence_after();
-      if (tid == 0) {
-        const uint32_t idU = idesc_bf16(128, kC), tpa = smem_u32(smem + kOffTp);
-#pragma unroll
-        for (int combo = 0; combo < 3; ++combo) {
-          const int ra = combo == 2 ? 32 : 0;                   // R^T hi, hi, lo
-          const uint32_t tb = tpa + (combo == 1 ? kMqBytes : 0);  // T hi, lo, hi
-#pragma unroll
-          for (int k0 = 0; k0 < kC; k0 += 16)
-            mma_ts(tmem + kColG, tmem + kColP + ra + k0 / 2, sdesc(tb + (k0 / 8) * kLbo, kLbo, kSboKt), idU,
-                   combo > 0 || k0 > 0);
-        }
-        mma_commit(mbar);
-      }
-      ok = __syncthreads_and(mbar_wait(mbar, phase, polls)) != 0;  // CTA-uniform
-      polls = kWaitPolls;
-      phase ^= 1;
-      fence_after();
-      if (!ok) break;
     }
+    fence_async_smem();  // Mq, for the tensor cores
+    ok = __syncthreads_and(okG && mbar_wait(mbar0 + 8 * kBarY, ch & 1)) != 0;  // Mk, Mq complete
+    fence_after();
+    if (!ok) break;
 
+    bool okP = true;
     {
-      // column c of U (from the UT product, or V), 16 tokens at a time: U^T and
-      // (wU)^T parts into TMEM, the A operands of the second MMAs; without the
-      // delta rule the scaling of Y_q^T and S^T (done during the inverse with it)
-      // shares these warpgroups: 4 U chunks + 4 Y rounds + 8 S rounds
-      auto u_parts = [&](int q) {
-        float x[16];
-        if (DELTA) {
-          uint32_t w[16];
-          tmem_ld16(my + kColG + q * 16, w);
-#pragma unroll
-          for (int j = 0; j < 16; ++j) x[j] = __uint_as_float(w[j]);
-        } else {
-#pragma unroll
-          for (int j = 0; j < 16; ++j) x[j] = __bfloat162float(vs[(q * 16 + j) * kD + c]);
-        }
+      // U^T and (wU)^T parts (tokens 16 q .. 16 q + 15 of column c) into TMEM,
+      // the A operands of the second MMAs
+      auto u_parts = [&](float (&x)[16], int q) {
         uint32_t hi[8], lo[8];
         split16(x, hi, lo);
         tmem_st8(my + kColP + q * 8, hi);
@@ -596,76 +514,177 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_st8(my + kColP + 64 + q * 8, hi);
         tmem_st8(my + kColP + 96 + q * 8, lo);
       };
-      const float eL = eA[kC - 1];
       if (DELTA) {
-        u_parts(wg);
-      } else if (wg < 2) {
-        u_parts(2 * wg);
-        u_parts(2 * wg + 1);
-        scale_s(eL, wg, wg + 1);
-      } else if (wg == 2) {
-        scale_y(eA, 0, 4);
-        scale_s(eL, 2, 3);
-      } else {
-        scale_s(eL, 3, 8);
+        // (I + Mk) U = R by blocked forward substitution: warpgroup a holds R and
+        // then U for tokens 16 a .. 16 a + 15 of column c.  Its diagonal block is
+        // solved in fp32 in registers, each solved value updating the rows below
+        // it at once (a chain of 15 FMAs); the blocks below the diagonal enter as
+        // tensor-core products, D^T += U_b^T Mk_{.,b}^T (U_b^T parts from TMEM,
+        // Mk parts from smem; three part products, rows 16 (b + 1) .. 63 into the
+        // G columns), issued by thread 0 as soon as warpgroup b has written U_b's
+        // parts (named barrier 1 + b), each completing on barrier P + b.
+        float u[16];
+        {
+          uint32_t w[16];
+          tmem_ld16(my + kColY + kC + wg * 16, w);
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {  // R_i = beta_i (v_i - e^{A_i} S^T k_i)
+            const int jj = wg * 16 + j;
+            u[j] = bs[jj] * (__bfloat162float(vs[jj * kD + c]) - eA[jj] * __uint_as_float(w[j]));
+          }
+        }
+        auto solve = [&]() {
+          const float *md = Mk + (wg * 16) * kLdMk + wg * 16;
+#pragma unroll
+          for (int l = 0; l < 15; ++l)
+#pragma unroll
+            for (int i = l + 1; i < 16; ++i) u[i] = fmaf(-md[i * kLdMk + l], u[l], u[i]);
+        };
+        // thread 0: the products of block b (after fence_after)
+        auto issue_sub = [&](int bb) {
+          const int n0 = 16 * (bb + 1);
+          const uint32_t idP = idesc_bf16(128, kC - n0), mkp = smem_u32(smem + kOffMkp);
+#pragma unroll
+          for (int combo = 0; combo < 3; ++combo) {
+            const int ua = combo == 2 ? 32 : 0;                      // U_b^T hi, hi, lo
+            const uint32_t mb = mkp + (combo == 1 ? kMqBytes : 0);   // Mk hi, lo, hi
+            mma_ts(tmem + kColG + n0, tmem + kColP + ua + bb * 8,
+                   sdesc(mb + (n0 >> 3) * kSboKt + 2 * bb * kLbo, kLbo, kSboKt), idP, bb > 0 || combo > 0);
+          }
+          mma_commit(mbar0 + 8 * (kBarP + bb));
+        };
+        if (wg > 0) {  // the products of the blocks above
+          okP = mbar_wait(mbar0 + 8 * (kBarP + wg - 1), ch & 1);
+          fence_after();
+          uint32_t w[16];
+          tmem_ld16(my + kColG + wg * 16, w);
+#pragma unroll
+          for (int j = 0; j < 16; ++j) u[j] -= __uint_as_float(w[j]);
+        }
+        solve();
+        u_parts(u, wg);
+        if (wg < 3) {
+          tmem_wait_st();
+          fence_before();
+        }
+        if (wg == 0) {
+          named_sync(1, 128);  // U_0's parts in TMEM
+          if (warp == 0) {
+            if (lane == 0) {
+              fence_after();
+              issue_sub(0);
+            }
+            named_sync(2, 160);  // U_1's parts
+            if (lane == 0) {
+              fence_after();
+              issue_sub(1);
+            }
+            named_sync(3, 160);  // U_2's parts
+            if (lane == 0) {
+              fence_after();
+              issue_sub(2);
+            }
+          }
+        } else if (wg < 3) {
+          named_arrive(1 + wg, 160);
+        }
+      } else {  // U = V, tokens 16 wg .. 16 wg + 15
+        float x[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) x[j] = __bfloat162float(vs[(wg * 16 + j) * kD + c]);
+        u_parts(x, wg);
       }
     }
+    if (DELTA) cmask |= 7u << kBarP;
     tmem_wait_st();
     fence_before();
-    __syncthreads();
+    ok = __syncthreads_and(okP) != 0;  // the waits on the block products, checked CTA-wide
     fence_after();
+    if (!ok) break;
 
-    // MMAs 2: O^T += U^T Mq^T (three part products), S^T += (wU)^T K
-    if (tid == 0) {
-      const uint32_t idO = idesc_bf16(128, kC), idS = idesc_bf16(128, kD);
-      const uint32_t mq = smem_u32(smem + kOffMq), kt = smem_u32(smem + kOffKt);
+    // MMAs 2, from four issuing threads: the part products of U^T Mq^T (U^T hi
+    // Mq hi, U^T hi Mq lo, U^T lo Mq hi into the K half of Y (read by now), the
+    // G columns and the spare columns; threads 0, 32, 64) and S^T += (wU)^T K
+    // (thread 96); O^T = e^A scale Y_q^T + the three parts
+    if (tid == 0 || tid == 32 || tid == 64) {
+      const int combo = tid >> 5;
+      const uint32_t idO = idesc_bf16(128, kC), mq = smem_u32(smem + kOffMq);
+      const uint32_t dcol = combo == 0 ? kColY + kC : combo == 1 ? kColG : kColX;
+      const int ua = combo == 2 ? 32 : 0;
+      const uint32_t mb = mq + (combo == 1 ? kMqBytes : 0);
 #pragma unroll
-      for (int combo = 0; combo < 3; ++combo) {
-        const int ua = combo == 2 ? 32 : 0;                    // U^T hi, hi, lo
-        const uint32_t mb = mq + (combo == 1 ? kMqBytes : 0);  // Mq hi, lo, hi
-#pragma unroll
-        for (int k0 = 0; k0 < kC; k0 += 16)
-          mma_ts(tmem + kColY, tmem + kColP + ua + k0 / 2, sdesc(mb + (k0 / 8) * kLbo, kLbo, kSboKt),
-                 idO, 1);
-      }
+      for (int k0 = 0; k0 < kC; k0 += 16)
+        mma_ts(tmem + dcol, tmem + kColP + ua + k0 / 2, sdesc(mb + (k0 / 8) * kLbo, kLbo, kSboKt), idO, k0 > 0);
+      mma_commit(mbar0 + 8 * kBarO);
+    } else if (tid == 96) {
+      const uint32_t idS = idesc_bf16(128, kD), kt = smem_u32(smem + kOffKt + (ch & 1) * kKtBytes);
 #pragma unroll
       for (int part = 0; part < 2; ++part)
 #pragma unroll
         for (int k0 = 0; k0 < kC; k0 += 16)
           mma_ts(tmem + kColS, tmem + kColP + 64 + part * 32 + k0 / 2,
                  sdesc(kt + (k0 / 8) * kLbo, kLbo, kSboKt), idS, 1);
-      mma_commit(mbar);
+      mma_commit(mbar0 + 8 * kBarS);
     }
-    ok = __syncthreads_and(mbar_wait(mbar, phase, polls)) != 0;  // CTA-uniform
-    polls = kWaitPolls;
-    phase ^= 1;
-    fence_after();
-    if (!ok) break;
+    cmask |= (1u << kBarO) | (1u << kBarS);
+    // while they run: the next chunk's K^T (the other buffer) and gates (this
+    // chunk's are no longer read)
+    if (ch + 1 < nchunks) {
+      if (!land(ch + 1)) break;
+      prep(ch + 1);
+    }
+    if (!wait_bar(kBarO, ch)) break;
 
-    // outputs (tokens 16 wg .. 16 wg + 15 of column c) and the next chunk's S^T
-    // parts (state rows 32 wg .. 32 wg + 31)
+    // outputs (tokens 16 wg .. 16 wg + 15 of column c, the sum of the three
+    // part products) into a staging tile [token][column] over this chunk's X
+    // (read by now), leaving by one TMA store (thread 64), or one bulk copy of
+    // 512 bytes per prompt token for a last, partial chunk; then the next
+    // chunk's S^T parts (state rows 32 wg .. 32 wg + 31)
     {
-      uint32_t w[16];
+      uint32_t w[16], w1[16];
+      float o[16];
       tmem_ld16(my + kColY + wg * 16, w);
+      tmem_ld16(my + kColY + kC + wg * 16, w1);
 #pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        const int i = wg * 16 + j;
-        if (t0 + i < L) io.o[((b * Tp + t0 + i) * P.Hv + h) * kD + c] = __uint_as_float(w[j]);
-      }
-      if (ch + 1 < nchunks) {
-#pragma unroll 1
-        for (int q = 0; q < 2; ++q) {
-          const int r0 = wg * 2 + q;
-          uint32_t w16[16];
-          tmem_ld16(my + kColS + r0 * 16, w16);
-          float x[16];
+      for (int j = 0; j < 16; ++j)
+        o[j] = fmaf(P.scale * eA[wg * 16 + j], __uint_as_float(w[j]), __uint_as_float(w1[j]));
+      tmem_ld16(my + kColG + wg * 16, w);
+      tmem_ld16(my + kColX + wg * 16, w1);
+      float *ost = reinterpret_cast<float *>(st);
 #pragma unroll
-          for (int j = 0; j < 16; ++j) x[j] = __uint_as_float(w16[j]);
-          put_parts16(x, r0);
-        }
-        tmem_wait_st();
-      }
+      for (int j = 0; j < 16; ++j)
+        ost[(wg * 16 + j) * kD + c] = o[j] + (__uint_as_float(w[j]) + __uint_as_float(w1[j]));
+      fence_async_smem();
     }
+    if (!wait_bar(kBarS, ch)) break;
+    if (t0 + kC <= L) {
+      if (tid == 64) tma3d_store(&maps.o, 0, h, (int)(b * Tp + t0), xs);
+    } else if (tid < L - t0) {
+      bulk_store(io.o + ((b * Tp + t0 + tid) * P.Hv + h) * kD, xs + tid * kD * 4, kD * 4);
+    }
+    if (ch + 1 < nchunks) {
+      // the next chunk's S^T parts, and its decay e^{A_{C-1}} applied to S^T
+      const float eLn = gates(ch + 1)[kC + kC - 1];
+#pragma unroll 1
+      for (int q = 0; q < 2; ++q) {
+        const int r0 = wg * 2 + q;
+        uint32_t w16[16];
+        tmem_ld16(my + kColS + r0 * 16, w16);
+        float x[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          x[j] = __uint_as_float(w16[j]);
+          w16[j] = __float_as_uint(eLn * x[j]);
+        }
+        put_parts16(x, r0);
+        tmem_st16(my + kColS + r0 * 16, w16);
+      }
+      tmem_wait_st();
+    }
+    fence_async_smem();  // the next stage's copies and K^T, for the tensor cores
+    fence_before();
+    __syncthreads();
+    fence_after();
   }
 
   if (ok) {
@@ -678,10 +697,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     if (tid == 0) record_error(P.err, kErrTimeout, d.req, h);
-    // the products that timed out may still be running: one more bounded wait on
-    // their commit (phase already advanced) before TMEM is released; if that
-    // gives up too, the more severe kind replaces the first one
-    const bool drained = mbar_wait(mbar, phase ^ 1);
+    // the products and copies that timed out may still be running: one more
+    // bounded wait on the last commit and on the copies in flight before TMEM
+    // and shared memory are released; if that gives up too, the more severe
+    // kind replaces the first one
+    bool drained = true;
+    for (int k = 0; k < kBarF; ++k)
+      if (cmask & (1u << k)) drained = mbar_wait(mbar0 + 8 * k, ch_at & 1) && drained;
+    if (pending >= 0) drained = mbar_wait(mbar0 + 8 * (kBarF + (pending & 1)), (pending >> 1) & 1) && drained;
     if (!drained && tid == 0) {
       atomicExch(&P.err[0], (int32_t)kErrTimeoutDrain);
       P.err[1] = d.req;
@@ -689,6 +712,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
   asm volatile("cp.async.wait_group 0;\n" ::: "memory");
+  bulk_wait_all();  // this thread's output copies
   fence_before();
   __syncthreads();
   fence_after();
@@ -698,13 +722,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 }  // namespace
 
 cudaError_t launch_prefill_tc(const PoolView &P, const RowBatch &rows, const TokenIO &io,
-                              int variant, cudaStream_t stream) {
+                              const PrefillMaps &maps, int variant, cudaStream_t stream) {
   if (rows.count <= 0) return cudaSuccess;
   dim3 grid(P.Hv, rows.count);
   auto run = [&](auto kernel) -> cudaError_t {
     cudaError_t e = ensure_smem((const void *)kernel, kSmemBytes);
     if (e != cudaSuccess) return e;
-    kernel<<<grid, kThreads, kSmemBytes, stream>>>(P, rows, io, prefill_first_wait_polls());
+    kernel<<<grid, kThreads, kSmemBytes, stream>>>(P, rows, io, maps, prefill_first_wait_polls());
     return cudaGetLastError();
   };
   switch (variant) {
