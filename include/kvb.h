@@ -332,9 +332,10 @@ int kvb_get_error(kvb_pool *pool, kvb_stream_t stream, int32_t *detail);
 
 /* Testing hook for the device-side failure path (host only, process-wide).
    The tensor-core prefill (bf16, d = 128) waits for its tensor-core products
-   with bounded polls.  This caps the first such wait of every CTA of later
-   kvb_prefill launches at `polls` polls (0 restores the default bound, about
-   2^20 polls), so a test can make that wait run out without any fault: the CTA
+   and copies with bounded polls.  This caps the first wait on its products in
+   every CTA of later kvb_prefill launches at `polls` non-blocking polls (0
+   restores the default bound of 2^16 blocking polls, each up to about a
+   microsecond), so a test can make that wait run out without any fault: the CTA
    records kind 2 in the error word, waits with the full bound for the products
    still in flight, releases its tensor memory and returns, and the context
    stays usable.  KVB_E_ARG for polls < 0. */

@@ -34,8 +34,8 @@ constexpr int kC = 64, kD = 128, kThreads = 512;  // four warpgroups share every
 constexpr uint32_t kColS = 0;     // S^T fp32            [128 lanes x 128]
 constexpr uint32_t kColP = 128;   // A parts: S^T hi/lo (64 + 64), later U^T hi/lo, (wU)^T hi/lo (32 each)
 constexpr uint32_t kColY = 256;   // Y^T fp32 (tokens: 0..63 q, 64..127 k); O^T in 0..63
-constexpr uint32_t kColG = 384;   // G fp32 (lane = token of [Q;K], column = key token); then U^T
-constexpr uint32_t kColX = 448;   // a further 64-column accumulator (part products issued apart)
+constexpr uint32_t kColD = 384;   // the delta rule's block products; then an output part product
+constexpr uint32_t kColG = 448;   // G fp32 (lane = token of [Q;K], column = key token), a chunk ahead
 constexpr uint32_t kTmemCols = 512;
 // shared memory (bytes)
 constexpr int kXBytes = 2 * kC * kD * 2;        // [Q;K] bf16, K-major, 128-byte swizzle (32 KB)
@@ -51,8 +51,9 @@ constexpr int kOffKt = 2 * kStage;
 constexpr int kOffMq = kOffKt + 2 * kKtBytes;   // [2 parts]
 constexpr int kOffMk = kOffMq + 2 * kMqBytes;
 constexpr int kOffMkp = kOffMk + kMkBytes;      // Mk as bf16 hi / lo parts, core-matrix K-major
-constexpr int kOffA = kOffMkp + 2 * kMqBytes;   // gates per chunk parity: [2][Acum, e^A, w][C]
-constexpr int kSmemBytes = kOffA + 2 * 3 * kC * 4;
+constexpr int kGateF = 8 * kC;                   // floats of one chunk's gate tables (see gates())
+constexpr int kOffA = kOffMkp + 2 * kMqBytes;   // gate tables per chunk parity
+constexpr int kSmemBytes = kOffA + 2 * kGateF * 4;
 // core-matrix strides (bytes): 8 rows x 16 bytes per core matrix, k groups adjacent
 constexpr uint32_t kLbo = 128;
 constexpr uint32_t kSboKt = (kC / 8) * 128;     // K^T and Mq: 64 tokens per row group
@@ -61,9 +62,9 @@ static_assert(kStage % 1024 == 0 && kKtBytes % 1024 == 0 && kMqBytes % 1024 == 0
 // completion barriers, one completion each per chunk (so phase parity = chunk &
 // 1): G, Y (first products), O and S (second products), P + b (the delta rule's
 // products Mk_{.,b} U_b, b = 0 .. 2); then the two stages' landing barriers
-// (TMA bytes), one completion per use.  O completes on three commits (its part
-// products are issued by three threads into separate accumulators), the others
-// on one.
+// (TMA bytes), one completion per use.  G is issued a chunk ahead (its k-th
+// completion is chunk k's).  O completes on two commits (its part products are
+// issued by two threads into separate accumulators), the others on one.
 constexpr int kBarG = 0, kBarY = 1, kBarO = 2, kBarS = 3, kBarP = 4, kBarF = 7, kBars = 9;
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
@@ -99,17 +100,25 @@ __device__ __forceinline__ void mma_ts(uint32_t d, uint32_t a, uint64_t b, uint3
 __device__ __forceinline__ void mma_commit(uint32_t mbar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(mbar));
 }
-// Bounded wait on an mbarrier phase: at most `polls` polls (the default is about
-// 50 ms); false on timeout.
-constexpr int kWaitPolls = 1 << 20;
+// Bounded wait on an mbarrier phase: at most `polls` polls, false on timeout.
+// try_wait lets the hardware suspend the thread until the phase completes (or a
+// short time limit, about a microsecond, passes), so waiting warps wake at once
+// and take no issue slots meanwhile; the default bound is some tens of ms.  A
+// capped wait (fewer polls: the failure-path test hook) polls without
+// suspending, so that it gives up after that many looks.
+constexpr int kWaitPolls = 1 << 16;
 __device__ __forceinline__ bool mbar_wait(uint32_t mbar, uint32_t parity, int polls = kWaitPolls) {
   for (int it = 0; it < polls; ++it) {
     uint32_t done;
-    asm volatile("{\n\t.reg .pred p;\n\tmbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-                 "selp.u32 %0, 1, 0, p;\n\t}"
-                 : "=r"(done) : "r"(mbar), "r"(parity));
+    if (polls < kWaitPolls)
+      asm volatile("{\n\t.reg .pred p;\n\tmbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+                   "selp.u32 %0, 1, 0, p;\n\t}"
+                   : "=r"(done) : "r"(mbar), "r"(parity) : "memory");
+    else
+      asm volatile("{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+                   "selp.u32 %0, 1, 0, p;\n\t}"
+                   : "=r"(done) : "r"(mbar), "r"(parity) : "memory");
     if (done) return true;
-    __nanosleep(32);
   }
   return false;
 }
@@ -211,8 +220,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ __align__(1024) uint8_t smem[];
   __shared__ uint64_t mbar_s[kBars];
   __shared__ uint32_t tmem_s;
-  // cumulative log-gates A, e^A and w = e^{A_{C-1} - A} of chunk cc
-  auto gates = [&](int cc) { return reinterpret_cast<float *>(smem + kOffA) + (cc & 1) * 3 * kC; };
+  // gate tables of chunk cc: the cumulative log-gates A, e^A, w = e^{A_{C-1} - A},
+  // F_i = e^{A_i - A_{16 (i / 16)}} and E_{a,j} = e^{A_{16 a} - A_j} (a = 0 .. 3),
+  // so that e^{A_i - A_j} = F_i E_{i / 16, j} (each factor spans at most one
+  // 16-token block of growth, or is a decay)
+  auto gates = [&](int cc) { return reinterpret_cast<float *>(smem + kOffA) + (cc & 1) * kGateF; };
   float *Mk = reinterpret_cast<float *>(smem + kOffMk);
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -232,7 +244,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (tid == 0) {
 #pragma unroll
     for (int k = 0; k < kBars; ++k)
-      asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(mbar0 + 8 * k), "r"(k == kBarO ? 3 : 1));
+      asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(mbar0 + 8 * k), "r"(k == kBarO ? 2 : 1));
     asm volatile("fence.mbarrier_init.release.cluster;");
   }
   if (warp == 0) {
@@ -276,6 +288,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   fence_after();
   const uint32_t tmem = tmem_s;
   int pending = -1;  // the chunk whose copies are issued and not yet waited for
+  int gpend = -1;    // the chunk whose G is issued and not yet waited for
   if (nchunks > 0) {
     issue(0);
     pending = 0;
@@ -285,9 +298,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t my = tmem + lane_base;  // this thread's lane, column 0
   const int c = lt;                      // as a state column
   bool ok = true;
-  // poll bound of the next completion wait: the first one may be capped by the
-  // failure-path test hook (first_polls > 0), every later one has the default
-  int polls = first_polls > 0 ? first_polls : kWaitPolls;
+  // poll bound of the waits on the products: those of the first chunk may be
+  // capped by the failure-path test hook (first_polls > 0), later ones have the
+  // default
+  const int cap = first_polls > 0 ? first_polls : kWaitPolls;
+  auto polls_at = [&](int chn) { return chn == 0 ? cap : kWaitPolls; };
 
   // bf16 hi / lo parts of 16 state rows (16 r0 .. 16 r0 + 15) of column c into the
   // A region (the operand of Y^T = S^T X^T)
@@ -303,7 +318,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // x 8 dims, 16-byte pieces of the swizzled rows: piece p of row t sits at
   // p ^ (t & 7)) transposed into K^T's core matrices (8 dims x 8 tokens) by
   // ldmatrix.trans + stmatrix, four per warp instruction; warp w takes tiles
-  // 8 w .. 8 w + 7 (token group tile & 7, dim group tile >> 3).  Gates: warp 3.
+  // 8 w .. 8 w + 7 (token group tile & 7, dim group tile >> 3).  Gate tables: warps 4 .. 7.
   auto prep = [&](int cc) {
     const uint8_t *stc = smem + (cc & 1) * kStage;
     const uint32_t xs_u = smem_u32(stc), kt_u = smem_u32(smem + kOffKt + (cc & 1) * kKtBytes);
@@ -319,9 +334,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       asm volatile("stmatrix.sync.aligned.m8n8.x4.shared.b16 [%0], {%1,%2,%3,%4};"
                    ::"r"(dst), "r"(r0), "r"(r1), "r"(r2), "r"(r3) : "memory");
     }
-    if (warp == 3) {
+    if (warp >= 4 && warp < 8) {  // gate tables: each of warps 4 .. 7 scans the gates and fills a share
       const float *gsc = reinterpret_cast<const float *>(stc + kXBytes + kVBytes);
-      float *Acum = gates(cc), *eA = Acum + kC, *wL = eA + kC;
+      float *Acum = gates(cc), *eA = Acum + kC, *wL = eA + kC, *F = wL + kC, *E = F + kC;
       float a0 = GATED ? gsc[lane] : 0.f, a1 = GATED ? gsc[lane + 32] : 0.f;
 #pragma unroll
       for (int off = 1; off < 32; off <<= 1) {
@@ -332,13 +347,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       a1 += __shfl_sync(kFull, a0, 31);
-      const float AL = __shfl_sync(kFull, a1, 31);
-      Acum[lane] = a0;
-      Acum[lane + 32] = a1;
-      eA[lane] = expf(a0);
-      eA[lane + 32] = expf(a1);
-      wL[lane] = expf(AL - a0);
-      wL[lane + 32] = expf(AL - a1);
+      if (warp == 4) {
+        Acum[lane] = a0;
+        Acum[lane + 32] = a1;
+        eA[lane] = expf(a0);
+        eA[lane + 32] = expf(a1);
+      } else if (warp == 5) {
+        const float AL = __shfl_sync(kFull, a1, 31);
+        wL[lane] = expf(AL - a0);
+        wL[lane + 32] = expf(AL - a1);
+        F[lane] = expf(a0 - __shfl_sync(kFull, a0, lane & 16));
+        F[lane + 32] = expf(a1 - __shfl_sync(kFull, a1, lane & 16));
+      } else {
+        const int a = (warp - 6) * 2;  // E rows a, a + 1 (A_{16 a}: lane 16 a of the token scan)
+        const float B0 = __shfl_sync(kFull, a < 2 ? a0 : a1, 0), B1 = __shfl_sync(kFull, a < 2 ? a0 : a1, 16);
+        E[a * kC + lane] = expf(B0 - a0);
+        E[a * kC + lane + 32] = expf(B0 - a1);
+        E[(a + 1) * kC + lane] = expf(B1 - a0);
+        E[(a + 1) * kC + lane + 32] = expf(B1 - a1);
+      }
     }
   };
   // CTA-uniform: chunk cc's copies landed (bounded wait on the TMA bytes, then
@@ -359,11 +386,28 @@ __global__ void __launch_bounds__(kThreads, 1)
                                : stc + kXBytes + t * 256 + (pc - 32) * 16;
         *reinterpret_cast<uint4 *>(dst) = make_uint4(0u, 0u, 0u, 0u);
       }
+      fence_async_smem();  // the zeros, for the tensor cores (G is issued next)
       __syncthreads();
     }
     return true;
   };
-  if (nchunks > 0 && land(0)) prep(0);
+  // G = X K^T of chunk cc (exact; thread 64, after cc landed), into the G columns
+  auto issue_g = [&](int cc) {
+    if (tid == 64) {
+      const uint32_t xg = smem_u32(smem + (cc & 1) * kStage), idG = idesc_bf16(128, kC);
+#pragma unroll
+      for (int ks = 0; ks < kD / 16; ++ks) {  // X rows: tokens of [Q;K]; the keys from row kC
+        const uint32_t xk = xg + (ks >> 2) * kXHalf + (ks & 3) * 32;
+        mma_ss(tmem + kColG, sdesc_sw128(xk), sdesc_sw128(xk + kC * 128), idG, ks > 0);
+      }
+      mma_commit(mbar0 + 8 * kBarG);
+    }
+    gpend = cc;
+  };
+  if (nchunks > 0 && land(0)) {
+    issue_g(0);
+    prep(0);
+  }
   // this warpgroup's 32 state rows of column c: their parts (the operand of the
   // first Y^T), and e^{A_{C-1}} S^T in fp32, the state ready for chunk 0's
   // update (each chunk's decay is applied when its predecessor's parts are made)
@@ -395,8 +439,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   int ch_at = 0;  // the chunk the loop is in
   // CTA-uniform bounded wait on barrier k of chunk ch (parity ch & 1)
   auto wait_bar = [&](int k, int chn) -> bool {
-    ok = __syncthreads_and(mbar_wait(mbar0 + 8 * k, chn & 1, polls)) != 0;
-    polls = kWaitPolls;
+    ok = __syncthreads_and(mbar_wait(mbar0 + 8 * k, chn & 1, polls_at(chn))) != 0;
     fence_after();
     return ok;
   };
@@ -408,22 +451,35 @@ __global__ void __launch_bounds__(kThreads, 1)
     const KT *vs = reinterpret_cast<const KT *>(st + kXBytes);
     const float *gs = reinterpret_cast<const float *>(st + kXBytes + kVBytes);
     const float *bs = gs + kC;
-    const float *Acum = gates(ch), *eA = Acum + kC, *wL = eA + kC;
+    const float *Acum = gates(ch), *eA = Acum + kC, *wL = eA + kC, *Fg = wL + kC, *Eg = Fg + kC;
     const int t0 = ch * kC;
     // (chunk ch staged, its K^T and gates built, S^T's parts in TMEM, S^T
     // already decayed by e^{A_{C-1}})
 
-    // MMAs 1, from two issuing threads: G = X K^T (exact; thread 0) and Y^T =
-    // S^T X^T (S^T as hi + lo parts; thread 32)
-    if (tid == 0) {
-      const uint32_t idG = idesc_bf16(128, kC);
+    // G (issued with the previous chunk): each thread waits by itself (the
+    // CTA-wide check of this wait comes with the one on Y) and takes its 16
+    // entries before this chunk's products are issued, since a TMEM load waits
+    // for the tensor core's products in flight
+    const int j0 = wg * 16;
+    float gr[16];
+    const bool okG = mbar_wait(mbar0 + 8 * kBarG, ch & 1, polls_at(ch));
+    gpend = -1;
+    fence_after();
+    {
+      uint32_t w[16];
+      tmem_ld16(my + kColG + j0, w);
 #pragma unroll
-      for (int ks = 0; ks < kD / 16; ++ks) {  // X rows: tokens of [Q;K]; the keys from row kC
-        const uint32_t xk = xs + (ks >> 2) * kXHalf + (ks & 3) * 32;
-        mma_ss(tmem + kColG, sdesc_sw128(xk), sdesc_sw128(xk + kC * 128), idG, ks > 0);
-      }
-      mma_commit(mbar0 + 8 * kBarG);
-    } else if (tid == 32) {
+      for (int j = 0; j < 16; ++j) gr[j] = __uint_as_float(w[j]);
+    }
+    fence_before();
+    if (warp == 1)  // every warp has its G entries (named barrier 4)
+      named_sync(4, kThreads);
+    else
+      named_arrive(4, kThreads);
+
+    // MMAs 1 (thread 32): Y^T = S^T X^T (S^T as hi + lo parts)
+    if (tid == 32) {
+      fence_after();
       const uint32_t idY = idesc_bf16(128, 2 * kC);
 #pragma unroll
       for (int part = 0; part < 2; ++part)
@@ -434,35 +490,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       mma_commit(mbar0 + 8 * kBarY);
     }
-    cmask = (1u << kBarG) | (1u << kBarY);
+    cmask = 1u << kBarY;
     // while the products run: the next chunk's copies (into the other stage, free
     // since the previous chunk finished)
     if (ch + 1 < nchunks) {
       issue(ch + 1);
       pending = ch + 1;
     }
-    // G: each thread waits by itself and starts its Gram rows; the CTA-wide
-    // check of this wait comes with the one on Y
-    const bool okG = mbar_wait(mbar0 + 8 * kBarG, ch & 1, polls);
-    polls = kWaitPolls;
-    fence_after();
-
     // Gram rows, key tokens split by warpgroup: thread (i, wg) builds entries
-    // j = 16 wg .. 16 wg + 15 of row i of Mq (parts, smem) or Mk (fp32)
+    // j = 16 wg .. 16 wg + 15 of row i of Mq (parts, smem) or Mk (fp32 and parts)
     {
-      const int i = lt, j0 = wg * 16;
-      float gr[16];
-      {
-        uint32_t w[16];
-        tmem_ld16(my + kColG + j0, w);
-#pragma unroll
-        for (int j = 0; j < 16; ++j) gr[j] = __uint_as_float(w[j]);
-      }
+      const int i = lt;
       if (i < kC) {  // Mq[i][j] = scale e^{A_i-A_j} q_i.k_j, j <= i
-        const float Ai = Acum[i];
+        const float sF = P.scale * Fg[i];
+        const float *Er = Eg + (i >> 4) * kC + j0;
         float x[16];
 #pragma unroll
-        for (int j = 0; j < 16; ++j) x[j] = j0 + j <= i ? P.scale * __expf(Ai - Acum[j0 + j]) * gr[j] : 0.f;
+        for (int j = 0; j < 16; ++j) x[j] = j0 + j <= i ? sF * Er[j] * gr[j] : 0.f;
         uint32_t hi[8], lo[8];
         split16(x, hi, lo);
         uint8_t *mq = smem + kOffMq;
@@ -475,10 +519,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       } else if (DELTA) {  // Mk[i'][j] = beta_i' e^{A_i'-A_j} k_i'.k_j, j < i': fp32 and parts
         const int ip = i - kC;
-        const float Ai = Acum[ip], bi = bs[ip];
+        const float bF = bs[ip] * Fg[ip];
+        const float *Er = Eg + (ip >> 4) * kC + j0;
         float x[16];
 #pragma unroll
-        for (int j = 0; j < 16; ++j) x[j] = j0 + j < ip ? bi * __expf(Ai - Acum[j0 + j]) * gr[j] : 0.f;
+        for (int j = 0; j < 16; ++j) x[j] = j0 + j < ip ? bF * Er[j] * gr[j] : 0.f;
 #pragma unroll
         for (int j = 0; j < 16; j += 4)
           *reinterpret_cast<float4 *>(&Mk[ip * kLdMk + j0 + j]) = make_float4(x[j], x[j + 1], x[j + 2], x[j + 3]);
@@ -495,7 +540,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     fence_async_smem();  // Mq, for the tensor cores
-    ok = __syncthreads_and(okG && mbar_wait(mbar0 + 8 * kBarY, ch & 1)) != 0;  // Mk, Mq complete
+    ok = __syncthreads_and(okG && mbar_wait(mbar0 + 8 * kBarY, ch & 1, polls_at(ch))) != 0;  // Mk, Mq complete
     fence_after();
     if (!ok) break;
 
@@ -548,16 +593,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int combo = 0; combo < 3; ++combo) {
             const int ua = combo == 2 ? 32 : 0;                      // U_b^T hi, hi, lo
             const uint32_t mb = mkp + (combo == 1 ? kMqBytes : 0);   // Mk hi, lo, hi
-            mma_ts(tmem + kColG + n0, tmem + kColP + ua + bb * 8,
+            mma_ts(tmem + kColD + n0, tmem + kColP + ua + bb * 8,
                    sdesc(mb + (n0 >> 3) * kSboKt + 2 * bb * kLbo, kLbo, kSboKt), idP, bb > 0 || combo > 0);
           }
           mma_commit(mbar0 + 8 * (kBarP + bb));
         };
         if (wg > 0) {  // the products of the blocks above
-          okP = mbar_wait(mbar0 + 8 * (kBarP + wg - 1), ch & 1);
+          okP = mbar_wait(mbar0 + 8 * (kBarP + wg - 1), ch & 1, polls_at(ch));
           fence_after();
           uint32_t w[16];
-          tmem_ld16(my + kColG + wg * 16, w);
+          tmem_ld16(my + kColD + wg * 16, w);
 #pragma unroll
           for (int j = 0; j < 16; ++j) u[j] -= __uint_as_float(w[j]);
         }
@@ -602,19 +647,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     fence_after();
     if (!ok) break;
 
-    // MMAs 2, from four issuing threads: the part products of U^T Mq^T (U^T hi
-    // Mq hi, U^T hi Mq lo, U^T lo Mq hi into the K half of Y (read by now), the
-    // G columns and the spare columns; threads 0, 32, 64) and S^T += (wU)^T K
-    // (thread 96); O^T = e^A scale Y_q^T + the three parts
-    if (tid == 0 || tid == 32 || tid == 64) {
-      const int combo = tid >> 5;
+    // MMAs 2, from three issuing threads: the part products of U^T Mq^T (U^T hi
+    // Mq hi into the K half of Y (read by now; thread 0), U^T hi Mq lo + U^T lo
+    // Mq hi into the D columns (thread 32)) and S^T += (wU)^T K (thread 96);
+    // O^T = e^A scale Y_q^T + the two accumulators
+    if (tid == 0 || tid == 32) {
       const uint32_t idO = idesc_bf16(128, kC), mq = smem_u32(smem + kOffMq);
-      const uint32_t dcol = combo == 0 ? kColY + kC : combo == 1 ? kColG : kColX;
-      const int ua = combo == 2 ? 32 : 0;
-      const uint32_t mb = mq + (combo == 1 ? kMqBytes : 0);
+      const uint32_t dcol = tid == 0 ? kColY + kC : kColD;
 #pragma unroll
-      for (int k0 = 0; k0 < kC; k0 += 16)
-        mma_ts(tmem + dcol, tmem + kColP + ua + k0 / 2, sdesc(mb + (k0 / 8) * kLbo, kLbo, kSboKt), idO, k0 > 0);
+      for (int combo = tid == 0 ? 0 : 1; combo < (tid == 0 ? 1 : 3); ++combo) {
+        const int ua = combo == 2 ? 32 : 0;                    // U^T hi, hi, lo
+        const uint32_t mb = mq + (combo == 1 ? kMqBytes : 0);  // Mq hi, lo, hi
+#pragma unroll
+        for (int k0 = 0; k0 < kC; k0 += 16)
+          mma_ts(tmem + dcol, tmem + kColP + ua + k0 / 2, sdesc(mb + (k0 / 8) * kLbo, kLbo, kSboKt), idO,
+                 combo == 2 || k0 > 0);
+      }
       mma_commit(mbar0 + 8 * kBarO);
     } else if (tid == 96) {
       const uint32_t idS = idesc_bf16(128, kD), kt = smem_u32(smem + kOffKt + (ch & 1) * kKtBytes);
@@ -631,6 +679,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // chunk's are no longer read)
     if (ch + 1 < nchunks) {
       if (!land(ch + 1)) break;
+      issue_g(ch + 1);  // the G columns were read by this chunk's Gram rows
       prep(ch + 1);
     }
     if (!wait_bar(kBarO, ch)) break;
@@ -648,12 +697,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int j = 0; j < 16; ++j)
         o[j] = fmaf(P.scale * eA[wg * 16 + j], __uint_as_float(w[j]), __uint_as_float(w1[j]));
-      tmem_ld16(my + kColG + wg * 16, w);
-      tmem_ld16(my + kColX + wg * 16, w1);
+      tmem_ld16(my + kColD + wg * 16, w);
       float *ost = reinterpret_cast<float *>(st);
 #pragma unroll
-      for (int j = 0; j < 16; ++j)
-        ost[(wg * 16 + j) * kD + c] = o[j] + (__uint_as_float(w[j]) + __uint_as_float(w1[j]));
+      for (int j = 0; j < 16; ++j) ost[(wg * 16 + j) * kD + c] = o[j] + __uint_as_float(w[j]);
       fence_async_smem();
     }
     if (!wait_bar(kBarS, ch)) break;
@@ -704,6 +751,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool drained = true;
     for (int k = 0; k < kBarF; ++k)
       if (cmask & (1u << k)) drained = mbar_wait(mbar0 + 8 * k, ch_at & 1) && drained;
+    if (gpend >= 0) drained = mbar_wait(mbar0 + 8 * kBarG, gpend & 1) && drained;
     if (pending >= 0) drained = mbar_wait(mbar0 + 8 * (kBarF + (pending & 1)), (pending >> 1) & 1) && drained;
     if (!drained && tid == 0) {
       atomicExch(&P.err[0], (int32_t)kErrTimeoutDrain);
