@@ -125,13 +125,13 @@ def test_prefill_errors():
 
 def test_prefill_wait_timeout_reports_and_recovers():
     """The tensor-core prefill waits for its tensor-core products with bounded polls.
-    A test hook caps the first wait of every CTA at one poll, so it runs out while
-    the products are still in flight: each CTA records a timeout (kind 2) in the
-    error word, waits with the full bound for those products, releases its tensor
-    memory and returns; nothing faults.  The same context then runs a normal
-    prefill that matches the recurrence.  The prompt is one chunk, so the first wait
-    follows the products' issue directly (with a second chunk, the copies of that
-    chunk are issued in between, and the products may be done by then)."""
+    A test hook caps every wait on the products of a CTA's first chunk at one
+    non-blocking poll, so one of them runs out while its products are still in
+    flight (the delta rule's block products are issued only after the first
+    block's solve, right before the next warpgroup looks): each CTA records a
+    timeout (kind 2) in the error word, waits with the full bound for the products
+    and copies in flight, releases its tensor memory and returns; nothing faults.
+    The same context then runs a normal prefill that matches the recurrence."""
     kvb = kvb_mod()
     layer = I.Layer(I.GATED_DELTA, 2, 4, 128, 128, "bf16", qk_dist="l2norm")
     B, L = 2, 50
