@@ -257,7 +257,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   // 64 elements, 128-byte swizzle), v rows into V, the landing barrier of the
   // stage counting the bytes (thread 64, which also sends the outputs staged in
   // X two chunks earlier: those must have left first); gates and beta as plain
-  // copies, zero past the prompt (warps 2 and 3)
+  // copies, zero past the prompt (64 threads from kGateTid: under the delta rule
+  // warpgroup 3, which prepares the next chunk by itself)
+  constexpr int kGateTid = DELTA ? 384 : 64;
   auto issue = [&](int cc) {
     const uint32_t st_u = smem_u32(smem + (cc & 1) * kStage);
     if (tid == 64) {
@@ -272,8 +274,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tma3d(st_u + kXBytes, &maps.v, 0, h, z, full);
     }
-    if (tid >= 64 && tid < 64 + kC) {
-      const int j = tid - 64;
+    if (tid >= kGateTid && tid < kGateTid + kC) {
+      const int j = tid - kGateTid;
       const bool ok = cc * kC + j < L;
       const size_t row = b * Tp + (ok ? cc * kC + j : L - 1);
       const uint32_t gs = st_u + kXBytes + kVBytes;
@@ -317,14 +319,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   // staged X, and its cumulative gates.  K^T: 8 x 8 tiles of the keys (8 tokens
   // x 8 dims, 16-byte pieces of the swizzled rows: piece p of row t sits at
   // p ^ (t & 7)) transposed into K^T's core matrices (8 dims x 8 tokens) by
-  // ldmatrix.trans + stmatrix, four per warp instruction; warp w takes tiles
-  // 8 w .. 8 w + 7 (token group tile & 7, dim group tile >> 3).  Gate tables: warps 4 .. 7.
-  auto prep = [&](int cc) {
+  // ldmatrix.trans + stmatrix, four per warp instruction, the tiles (token group
+  // tile & 7, dim group tile >> 3) split evenly over the working warps.
+  auto prep = [&](int cc, int w0, int nw) {  // by warps w0 .. w0 + nw - 1 (16, or a warpgroup's 4)
     const uint8_t *stc = smem + (cc & 1) * kStage;
     const uint32_t xs_u = smem_u32(stc), kt_u = smem_u32(smem + kOffKt + (cc & 1) * kKtBytes);
-#pragma unroll
-    for (int q = 0; q < 2; ++q) {
-      const int tile = warp * 8 + q * 4 + (lane >> 3), jg = tile & 7, dg = tile >> 3, row = lane & 7;
+    const int wr = warp - w0, per = 128 / nw;  // this warp's rank; K^T tiles per warp
+#pragma unroll 2
+    for (int q = 0; q < per; q += 4) {
+      const int tile = wr * per + q + (lane >> 3), jg = tile & 7, dg = tile >> 3, row = lane & 7;
       const uint32_t src =
           xs_u + (dg >> 3) * kXHalf + (kC + jg * 8 + row) * 128 + (uint32_t)(((dg & 7) ^ row) << 4);
       const uint32_t dst = kt_u + dg * kSboKt + jg * kLbo + row * 16;
@@ -334,7 +337,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       asm volatile("stmatrix.sync.aligned.m8n8.x4.shared.b16 [%0], {%1,%2,%3,%4};"
                    ::"r"(dst), "r"(r0), "r"(r1), "r"(r2), "r"(r3) : "memory");
     }
-    if (warp >= 4 && warp < 8) {  // gate tables: each of warps 4 .. 7 scans the gates and fills a share
+    const int role = wr - (nw == 16 ? 4 : 0);  // gate tables: four warps scan the gates, each fills a share
+    if (role >= 0 && role < 4) {
       const float *gsc = reinterpret_cast<const float *>(stc + kXBytes + kVBytes);
       float *Acum = gates(cc), *eA = Acum + kC, *wL = eA + kC, *F = wL + kC, *E = F + kC;
       float a0 = GATED ? gsc[lane] : 0.f, a1 = GATED ? gsc[lane + 32] : 0.f;
@@ -347,19 +351,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       a1 += __shfl_sync(kFull, a0, 31);
-      if (warp == 4) {
+      if (role == 0) {
         Acum[lane] = a0;
         Acum[lane + 32] = a1;
         eA[lane] = expf(a0);
         eA[lane + 32] = expf(a1);
-      } else if (warp == 5) {
+      } else if (role == 1) {
         const float AL = __shfl_sync(kFull, a1, 31);
         wL[lane] = expf(AL - a0);
         wL[lane + 32] = expf(AL - a1);
         F[lane] = expf(a0 - __shfl_sync(kFull, a0, lane & 16));
         F[lane + 32] = expf(a1 - __shfl_sync(kFull, a1, lane & 16));
       } else {
-        const int a = (warp - 6) * 2;  // E rows a, a + 1 (A_{16 a}: lane 16 a of the token scan)
+        const int a = (role - 2) * 2;  // E rows a, a + 1 (A_{16 a}: lane 16 a of the token scan)
         const float B0 = __shfl_sync(kFull, a < 2 ? a0 : a1, 0), B1 = __shfl_sync(kFull, a < 2 ? a0 : a1, 16);
         E[a * kC + lane] = expf(B0 - a0);
         E[a * kC + lane + 32] = expf(B0 - a1);
@@ -406,7 +410,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   };
   if (nchunks > 0 && land(0)) {
     issue_g(0);
-    prep(0);
+    prep(0, 0, 16);
   }
   // this warpgroup's 32 state rows of column c: their parts (the operand of the
   // first Y^T), and e^{A_{C-1}} S^T in fp32, the state ready for chunk 0's
@@ -544,7 +548,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     fence_after();
     if (!ok) break;
 
-    bool okP = true;
+    bool okP = true, okL = true;
     {
       // U^T and (wU)^T parts (tokens 16 q .. 16 q + 15 of column c) into TMEM,
       // the A operands of the second MMAs
@@ -598,6 +602,27 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           mma_commit(mbar0 + 8 * (kBarP + bb));
         };
+        if (wg == 3 && ch + 1 < nchunks) {
+          // meanwhile: chunk ch + 1 landed (the TMA bytes, this warpgroup's own
+          // gate copies; a partial last chunk's rows past the prompt zeroed), its
+          // K^T and gate tables (named barrier 5 over the warpgroup)
+          asm volatile("cp.async.wait_group 0;\n" ::: "memory");
+          okL = mbar_wait(mbar0 + 8 * (kBarF + ((ch + 1) & 1)), ((ch + 1) >> 1) & 1);
+          const int nv = L - (ch + 1) * kC;
+          if (nv < kC) {
+            uint8_t *stc = smem + ((ch + 1) & 1) * kStage;
+            for (int idx = tid - 384; idx < (kC - nv) * 48; idx += 128) {
+              const int t = nv + idx / 48, pc = idx % 48;
+              uint8_t *dst = pc < 32 ? stc + (pc >> 4) * kXHalf + ((pc >> 3) & 1) * (kC * 128) + t * 128 + (pc & 7) * 16
+                                     : stc + kXBytes + t * 256 + (pc - 32) * 16;
+              *reinterpret_cast<uint4 *>(dst) = make_uint4(0u, 0u, 0u, 0u);
+            }
+            fence_async_smem();
+          }
+          named_sync(5, 128);
+          prep(ch + 1, 12, 4);
+          fence_async_smem();  // K^T, for the tensor cores
+        }
         if (wg > 0) {  // the products of the blocks above
           okP = mbar_wait(mbar0 + 8 * (kBarP + wg - 1), ch & 1, polls_at(ch));
           fence_after();
@@ -643,7 +668,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (DELTA) cmask |= 7u << kBarP;
     tmem_wait_st();
     fence_before();
-    ok = __syncthreads_and(okP) != 0;  // the waits on the block products, checked CTA-wide
+    ok = __syncthreads_and(okP && okL) != 0;  // the waits on the block products (and landing), CTA-wide
     fence_after();
     if (!ok) break;
 
@@ -678,9 +703,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     // while they run: the next chunk's K^T (the other buffer) and gates (this
     // chunk's are no longer read)
     if (ch + 1 < nchunks) {
-      if (!land(ch + 1)) break;
+      if (DELTA) {  // landed and prepared by warpgroup 3 during the substitution
+        pending = -1;
+      } else {
+        if (!land(ch + 1)) break;
+        prep(ch + 1, 0, 16);
+      }
       issue_g(ch + 1);  // the G columns were read by this chunk's Gram rows
-      prep(ch + 1);
     }
     if (!wait_bar(kBarO, ch)) break;
 
