@@ -260,6 +260,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // copies, zero past the prompt (64 threads from kGateTid: under the delta rule
   // warpgroup 3, which prepares the next chunk by itself)
   constexpr int kGateTid = DELTA ? 384 : 64;
+  constexpr int kYTid = 384;  // the issuer of Y (warp 12)
   auto issue = [&](int cc) {
     const uint32_t st_u = smem_u32(smem + (cc & 1) * kStage);
     if (tid == 64) {
@@ -433,6 +434,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     tmem_wait_st();
   }
+  // Mq's entries in rows 0 .. 31 and key columns 32 .. 63 (above the diagonal)
+  // stay zero: written once here, skipped by the Gram rows
+  for (int k = tid; k < 2 * 4 * 4 * 8; k += kThreads) {  // part, row group, k group, row
+    const int part = k >> 7, rg = (k >> 5) & 3, kg = 4 + ((k >> 3) & 3), r = k & 7;
+    *reinterpret_cast<uint4 *>(smem + kOffMq + part * kMqBytes + rg * kSboKt + kg * kLbo + r * 16) =
+        make_uint4(0u, 0u, 0u, 0u);
+  }
   fence_async_smem();
   fence_before();
   __syncthreads();
@@ -460,10 +468,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     // (chunk ch staged, its K^T and gates built, S^T's parts in TMEM, S^T
     // already decayed by e^{A_{C-1}})
 
+    // MMAs 1: Y^T = S^T X^T (S^T as hi + lo parts), by thread 384: warp 12 (like
+    // warp 8) holds Gram entries that are all above the diagonal, written once
+    if (tid == kYTid) {
+      const uint32_t idY = idesc_bf16(128, 2 * kC);
+#pragma unroll
+      for (int part = 0; part < 2; ++part)
+#pragma unroll
+        for (int ks = 0; ks < kD / 16; ++ks) {
+          const uint64_t bx = sdesc_sw128(xs + (ks >> 2) * kXHalf + (ks & 3) * 32);
+          mma_ts(tmem + kColY, tmem + kColP + part * 64 + ks * 8, bx, idY, part > 0 || ks > 0);
+        }
+      mma_commit(mbar0 + 8 * kBarY);
+    }
     // G (issued with the previous chunk): each thread waits by itself (the
-    // CTA-wide check of this wait comes with the one on Y) and takes its 16
-    // entries before this chunk's products are issued, since a TMEM load waits
-    // for the tensor core's products in flight
+    // CTA-wide check of this wait comes with the one on Y) and takes its 16 entries
     const int j0 = wg * 16;
     float gr[16];
     const bool okG = mbar_wait(mbar0 + 8 * kBarG, ch & 1, polls_at(ch));
@@ -475,25 +494,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int j = 0; j < 16; ++j) gr[j] = __uint_as_float(w[j]);
     }
-    fence_before();
-    if (warp == 1)  // every warp has its G entries (named barrier 4)
-      named_sync(4, kThreads);
-    else
-      named_arrive(4, kThreads);
 
-    // MMAs 1 (thread 32): Y^T = S^T X^T (S^T as hi + lo parts)
-    if (tid == 32) {
-      fence_after();
-      const uint32_t idY = idesc_bf16(128, 2 * kC);
-#pragma unroll
-      for (int part = 0; part < 2; ++part)
-#pragma unroll
-        for (int ks = 0; ks < kD / 16; ++ks) {
-          const uint64_t bx = sdesc_sw128(xs + (ks >> 2) * kXHalf + (ks & 3) * 32);
-          mma_ts(tmem + kColY, tmem + kColP + part * 64 + ks * 8, bx, idY, part > 0 || ks > 0);
-        }
-      mma_commit(mbar0 + 8 * kBarY);
-    }
     cmask = 1u << kBarY;
     // while the products run: the next chunk's copies (into the other stage, free
     // since the previous chunk finished)
@@ -503,7 +504,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     // Gram rows, key tokens split by warpgroup: thread (i, wg) builds entries
     // j = 16 wg .. 16 wg + 15 of row i of Mq (parts, smem) or Mk (fp32 and parts)
-    {
+    if (warp != 8 && warp != 12) {
       const int i = lt;
       if (i < kC) {  // Mq[i][j] = scale e^{A_i-A_j} q_i.k_j, j <= i
         const float sF = P.scale * Fg[i];
