@@ -220,10 +220,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ __align__(1024) uint8_t smem[];
   __shared__ uint64_t mbar_s[kBars];
   __shared__ uint32_t tmem_s;
-  // gate tables of chunk cc: the cumulative log-gates A, e^A, w = e^{A_{C-1} - A},
-  // F_i = e^{A_i - A_{16 (i / 16)}} and E_{a,j} = e^{A_{16 a} - A_j} (a = 0 .. 3),
-  // so that e^{A_i - A_j} = F_i E_{i / 16, j} (each factor spans at most one
-  // 16-token block of growth, or is a decay)
+  // gate tables of chunk cc: the cumulative log-gates A, e^A, w = e^{A_{C-1} - A}
+  // (then a spare row) and E_{a,j} = e^{A_{16 a} - A_j} (a = 0 .. 3), so that
+  // e^{A_i - A_j} = e^{A_i - A_{16 a}} E_{a,j} for any a (a factor spans at most
+  // one 16-token block of growth where the other is a decay)
   auto gates = [&](int cc) { return reinterpret_cast<float *>(smem + kOffA) + (cc & 1) * kGateF; };
   float *Mk = reinterpret_cast<float *>(smem + kOffMk);
 
@@ -341,7 +341,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int role = wr - (nw == 16 ? 4 : 0);  // gate tables: four warps scan the gates, each fills a share
     if (role >= 0 && role < 4) {
       const float *gsc = reinterpret_cast<const float *>(stc + kXBytes + kVBytes);
-      float *Acum = gates(cc), *eA = Acum + kC, *wL = eA + kC, *F = wL + kC, *E = F + kC;
+      float *Acum = gates(cc), *eA = Acum + kC, *wL = eA + kC, *E = wL + 2 * kC;
       float a0 = GATED ? gsc[lane] : 0.f, a1 = GATED ? gsc[lane + 32] : 0.f;
 #pragma unroll
       for (int off = 1; off < 32; off <<= 1) {
@@ -361,8 +361,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float AL = __shfl_sync(kFull, a1, 31);
         wL[lane] = expf(AL - a0);
         wL[lane + 32] = expf(AL - a1);
-        F[lane] = expf(a0 - __shfl_sync(kFull, a0, lane & 16));
-        F[lane + 32] = expf(a1 - __shfl_sync(kFull, a1, lane & 16));
       } else {
         const int a = (role - 2) * 2;  // E rows a, a + 1 (A_{16 a}: lane 16 a of the token scan)
         const float B0 = __shfl_sync(kFull, a < 2 ? a0 : a1, 0), B1 = __shfl_sync(kFull, a < 2 ? a0 : a1, 16);
@@ -463,7 +461,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const KT *vs = reinterpret_cast<const KT *>(st + kXBytes);
     const float *gs = reinterpret_cast<const float *>(st + kXBytes + kVBytes);
     const float *bs = gs + kC;
-    const float *Acum = gates(ch), *eA = Acum + kC, *wL = eA + kC, *Fg = wL + kC, *Eg = Fg + kC;
+    const float *Acum = gates(ch), *eA = Acum + kC, *wL = eA + kC, *Eg = wL + 2 * kC;
     const int t0 = ch * kC;
     // (chunk ch staged, its K^T and gates built, S^T's parts in TMEM, S^T
     // already decayed by e^{A_{C-1}})
@@ -504,11 +502,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     // Gram rows, key tokens split by warpgroup: thread (i, wg) builds entries
     // j = 16 wg .. 16 wg + 15 of row i of Mq (parts, smem) or Mk (fp32 and parts)
+    // e^{A_i - A_j} = e^{A_i - A_{j0}} E_{wg, j} (j0 = 16 wg): one exponential per
+    // thread, and a table row shared by the warp
     if (warp != 8 && warp != 12) {
       const int i = lt;
+      const float *Er = Eg + wg * kC + j0;
       if (i < kC) {  // Mq[i][j] = scale e^{A_i-A_j} q_i.k_j, j <= i
-        const float sF = P.scale * Fg[i];
-        const float *Er = Eg + (i >> 4) * kC + j0;
+        const float sF = i >= j0 ? P.scale * expf(Acum[i] - Acum[j0]) : 0.f;
         float x[16];
 #pragma unroll
         for (int j = 0; j < 16; ++j) x[j] = j0 + j <= i ? sF * Er[j] * gr[j] : 0.f;
@@ -522,25 +522,31 @@ __global__ void __launch_bounds__(kThreads, 1)
           *reinterpret_cast<uint4 *>(mq + kMqBytes + off) =
               make_uint4(lo[4 * q], lo[4 * q + 1], lo[4 * q + 2], lo[4 * q + 3]);
         }
-      } else if (DELTA) {  // Mk[i'][j] = beta_i' e^{A_i'-A_j} k_i'.k_j, j < i': fp32 and parts
+      } else if (DELTA && wg <= ((i - kC) >> 4)) {
+        // Mk[i'][j] = beta_i' e^{A_i'-A_j} k_i'.k_j, j < i': the diagonal block in
+        // fp32 (the in-register solves), the blocks below it as bf16 parts (the
+        // tensor-core block products); the blocks above it are never read
         const int ip = i - kC;
-        const float bF = bs[ip] * Fg[ip];
-        const float *Er = Eg + (ip >> 4) * kC + j0;
+        const float bF = bs[ip] * expf(Acum[ip] - Acum[j0]);
         float x[16];
 #pragma unroll
         for (int j = 0; j < 16; ++j) x[j] = j0 + j < ip ? bF * Er[j] * gr[j] : 0.f;
+        if (wg == (ip >> 4)) {
 #pragma unroll
-        for (int j = 0; j < 16; j += 4)
-          *reinterpret_cast<float4 *>(&Mk[ip * kLdMk + j0 + j]) = make_float4(x[j], x[j + 1], x[j + 2], x[j + 3]);
-        uint32_t hi[8], lo[8];
-        split16(x, hi, lo);
-        uint8_t *mkp = smem + kOffMkp;
+          for (int j = 0; j < 16; j += 4)
+            *reinterpret_cast<float4 *>(&Mk[ip * kLdMk + j0 + j]) = make_float4(x[j], x[j + 1], x[j + 2], x[j + 3]);
+        } else {
+          uint32_t hi[8], lo[8];
+          split16(x, hi, lo);
+          uint8_t *mkp = smem + kOffMkp;
 #pragma unroll
-        for (int q = 0; q < 2; ++q) {
-          const int off = (ip >> 3) * kSboKt + (wg * 2 + q) * kLbo + (ip & 7) * 16;
-          *reinterpret_cast<uint4 *>(mkp + off) = make_uint4(hi[4 * q], hi[4 * q + 1], hi[4 * q + 2], hi[4 * q + 3]);
-          *reinterpret_cast<uint4 *>(mkp + kMqBytes + off) =
-              make_uint4(lo[4 * q], lo[4 * q + 1], lo[4 * q + 2], lo[4 * q + 3]);
+          for (int q = 0; q < 2; ++q) {
+            const int off = (ip >> 3) * kSboKt + (wg * 2 + q) * kLbo + (ip & 7) * 16;
+            *reinterpret_cast<uint4 *>(mkp + off) =
+                make_uint4(hi[4 * q], hi[4 * q + 1], hi[4 * q + 2], hi[4 * q + 3]);
+            *reinterpret_cast<uint4 *>(mkp + kMqBytes + off) =
+                make_uint4(lo[4 * q], lo[4 * q + 1], lo[4 * q + 2], lo[4 * q + 3]);
+          }
         }
       }
     }
