@@ -531,10 +531,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         float x[16];
 #pragma unroll
         for (int j = 0; j < 16; ++j) x[j] = j0 + j < ip ? bF * Er[j] * gr[j] : 0.f;
-        if (wg == (ip >> 4)) {
+        if (wg == (ip >> 4)) {  // column-major: [block][column l][row i]
+          float *mt = Mk + (ip >> 4) * 256 + (ip & 15);
 #pragma unroll
-          for (int j = 0; j < 16; j += 4)
-            *reinterpret_cast<float4 *>(&Mk[ip * kLdMk + j0 + j]) = make_float4(x[j], x[j + 1], x[j + 2], x[j + 3]);
+          for (int j = 0; j < 16; ++j) mt[j * 16] = x[j];
         } else {
           uint32_t hi[8], lo[8];
           split16(x, hi, lo);
@@ -559,16 +559,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     {
       // U^T and (wU)^T parts (tokens 16 q .. 16 q + 15 of column c) into TMEM,
       // the A operands of the second MMAs
-      auto u_parts = [&](float (&x)[16], int q) {
+      auto u_parts = [&](float (&x)[16], int q, bool weighted) {
         uint32_t hi[8], lo[8];
-        split16(x, hi, lo);
-        tmem_st8(my + kColP + q * 8, hi);
-        tmem_st8(my + kColP + 32 + q * 8, lo);
+        if (weighted) {
+          float y[16];
 #pragma unroll
-        for (int j = 0; j < 16; ++j) x[j] *= wL[q * 16 + j];
-        split16(x, hi, lo);
-        tmem_st8(my + kColP + 64 + q * 8, hi);
-        tmem_st8(my + kColP + 96 + q * 8, lo);
+          for (int j = 0; j < 16; ++j) y[j] = x[j] * wL[q * 16 + j];
+          split16(y, hi, lo);
+          tmem_st8(my + kColP + 64 + q * 8, hi);
+          tmem_st8(my + kColP + 96 + q * 8, lo);
+        } else {
+          split16(x, hi, lo);
+          tmem_st8(my + kColP + q * 8, hi);
+          tmem_st8(my + kColP + 32 + q * 8, lo);
+        }
       };
       if (DELTA) {
         // (I + Mk) U = R by blocked forward substitution: warpgroup a holds R and
@@ -589,12 +593,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             u[j] = bs[jj] * (__bfloat162float(vs[jj * kD + c]) - eA[jj] * __uint_as_float(w[j]));
           }
         }
-        auto solve = [&]() {
-          const float *md = Mk + (wg * 16) * kLdMk + wg * 16;
+        auto solve = [&]() {  // the diagonal block, column-major: column l in 16 floats
+          const float4 *md = reinterpret_cast<const float4 *>(Mk + wg * 256);
 #pragma unroll
           for (int l = 0; l < 15; ++l)
 #pragma unroll
-            for (int i = l + 1; i < 16; ++i) u[i] = fmaf(-md[i * kLdMk + l], u[l], u[i]);
+            for (int i4 = (l + 1) >> 2; i4 < 4; ++i4) {
+              const float4 m = md[l * 4 + i4];
+              if (4 * i4 > l) u[4 * i4] = fmaf(-m.x, u[l], u[4 * i4]);
+              if (4 * i4 + 1 > l) u[4 * i4 + 1] = fmaf(-m.y, u[l], u[4 * i4 + 1]);
+              if (4 * i4 + 2 > l) u[4 * i4 + 2] = fmaf(-m.z, u[l], u[4 * i4 + 2]);
+              u[4 * i4 + 3] = fmaf(-m.w, u[l], u[4 * i4 + 3]);
+            }
         };
         // thread 0: the products of block b (after fence_after)
         auto issue_sub = [&](int bb) {
@@ -639,7 +649,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int j = 0; j < 16; ++j) u[j] -= __uint_as_float(w[j]);
         }
         solve();
-        u_parts(u, wg);
+        u_parts(u, wg, false);
         if (wg < 3) {
           tmem_wait_st();
           fence_before();
@@ -665,11 +675,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         } else if (wg < 3) {
           named_arrive(1 + wg, 160);
         }
+        u_parts(u, wg, true);  // (wU)^T, for the state update only
       } else {  // U = V, tokens 16 wg .. 16 wg + 15
         float x[16];
 #pragma unroll
         for (int j = 0; j < 16; ++j) x[j] = __bfloat162float(vs[(wg * 16 + j) * kD + c]);
-        u_parts(x, wg);
+        u_parts(x, wg, false);
+        u_parts(x, wg, true);
       }
     }
     if (DELTA) cmask |= 7u << kBarP;
