@@ -153,6 +153,23 @@ __device__ __forceinline__ void split16(const float (&x)[16], uint32_t (&hi)[8],
 #pragma unroll
   for (int j = 0; j < 8; ++j) split_pair(x[2 * j], x[2 * j + 1], hi[j], lo[j]);
 }
+// 16 columns without waiting (tmem_wait_ld completes every load issued before it)
+__device__ __forceinline__ void tmem_ld16_async(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+// after tmem_wait_ld: ties the loaded registers to the wait, so that no use of
+// them is scheduled before it
+__device__ __forceinline__ void tmem_loaded(uint32_t (&r)[16]) {
+  asm volatile(""
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
+                 "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]),
+                 "+r"(r[15]));
+}
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
@@ -738,17 +755,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     // 512 bytes per prompt token for a last, partial chunk; then the next
     // chunk's S^T parts (state rows 32 wg .. 32 wg + 31)
     {
-      uint32_t w[16], w1[16];
-      float o[16];
-      tmem_ld16(my + kColY + wg * 16, w);
-      tmem_ld16(my + kColY + kC + wg * 16, w1);
-#pragma unroll
-      for (int j = 0; j < 16; ++j)
-        o[j] = fmaf(P.scale * eA[wg * 16 + j], __uint_as_float(w[j]), __uint_as_float(w1[j]));
-      tmem_ld16(my + kColD + wg * 16, w);
+      uint32_t w[16], w1[16], w2[16];
+      tmem_ld16_async(my + kColY + wg * 16, w);
+      tmem_ld16_async(my + kColY + kC + wg * 16, w1);
+      tmem_ld16_async(my + kColD + wg * 16, w2);
+      tmem_wait_ld();
+      tmem_loaded(w);
+      tmem_loaded(w1);
+      tmem_loaded(w2);
       float *ost = reinterpret_cast<float *>(st);
 #pragma unroll
-      for (int j = 0; j < 16; ++j) ost[(wg * 16 + j) * kD + c] = o[j] + __uint_as_float(w[j]);
+      for (int j = 0; j < 16; ++j)
+        ost[(wg * 16 + j) * kD + c] =
+            fmaf(P.scale * eA[wg * 16 + j], __uint_as_float(w[j]), __uint_as_float(w1[j])) + __uint_as_float(w2[j]);
       fence_async_smem();
     }
     if (!wait_bar(kBarS, ch)) break;
@@ -760,19 +779,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (ch + 1 < nchunks) {
       // the next chunk's S^T parts, and its decay e^{A_{C-1}} applied to S^T
       const float eLn = gates(ch + 1)[kC + kC - 1];
-#pragma unroll 1
+      uint32_t wa[16], wb[16];
+      tmem_ld16_async(my + kColS + wg * 32, wa);
+      tmem_ld16_async(my + kColS + wg * 32 + 16, wb);
+      tmem_wait_ld();
+      tmem_loaded(wa);
+      tmem_loaded(wb);
+#pragma unroll
       for (int q = 0; q < 2; ++q) {
-        const int r0 = wg * 2 + q;
-        uint32_t w16[16];
-        tmem_ld16(my + kColS + r0 * 16, w16);
+        uint32_t (&w16)[16] = q ? wb : wa;
         float x[16];
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
           x[j] = __uint_as_float(w16[j]);
           w16[j] = __float_as_uint(eLn * x[j]);
         }
-        put_parts16(x, r0);
-        tmem_st16(my + kColS + r0 * 16, w16);
+        put_parts16(x, wg * 2 + q);
+        tmem_st16(my + kColS + wg * 32 + q * 16, w16);
       }
       tmem_wait_st();
     }
