@@ -59,12 +59,13 @@ constexpr uint32_t kLbo = 128;
 constexpr uint32_t kSboKt = (kC / 8) * 128;     // K^T and Mq: 64 tokens per row group
 static_assert(kSmemBytes <= 227 * 1024, "one CTA's shared memory");
 static_assert(kStage % 1024 == 0 && kKtBytes % 1024 == 0 && kMqBytes % 1024 == 0, "alignment");
+static_assert(kMqBytes == (kC / 8) * kSboKt, "Mq's lo part continues its hi part's row groups");
+static_assert(kColD == kColY + 2 * kC && kColG == kColD + kC, "the output product's 128 columns");
 // completion barriers, one completion each per chunk (so phase parity = chunk &
 // 1): G, Y (first products), O and S (second products), P + b (the delta rule's
 // products Mk_{.,b} U_b, b = 0 .. 2); then the two stages' landing barriers
-// (TMA bytes), one completion per use.  G is issued a chunk ahead (its k-th
-// completion is chunk k's).  O completes on two commits (its part products are
-// issued by two threads into separate accumulators), the others on one.
+// (TMA bytes), one completion per use, each on one commit.  G is issued a chunk
+// ahead (its k-th completion is chunk k's).
 constexpr int kBarG = 0, kBarY = 1, kBarO = 2, kBarS = 3, kBarP = 4, kBarF = 7, kBars = 9;
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
@@ -261,7 +262,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (tid == 0) {
 #pragma unroll
     for (int k = 0; k < kBars; ++k)
-      asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(mbar0 + 8 * k), "r"(k == kBarO ? 2 : 1));
+      asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(mbar0 + 8 * k));
     asm volatile("fence.mbarrier_init.release.cluster;");
   }
   if (warp == 0) {
@@ -708,22 +709,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     fence_after();
     if (!ok) break;
 
-    // MMAs 2, from three issuing threads: the part products of U^T Mq^T (U^T hi
-    // Mq hi into the K half of Y (read by now; thread 0), U^T hi Mq lo + U^T lo
-    // Mq hi into the D columns (thread 32)) and S^T += (wU)^T K (thread 96);
-    // O^T = e^A scale Y_q^T + the two accumulators
-    if (tid == 0 || tid == 32) {
-      const uint32_t idO = idesc_bf16(128, kC), mq = smem_u32(smem + kOffMq);
-      const uint32_t dcol = tid == 0 ? kColY + kC : kColD;
+    // MMAs 2, from two issuing threads: U^T Mq^T (thread 0) and S^T += (wU)^T K
+    // (thread 96).  Mq's hi and lo parts lie back to back (8 row groups each), so
+    // U^T hi [Mq hi; Mq lo]^T is one product of 128 columns (the K half of Y, read
+    // by now, and the D columns), and U^T lo Mq hi^T adds onto its first half:
+    // O^T = e^A scale Y_q^T + both halves
+    if (tid == 0) {
+      const uint32_t idO2 = idesc_bf16(128, 2 * kC), idO = idesc_bf16(128, kC), mq = smem_u32(smem + kOffMq);
 #pragma unroll
-      for (int combo = tid == 0 ? 0 : 1; combo < (tid == 0 ? 1 : 3); ++combo) {
-        const int ua = combo == 2 ? 32 : 0;                    // U^T hi, hi, lo
-        const uint32_t mb = mq + (combo == 1 ? kMqBytes : 0);  // Mq hi, lo, hi
+      for (int k0 = 0; k0 < kC; k0 += 16)
+        mma_ts(tmem + kColY + kC, tmem + kColP + k0 / 2, sdesc(mq + (k0 / 8) * kLbo, kLbo, kSboKt), idO2, k0 > 0);
 #pragma unroll
-        for (int k0 = 0; k0 < kC; k0 += 16)
-          mma_ts(tmem + dcol, tmem + kColP + ua + k0 / 2, sdesc(mb + (k0 / 8) * kLbo, kLbo, kSboKt), idO,
-                 combo == 2 || k0 > 0);
-      }
+      for (int k0 = 0; k0 < kC; k0 += 16)
+        mma_ts(tmem + kColY + kC, tmem + kColP + 32 + k0 / 2, sdesc(mq + (k0 / 8) * kLbo, kLbo, kSboKt), idO, 1);
       mma_commit(mbar0 + 8 * kBarO);
     } else if (tid == 96) {
       const uint32_t idS = idesc_bf16(128, kD), kt = smem_u32(smem + kOffKt + (ch & 1) * kKtBytes);
