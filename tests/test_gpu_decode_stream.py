@@ -153,18 +153,23 @@ def _stack(hist):
     return {key: np.stack(val) for key, val in hist.items()}
 
 
-@pytest.mark.parametrize("layer,B", [
-    (I.Layer(I.GATED_DELTA, 8, 32, 128, 128, "bf16", qk_dist="l2norm"), 160),
-    (I.Layer(I.GATED, 16, 16, 128, 128, "f32"), 200),
-    (I.Layer(I.PLAIN, 16, 16, 128, 128, "bf16"), 200),
-    (I.Layer(I.GATED_DELTA, 16, 16, 128, 128, "f32", qk_dist="l2norm"), 120),
-], ids=["gated_delta_bf16", "gated_f32", "plain_bf16", "gated_delta_f32"])
-def test_short_ctx_large_batch(layer, B):
+@pytest.mark.parametrize("layer,B,bs", [
+    (I.Layer(I.GATED_DELTA, 8, 32, 128, 128, "bf16", qk_dist="l2norm"), 160, 4),
+    (I.Layer(I.GATED, 16, 16, 128, 128, "f32"), 200, 4),
+    (I.Layer(I.PLAIN, 16, 16, 128, 128, "bf16"), 200, 4),
+    (I.Layer(I.GATED_DELTA, 16, 16, 128, 128, "f32", qk_dist="l2norm"), 120, 4),
+    (I.Layer(I.GATED, 16, 16, 128, 128, "bf16"), 200, 8),
+    (I.Layer(I.PLAIN, 8, 16, 128, 128, "bf16"), 160, 16),
+], ids=["gated_delta_bf16", "gated_f32", "plain_bf16", "gated_delta_f32", "gated_bf16_bs8",
+        "plain_bf16_grouped_bs16"])
+def test_short_ctx_large_batch(layer, B, bs):
     """Short-context decode of B requests (no state) growing to ragged lengths
-    1..64 in 64-slot buffers (block ids beyond the row descriptor's come from the
-    block table), launches from B rows down to a handful.  Sampled outputs against
-    the oracle's buffer-only decode, all lengths bit for bit."""
-    bs, nb = 4, 16  # blocks 8..15 come from the block table
+    1..64 in 64-slot buffers, launches from B rows down to a handful.  With 4-token
+    blocks the ids beyond the row descriptor's come from the block table; 8- and
+    16-token blocks (the bench's size, and a grouped layer) cover whole blocks per
+    id.  Sampled outputs against the oracle's buffer-only decode, all lengths bit
+    for bit."""
+    nb = 64 // bs
     cap = nb * bs
     rng = np.random.default_rng(740 + layer.variant + B)
     pool = make_pool(layer, 8, B, nb, bs, num_blocks=B * nb + 8, num_slots=1)
