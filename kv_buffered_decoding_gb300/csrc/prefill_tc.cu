@@ -259,12 +259,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t mbar0 = smem_u32(&mbar_s[0]);  // barrier k at mbar0 + 8 k
   const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;  // this warp's TMEM lanes
 
-  if (tid == 0) {
-#pragma unroll
-    for (int k = 0; k < kBars; ++k)
-      asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(mbar0 + 8 * k));
-    asm volatile("fence.mbarrier_init.release.cluster;");
-  }
   if (warp == 0) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&tmem_s)),
                  "r"(kTmemCols));
@@ -279,9 +273,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   // warpgroup 3, which prepares the next chunk by itself)
   constexpr int kGateTid = DELTA ? 384 : 64;
   constexpr int kYTid = 384;  // the issuer of Y (warp 12)
-  auto issue = [&](int cc) {
+  auto issue = [&](int cc, int tma_tid) {
     const uint32_t st_u = smem_u32(smem + (cc & 1) * kStage);
-    if (tid == 64) {
+    if (tid == tma_tid) {
       bulk_wait_read();
       const uint32_t full = mbar0 + 8 * (kBarF + (cc & 1));
       const int z = (int)(b * Tp + (size_t)cc * kC);  // first token row of the chunk
@@ -304,16 +298,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     asm volatile("cp.async.commit_group;\n" ::: "memory");
   };
 
+  // the barriers, and chunk 0's copies at once (thread 0 right after the init;
+  // the TMEM allocation above runs meanwhile)
+  if (tid == 0) {
+#pragma unroll
+    for (int k = 0; k < kBars; ++k)
+      asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(mbar0 + 8 * k));
+    asm volatile("fence.mbarrier_init.release.cluster;");
+  }
+  if (nchunks > 0) issue(0, 0);
+  int pending = nchunks > 0 ? 0 : -1;  // the chunk whose copies are issued and not yet waited for
+  int gpend = -1;                      // the chunk whose G is issued and not yet waited for
   fence_before();
   __syncthreads();
   fence_after();
   const uint32_t tmem = tmem_s;
-  int pending = -1;  // the chunk whose copies are issued and not yet waited for
-  int gpend = -1;    // the chunk whose G is issued and not yet waited for
-  if (nchunks > 0) {
-    issue(0);
-    pending = 0;
-  }
   const int lt = tid & 127;              // this thread's TMEM lane
   const int wg = tid >> 7;               // warpgroup: which quarter of each lane's columns
   const uint32_t my = tmem + lane_base;  // this thread's lane, column 0
@@ -425,28 +424,31 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     gpend = cc;
   };
+  // this warpgroup's 32 state rows of column c, read while chunk 0 lands
+  float s0[32];
+#pragma unroll
+  for (int j = 0; j < 32; ++j) s0[j] = from_zero ? 0.f : Sg[(size_t)(wg * 32 + j) * kD + c];
   if (nchunks > 0 && land(0)) {
     issue_g(0);
     prep(0, 0, 16);
   }
-  // this warpgroup's 32 state rows of column c: their parts (the operand of the
-  // first Y^T), and e^{A_{C-1}} S^T in fp32, the state ready for chunk 0's
-  // update (each chunk's decay is applied when its predecessor's parts are made)
+  // their parts (the operand of the first Y^T), and e^{A_{C-1}} S^T in fp32, the
+  // state ready for chunk 0's update (each chunk's decay is applied when its
+  // predecessor's parts are made)
   {
     __syncthreads();  // chunk 0's gates
     const float eL = nchunks > 0 ? gates(0)[kC + kC - 1] : 1.f;
-#pragma unroll 1
+#pragma unroll
     for (int q = 0; q < 2; ++q) {
-      const int r0 = wg * 2 + q;  // 16-row piece
       float x[16];
       uint32_t w[16];
 #pragma unroll
       for (int j = 0; j < 16; ++j) {
-        x[j] = from_zero ? 0.f : Sg[(size_t)(r0 * 16 + j) * kD + c];
+        x[j] = s0[q * 16 + j];
         w[j] = __float_as_uint(eL * x[j]);
       }
-      tmem_st16(my + kColS + r0 * 16, w);
-      put_parts16(x, r0);
+      tmem_st16(my + kColS + (wg * 2 + q) * 16, w);
+      put_parts16(x, wg * 2 + q);
     }
     tmem_wait_st();
   }
@@ -515,7 +517,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // while the products run: the next chunk's copies (into the other stage, free
     // since the previous chunk finished)
     if (ch + 1 < nchunks) {
-      issue(ch + 1);
+      issue(ch + 1, 64);
       pending = ch + 1;
     }
     // Gram rows, key tokens split by warpgroup: thread (i, wg) builds entries
