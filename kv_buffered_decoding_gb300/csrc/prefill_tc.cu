@@ -259,11 +259,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t mbar0 = smem_u32(&mbar_s[0]);  // barrier k at mbar0 + 8 k
   const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;  // this warp's TMEM lanes
 
-  if (warp == 0) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&tmem_s)),
-                 "r"(kTmemCols));
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
-  }
 
   // stage chunk cc: q and k rows of the chunk by TMA into X (two d_k halves of
   // 64 elements, 128-byte swizzle), v rows into V, the landing barrier of the
@@ -298,8 +293,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     asm volatile("cp.async.commit_group;\n" ::: "memory");
   };
 
-  // the barriers, and chunk 0's copies at once (thread 0 right after the init;
-  // the TMEM allocation above runs meanwhile)
+  // the barriers, and chunk 0's copies at once (thread 0 right after the init),
+  // then the TMEM allocation
   if (tid == 0) {
 #pragma unroll
     for (int k = 0; k < kBars; ++k)
@@ -309,6 +304,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (nchunks > 0) issue(0, 0);
   int pending = nchunks > 0 ? 0 : -1;  // the chunk whose copies are issued and not yet waited for
   int gpend = -1;                      // the chunk whose G is issued and not yet waited for
+  if (warp == 0) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&tmem_s)),
+                 "r"(kTmemCols));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+  }
   fence_before();
   __syncthreads();
   fence_after();
