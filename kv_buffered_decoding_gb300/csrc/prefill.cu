@@ -511,8 +511,9 @@ cudaError_t launch_prefill(const PoolView &P, const RowBatch &rows, const TokenI
                            int variant, int dtype, int d, cudaStream_t stream) {
   if (rows.count <= 0) return cudaSuccess;
   if (dtype == 1 && d == 128 && (reinterpret_cast<uintptr_t>(io.o) & 15) == 0) {
-    // the tensor-core kernel moves its tiles by TMA: 16-byte aligned buffers
-    // only; others take the mma.sync kernel below
+    // the tensor-core kernel moves its tiles by TMA (the boundary admits only
+    // 16-byte aligned token buffers); where the driver cannot encode the tensor
+    // maps, the mma.sync kernel below runs instead
     PrefillMaps maps;
     if (encode_prefill_maps(&maps, io, P.Hk, P.Hv) == cudaSuccess)
       return launch_prefill_tc(P, rows, io, maps, variant, stream);

@@ -81,6 +81,45 @@ def test_prefill_matches_recurrence(layer, from_zero):
     assert pool.get_error() is None
 
 
+def test_prefill_unaligned_buffers_rejected():
+    """Token buffers must start on a 16-byte boundary (the prefill kernels stage
+    tiles with 16-byte copies and TMA): an output or key buffer 4 bytes off it is
+    refused with KVB_E_ARG before any launch, the output and the state stay as
+    they were, and an aligned call then runs normally."""
+    kvb = kvb_mod()
+    layer = I.Layer(I.GATED_DELTA, 2, 4, 128, 128, "bf16", qk_dist="l2norm")
+    rng = np.random.default_rng(305)
+    B, L = 2, 70
+    pool = make_pool(layer, 4, B, 1, 8)
+    for r in range(B):
+        pool.set_request(r, r, [r])
+    S0 = I.draw_state(rng, layer, B)
+    pool.state.copy_(torch.from_numpy(S0))
+    tok = I.draw_tokens(rng, layer, (B, L))
+    q, k, v, log_g, beta = token_tensors(tok, layer, slice(None))
+    n_o = B * L * layer.n_v_heads * layer.d_v
+    big = torch.full((n_o + 1,), float("nan"), device="cuda")
+    o_bad = big[1:].view(B, L, layer.n_v_heads, layer.d_v)
+    assert o_bad.data_ptr() % 16 == 4
+    kbig = torch.empty(k.numel() + 2, dtype=k.dtype, device="cuda")
+    k_bad = kbig[2:].view(k.shape)
+    k_bad.copy_(k)
+    assert k_bad.data_ptr() % 16 == 4
+    for args in ((q, k, v, log_g, beta, o_bad), (q, k_bad, v, log_g, beta, None)):
+        with pytest.raises(kvb.KvbError) as ex:
+            pool.prefill(np.arange(B), *args[:5], o=args[5], from_zero=True)
+        assert ex.value.status == kvb.KVB_E_ARG
+    torch.cuda.synchronize()
+    assert torch.isnan(big).all()
+    assert np.array_equal(pool.state.cpu().numpy(), S0)
+    o = pool.prefill(np.arange(B), q, k, v, log_g, beta, from_zero=True).cpu().numpy()
+    zero = np.zeros((layer.n_v_heads, layer.d_k, layer.d_v))
+    for r in range(B):
+        o_ref, _, _ = oracle.decode_sequence(zero, _prompt(tok, r, L), layer.variant)
+        assert rel_err(o[r], o_ref) <= tol_for(layer), r
+    assert pool.get_error() is None
+
+
 def test_prefill_long_prompt_gated_delta():
     """Sixteen chunks (1024 tokens): rounding does not build up across chunks."""
     layer = I.Layer(I.GATED_DELTA, 1, 2, 128, 128, "bf16", qk_dist="l2norm")
