@@ -329,7 +329,7 @@ def measure_paths(kvb, torch, dev, peak):
 
     verify: T = 4 drafts per request against the stored state, accepted with j = 0 so
     every round sees the same buffer; flush: fold 8 buffered tokens per request into the
-    state; short_ctx: buffer-only decode of requests holding 32..47 tokens.  Each entry
+    state; short_ctx: buffer-only decode of requests holding 32..44 tokens.  Each entry
     reports microseconds per call, algorithmic GB/s (raw q/k/v/gate/beta/state/output
     bytes, as for decode) and the fraction of the peak.
     """

@@ -437,24 +437,34 @@ __global__ void __launch_bounds__(128) short_mma_kernel(const PoolView P,
 // lo to about 16 significant bits).  The output is a second pass,
 // o^T = V^T [w_hi w_lo], with V^T as A read from the row-major value rows by
 // ldmatrix.trans and the two weight columns as B; warp w owns output columns
-// 32w .. 32w + 31, so no partial sums cross warps.  Rows are padded to
-// multiples of 16 tokens (the products' M and K); the padded value rows are
-// zeroed and their weights are 0.
+// 32w .. 32w + 31, so no partial sums cross warps.  The products' M and K run
+// in steps of 16 tokens: the value rows are padded to a multiple of 16 (the
+// padded rows zeroed, their weights 0); the key rows are not, and a score tile
+// that runs past them reads value rows, whose dots are discarded.  Key and
+// value rows are 256 bytes with their 16-byte chunks XOR-swizzled on the low
+// three bits of the row (chunk c of row r at c ^ (r & 7)), so the eight rows of
+// an ldmatrix read hit distinct banks without padding.  At up to 44 buffered
+// tokens a CTA then needs under 24.9 KB, and nine CTAs fit on an SM: a batch
+// of 256 rows x 16 heads is three full waves instead of three and a third.
 struct ShortTcLayout {
   uint32_t kr, vr, as, ws, koff, voff, qrow, bytes;
 };
 __host__ __device__ inline ShortTcLayout short_tc_layout(int nmax) {
   const uint32_t LP = (uint32_t)(nmax + 1 + 15) & ~15u;
   ShortTcLayout l;
-  l.kr = 0;                           // [LP][XS] bf16 keys (row n: k_t)
-  l.vr = l.kr + LP * kSXS * 2;        // [LP][XS] bf16 values (row n: v_t)
-  l.as = l.vr + LP * kSXS * 2;        // [LP] cumulative log-gates
+  l.kr = 0;                           // [nmax + 1][128] bf16 keys (row n: k_t)
+  l.vr = l.kr + (nmax + 1) * 256;     // [LP][128] bf16 values (row n: v_t)
+  l.as = l.vr + LP * 256;             // [LP] cumulative log-gates
   l.ws = l.as + LP * 4;               // [LP] weights, bf16 hi parts then [LP] lo parts
-  l.koff = l.ws + LP * 4;             // [LP] key row offsets (elements)
-  l.voff = l.koff + LP * 8;           // [LP] value row indices
-  l.qrow = l.voff + LP * 8;           // q (bf16)
+  l.koff = l.ws + LP * 4;             // [LP] key rows
+  l.voff = l.koff + LP * 4;           // [LP] value rows
+  l.qrow = l.voff + LP * 4;           // q (bf16)
   l.bytes = l.qrow + 128 * 2;
   return l;
+}
+// Byte offset of 16-byte chunk c of row r in a region of swizzled 256-byte rows.
+__device__ __forceinline__ uint32_t swz(int r, int c) {
+  return (uint32_t)(r * 256 + ((c ^ (r & 7)) << 4));
 }
 
 __device__ __forceinline__ void mma_bf16_full(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
@@ -465,12 +475,12 @@ __device__ __forceinline__ void mma_bf16_full(float (&d)[4], uint32_t a0, uint32
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 template <int VARIANT>
-__global__ void __launch_bounds__(128) short_tc_kernel(const PoolView P,
+__global__ void __launch_bounds__(128, 9) short_tc_kernel(const PoolView P,
                                                         const __grid_constant__ RowBatch rows,
                                                         const TokenIO io, FastDiv hv_div) {
   static_assert(VARIANT != kGatedDelta, "the delta rule keeps short_mma_kernel");
   using KT = __nv_bfloat16;
-  constexpr int D = 128, XS = kSXS, NW = 4;
+  constexpr int D = 128, NW = 4;
   constexpr bool GATED = VARIANT != kPlain;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int g = lane >> 2, t = lane & 3;
@@ -484,13 +494,14 @@ __global__ void __launch_bounds__(128) short_tc_kernel(const PoolView P,
   const int LP = (io.lmax + 1 + 15) & ~15;
 
   extern __shared__ __align__(16) uint8_t sm[];
-  KT *Kr = reinterpret_cast<KT *>(sm + lay.kr);
-  KT *Vr = reinterpret_cast<KT *>(sm + lay.vr);
+  uint8_t *Kr = sm + lay.kr;  // swizzled rows (swz)
+  uint8_t *Vr = sm + lay.vr;
   float *As = reinterpret_cast<float *>(sm + lay.as);
   KT *whi = reinterpret_cast<KT *>(sm + lay.ws);
   KT *wlo = whi + LP;
-  size_t *koff = reinterpret_cast<size_t *>(sm + lay.koff);
-  size_t *voff = reinterpret_cast<size_t *>(sm + lay.voff);
+  // buffer rows of the tokens (a pool's rows are far fewer than 2^32: 256 bytes each)
+  uint32_t *krow = reinterpret_cast<uint32_t *>(sm + lay.koff);
+  uint32_t *vrow = reinterpret_cast<uint32_t *>(sm + lay.voff);
   KT *qs = reinterpret_cast<KT *>(sm + lay.qrow);
 
   // 1. where tokens 0..n live (one thread per token)
@@ -498,8 +509,8 @@ __global__ void __launch_bounds__(128) short_tc_kernel(const PoolView P,
   if (tid < L) {
     const int gr = buffer_row(P, d, tid);
     bad = gr < 0;
-    koff[tid] = gr >= 0 ? kv_row(P, gr, hq, P.Hk) * D : 0;
-    voff[tid] = gr >= 0 ? kv_row(P, gr, h, P.Hv) : 0;
+    krow[tid] = gr >= 0 ? (uint32_t)kv_row(P, gr, hq, P.Hk) : 0u;
+    vrow[tid] = gr >= 0 ? (uint32_t)kv_row(P, gr, h, P.Hv) : 0u;
   }
   if (__syncthreads_or(bad)) return;  // recorded in the error word; CTA-uniform
 
@@ -510,29 +521,29 @@ __global__ void __launch_bounds__(128) short_tc_kernel(const PoolView P,
   // first group: what the score pass needs (keys, q, gates); second: the values,
   // still in flight while the scores are formed
   for (int c = tid; c < n * 16; c += 128) {
-    const int i = c >> 4, p = (c & 15) * 8;
-    scp16(Kr + i * XS + p, kb + koff[i] + p);
+    const int i = c >> 4, p = c & 15;
+    scp16(Kr + swz(i, p), kb + (size_t)krow[i] * D + p * 8);
   }
   if (tid < 32) {
-    const int p = (tid & 15) * 8;
-    if (tid < 16) scp16(qs + p, static_cast<const KT *>(io.q) + (b * P.Hk + hq) * D + p);
-    else scp16(Kr + n * XS + p, static_cast<const KT *>(io.k) + (b * P.Hk + hq) * D + p);
+    const int p = tid & 15;
+    if (tid < 16) scp16(qs + p * 8, static_cast<const KT *>(io.q) + (b * P.Hk + hq) * D + p * 8);
+    else scp16(Kr + swz(n, p), static_cast<const KT *>(io.k) + (b * P.Hk + hq) * D + p * 8);
   }
-  if (GATED && tid >= 64 && tid - 64 < n) scp4(As + tid - 64, P.gbuf + voff[tid - 64]);
+  if (GATED && tid >= 64 && tid - 64 < n) scp4(As + tid - 64, P.gbuf + vrow[tid - 64]);
   asm volatile("cp.async.commit_group;\n" ::: "memory");
   for (int c = tid; c < n * 16; c += 128) {
-    const int i = c >> 4, p = (c & 15) * 8;
-    scp16(Vr + i * XS + p, vb + voff[i] * D + p);
+    const int i = c >> 4, p = c & 15;
+    scp16(Vr + swz(i, p), vb + (size_t)vrow[i] * D + p * 8);
   }
   if (tid >= 32 && tid < 48) {
-    const int p = (tid & 15) * 8;
-    scp16(Vr + n * XS + p, static_cast<const KT *>(io.v) + (b * P.Hv + h) * D + p);
+    const int p = tid & 15;
+    scp16(Vr + swz(n, p), static_cast<const KT *>(io.v) + (b * P.Hv + h) * D + p * 8);
   }
   asm volatile("cp.async.commit_group;\n" ::: "memory");
   // meanwhile: zero the padded value rows (the output product reads them) and
   // the padded tokens' weights
   for (int c = tid; c < (LP - L) * 16; c += 128)
-    *reinterpret_cast<uint4 *>(Vr + (L + (c >> 4)) * XS + (c & 15) * 8) = make_uint4(0u, 0u, 0u, 0u);
+    *reinterpret_cast<uint4 *>(Vr + (L + (c >> 4)) * 256 + (c & 15) * 16) = make_uint4(0u, 0u, 0u, 0u);
   if (tid >= L && tid < LP) whi[tid] = wlo[tid] = __float2bfloat16_rn(0.f);
   const float a_t = GATED && io.log_g ? io.log_g[b * P.Hv + h] : 0.f;
   asm volatile("cp.async.wait_group 1;\n" ::: "memory");  // keys, q and gates
@@ -551,19 +562,23 @@ __global__ void __launch_bounds__(128) short_tc_kernel(const PoolView P,
       bq[ks][1] = g == 0 ? *reinterpret_cast<const uint32_t *>(qs + 16 * ks + 2 * t + 8) : 0u;
     }
     const int mtiles = (L + 15) >> 4;
+    // lane l addresses row l & 15 of a tile (row & 7 == l & 7) and chunk 2 ks + (l >> 4)
     const uint32_t kaddr = static_cast<uint32_t>(__cvta_generic_to_shared(Kr)) +
-                           (uint32_t)((lane & 15) * XS * 2 + (lane >> 4) * 16);
+                           (uint32_t)((lane & 15) * 256);
+    const int xr = lane & 7, ch = lane >> 4;
     for (int mt = warp; mt < mtiles; mt += NW) {
       // two accumulator chains (even and odd k-steps) halve the dependent MMA chain
       float acc[4] = {0.f, 0.f, 0.f, 0.f}, acc2[4] = {0.f, 0.f, 0.f, 0.f};
-      const uint32_t ka = kaddr + (uint32_t)(mt * 16 * XS * 2);
+      const uint32_t ka = kaddr + (uint32_t)(mt * 16 * 256);
 #pragma unroll
       for (int ks = 0; ks < 8; ks += 2) {
         uint32_t a0, a1, a2, a3, c0, c1, c2, c3;
         asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
-                     : "=r"(a0), "=r"(a1), "=r"(a2), "=r"(a3) : "r"(ka + ks * 32));
+                     : "=r"(a0), "=r"(a1), "=r"(a2), "=r"(a3)
+                     : "r"(ka + (uint32_t)(((2 * ks + ch) ^ xr) << 4)));
         asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
-                     : "=r"(c0), "=r"(c1), "=r"(c2), "=r"(c3) : "r"(ka + ks * 32 + 32));
+                     : "=r"(c0), "=r"(c1), "=r"(c2), "=r"(c3)
+                     : "r"(ka + (uint32_t)(((2 * ks + 2 + ch) ^ xr) << 4)));
         mma_bf16_full(acc, a0, a1, a2, a3, bq[ks][0], bq[ks][1]);
         mma_bf16_full(acc2, c0, c1, c2, c3, bq[ks + 1][0], bq[ks + 1][1]);
       }
@@ -593,19 +608,22 @@ __global__ void __launch_bounds__(128) short_tc_kernel(const PoolView P,
   float oc[2][4];
 #pragma unroll
   for (int mt = 0; mt < 2; ++mt) oc[mt][0] = oc[mt][1] = oc[mt][2] = oc[mt][3] = 0.f;
+  // lane l addresses row (l & 7) + 8 (l >> 4) of a 16-token step (row & 7 == l & 7)
+  // and chunk 4 w + ((l >> 3) & 1) + 2 mt
   const uint32_t vaddr = static_cast<uint32_t>(__cvta_generic_to_shared(Vr)) +
-                         (uint32_t)((((lane & 7) + ((lane >> 4) << 3)) * XS * 2) +
-                                    (4 * warp + ((lane >> 3) & 1)) * 16);
+                         (uint32_t)(((lane & 7) + ((lane >> 4) << 3)) * 256);
+  const int vch = 4 * warp + ((lane >> 3) & 1), vx = lane & 7;
+  const uint32_t vo0 = (uint32_t)((vch ^ vx) << 4), vo1 = (uint32_t)(((vch + 2) ^ vx) << 4);
   const KT *wsrc = g == 0 ? whi : wlo;
   for (int kk = 0; kk < LP / 16; ++kk) {
     const uint32_t b0 = g < 2 ? *reinterpret_cast<const uint32_t *>(wsrc + 16 * kk + 2 * t) : 0u;
     const uint32_t b1 = g < 2 ? *reinterpret_cast<const uint32_t *>(wsrc + 16 * kk + 2 * t + 8) : 0u;
-    const uint32_t va = vaddr + (uint32_t)(16 * kk * XS * 2);
+    const uint32_t va = vaddr + (uint32_t)(16 * kk * 256);
 #pragma unroll
     for (int mt = 0; mt < 2; ++mt) {
       uint32_t a0, a1, a2, a3;
       asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
-                   : "=r"(a0), "=r"(a1), "=r"(a2), "=r"(a3) : "r"(va + mt * 32));
+                   : "=r"(a0), "=r"(a1), "=r"(a2), "=r"(a3) : "r"(va + (mt ? vo1 : vo0)));
       mma_bf16_full(oc[mt], a0, a1, a2, a3, b0, b1);
     }
   }
@@ -621,14 +639,14 @@ __global__ void __launch_bounds__(128) short_tc_kernel(const PoolView P,
     }
   }
   if (tid < 16) {
-    *reinterpret_cast<uint4 *>(static_cast<KT *>(P.vbuf) + voff[n] * D + tid * 8) =
-        *reinterpret_cast<const uint4 *>(Vr + n * XS + tid * 8);
+    *reinterpret_cast<uint4 *>(static_cast<KT *>(P.vbuf) + (size_t)vrow[n] * D + tid * 8) =
+        *reinterpret_cast<const uint4 *>(Vr + swz(n, tid));
   } else if (tid < 32 && h % group == 0) {
-    *reinterpret_cast<uint4 *>(static_cast<KT *>(P.kbuf) + koff[n] + (tid - 16) * 8) =
-        *reinterpret_cast<const uint4 *>(Kr + n * XS + (tid - 16) * 8);
+    *reinterpret_cast<uint4 *>(static_cast<KT *>(P.kbuf) + (size_t)krow[n] * D + (tid - 16) * 8) =
+        *reinterpret_cast<const uint4 *>(Kr + swz(n, tid - 16));
   } else if (tid == 32) {
-    P.gbuf[voff[n]] = GATED ? A_t : 0.f;  // cumulative
-    P.bbuf[voff[n]] = 0.f;
+    P.gbuf[vrow[n]] = GATED ? A_t : 0.f;  // cumulative
+    P.bbuf[vrow[n]] = 0.f;
     if (h == 0) P.dlen[d.req] = n + 1;
   }
 }
