@@ -23,6 +23,8 @@
 // inside the warp.  The state tile stays in
 // registers from its load to the fold, so S crosses HBM once per step (twice
 // on a fold step, once in each direction).
+#include <type_traits>
+
 #include "kvb_device.cuh"
 
 namespace kvb {
@@ -45,9 +47,11 @@ __global__ void __launch_bounds__(2 * D / NSPLIT, 512 / (2 * D / NSPLIT))
   const int n = RECURRENT ? 0 : d.n;
   const bool fold = RECURRENT || (d.flags & kFlagFlush);
 
+  // staged rows of the folded tokens, in the orders of fold_tile (kvb_device.cuh)
+  constexpr int KST = DK + 8, UST = DV + 8;
   extern __shared__ float4 dyn_smem[];
-  float *ks = reinterpret_cast<float *>(dyn_smem);  // [lmax][DK] keys of folded tokens
-  float *us = ks + (size_t)io.lmax * DK;            // [lmax][DV] their u
+  float *ks = reinterpret_cast<float *>(dyn_smem);  // [lmax][KST] keys of folded tokens
+  float *us = ks + (size_t)io.lmax * KST;           // [lmax][UST] their u
   __shared__ __align__(16) float qs[DK];
   __shared__ __align__(16) float kts[DK];
   __shared__ float wt[kMaxTok], sc[kMaxTok], cc[kMaxTok];
@@ -194,8 +198,9 @@ __global__ void __launch_bounds__(2 * D / NSPLIT, 512 / (2 * D / NSPLIT))
     if (fold) {
 #pragma unroll
       for (int e = 0; e < E; ++e) {
-        ks[i0 * DK + lane * E + e] = ka[e];
-        if (i1 <= n) ks[i1 * DK + lane * E + e] = kb[e];
+        const int kp = fold_kpos<RPT>(lane * E + e);
+        ks[i0 * KST + kp] = ka[e];
+        if (i1 <= n) ks[i1 * KST + kp] = kb[e];
       }
     }
   }
@@ -216,7 +221,7 @@ __global__ void __launch_bounds__(2 * D / NSPLIT, 512 / (2 * D / NSPLIT))
     const float w = wt[i];
     fma4(po, w * sc[i], ui);
     if (DELTA) fma4(pc, w * cc[i], ui);
-    if (fold) *reinterpret_cast<float4 *>(&us[i * DV + col0]) = ui;
+    if (fold) fold_stage_u(&us[i * UST + col0], ui);
   }
   po = rows_sum4(po);
   if (DELTA) pc = rows_sum4(pc);
@@ -235,7 +240,7 @@ __global__ void __launch_bounds__(2 * D / NSPLIT, 512 / (2 * D / NSPLIT))
       st4(static_cast<KT *>(P.vbuf) + voff[n] * DV + col0, vt);
       if (DELTA) st4(P.ubuf + voff[n] * DV + col0, ut);
     }
-    if (fold) *reinterpret_cast<float4 *>(&us[n * DV + col0]) = ut;
+    if (fold) fold_stage_u(&us[n * UST + col0], ut);
   }
   if (!RECURRENT && lead) {
     if (h % group == 0)
@@ -248,22 +253,13 @@ __global__ void __launch_bounds__(2 * D / NSPLIT, 512 / (2 * D / NSPLIT))
   }
 
   // 7. fold: S <- e^{A_t} S0 + sum_{i<=n} k_i (w_i u_i)^T, a rank-(n+1) update of the
-  //    register tile, written back once
+  //    register tile (on the tensor cores above rank 4), written back once
   if (fold && has_state) {
     __syncthreads();
 #pragma unroll
     for (int j = 0; j < RPT; ++j) s[j] = mul4(e_t, s[j]);
-    for (int i = 0; i <= n; ++i) {
-      const float4 u = mul4(wt[i], *reinterpret_cast<const float4 *>(&us[i * DV + col0]));
-#pragma unroll
-      for (int j = 0; j < RPT; j += 4) {
-        const float4 k4 = *reinterpret_cast<const float4 *>(&ks[i * DK + row0 + j]);
-        fma4(s[j], k4.x, u);
-        fma4(s[j + 1], k4.y, u);
-        fma4(s[j + 2], k4.z, u);
-        fma4(s[j + 3], k4.w, u);
-      }
-    }
+    fold_tile<RPT, std::is_same<KT, __nv_bfloat16>::value>(s, ks, KST, us, UST, col0 - 4 * (lane & 3),
+                                                            wt, n, lane);
 #pragma unroll
     for (int j = 0; j < RPT; ++j) st_stream4(Sp + (row0 + j) * DV + col0, s[j]);
   }
@@ -305,7 +301,7 @@ template <typename KT, int VARIANT, int D, bool REC>
 static cudaError_t run_decode(const PoolView &P, const RowBatch &rows, const TokenIO &io,
                               cudaStream_t stream) {
   constexpr int NS = (D == 128) ? KVB_DECODE_SPLIT : 1;
-  const size_t smem = (size_t)io.lmax * 2 * D * sizeof(float);
+  const size_t smem = (size_t)io.lmax * 2 * (D + 8) * sizeof(float);
   cudaError_t e = ensure_smem((const void *)decode_kernel<KT, VARIANT, D, REC, NS>, smem);
   if (e != cudaSuccess) return e;
   dim3 grid(P.Hv * NS, rows.count);

@@ -15,6 +15,8 @@
 // while every resident CTA of an SM computes.  The tile is stored with its
 // 16-byte chunks XOR-swizzled on row bit 4, so the per-thread reads (16 rows x
 // 4 columns) are free of bank conflicts.
+#include <type_traits>
+
 #include "kvb_device.cuh"
 
 namespace kvb {
@@ -23,6 +25,18 @@ namespace {
 constexpr int kD = 128, kCW = 64;       // head dim; state columns per item
 constexpr int kTileF4 = kD * kCW / 4;   // float4 chunks of a tile (2048)
 constexpr int kStreamThreads = 128;
+
+// A folding unit of a bf16 pool runs its rank update on the tensor cores
+// (fold_tile, kvb_device.cuh) from rows restaged in that routine's orders: the
+// keys of tokens 0..n over all state rows, and the current half's u.  fp32
+// pools keep FMAs (their restaged rows would cost a resident CTA per SM).
+constexpr int kFoldKS = kD + 8, kFoldUS = kCW + 8;  // staged row strides (floats)
+template <typename KT>
+constexpr bool kFoldOnTc = std::is_same<KT, __nv_bfloat16>::value;
+template <typename KT>
+constexpr size_t fold_stage_bytes() {
+  return kFoldOnTc<KT> ? (size_t)(kStageTok + 1) * (kFoldKS + kFoldUS) * sizeof(float) : 0;
+}
 
 // The small operands of one head (double-buffered); the state tile has a
 // single buffer, refilled as soon as a tile has moved into registers.
@@ -75,6 +89,8 @@ __global__ void __launch_bounds__(kStreamThreads, 4)
   extern __shared__ float4 dyn_smem[];
   float4 *tile = dyn_smem;                                // [kTileF4] swizzled
   St *stages = reinterpret_cast<St *>(dyn_smem + kTileF4);  // [2]
+  float *fks = reinterpret_cast<float *>(stages + 2);       // [kStageTok + 1][kFoldKS] (bf16 pools)
+  float *fus = fks + (kStageTok + 1) * kFoldKS;             // [kStageTok + 1][kFoldUS]
   __shared__ __align__(16) float qs[kD], kts[kD];
   __shared__ float wt[kStageTok + 1], sc[kStageTok + 1], cc[kStageTok + 1];
   __shared__ float e_t_s, At_s;
@@ -294,7 +310,27 @@ __global__ void __launch_bounds__(kStreamThreads, 4)
     }
 
     // fold: S <- e^{A_t} S0 + sum_{i<=n} k_i (w_i u_i)^T, written back once
-    if (fold) {
+    if (fold && kFoldOnTc<KT>) {
+#pragma unroll
+      for (int j = 0; j < RPT; ++j) s[j] = mul4(e_t, s[j]);
+      // restage the unit's keys (first half; they serve both) and this half's u,
+      // then the rank-(n+1) update (CTA-uniform: the whole CTA works on one unit)
+      if (lead)
+        for (int c = tid; c < (n + 1) * kD; c += kStreamThreads) {
+          const int i = c >> 7, p = c & (kD - 1), r = fold_krow<RPT>(p);
+          fks[i * kFoldKS + p] = i < n ? to_float(S.keys[i][r]) : kts[r];
+        }
+      for (int i = rsub; i <= n; i += 8)
+        fold_stage_u(&fus[i * kFoldUS + colL],
+                     i < n ? (DELTA ? *reinterpret_cast<const float4 *>(&S.uv[i][col0])
+                                    : raw4(reinterpret_cast<const KT *>(S.uv[i]) + col0))
+                           : ut);
+      __syncthreads();
+      fold_tile<RPT, true>(s, fks, kFoldKS, fus, kFoldUS, 16 * warp, wt, n, lane);
+      float *Sp = P.state + ((size_t)d.slot * P.Hv + h) * kD * kD;
+#pragma unroll
+      for (int j = 0; j < RPT; ++j) st_stream4(Sp + (size_t)(row0 + j) * kD + col0, s[j]);
+    } else if (fold) {
 #pragma unroll
       for (int j = 0; j < RPT; ++j) s[j] = mul4(e_t, s[j]);
       for (int i = 0; i <= n; ++i) {
@@ -384,6 +420,8 @@ __global__ void __launch_bounds__(kStreamThreads, 4)
   extern __shared__ float4 dyn_smem[];
   float4 *tile = dyn_smem;
   St *stages = reinterpret_cast<St *>(dyn_smem + kTileF4);
+  float *fks = reinterpret_cast<float *>(stages + 2);  // [kStageTok + 1][kFoldKS] (bf16 pools)
+  float *fus = fks + (kStageTok + 1) * kFoldKS;        // [kStageTok + 1][kFoldUS]
   __shared__ float wt[kStageTok];
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -451,16 +489,32 @@ __global__ void __launch_bounds__(kStreamThreads, 4)
   auto fold_half = [&](float4 (&s)[RPT], const St &S, int part, int y, int h) {
     const RowDesc &d = rows.r[y];
     const int L = d.n, col0 = part * kCW + colL;
-    for (int i = 0; i < L; ++i) {
-      const float4 u = mul4(wt[i], DELTA ? *reinterpret_cast<const float4 *>(&S.uv[i][col0])
-                                         : raw4(reinterpret_cast<const KT *>(S.uv[i]) + col0));
+    if constexpr (kFoldOnTc<KT>) {
+      // restage the unit's keys (first half; they serve both) and this half's u,
+      // then the rank-L update (CTA-uniform: the whole CTA works on one unit)
+      if (part == 0)
+        for (int c = tid; c < L * kD; c += kStreamThreads) {
+          const int i = c >> 7, p = c & (kD - 1);
+          fks[i * kFoldKS + p] = to_float(S.keys[i][fold_krow<RPT>(p)]);
+        }
+      for (int i = rsub; i < L; i += 8)
+        fold_stage_u(&fus[i * kFoldUS + colL],
+                     DELTA ? *reinterpret_cast<const float4 *>(&S.uv[i][col0])
+                           : raw4(reinterpret_cast<const KT *>(S.uv[i]) + col0));
+      __syncthreads();
+      fold_tile<RPT, true>(s, fks, kFoldKS, fus, kFoldUS, 16 * warp, wt, L - 1, lane);
+    } else {
+      for (int i = 0; i < L; ++i) {
+        const float4 u = mul4(wt[i], DELTA ? *reinterpret_cast<const float4 *>(&S.uv[i][col0])
+                                           : raw4(reinterpret_cast<const KT *>(S.uv[i]) + col0));
 #pragma unroll
-      for (int j = 0; j < RPT; j += 4) {
-        const float4 k4 = raw4(&S.keys[i][row0 + j]);
-        fma4(s[j], k4.x, u);
-        fma4(s[j + 1], k4.y, u);
-        fma4(s[j + 2], k4.z, u);
-        fma4(s[j + 3], k4.w, u);
+        for (int j = 0; j < RPT; j += 4) {
+          const float4 k4 = raw4(&S.keys[i][row0 + j]);
+          fma4(s[j], k4.x, u);
+          fma4(s[j + 1], k4.y, u);
+          fma4(s[j + 2], k4.z, u);
+          fma4(s[j + 3], k4.w, u);
+        }
       }
     }
     float *Sp = P.state + ((size_t)d.slot * P.Hv + h) * kD * kD;
@@ -509,7 +563,7 @@ __global__ void __launch_bounds__(kStreamThreads, 4)
 // Resident CTAs of the kernel on the current device (its persistent grid).
 template <typename KT, int VARIANT>
 int flush_ctas() {
-  constexpr size_t smem = kTileF4 * sizeof(float4) + 2 * sizeof(FStage<KT>);
+  constexpr size_t smem = kTileF4 * sizeof(float4) + 2 * sizeof(FStage<KT>) + fold_stage_bytes<KT>();
   int ctas = 0;
   return resident_ctas((const void *)flush_stream_kernel<KT, VARIANT>, kStreamThreads, smem,
                        &ctas) == cudaSuccess ? ctas : 0;
@@ -517,7 +571,7 @@ int flush_ctas() {
 
 template <typename KT, int VARIANT>
 cudaError_t run_flush_stream(const PoolView &P, const RowBatch &rows, cudaStream_t stream) {
-  constexpr size_t smem = kTileF4 * sizeof(float4) + 2 * sizeof(FStage<KT>);
+  constexpr size_t smem = kTileF4 * sizeof(float4) + 2 * sizeof(FStage<KT>) + fold_stage_bytes<KT>();
   const int cap = flush_ctas<KT, VARIANT>();
   if (cap <= 0) return kUnsupported;
   const int units = rows.count * P.Hv;
@@ -540,7 +594,7 @@ int fctas_for(int variant) {
 // Resident CTAs of the kernel on the current device (its persistent grid).
 template <typename KT, int VARIANT>
 int stream_ctas() {
-  constexpr size_t smem = kTileF4 * sizeof(float4) + 2 * sizeof(Stage<KT>);
+  constexpr size_t smem = kTileF4 * sizeof(float4) + 2 * sizeof(Stage<KT>) + fold_stage_bytes<KT>();
   int ctas = 0;
   return resident_ctas((const void *)decode_stream_kernel<KT, VARIANT>, kStreamThreads, smem,
                        &ctas) == cudaSuccess ? ctas : 0;
@@ -549,7 +603,7 @@ int stream_ctas() {
 template <typename KT, int VARIANT>
 cudaError_t run_stream(const PoolView &P, const RowBatch &rows, const TokenIO &io,
                        cudaStream_t stream) {
-  constexpr size_t smem = kTileF4 * sizeof(float4) + 2 * sizeof(Stage<KT>);
+  constexpr size_t smem = kTileF4 * sizeof(float4) + 2 * sizeof(Stage<KT>) + fold_stage_bytes<KT>();
   const int cap = stream_ctas<KT, VARIANT>();
   if (cap <= 0) return kUnsupported;
   const int units = rows.count * P.Hv;

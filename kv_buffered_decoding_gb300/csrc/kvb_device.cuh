@@ -245,4 +245,116 @@ __device__ __forceinline__ void mma_tf32(float (&d)[4], const uint32_t (&a)[4], 
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
+// The same product with the four accumulators of the tile given separately.
+__device__ __forceinline__ void mma_tf32(float &d0, float &d1, float &d2, float &d3,
+                                         const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm(
+      "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d0), "+f"(d1), "+f"(d2), "+f"(d3)
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// ------------------------------------------------------------------ the fold's rank update
+// The decode kernels hold a state tile in registers: lane (g = lane >> 2,
+// t = lane & 3) of a warp owns rows RPT g .. RPT g + RPT - 1 and columns
+// 4t .. 4t + 3 of the warp's 16 (s[j]: row RPT g + j).  A fold adds
+// sum_{i<=n} k_i (w_i u_i)^T.  Read as mma.sync m16n8k8 tiles, the same
+// registers are the accumulators when row r of row tile m is state row
+// RPT (r mod 8) + 2m + r / 8 and column c of column tile h is column
+// 4 (c / 2) + (c mod 2) + 2h: tile (m, h) holds s[2m] and s[2m + 1] (.x, .y for
+// h = 0; .z, .w for h = 1), so no value moves between lanes.  The staged keys
+// and values are stored in the matching orders (fold_kpos, fold_stage_u), so
+// that each operand fragment is one 64-bit shared load; a staged row stride of
+// 8 (mod 32) words keeps those loads free of bank conflicts.
+
+// Position of state row `row` (0 .. 8 RPT - 1) within a staged key row.
+template <int RPT>
+__device__ __forceinline__ int fold_kpos(int row) {
+  const int g = row / RPT, w = row - g * RPT;
+  return (w >> 1) * 16 + 2 * g + (w & 1);
+}
+// State row held at position p of a staged key row (the inverse of fold_kpos).
+template <int RPT>
+__device__ __forceinline__ int fold_krow(int p) {
+  return RPT * ((p & 15) >> 1) + 2 * (p >> 4) + (p & 1);
+}
+// Stage a lane's u values of columns 4t .. 4t + 3 of a 16-column block at p
+// (column 4t of the staged row) in fold order: columns 4t, 4t + 2, 4t + 1, 4t + 3.
+__device__ __forceinline__ void fold_stage_u(float *p, float4 u) {
+  *reinterpret_cast<float4 *>(p) = make_float4(u.x, u.z, u.y, u.w);
+}
+// s += sum_{i<=n} k_i (w_i u_i)^T over this warp's tile, for staged key rows
+// ks + i kst (fold_kpos order) and value rows us + i ust whose 16-column block
+// of this warp starts at ublk (fold order), weights wt[i].  Ranks up to 4 use
+// FMAs.  Larger ranks use the tensor cores, 8 tokens per k-step, with w_i u_i
+// split into tf32 hi and lo parts (about 21 significant bits).  The keys are
+// split too unless KEYS_TF32 (values that came from bf16 are exact in tf32).
+// Tokens past n enter as zeros.
+template <int RPT, bool KEYS_TF32>
+__device__ __forceinline__ void fold_tile(float4 (&s)[RPT], const float *ks, int kst,
+                                          const float *us, int ust, int ublk, const float *wt,
+                                          int n, int lane) {
+  const int g = lane >> 2, t = lane & 3;
+  if (n < 4) {
+    for (int i = 0; i <= n; ++i) {
+      const float4 uu = *reinterpret_cast<const float4 *>(us + i * ust + ublk + 4 * t);
+      const float w = wt[i];
+      const float4 u = make_float4(w * uu.x, w * uu.z, w * uu.y, w * uu.w);
+#pragma unroll
+      for (int j = 0; j < RPT; j += 2) {
+        const float2 k2 = *reinterpret_cast<const float2 *>(ks + i * kst + (j >> 1) * 16 + 2 * g);
+        fma4(s[j], k2.x, u);
+        fma4(s[j + 1], k2.y, u);
+      }
+    }
+    return;
+  }
+  for (int kk = 0; kk <= n; kk += 8) {
+    const int i0 = kk + t, i1 = i0 + 4;  // this lane's k rows t and t + 4
+    float2 u0 = make_float2(0.f, 0.f), u1 = u0;
+    float w0 = 0.f, w1 = 0.f;
+    if (i0 <= n) {
+      u0 = *reinterpret_cast<const float2 *>(us + i0 * ust + ublk + 2 * g);
+      w0 = wt[i0];
+    }
+    if (i1 <= n) {
+      u1 = *reinterpret_cast<const float2 *>(us + i1 * ust + ublk + 2 * g);
+      w1 = wt[i1];
+    }
+    uint32_t bh0[2], bl0[2], bh1[2], bl1[2];  // column tiles 0 and 1: k rows t, t + 4
+    split_tf32(w0 * u0.x, bh0[0], bl0[0]);
+    split_tf32(w1 * u1.x, bh0[1], bl0[1]);
+    split_tf32(w0 * u0.y, bh1[0], bl1[0]);
+    split_tf32(w1 * u1.y, bh1[1], bl1[1]);
+#pragma unroll
+    for (int m = 0; m < RPT / 2; ++m) {
+      float2 k0 = make_float2(0.f, 0.f), k1 = k0;
+      if (i0 <= n) k0 = *reinterpret_cast<const float2 *>(ks + i0 * kst + m * 16 + 2 * g);
+      if (i1 <= n) k1 = *reinterpret_cast<const float2 *>(ks + i1 * kst + m * 16 + 2 * g);
+      float4 &r0 = s[2 * m], &r1 = s[2 * m + 1];
+      if (KEYS_TF32) {
+        const uint32_t a[4] = {__float_as_uint(k0.x), __float_as_uint(k0.y), __float_as_uint(k1.x),
+                               __float_as_uint(k1.y)};
+        mma_tf32(r0.x, r0.y, r1.x, r1.y, a, bh0[0], bh0[1]);
+        mma_tf32(r0.z, r0.w, r1.z, r1.w, a, bh1[0], bh1[1]);
+        mma_tf32(r0.x, r0.y, r1.x, r1.y, a, bl0[0], bl0[1]);
+        mma_tf32(r0.z, r0.w, r1.z, r1.w, a, bl1[0], bl1[1]);
+      } else {
+        uint32_t a[4], al[4];
+        split_tf32(k0.x, a[0], al[0]);
+        split_tf32(k0.y, a[1], al[1]);
+        split_tf32(k1.x, a[2], al[2]);
+        split_tf32(k1.y, a[3], al[3]);
+        mma_tf32(r0.x, r0.y, r1.x, r1.y, a, bh0[0], bh0[1]);
+        mma_tf32(r0.z, r0.w, r1.z, r1.w, a, bh1[0], bh1[1]);
+        mma_tf32(r0.x, r0.y, r1.x, r1.y, a, bl0[0], bl0[1]);
+        mma_tf32(r0.z, r0.w, r1.z, r1.w, a, bl1[0], bl1[1]);
+        mma_tf32(r0.x, r0.y, r1.x, r1.y, al, bh0[0], bh0[1]);
+        mma_tf32(r0.z, r0.w, r1.z, r1.w, al, bh1[0], bh1[1]);
+      }
+    }
+  }
+}
+
 }  // namespace kvb
