@@ -11,11 +11,15 @@
 // CTAs per head at d = 128, 16 consecutive rows per lane as in decode).  At
 // L <= 64 this is 2 L flop per state element against 8 bytes of state traffic
 // per element (read + write), i.e. below the fp32 FMA ridge: the kernel is
-// bound by HBM, and the update runs on the FMA pipes.
+// bound by HBM.  Above rank 4 the update runs as mma.sync tf32 products on the
+// register tile in place (fold_tile, kvb_device.cuh), which issues far fewer
+// instructions than the FMAs.
 //
 // Used by kvb_flush, by kvb_accept when accepted drafts fill the buffer and by
 // kvb_promote (rows flagged kFlagFromZero start from S = 0); decode folds
 // in-kernel (decode.cu).
+#include <type_traits>
+
 #include "kvb_device.cuh"
 
 namespace kvb {
@@ -34,9 +38,11 @@ __global__ void __launch_bounds__(2 * D / NSPLIT, 512 / (2 * D / NSPLIT))
   const int hq = h / (P.Hv / P.Hk);
   const int L = d.n;
 
+  // staged rows in the orders of fold_tile (kvb_device.cuh)
+  constexpr int KST = DK + 8, UST = CW + 8;
   extern __shared__ float4 dyn_smem[];
-  float *ks = reinterpret_cast<float *>(dyn_smem);  // [L][DK] keys
-  float *us = ks + (size_t)L * DK;                  // [L][CW] w_i u_i for this CTA's columns
+  float *ks = reinterpret_cast<float *>(dyn_smem);  // [L][KST] keys
+  float *us = ks + (size_t)L * KST;                 // [L][UST] u_i for this CTA's columns
   __shared__ float wt[kMaxTok];
   __shared__ size_t koff[kMaxTok], voff[kMaxTok];
   __shared__ float eL_s;
@@ -80,11 +86,11 @@ __global__ void __launch_bounds__(2 * D / NSPLIT, 512 / (2 * D / NSPLIT))
     }
   }
   for (int idx = tid; idx < L * (DK / 4); idx += NT) {
-    const int i = idx / (DK / 4), c = (idx % (DK / 4)) * 4;
-    *reinterpret_cast<float4 *>(&ks[(size_t)i * DK + c]) =
-        ld4(static_cast<const KT *>(P.kbuf) + koff[i] + c);
+    const int i = idx / (DK / 4), c = (idx % (DK / 4)) * 4;  // rows c .. c + 3
+    const float4 k4 = ld4(static_cast<const KT *>(P.kbuf) + koff[i] + c);
+    *reinterpret_cast<float2 *>(&ks[(size_t)i * KST + fold_kpos<RPT>(c)]) = make_float2(k4.x, k4.y);
+    *reinterpret_cast<float2 *>(&ks[(size_t)i * KST + fold_kpos<RPT>(c + 2)]) = make_float2(k4.z, k4.w);
   }
-  __syncthreads();
   for (int idx = tid; idx < L * (CW / 4); idx += NT) {
     const int i = idx / (CW / 4), c = (idx % (CW / 4)) * 4;
     float4 u;
@@ -92,25 +98,16 @@ __global__ void __launch_bounds__(2 * D / NSPLIT, 512 / (2 * D / NSPLIT))
       u = ld4(P.ubuf + voff[i] * DV + part * CW + c);
     else
       u = ld4(static_cast<const KT *>(P.vbuf) + voff[i] * DV + part * CW + c);
-    *reinterpret_cast<float4 *>(&us[(size_t)i * CW + c]) = mul4(wt[i], u);
+    fold_stage_u(&us[(size_t)i * UST + c], u);
   }
-  __syncthreads();
+  __syncthreads();  // weights, keys and values staged
 
-  // S <- e^{A_L} S0 + sum_i k_i (w_i u_i)^T, keys four rows per 128-bit load
+  // S <- e^{A_L} S0 + sum_i k_i (w_i u_i)^T
   const float eL = eL_s;
 #pragma unroll
   for (int j = 0; j < RPT; ++j) s[j] = mul4(eL, s[j]);
-  for (int i = 0; i < L; ++i) {
-    const float4 u = *reinterpret_cast<const float4 *>(&us[(size_t)i * CW + colL]);
-#pragma unroll
-    for (int j = 0; j < RPT; j += 4) {
-      const float4 k4 = *reinterpret_cast<const float4 *>(&ks[(size_t)i * DK + row0 + j]);
-      fma4(s[j], k4.x, u);
-      fma4(s[j + 1], k4.y, u);
-      fma4(s[j + 2], k4.z, u);
-      fma4(s[j + 3], k4.w, u);
-    }
-  }
+  fold_tile<RPT, std::is_same<KT, __nv_bfloat16>::value>(s, ks, KST, us, UST, warp * 16, wt, L - 1,
+                                                          lane);
 #pragma unroll
   for (int j = 0; j < RPT; ++j) st_stream4(Sp + (row0 + j) * DV + col0, s[j]);
   if (h == 0 && part == 0 && tid == 0) P.dlen[d.req] = 0;
@@ -120,7 +117,7 @@ template <typename KT, int VARIANT, int D>
 static cudaError_t run_flush(const PoolView &P, const RowBatch &rows, int max_len,
                              cudaStream_t stream) {
   constexpr int NS = D == 128 ? 2 : 1;
-  const size_t smem = (size_t)max_len * (D + D / NS) * sizeof(float);
+  const size_t smem = (size_t)max_len * ((D + 8) + (D / NS + 8)) * sizeof(float);
   cudaError_t e = ensure_smem((const void *)flush_kernel<KT, VARIANT, D, NS>, smem);
   if (e != cudaSuccess) return e;
   dim3 grid(P.Hv * NS, rows.count);
