@@ -210,6 +210,42 @@ def _gdn_full(B, steps, seed, stagger, scale=1.0):
     return err_o.max(), err_s.max()
 
 
+@pytest.mark.parametrize("layer", [
+    I.Layer(I.GATED, 2, 4, 128, 128, "f32"),
+    I.Layer(I.GATED_DELTA, 2, 4, 128, 128, "f32", qk_dist="l2norm"),
+], ids=["gated_f32", "gated_delta_f32"])
+@pytest.mark.parametrize("m", [5, 8, 12])
+def test_fold_ranks_f32_d128(layer, m):
+    """Folds of rank 5 to 12 on an fp32 pool at d = 128, in the per-head decode and flush
+    kernels. Above rank 4 the rank update runs as tf32 tensor-core products with the fp32
+    keys split into two parts (three products per tile); ranks above 8 take two k-steps.
+    Every output and the state after every fold match the recurrence, and so does the state
+    after a final flush of m - 1 tokens."""
+    rng = np.random.default_rng(800 + m + 10 * layer.variant)
+    B, bs = 3, 4
+    steps = 3 * m - 1  # two folds, then m - 1 tokens left for the flush
+    nb = blocks_needed(m, bs)
+    pool = make_pool(layer, m, B, nb, bs)
+    S0 = I.draw_state(rng, layer, B)
+    pool.state.copy_(torch.from_numpy(S0))
+    for r in range(B):
+        pool.set_request(r, r, list(range(r * nb, (r + 1) * nb)))
+    tok = I.draw_tokens(rng, layer, (steps, B))
+    o_ref, _, states = oracle.decode_sequence(S0.astype(np.float64), tok, layer.variant,
+                                              keep_states=range(steps))
+    tol = tol_for(layer)
+    req = np.arange(B)
+    for t in range(steps):
+        o = pool.decode(req, *token_tensors(tok, layer, t)).cpu().numpy()
+        assert rel_err(o, o_ref[t]) <= tol, t
+        if (t + 1) % m == 0:
+            assert rel_err(pool.state.cpu().numpy(), states[t]) <= tol, t
+    assert (pool.get_lengths() == m - 1).all()
+    pool.flush(req)
+    assert rel_err(pool.state.cpu().numpy(), states[steps - 1]) <= tol
+    assert pool.get_error() is None
+
+
 def test_gdn_small_batch_full_compare():
     _gdn_full(4, 40, seed=20, stagger=True)
 
