@@ -430,7 +430,7 @@ __global__ void __launch_bounds__(128) short_mma_kernel(const PoolView P,
 // bf16 pools at d = 128 without the delta rule (u = v): one CTA of four warps
 // per (batch row, value head), both sums on the tensor cores.  The chunk
 // (tokens 0..n-1 buffered, token n the current one) arrives by 16-byte cp.async
-// copies in padded rows.  The score dots q.k_i are one mma.sync pass with the
+// copies in swizzled rows (below).  The score dots q.k_i are one mma.sync pass with the
 // keys as A (16 tokens per tile, fragments by ldmatrix; warp w: tiles w, w + 4)
 // and q as column 0 of B; the lanes holding a token's dot form its weight
 // w_i = scale e^{A_t-A_i} q.k_i and store it as bf16 hi and lo parts (w = hi +
